@@ -1,0 +1,334 @@
+"""Device-resident tropical einsum for GB300 (sm_103a): thin Python binding.
+
+Every function here marshals torch CUDA tensors into the C ABI declared in
+``include/tropical.h`` and calls ``libtropical_gb300.so``; all computation
+runs in that library's CUDA kernels.  There is no CPU fallback: if the
+library is missing the first call raises.
+
+Semirings: ``"maxplus"`` (max, +), ``"minplus"`` (min, +), ``"maxtimes"``
+(max, *).  Argmax tensors are int32.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TropicalError", "load", "permute_trace", "permute_pair", "gemm", "einsum", "contract_tree",
+    "tree_backtrack", "stats", "reset_stats", "sync_pool", "release_pool", "plan_describe", "version",
+    "SEMIRINGS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtropical_gb300.so")
+SEMIRINGS = {"maxplus": 0, "minplus": 1, "maxtimes": 2}
+_DTYPES = {torch.float32: 0, torch.int32: 1, torch.int64: 2}
+MAX_RANK = 32
+
+ERRORS = {
+    -1: "INVALID_ARG", -2: "HOST_POINTER", -3: "DEVICE_MISMATCH", -4: "DTYPE", -5: "SHAPE", -6: "SPEC",
+    -7: "OVERFLOW", -8: "CUDA", -9: "OOM", -10: "UNSUPPORTED",
+}
+
+
+class TropicalError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {message}")
+        self.code = code
+        self.name = ERRORS.get(code, str(code))
+
+
+class TropTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * MAX_RANK), ("stride", ctypes.c_int64 * MAX_RANK)]
+
+
+class TropNode(ctypes.Structure):
+    _fields_ = [("lhs", ctypes.c_int32), ("rhs", ctypes.c_int32), ("n_lhs", ctypes.c_int32),
+                ("n_rhs", ctypes.c_int32), ("n_out", ctypes.c_int32),
+                ("lhs_labels", ctypes.POINTER(ctypes.c_int32)), ("rhs_labels", ctypes.POINTER(ctypes.c_int32)),
+                ("out_labels", ctypes.POINTER(ctypes.c_int32))]
+
+
+_STAT_FIELDS = ["module_inits", "kernel_launches", "pool_allocs", "pool_hits", "pool_device_mallocs",
+                "pool_retired", "pool_released", "pool_event_waits", "pool_leaked", "pool_bytes_cached",
+                "stream_syncs"]
+
+
+class TropStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in _STAT_FIELDS]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m einsum_device_side_gb300.build` "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    TP = ctypes.POINTER(TropTensor)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "tropical_init": (I, [I]),
+        "tropical_permute_trace": (I, [TP, ctypes.c_char_p, I, TP, P, P]),
+        "tropical_permute_pair": (I, [TP, TP, ctypes.c_char_p, TP, TP, P]),
+        "tropical_gemm_strided_batched_argmax": (I, [I, I, I64, I64, I64, I64, P, I64, I64, I64, P, I64, I64, I64,
+                                                     P, I64, I64, I64, P, P]),
+        "tropical_einsum_pairwise": (I, [ctypes.c_char_p, TP, TP, I, TP, P, P]),
+        "tropical_contract_tree": (I, [I, TP, I, ctypes.POINTER(TropNode), I, TP, ctypes.POINTER(P), P]),
+        "tropical_tree_backtrack": (I, [I, TP, I, ctypes.POINTER(TropNode), ctypes.POINTER(P), I64, I, P, P]),
+        "tropical_sync_pool": (I, []),
+        "tropical_release_pool": (I, []),
+        "tropical_stats": (I, [ctypes.POINTER(TropStats)]),
+        "tropical_reset_stats": (None, []),
+        "tropical_last_error": (ctypes.c_char_p, []),
+        "tropical_version": (I, []),
+        "tropical_plan_describe": (I, [ctypes.c_char_p, I, i64p, i64p, I, i64p, i64p, ctypes.c_char_p, I]),
+        "tropical_debug_fail_next_event_records": (None, [I]),
+        "tropical_set_pool_capacity": (None, [I]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    del i32p
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = _lib.tropical_last_error().decode(errors="replace")
+        raise TropicalError(rc, msg)
+
+
+def _sr(semiring) -> int:
+    if isinstance(semiring, str):
+        return SEMIRINGS[semiring]
+    return int(semiring)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def tensor_desc(t: torch.Tensor) -> TropTensor:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > MAX_RANK:
+        raise ValueError("rank above 32")
+    d = TropTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPES[t.dtype]
+    d.rank = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _spec_shape(spec: str, shapes):
+    lhs, out = spec.replace(" ", "").split("->")
+    sizes = {}
+    for op, shp in zip(lhs.split(","), shapes):
+        for ch, s in zip(op, shp):
+            sizes.setdefault(ch, s)
+    return [sizes[ch] for ch in out]
+
+
+def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Tensor | None = None,
+                  argmax: bool | torch.Tensor = False, stream=None):
+    """Unary permute / diagonal gather / tropical trace.  Returns ``out`` or
+    ``(out, argmax)`` when ``argmax`` is True or a tensor."""
+    lib = load()
+    if out is None:
+        out = torch.empty(_spec_shape(spec, [x.shape]), dtype=x.dtype, device=x.device)
+    am = None
+    if isinstance(argmax, torch.Tensor):
+        am = argmax
+    elif argmax:
+        am = torch.empty(out.shape, dtype=torch.int32, device=x.device)
+    dx, do = tensor_desc(x), tensor_desc(out)
+    _check(lib.tropical_permute_trace(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
+                                      am.data_ptr() if am is not None and am.numel() else None, _stream(stream)))
+    return (out, am) if am is not None else out
+
+
+def permute_pair(val: torch.Tensor, arg: torch.Tensor, spec: str, out_val=None, out_arg=None, stream=None):
+    """Permute a result and its int32 argmax through one index mapping."""
+    lib = load()
+    shape = _spec_shape(spec, [val.shape])
+    if out_val is None:
+        out_val = torch.empty(shape, dtype=val.dtype, device=val.device)
+    if out_arg is None:
+        out_arg = torch.empty(shape, dtype=torch.int32, device=val.device)
+    a, b, c, d = tensor_desc(val), tensor_desc(arg), tensor_desc(out_val), tensor_desc(out_arg)
+    _check(lib.tropical_permute_pair(ctypes.byref(a), ctypes.byref(b), spec.encode(), ctypes.byref(c),
+                                     ctypes.byref(d), _stream(stream)))
+    return out_val, out_arg
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = True, out=None, out_argmax=None,
+         stream=None):
+    """Strided-batched tropical GEMM: A [batch, M, K], B [batch, K, N] (any
+    strides, batch stride 0 allowed).  Returns (C, argmax) or C."""
+    lib = load()
+    if A.dim() == 2:
+        A = A.unsqueeze(0)
+    if B.dim() == 2:
+        B = B.unsqueeze(0)
+    batch = max(A.shape[0], B.shape[0])
+    if A.shape[0] != batch:
+        A = A.expand(batch, *A.shape[1:])
+    if B.shape[0] != batch:
+        B = B.expand(batch, *B.shape[1:])
+    M, K = A.shape[1], A.shape[2]
+    N = B.shape[2]
+    if B.shape[1] != K:
+        raise ValueError("inner extents differ")
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=torch.float32, device=A.device)
+    am = None
+    if argmax:
+        am = out_argmax if out_argmax is not None else torch.empty((batch, M, N), dtype=torch.int32, device=A.device)
+        if am.stride() != out.stride():
+            raise ValueError("argmax must have the strides of out")
+    _check(lib.tropical_gemm_strided_batched_argmax(
+        _sr(semiring), 0, batch, M, N, K,
+        A.data_ptr() if A.numel() else None, A.stride(0), A.stride(1), A.stride(2),
+        B.data_ptr() if B.numel() else None, B.stride(0), B.stride(1), B.stride(2),
+        out.data_ptr() if out.numel() else None, out.stride(0), out.stride(1), out.stride(2),
+        am.data_ptr() if am is not None and am.numel() else None, _stream(stream)))
+    return (out, am) if argmax else out
+
+
+def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = True, out=None,
+           out_argmax=None, stream=None):
+    """Pairwise tropical einsum, e.g. ``einsum('zacd,zdce->zea', A, B)``.
+    Returns (out, argmax) or out."""
+    lib = load()
+    if out is None:
+        out = torch.empty(_spec_shape(spec, [A.shape, B.shape]), dtype=torch.float32, device=A.device)
+    am = None
+    if argmax:
+        am = out_argmax if out_argmax is not None else torch.empty(out.shape, dtype=torch.int32, device=A.device)
+    a, b, o = tensor_desc(A), tensor_desc(B), tensor_desc(out)
+    _check(lib.tropical_einsum_pairwise(spec.encode(), ctypes.byref(a), ctypes.byref(b), _sr(semiring),
+                                        ctypes.byref(o), am.data_ptr() if am is not None and am.numel() else None,
+                                        _stream(stream)))
+    return (out, am) if argmax else out
+
+
+class _NodeTable:
+    """Keeps the ctypes arrays of a node list alive for one call."""
+
+    def __init__(self, nodes):
+        self.keep = []
+        self.arr = (TropNode * len(nodes))()
+        for j, (lhs, rhs, ll, rl, ol) in enumerate(nodes):
+            n = self.arr[j]
+            n.lhs, n.rhs = lhs, (-1 if rhs is None else rhs)
+            for attr, cnt, labs in (("lhs_labels", "n_lhs", ll), ("rhs_labels", "n_rhs", rl or []),
+                                    ("out_labels", "n_out", ol)):
+                buf = (ctypes.c_int32 * max(1, len(labs)))(*labs)
+                self.keep.append(buf)
+                setattr(n, attr, ctypes.cast(buf, ctypes.POINTER(ctypes.c_int32)))
+                setattr(n, cnt, len(labs))
+
+
+def contract_tree(inputs, nodes, semiring="maxplus", out: torch.Tensor | None = None, node_argmax=None,
+                  stream=None):
+    """Run a contraction tree.  ``nodes``: list of (lhs_id, rhs_id_or_None,
+    lhs_labels, rhs_labels_or_None, out_labels) with integer labels; ids
+    0..len(inputs)-1 are inputs, len(inputs)+j is node j.  ``out`` must have
+    the root node's shape.  ``node_argmax``: optional list of int32 tensors or
+    None per node."""
+    lib = load()
+    descs = (TropTensor * max(1, len(inputs)))(*[tensor_desc(t) for t in inputs])
+    table = _NodeTable(nodes)
+    ams = None
+    if node_argmax is not None:
+        ams = (ctypes.c_void_p * len(nodes))(*[(t.data_ptr() if t is not None and t.numel() else None)
+                                               for t in node_argmax])
+    o = tensor_desc(out)
+    _check(lib.tropical_contract_tree(len(inputs), descs, len(nodes), table.arr, _sr(semiring), ctypes.byref(o),
+                                      ams, _stream(stream)))
+    return out
+
+
+def tree_backtrack(inputs, nodes, node_argmax, n_labels: int, root_index: int = 0, assignment=None, stream=None):
+    """Recover every eliminated label's value from the per-node argmaxes
+    (device-side walk).  Returns an int32 device tensor of n_labels (-1 where
+    undetermined)."""
+    lib = load()
+    dev = inputs[0].device if inputs else torch.device("cuda")
+    if assignment is None:
+        assignment = torch.empty(n_labels, dtype=torch.int32, device=dev)
+    descs = (TropTensor * max(1, len(inputs)))(*[tensor_desc(t) for t in inputs])
+    table = _NodeTable(nodes)
+    ams = (ctypes.c_void_p * len(nodes))(*[(t.data_ptr() if t is not None and t.numel() else None)
+                                           for t in node_argmax])
+    _check(lib.tropical_tree_backtrack(len(inputs), descs, len(nodes), table.arr, ams, root_index, n_labels,
+                                       assignment.data_ptr(), _stream(stream)))
+    return assignment
+
+
+def stats() -> dict:
+    lib = load()
+    s = TropStats()
+    _check(lib.tropical_stats(ctypes.byref(s)))
+    return {n: getattr(s, n) for n in _STAT_FIELDS}
+
+
+def reset_stats():
+    load().tropical_reset_stats()
+
+
+def sync_pool():
+    lib = load()
+    _check(lib.tropical_sync_pool())
+
+
+def release_pool():
+    lib = load()
+    _check(lib.tropical_release_pool())
+
+
+def set_pool_capacity(n: int):
+    load().tropical_set_pool_capacity(int(n))
+
+
+def debug_fail_next_event_records(n: int):
+    load().tropical_debug_fail_next_event_records(int(n))
+
+
+def init(device: int = 0):
+    lib = load()
+    _check(lib.tropical_init(int(device)))
+
+
+def version() -> int:
+    return load().tropical_version()
+
+
+def plan_describe(spec: str, shape_a, stride_a, shape_b, stride_b) -> str:
+    """Host-only: how the pairwise einsum would be lowered (no GPU needed)."""
+    lib = load()
+    buf = ctypes.create_string_buffer(1024)
+    arr = lambda v: (ctypes.c_int64 * max(1, len(v)))(*v)  # noqa: E731
+    _check(lib.tropical_plan_describe(spec.encode(), len(shape_a), arr(shape_a), arr(stride_a), len(shape_b),
+                                      arr(shape_b), arr(stride_b), buf, 1024))
+    return buf.value.decode()

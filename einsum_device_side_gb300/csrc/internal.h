@@ -1,0 +1,124 @@
+// internal.h -- declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/tropical.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "tropical.h"
+
+namespace trop {
+
+constexpr int MAXR = TROP_MAX_RANK;
+constexpr int MAXB = 12;  // batch dims a GEMM launch can carry
+
+// ---------------------------------------------------------------- errors
+int set_error(int code, const char* fmt, ...);
+void clear_error();
+int cuda_error(cudaError_t e, const char* what);  // TROP_ERR_CUDA with message
+
+#define TROP_TRY(expr)                    \
+    do {                                  \
+        int trop_rc_ = (expr);            \
+        if (trop_rc_ != TROP_OK) return trop_rc_; \
+    } while (0)
+
+// ---------------------------------------------------------------- device
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int max_threads_per_sm;
+    size_t smem_per_sm;
+    size_t l2_bytes;
+};
+// Set up the current device once; fills *info.
+int ensure_device(const DeviceInfo** info);
+// Validate a device pointer for the current device (nbytes > 0 only).
+int check_device_pointer(const void* p, const char* name);
+
+// ---------------------------------------------------------------- counters
+void count_launches(int64_t n);
+void count_module_init();
+void count_pool(int field, int64_t n);  // field: see pool.cu
+enum { ST_ALLOC, ST_HIT, ST_MALLOC, ST_RETIRED, ST_RELEASED, ST_EVWAIT, ST_LEAKED, ST_BYTES };
+
+// ---------------------------------------------------------------- pool
+// Workspace blocks, released only after an event recorded on the stream
+// that last used them completes (see pool.cu).
+int pool_alloc(size_t bytes, cudaStream_t stream, void** out);
+void pool_retire(void* ptr, cudaStream_t stream);
+
+// ---------------------------------------------------------------- fast divmod
+// Unsigned 32-bit division by a runtime-invariant divisor with a
+// precomputed multiplier (Granlund & Montgomery, "Division by invariant
+// integers using multiplication", PLDI 1994): q = umulhi(n, mul) >> shift.
+struct FastDiv {
+    uint32_t d, mul, shift;
+};
+FastDiv make_fastdiv(uint32_t d);
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f)
+{
+    return f.mul == 0 ? (n >> f.shift) : (__umulhi(n, f.mul) >> f.shift);
+}
+#endif
+
+// ---------------------------------------------------------------- launches
+// Gather / permute over `rank` dims (output order, last fastest).  Optional
+// companion int32 tensor moved through the same index mapping.
+struct GatherDesc {
+    int rank;
+    int64_t size[MAXR];
+    int64_t s_in[MAXR];
+    int64_t s_out[MAXR];
+    int64_t s_in2[MAXR];
+    int64_t s_out2[MAXR];
+};
+int launch_gather(const void* in, void* out, int elem_bytes, const int32_t* in2, int32_t* out2,
+                  const GatherDesc& d, cudaStream_t s);
+
+// (+)-reduction over `red` dims for every element of `out` dims.
+struct ReduceDesc {
+    int out_rank;
+    int64_t out_size[MAXR];
+    int64_t out_s_in[MAXR];
+    int64_t out_s_out[MAXR];
+    int64_t out_s_arg[MAXR];
+    int red_rank;
+    int64_t red_size[MAXR];
+    int64_t red_s_in[MAXR];
+};
+int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* argmax,
+                  const ReduceDesc& d, cudaStream_t s);
+
+// Strided-batched tropical GEMM with a multi-dimensional batch.
+struct GemmDesc {
+    int semiring;
+    int64_t M, N, K;
+    const float* A;
+    const float* B;
+    float* C;
+    int32_t* I;  // nullable
+    int64_t sAm, sAk, sBk, sBn, sCm, sCn, sIm, sIn;
+    int nb;
+    int64_t bsize[MAXB];
+    int64_t sAb[MAXB], sBb[MAXB], sCb[MAXB], sIb[MAXB];
+};
+int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name);
+
+// Tree back-tracking (backtrack.cu).
+struct BtNode {
+    const int32_t* argmax;  // nullable
+    int n_out;              // output labels (row-major, last fastest)
+    int n_k;                // argmax labels (row-major, last fastest)
+    int lab_off;            // offset into the label table: n_out out labels then n_k argmax labels
+};
+int launch_backtrack(const BtNode* nodes_dev, int n_nodes, const int32_t* labels_dev,
+                     const int64_t* sizes_dev, int64_t root_index, int n_labels,
+                     int32_t* assignment, cudaStream_t s);
+
+size_t dtype_bytes(int dtype);
+
+}  // namespace trop

@@ -1,0 +1,445 @@
+// runtime.cpp -- once-per-device set-up, error state, counters, and the
+// workspace pool whose blocks are released only through CUDA events.
+//
+// Workspace retirement follows the tenferro-rs design note "cuTENSOR
+// workspace retirement without a stream barrier": a block that is no longer
+// needed gets an event recorded on the stream that last used it and joins a
+// bounded retirement queue (Proposal, items 2-4).  The queue is drained --
+// events queried, completed blocks returned to the free lists -- right
+// before every allocation and on an explicit tropical_sync_pool()
+// ("Open decisions" 1).  At capacity (default 16) the oldest retirement is
+// resolved with an event wait; if recording the event fails the block is
+// leaked, never reused ("Open decisions" 2: leak rather than race).  Unlike
+// that note there is no stream-barrier fallback at all: no code path here
+// calls cudaStreamSynchronize or cudaDeviceSynchronize.
+//
+// One refinement: a retiring block may be handed to a new request on the
+// SAME stream before its event completes, because stream order already puts
+// the new work after the old (the usual stream-ordered caching rule).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <deque>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace trop {
+
+// ------------------------------------------------------------------ errors
+static thread_local std::string g_last_error;
+
+int set_error(int code, const char* fmt, ...)
+{
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+void clear_error() { g_last_error.clear(); }
+
+int cuda_error(cudaError_t e, const char* what)
+{
+    return set_error(TROP_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+size_t dtype_bytes(int dtype)
+{
+    switch (dtype) {
+    case TROP_F32: return 4;
+    case TROP_I32: return 4;
+    case TROP_I64: return 8;
+    default: return 0;
+    }
+}
+
+// ------------------------------------------------------------------ counters
+static std::atomic<int64_t> c_module_inits{0}, c_launches{0}, c_stream_syncs{0};
+static std::atomic<int64_t> c_pool[8];
+
+void count_launches(int64_t n) { c_launches += n; }
+void count_module_init() { c_module_inits += 1; }
+void count_pool(int field, int64_t n) { c_pool[field] += n; }
+
+// ------------------------------------------------------------------ fast divmod
+FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f{};
+    f.d = d ? d : 1;
+    uint32_t l = 0;
+    while (l < 32 && (uint64_t(1) << l) < f.d) ++l;  // l = ceil(log2 d)
+    if ((f.d & (f.d - 1)) == 0) {                     // power of two: plain shift
+        f.mul = 0;
+        f.shift = l;
+        return f;
+    }
+    // m = floor(2^(32+l) / d) + 1 fits 33 bits; keep the low 32 and fold the
+    // top bit into the formula q = (umulhi(n, m') + n) >> l ... to stay in 32-bit
+    // arithmetic we instead use the 31-bit-safe variant with n < 2^31:
+    //   mul = ceil(2^(31+l) / d), q = umulhi(n, mul) >> (l - 1)
+    // which is exact for all n < 2^31 (all index arithmetic here is below 2^31).
+    uint64_t m = ((uint64_t(1) << (31 + l)) + f.d - 1) / f.d;
+    f.mul = (uint32_t)m;
+    f.shift = l - 1;
+    return f;
+}
+
+// ------------------------------------------------------------------ device set-up
+static std::mutex g_dev_mu;
+static DeviceInfo g_dev[64];
+static bool g_dev_ready[64];
+
+extern int register_kernels_for_device();  // kernels.cu: loads kernels once
+
+int ensure_device(const DeviceInfo** info)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return set_error(TROP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ready[dev]) {
+        cudaDeviceProp p;
+        e = cudaGetDeviceProperties(&p, dev);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetDeviceProperties");
+        if (p.major < 10)
+            return set_error(TROP_ERR_UNSUPPORTED, "device %d is sm_%d%d; this build targets sm_103a", dev,
+                             p.major, p.minor);
+        DeviceInfo& d = g_dev[dev];
+        d.device = dev;
+        d.sm_count = p.multiProcessorCount;
+        d.max_threads_per_sm = p.maxThreadsPerMultiProcessor;
+        d.smem_per_sm = p.sharedMemPerMultiprocessor;
+        d.l2_bytes = (size_t)p.l2CacheSize;
+        int rc = register_kernels_for_device();
+        if (rc != TROP_OK) return rc;
+        g_dev_ready[dev] = true;
+        count_module_init();
+    }
+    if (info) *info = &g_dev[dev];
+    return TROP_OK;
+}
+
+int check_device_pointer(const void* p, const char* name)
+{
+    if (!p) return set_error(TROP_ERR_INVALID_ARG, "%s is NULL", name);
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(TROP_ERR_HOST_POINTER, "%s (%p) is not a CUDA device pointer (%s)", name, p,
+                         cudaGetErrorString(e));
+    }
+    if (a.type == cudaMemoryTypeUnregistered || a.type == cudaMemoryTypeHost)
+        return set_error(TROP_ERR_HOST_POINTER, "%s (%p) is host memory; device memory is required", name, p);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (a.type == cudaMemoryTypeDevice && a.device != dev)
+        return set_error(TROP_ERR_DEVICE_MISMATCH, "%s lives on device %d, current device is %d", name,
+                         a.device, dev);
+    return TROP_OK;
+}
+
+// ------------------------------------------------------------------ pool
+namespace {
+
+struct Block {
+    void* ptr;
+    size_t bytes;
+    int device;
+};
+
+struct Retiring {
+    Block b;
+    cudaEvent_t ev;
+    cudaStream_t stream;
+};
+
+struct Pool {
+    std::mutex mu;
+    std::multimap<size_t, Block> free_;  // keyed by size
+    std::map<void*, Block> live_;        // handed out, not yet retired
+    std::deque<Retiring> retiring_;
+    std::vector<cudaEvent_t> events_;    // idle events for reuse
+    int capacity = 16;
+    int fail_records = 0;                // test hook
+    size_t cached_bytes = 0;
+
+    cudaEvent_t get_event()
+    {
+        if (!events_.empty()) {
+            cudaEvent_t e = events_.back();
+            events_.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return e;
+    }
+
+    void to_free(const Block& b) { free_.emplace(b.bytes, b); }
+
+    // query pending events in order; release the completed prefix and any
+    // completed entry behind an incomplete one
+    void drain_locked()
+    {
+        for (auto it = retiring_.begin(); it != retiring_.end();) {
+            cudaError_t q = cudaEventQuery(it->ev);
+            if (q == cudaSuccess) {
+                to_free(it->b);
+                events_.push_back(it->ev);
+                count_pool(ST_RELEASED, 1);
+                it = retiring_.erase(it);
+            } else {
+                if (q != cudaErrorNotReady) cudaGetLastError();
+                ++it;
+            }
+        }
+    }
+
+    int wait_oldest_locked()
+    {
+        Retiring r = retiring_.front();
+        retiring_.pop_front();
+        cudaError_t e = cudaEventSynchronize(r.ev);
+        count_pool(ST_EVWAIT, 1);
+        if (e != cudaSuccess) {
+            // cannot prove completion: leak the block rather than race
+            cudaGetLastError();
+            cached_bytes -= r.b.bytes;
+            count_pool(ST_LEAKED, 1);
+            return TROP_OK;
+        }
+        to_free(r.b);
+        events_.push_back(r.ev);
+        count_pool(ST_RELEASED, 1);
+        return TROP_OK;
+    }
+};
+
+Pool& pool()
+{
+    static Pool* p = [] {
+        Pool* q = new Pool();
+        if (const char* env = std::getenv("TROP_POOL_CAPACITY")) {
+            int c = std::atoi(env);
+            q->capacity = c < 1 ? 1 : c;
+        }
+        return q;
+    }();
+    return *p;
+}
+
+size_t round_bytes(size_t n)
+{
+    const size_t g = n < (size_t(1) << 20) ? 512 : (size_t(1) << 16);
+    return (n + g - 1) / g * g;
+}
+
+}  // namespace
+
+int pool_alloc(size_t bytes, cudaStream_t stream, void** out)
+{
+    *out = nullptr;
+    if (bytes == 0) bytes = 1;
+    const size_t want = round_bytes(bytes);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    Pool& P = pool();
+    std::lock_guard<std::mutex> lk(P.mu);
+    count_pool(ST_ALLOC, 1);
+    P.drain_locked();
+    // best fit among free blocks of this device, at most 2x the request
+    for (auto it = P.free_.lower_bound(want); it != P.free_.end() && it->first <= 2 * want; ++it) {
+        if (it->second.device != dev) continue;
+        Block b = it->second;
+        P.free_.erase(it);
+        P.live_[b.ptr] = b;
+        count_pool(ST_HIT, 1);
+        *out = b.ptr;
+        return TROP_OK;
+    }
+    // a block still retiring on this same stream is safe by stream order
+    for (auto it = P.retiring_.begin(); it != P.retiring_.end(); ++it) {
+        if (it->stream != stream || it->b.device != dev) continue;
+        if (it->b.bytes < want || it->b.bytes > 2 * want) continue;
+        Block b = it->b;
+        P.events_.push_back(it->ev);
+        P.retiring_.erase(it);
+        P.live_[b.ptr] = b;
+        count_pool(ST_HIT, 1);
+        *out = b.ptr;
+        return TROP_OK;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, want);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        // give back everything cached on this device and retry once
+        while (!P.retiring_.empty()) P.wait_oldest_locked();
+        for (auto it = P.free_.begin(); it != P.free_.end();) {
+            if (it->second.device == dev) {
+                cudaFree(it->second.ptr);
+                P.cached_bytes -= it->second.bytes;
+                it = P.free_.erase(it);
+            } else {
+                ++it;
+            }
+        }
+        e = cudaMalloc(&p, want);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return set_error(TROP_ERR_OOM, "workspace allocation of %zu bytes failed: %s", want,
+                             cudaGetErrorString(e));
+        }
+    }
+    count_pool(ST_MALLOC, 1);
+    P.cached_bytes += want;
+    Block b{p, want, dev};
+    P.live_[p] = b;
+    *out = p;
+    return TROP_OK;
+}
+
+void pool_retire(void* ptr, cudaStream_t stream)
+{
+    if (!ptr) return;
+    Pool& P = pool();
+    std::lock_guard<std::mutex> lk(P.mu);
+    auto it = P.live_.find(ptr);
+    if (it == P.live_.end()) return;
+    Block b = it->second;
+    P.live_.erase(it);
+    count_pool(ST_RETIRED, 1);
+    cudaEvent_t ev = nullptr;
+    bool ok = false;
+    if (P.fail_records > 0) {
+        --P.fail_records;  // injected failure
+    } else {
+        ev = P.get_event();
+        if (ev) {
+            cudaError_t e = cudaEventRecord(ev, stream);
+            if (e == cudaSuccess) ok = true;
+            else {
+                cudaGetLastError();
+                P.events_.push_back(ev);
+            }
+        }
+    }
+    if (!ok) {  // no completion witness: leak rather than race
+        P.cached_bytes -= b.bytes;
+        count_pool(ST_LEAKED, 1);
+        return;
+    }
+    while ((int)P.retiring_.size() >= P.capacity) P.wait_oldest_locked();
+    P.retiring_.push_back(Retiring{b, ev, stream});
+}
+
+}  // namespace trop
+
+// ====================================================================== C ABI
+using namespace trop;
+
+extern "C" int tropical_init(int device)
+{
+    clear_error();
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (device != cur) {
+        e = cudaSetDevice(device);
+        if (e != cudaSuccess) return cuda_error(e, "cudaSetDevice");
+    }
+    int rc = ensure_device(nullptr);
+    if (device != cur) cudaSetDevice(cur);
+    return rc;
+}
+
+extern "C" int tropical_sync_pool(void)
+{
+    clear_error();
+    Pool& P = pool();
+    std::lock_guard<std::mutex> lk(P.mu);
+    while (!P.retiring_.empty()) P.wait_oldest_locked();
+    return TROP_OK;
+}
+
+extern "C" int tropical_release_pool(void)
+{
+    clear_error();
+    Pool& P = pool();
+    std::lock_guard<std::mutex> lk(P.mu);
+    while (!P.retiring_.empty()) P.wait_oldest_locked();
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : P.free_) {
+        cudaSetDevice(kv.second.device);
+        cudaFree(kv.second.ptr);
+        P.cached_bytes -= kv.second.bytes;
+    }
+    cudaSetDevice(cur);
+    P.free_.clear();
+    for (cudaEvent_t e : P.events_) cudaEventDestroy(e);
+    P.events_.clear();
+    return TROP_OK;
+}
+
+extern "C" int tropical_stats(trop_stats* out)
+{
+    if (!out) return set_error(TROP_ERR_INVALID_ARG, "stats pointer is NULL");
+    out->module_inits = c_module_inits.load();
+    out->kernel_launches = c_launches.load();
+    out->pool_allocs = c_pool[ST_ALLOC].load();
+    out->pool_hits = c_pool[ST_HIT].load();
+    out->pool_device_mallocs = c_pool[ST_MALLOC].load();
+    out->pool_retired = c_pool[ST_RETIRED].load();
+    out->pool_released = c_pool[ST_RELEASED].load();
+    out->pool_event_waits = c_pool[ST_EVWAIT].load();
+    out->pool_leaked = c_pool[ST_LEAKED].load();
+    {
+        Pool& P = pool();
+        std::lock_guard<std::mutex> lk(P.mu);
+        out->pool_bytes_cached = (int64_t)P.cached_bytes;
+    }
+    out->stream_syncs = c_stream_syncs.load();
+    return TROP_OK;
+}
+
+extern "C" void tropical_reset_stats(void)
+{
+    c_launches = 0;
+    c_stream_syncs = 0;
+    for (int i = 0; i < 7; ++i) c_pool[i] = 0;  // ST_BYTES is derived, module_inits kept
+}
+
+extern "C" const char* tropical_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int tropical_version(void) { return 1; }
+
+extern "C" void tropical_debug_fail_next_event_records(int count)
+{
+    Pool& P = pool();
+    std::lock_guard<std::mutex> lk(P.mu);
+    P.fail_records = count < 0 ? 0 : count;
+}
+
+extern "C" void tropical_set_pool_capacity(int capacity)
+{
+    Pool& P = pool();
+    std::lock_guard<std::mutex> lk(P.mu);
+    P.capacity = capacity < 1 ? 1 : capacity;
+}

@@ -1,0 +1,264 @@
+/*
+ * tropical.h -- C ABI of the device-resident tropical einsum library
+ * (libtropical_gb300.so, sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * Pairwise tropical-semiring einsum kept on the device end to end:
+ *   unary diagonal/trace pre-pass -> operand permute -> strided-batched
+ *   tropical GEMM with argmax -> output permute (value and argmax through one
+ *   index mapping), driven by a contraction-tree executor whose intermediates
+ *   never leave device memory.
+ *
+ * Sources (web pages this library follows; section names are the pages' own):
+ *  [I52]  omeinsum-rs issue #52, "GPU tropical path: keep tensors
+ *         device-resident + device-side permute": Summary; "Why Julia is
+ *         naturally fast"; "Proposed plan" steps 1-3; "Resolved design for
+ *         step 3" kernels (a) permute/strided gather and (b) diagonal/trace
+ *         gather + max/min reduce; "Acceptance criteria".
+ *  [PR35] tropical-gemm PR #35, "batched GPU ops with DLPack zero-copy
+ *         output": Summary (batched max-plus / min-plus / maxmul f32 kernels
+ *         with argmax; rejecting host memory; zero-sized dimension guards;
+ *         same-device validation).
+ *  [WR]   tenferro-rs design note "cuTENSOR workspace retirement without a
+ *         stream barrier": Proposal (event on the owning stream + retirement
+ *         queue) and "Open decisions" 1-2 (drain before allocation, bound 16,
+ *         event wait at capacity, leak rather than race).
+ *
+ * Semirings (PR35 names them; their neutral elements are not given on the
+ * pages and follow the usual tropical definitions):
+ *     TROP_MAXPLUS : a (+) b = max(a,b), a (x) b = a + b, zero = -inf
+ *     TROP_MINPLUS : a (+) b = min(a,b), a (x) b = a + b, zero = +inf
+ *     TROP_MAXTIMES: a (+) b = max(a,b), a (x) b = a * b, zero = 0
+ * Each (x) rounds once in IEEE binary32 (round to nearest even, subnormals
+ * kept); each (+) is exact, so results do not depend on evaluation order.
+ * Argmax: the smallest contracted linear index that reaches the result; 0
+ * when no term beats the semiring zero (e.g. an empty contraction).
+ * Preconditions (not checked): no NaN; no -0.0; max-plus operands below
+ * +inf and min-plus operands above -inf; max-times operands finite and
+ * nonnegative (negative products are clamped by the zero 0).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Tensor data pointers are DEVICE pointers of the current device
+ *    (cudaMalloc / torch CUDA storage, or managed memory).  Host pointers are
+ *    rejected with TROP_ERR_HOST_POINTER [PR35 Summary "Reject CudaHost"];
+ *    pointers of another device with TROP_ERR_DEVICE_MISMATCH.
+ *  - Strides are in ELEMENTS and may be 0 (broadcast) for inputs.  Outputs
+ *    must not overlap themselves or the inputs (not checked).
+ *  - The caller owns every input, output and argmax buffer.  The library owns
+ *    only its workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous on it: results are valid once the
+ *    stream reaches the point of the call.  No call synchronizes a stream.
+ *  - Return value: TROP_OK (0) or a negative TROP_ERR_* code.  The message of
+ *    the last failure on the calling thread is tropical_last_error().  No C++
+ *    exception crosses this boundary.  Validation failures launch nothing.
+ *  - Zero-sized dimensions are allowed [PR35 Summary]: an empty output is a
+ *    no-op; an empty contraction writes the semiring zero and argmax 0.
+ *  - Thread safety: calls may come from several host threads; library state
+ *    (module set-up, workspace pool, counters) is internally locked.
+ */
+#ifndef TROPICAL_GB300_H
+#define TROPICAL_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TROP_MAX_RANK 32
+
+typedef enum { TROP_MAXPLUS = 0, TROP_MINPLUS = 1, TROP_MAXTIMES = 2 } trop_semiring;
+typedef enum { TROP_F32 = 0, TROP_I32 = 1, TROP_I64 = 2 } trop_dtype;
+
+enum {
+    TROP_OK = 0,
+    TROP_ERR_INVALID_ARG = -1,     /* null pointer, bad enum, rank or id out of range */
+    TROP_ERR_HOST_POINTER = -2,    /* a data pointer is host memory */
+    TROP_ERR_DEVICE_MISMATCH = -3, /* a data pointer belongs to another device */
+    TROP_ERR_DTYPE = -4,           /* unsupported or mismatched dtype */
+    TROP_ERR_SHAPE = -5,           /* extents disagree with the spec or each other */
+    TROP_ERR_SPEC = -6,            /* einsum spec does not parse / is inconsistent */
+    TROP_ERR_OVERFLOW = -7,        /* contracted extent does not fit an int32 argmax */
+    TROP_ERR_CUDA = -8,            /* a CUDA runtime call or launch failed */
+    TROP_ERR_OOM = -9,             /* workspace allocation failed */
+    TROP_ERR_UNSUPPORTED = -10     /* valid request this build does not handle */
+};
+
+/* A strided tensor view.  data: device pointer (may be NULL when an extent is
+ * 0); shape/stride: first `rank` entries used, strides in elements. */
+typedef struct {
+    void* data;
+    int32_t dtype; /* trop_dtype */
+    int32_t rank;  /* 0 .. TROP_MAX_RANK */
+    int64_t shape[TROP_MAX_RANK];
+    int64_t stride[TROP_MAX_RANK];
+} trop_tensor;
+
+/* One node of a contraction tree (see tropical_contract_tree).  Operand ids:
+ * 0 .. n_inputs-1 are the tree's inputs, n_inputs + j is node j's output
+ * (j smaller than this node's index).  rhs = -1 makes a unary node (diagonal /
+ * trace / permute of lhs).  Labels are integers in [0, 65535]; a label
+ * repeated inside one operand is a diagonal, a label absent from out_labels
+ * is reduced with (+). */
+typedef struct {
+    int32_t lhs, rhs;
+    int32_t n_lhs, n_rhs, n_out;
+    const int32_t* lhs_labels;
+    const int32_t* rhs_labels;
+    const int32_t* out_labels;
+} trop_node;
+
+/* Counters since load (or since tropical_reset_stats). */
+typedef struct {
+    int64_t module_inits;        /* per-device kernel set-ups (once per device) */
+    int64_t kernel_launches;     /* kernels launched by this library */
+    int64_t pool_allocs;         /* workspace requests */
+    int64_t pool_hits;           /* requests served from cached blocks */
+    int64_t pool_device_mallocs; /* cudaMalloc calls made by the pool */
+    int64_t pool_retired;        /* blocks handed to the retirement queue */
+    int64_t pool_released;       /* retired blocks whose event completed */
+    int64_t pool_event_waits;    /* queue at capacity: waited on the oldest event */
+    int64_t pool_leaked;         /* event record failed: block leaked, never reused */
+    int64_t pool_bytes_cached;   /* bytes held by the pool (free + retiring) */
+    int64_t stream_syncs;        /* stream synchronizations issued (stays 0) */
+} trop_stats;
+
+/* Set up the kernels for `device` once (kernel attributes, device
+ * properties, workspace pool) [I52 "Proposed plan" step 1: the context and
+ * module are created once, not per node].  Idempotent; every other entry
+ * point calls it for the current device.  Errors: TROP_ERR_CUDA. */
+int tropical_init(int device);
+
+/* Unary op [I52 "Resolved design for step 3", kernels (a) and (b)]:
+ *   spec "in->out" over letters a-z A-Z, e.g. "abcdef->fbdcae" (permute),
+ *   "iijk->ijk" (diagonal gather), "iijk->jk" (diagonal + (+)-reduce over i).
+ *   out[o] = (+) over the labels of `in` absent from the output of
+ *   in[diagonal position], in the semiring `semiring`; with no such label
+ *   this is a strided gather (any dtype; semiring only checked for range).
+ * in, out:  same dtype (f32, i32 or i64); out.shape must equal the output
+ *           label extents; out may be strided.
+ * argmax:   nullable int32 buffer, contiguous row-major in out's shape: the
+ *           row-major linear index over the reduced labels (first-appearance
+ *           order in `in`) of the winner, 0 if nothing is reduced.
+ * Errors: INVALID_ARG, SPEC, SHAPE, DTYPE, HOST_POINTER, DEVICE_MISMATCH,
+ *         OVERFLOW (reduced extent > INT32_MAX with argmax), CUDA, OOM. */
+int tropical_permute_trace(const trop_tensor* in, const char* spec, int semiring,
+                           const trop_tensor* out, int32_t* argmax, void* stream);
+
+/* Output permute of a result and its argmax through ONE index mapping
+ * [I52 "Resolved design for step 3": the float result and the argmax must be
+ * permuted with bit-for-bit identical index mappings].  spec is a pure
+ * permutation "abc->cab" (no repeated or dropped label).  val_in/val_out are
+ * f32, i32 or i64 of equal dtype; arg_in/arg_out are int32 tensors of the
+ * same shapes as val_in/val_out (any strides).  One kernel launch moves both. */
+int tropical_permute_pair(const trop_tensor* val_in, const trop_tensor* arg_in, const char* spec,
+                          const trop_tensor* val_out, const trop_tensor* arg_out, void* stream);
+
+/* Strided-batched tropical GEMM with argmax [PR35 Summary: the batched
+ * max-plus / min-plus / maxmul f32 kernels with argmax]:
+ *   C[b,m,n] = (+)_{k<K} A[b,m,k] (x) B[b,k,n]
+ *   argmax[b,m,n] = smallest k reaching C[b,m,n] (0 if none beats zero).
+ * Element (b,m,k) of A is A[b*sAb + m*sAm + k*sAk]; likewise B and C.
+ * argmax (nullable, int32) uses C's strides.  dtype must be TROP_F32.
+ * Errors: INVALID_ARG (negative extent, null pointer with nonzero extent),
+ *         DTYPE, OVERFLOW (K > INT32_MAX with argmax), HOST_POINTER,
+ *         DEVICE_MISMATCH, CUDA. */
+int tropical_gemm_strided_batched_argmax(int semiring, int dtype,
+                                         int64_t batch, int64_t M, int64_t N, int64_t K,
+                                         const void* A, int64_t sAb, int64_t sAm, int64_t sAk,
+                                         const void* B, int64_t sBb, int64_t sBk, int64_t sBn,
+                                         void* C, int64_t sCb, int64_t sCm, int64_t sCn,
+                                         int32_t* argmax, void* stream);
+
+/* Pairwise tropical einsum [I52 Summary and "Resolved design for step 3";
+ * PR35 Summary]:  spec "zacd,zdce->zea" over letters a-z A-Z.
+ *   out[o] = (+) over all assignments of the labels absent from the output
+ *            of A[..] (x) B[..]   (f32 only)
+ *   argmax[o] = row-major linear index over the CONTRACTED labels (present
+ *            in both operands, absent from the output), ordered by first
+ *            appearance in A's spec, of the smallest index reaching out[o].
+ *            Labels present in only one operand and absent from the output
+ *            are (+)-reduced first (a unary pre-pass) and are not part of
+ *            the argmax.  No contracted label: argmax 0.
+ * Lowering: diagonal/trace pre-pass per operand, permutes only where an
+ * operand's strides cannot feed the GEMM directly, strided-batched GEMM
+ * writing value and argmax through the output's own strides, or into a
+ * workspace followed by the one-mapping pair permute.
+ * argmax: nullable int32, contiguous row-major in out's shape.
+ * Errors: as tropical_permute_trace, plus OVERFLOW when the contracted extent
+ *         exceeds INT32_MAX with argmax. */
+int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, const trop_tensor* B,
+                             int semiring, const trop_tensor* out, int32_t* argmax, void* stream);
+
+/* Contraction-tree executor [I52 Summary, "Why Julia is naturally fast"
+ * row 1, "Acceptance criteria" 1: intermediates stay in device memory across
+ * the whole tree].  Runs nodes 0..n_nodes-1 in order; node j's output lives
+ * in pool workspace (contiguous, row-major in its out_labels order) until
+ * its last consumer has been enqueued, then is retired through an event on
+ * `stream` [WR Proposal].  The last node writes `out` (strided allowed).
+ * node_argmax: nullable array of n_nodes nullable int32 device buffers; entry
+ *   j receives node j's argmax (contiguous, node output shape), with the
+ *   meaning of tropical_einsum_pairwise (binary) or tropical_permute_trace
+ *   (unary).
+ * All inputs must share out's dtype; binary nodes need f32.
+ * Errors: as the pairwise/unary calls, plus INVALID_ARG for bad operand ids.
+ * Validation of the whole tree happens before the first launch. */
+int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, int n_nodes,
+                           const trop_node* nodes, int semiring, const trop_tensor* out,
+                           int32_t* const* node_argmax, void* stream);
+
+/* Argmax back-tracking through a contraction tree, on the device.  Given the
+ * tree of tropical_contract_tree, every node's argmax buffer and the linear
+ * index `root_index` of an element of the last node's output (0 for a scalar
+ * root), writes assignment[l] = the value of label l in the optimal
+ * configuration, for l in [0, n_labels); labels whose value no argmax
+ * determines (one-operand labels reduced inside a binary node, or nodes
+ * whose argmax buffer is NULL) are -1.  assignment: int32 device buffer of
+ * n_labels entries.  One device thread walks the nodes backwards; nothing
+ * is copied to the host. */
+int tropical_tree_backtrack(int n_inputs, const trop_tensor* inputs, int n_nodes,
+                            const trop_node* nodes, int32_t* const* node_argmax,
+                            int64_t root_index, int n_labels, int32_t* assignment, void* stream);
+
+/* Drain the workspace retirement queue: wait for every pending event and
+ * return the blocks to the pool [WR "Open decisions" 1: explicit
+ * synchronize() is a drain point].  The only call that may block the host. */
+int tropical_sync_pool(void);
+
+/* Drain, then free every cached workspace block (teardown). */
+int tropical_release_pool(void);
+
+int tropical_stats(trop_stats* out);
+void tropical_reset_stats(void);
+
+/* Message of the last failure on this host thread ("" if none). */
+const char* tropical_last_error(void);
+
+/* Library / ABI version (increments on incompatible changes). */
+int tropical_version(void);
+
+/* Host-only planner inspection (no device work, no GPU needed): describes how
+ * tropical_einsum_pairwise would lower `spec` for operands with the given
+ * shapes/strides and a contiguous output, as one line of text in buf.
+ * Returns TROP_OK or an error code (SPEC, SHAPE, INVALID_ARG). */
+int tropical_plan_describe(const char* spec, int rank_a, const int64_t* shape_a, const int64_t* stride_a,
+                           int rank_b, const int64_t* shape_b, const int64_t* stride_b,
+                           char* buf, int buflen);
+
+/* Test hook for the leak-rather-than-race path [WR "Open decisions" 2]:
+ * the next `count` retirements behave as if recording their CUDA event had
+ * failed (the block is then leaked, never reused).  Host-side only. */
+void tropical_debug_fail_next_event_records(int count);
+
+/* Set the retirement-queue bound (default 16, or TROP_POOL_CAPACITY from the
+ * environment at load).  Values < 1 are clamped to 1. */
+void tropical_set_pool_capacity(int capacity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TROPICAL_GB300_H */
