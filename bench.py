@@ -1,0 +1,413 @@
+"""Benchmark of the device-resident tropical einsum path on GB300.
+
+Headline workload (one "step"): strided-batched tropical GEMM with int32
+argmax, batch 64 x M=N=K=256, f32, for each of max-plus and min-plus
+(entries uniform(-1,1)) and max-times (entries uniform(0,1)) -- three
+launches through the C ABI.  Metric: semiring-ops/s (one op = one (x) and
+one (+)), whole job; roofline: the FP32 ALU peak SMs x 128 lanes x clock / 2.
+
+The same run also measures the other workloads of the path (permute and
+trace GB/s against HBM, the pairwise einsum 'zacd,zdce->zea', the 24x24
+spin-glass contraction tree), reported under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (the path has no exchange step); rank 0 prints one
+JSON line.  --impl reference times the CPU oracle instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+GEMM_B, GEMM_M, GEMM_N, GEMM_K = 64, 256, 256, 256
+OPS_PER_GEMM = GEMM_B * GEMM_M * GEMM_N * GEMM_K
+SEMIRINGS = (0, 1, 2)
+METRIC = "tropical GEMM G semiring-ops/s (% of FP32 ALU peak); permute/trace GB/s (% HBM)"
+N_SETS = 3  # independent input sets rotated across steps: 288 MiB of inputs > 129 MB L2
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+    f = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(f):
+        d = json.load(open(f))
+        p.update({k: d[k] for k in ("hbm_gbs", "sm_max_mhz") if k in d})
+        p["source"] = "measured"
+    return p
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    def __init__(self, index=0, period_ms=20):
+        self.cmd = ["nvidia-smi", f"--id={index}",
+                    "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                    "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                    "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                    "--format=csv,noheader,nounits", f"-lms={period_ms}"]
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def mark(self):
+        return len(self.rows)
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self, start, end):
+        rows = self.rows[start:end] or self.rows[-3:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 4 + i and r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_init():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier_max(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.barrier()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def cpu_sample_rate(target_s=12.0):
+    """Oracle semiring-ops/s on a bounded sample of the headline workload."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    total_ops, elapsed, outs = 0, 0.0, 0
+    n = 4096
+    for sr in SEMIRINGS:
+        a, b = synth.gemm_batched_inputs(sr)
+        budget = target_s / 3
+        t_sr = 0.0
+        while t_sr < budget:
+            s = rng.choice(GEMM_B * GEMM_M * GEMM_N, size=n, replace=False).astype(np.int64)
+            t0 = time.perf_counter()
+            oracle.gemm(a, b, sr, samples=s, nthreads=cores)
+            dt = time.perf_counter() - t0
+            t_sr += dt
+            total_ops += n * GEMM_K
+            outs += n
+            if dt < budget / 8:
+                n = min(n * 2, GEMM_B * GEMM_M * GEMM_N)
+        elapsed += t_sr
+    return {"value": total_ops / elapsed / 1e9, "unit": "G semiring-ops/s", "cores": cores, "kind": "oracle",
+            "sample": f"{outs} sampled outputs (x K=256 terms) of the batch-64 256^3 GEMMs, 3 semirings, "
+                      f"OpenMP over {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    steps = []
+    # keep the whole reference run within about three minutes whatever K and W are
+    per = max(0.3, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_sample_rate(target_s=per)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        steps.append(cpu_sample_rate(target_s=per))
+    dt = time.perf_counter() - t0
+    val = statistics.median([s["value"] for s in steps])
+    cb = dict(steps[0])
+    cb["value"] = val
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "G semiring-ops/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "batched tropical GEMM + argmax, batch 64 x 256^3, maxplus/minplus/maxtimes",
+                   "sample": cb["sample"]},
+        "cpu_baseline": cb,
+        "e2e": {"value": val, "unit": "G semiring-ops/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def secondary(trop, torch, pk, reps=20):
+    """Other workloads of the path: permute / trace GB/s, einsum, spin glass."""
+    out = {}
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        s, e = ev(), ev()
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps / 1e3
+
+    for dt in ("f32", "i32"):
+        x, perm = synth.permute_inputs(dt)
+        xd = torch.from_numpy(x).cuda()
+        src = "abcdef"
+        spec = src + "->" + "".join(src[p] for p in perm)
+        y = torch.empty([16] * 6, dtype=xd.dtype, device="cuda")
+        t = timed(lambda: trop.permute_trace(xd, spec, out=y), reps)
+        gbs = 2 * x.nbytes / t / 1e9
+        out[f"permute_16^6_{dt}"] = {"spec": spec, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "us": t * 1e6}
+    tr = torch.from_numpy(synth.trace_inputs()).cuda()
+    yo = torch.empty((128, 64, 64), device="cuda")
+    t = timed(lambda: trop.permute_trace(tr, "iijk->ijk", out=yo), reps)
+    gbs = 2 * 128 * 64 * 64 * 4 / t / 1e9
+    out["trace_iijk->ijk"] = {"GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "us": t * 1e6}
+    A, B = synth.einsum_inputs()
+    Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    o = torch.empty((16, 512, 512), device="cuda")
+    oa = torch.empty((16, 512, 512), dtype=torch.int32, device="cuda")
+    t = timed(lambda: trop.einsum("zacd,zdce->zea", Ad, Bd, out=o, out_argmax=oa), 5)
+    ops = 16 * 512 * 512 * 1024
+    out["einsum_zacd,zdce->zea"] = {"ms": t * 1e3, "G semiring-ops/s": ops / t / 1e9}
+    return out
+
+
+def ising_run(trop, torch):
+    from einsum_device_side_gb300 import ising
+    jh, jv = synth.ising_couplings()
+    inputs, nodes, n_labels, need = ising.build_network(jh, jv)
+    dev_inputs = [torch.from_numpy(t).cuda() for t in inputs]
+    am = [None] * len(nodes)
+    for j in need:
+        am[j] = torch.empty([2] * len(nodes[j][4]), dtype=torch.int32, device="cuda")
+    out = torch.empty((), device="cuda")
+    trop.contract_tree(dev_inputs, nodes, "maxplus", out, am)     # warm-up (pool growth)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    s.record()
+    trop.contract_tree(dev_inputs, nodes, "maxplus", out, am)
+    assign = trop.tree_backtrack(dev_inputs, nodes, am, n_labels, 0)
+    e.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    w = float(out.item())
+    spins = ising.spins_from_assignment(assign.cpu().numpy(), 24, 24)
+    ok = ising.energy(jh, jv, spins) == -w
+    steps = sum(1 for j in need) - 1
+    bytes_moved = steps * (3 * 4 << 24)
+    gpu_s = s.elapsed_time(e) / 1e3
+    del am
+    return {"W": w, "E0": -w, "backtrack_energy_consistent": bool(ok), "gpu_ms": gpu_s * 1e3,
+            "host_wall_ms": wall * 1e3, "contracting_steps": steps, "nodes": len(nodes),
+            "GB/s_state_stream": bytes_moved / gpu_s / 1e9}
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import einsum_device_side_gb300 as trop
+
+    torch.cuda.set_device(local)
+    trop.init(local)
+    pk = peaks()
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    peak_ops = sms * 128 * pk["sm_max_mhz"] * 1e6 / 2
+
+    sets = []
+    for rot in range(N_SETS):
+        per = []
+        for sr in SEMIRINGS:
+            a, b = synth.gemm_batched_inputs(sr)
+            ad = torch.from_numpy(a).cuda()
+            bd = torch.from_numpy(b).cuda()
+            if rot:
+                # distinct copies so successive steps read cold data (same values)
+                ad, bd = ad.clone(), bd.clone()
+            per.append((sr, ad, bd))
+        sets.append(per)
+    outs = [(torch.empty((GEMM_B, GEMM_M, GEMM_N), device="cuda"),
+             torch.empty((GEMM_B, GEMM_M, GEMM_N), dtype=torch.int32, device="cuda")) for _ in SEMIRINGS]
+    stream = torch.cuda.current_stream()
+
+    def step(i, events=None):
+        for j, (sr, ad, bd) in enumerate(sets[i % N_SETS]):
+            if events is not None:
+                events[j][0].record(stream)
+            trop.gemm(ad, bd, sr, out=outs[j][0], out_argmax=outs[j][1])
+            if events is not None:
+                events[j][1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in SEMIRINGS]
+           for _ in range(args.steps)]
+    launches0 = trop.stats()["kernel_launches"]
+    with ClockSampler(local) as clk:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        m0 = clk.mark()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        m1 = clk.mark()
+        if world > 1:
+            dist.barrier()
+        time.sleep(0.05)
+        clocks = clk.summary(m0, max(m1, m0 + 1))
+    launches = trop.stats()["kernel_launches"] - launches0
+    region_s = t_start.elapsed_time(t_end) / 1e3
+    region_s = barrier_max(region_s, world)
+    per_launch = [evs[i][j][0].elapsed_time(evs[i][j][1]) / 1e3 for i in range(args.steps) for j in range(3)]
+    avg_launch = statistics.mean(per_launch)
+    value = world * args.steps * len(SEMIRINGS) * OPS_PER_GEMM / region_s / 1e9
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    h_in = [(torch.from_numpy(synth.gemm_batched_inputs(sr)[0]).pin_memory(),
+             torch.from_numpy(synth.gemm_batched_inputs(sr)[1]).pin_memory()) for sr in SEMIRINGS]
+    h_out = [(torch.empty((GEMM_B, GEMM_M, GEMM_N)).pin_memory(),
+              torch.empty((GEMM_B, GEMM_M, GEMM_N), dtype=torch.int32).pin_memory()) for _ in SEMIRINGS]
+    d_in = [(torch.empty_like(a, device="cuda"), torch.empty_like(b, device="cuda")) for a, b in h_in]
+
+    def e2e_step():
+        for j, sr in enumerate(SEMIRINGS):
+            d_in[j][0].copy_(h_in[j][0], non_blocking=True)
+            d_in[j][1].copy_(h_in[j][1], non_blocking=True)
+            trop.gemm(d_in[j][0], d_in[j][1], sr, out=outs[j][0], out_argmax=outs[j][1])
+            h_out[j][0].copy_(outs[j][0], non_blocking=True)
+            h_out[j][1].copy_(outs[j][1], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e.record()
+    torch.cuda.synchronize()
+    e2e_s = barrier_max(s.elapsed_time(e) / 1e3 / e2e_steps, world)
+    h2d = sum(a.numel() * 4 + b.numel() * 4 for a, b in h_in)
+    d2h = sum(c.numel() * 4 + i.numel() * 4 for c, i in h_out)
+
+    workloads = {}
+    if not args.no_secondary:
+        workloads = secondary(trop, torch, pk)
+        if not args.no_ising:
+            try:
+                workloads["ising_24x24"] = ising_run(trop, torch)
+            except Exception as ex:  # report, do not hide
+                workloads["ising_24x24"] = {"error": repr(ex)}
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        cpu = cpu_sample_rate()
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "gemm_tiled_traffic.json")
+    if os.path.exists(tfile):
+        traffic = json.load(open(tfile)).get("bytes_per_launch")
+    achieved = OPS_PER_GEMM / avg_launch / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "G semiring-ops/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "strided-batched tropical GEMM + int32 argmax, batch 64 x M=N=K=256, "
+                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 launches",
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"{N_SETS} rotated input sets (288 MiB of operands) so each step reads cold inputs"},
+        "roofline": {"bound": "alu", "kernel": "k_gemm_tiled", "achieved": achieved, "peak": peak_ops / 1e9,
+                     "unit": "G semiring-ops/s", "frac": achieved / (peak_ops / 1e9), "traffic": traffic,
+                     "peak_def": f"{sms} SMs x 128 FP32 lanes x {pk['sm_max_mhz']:.0f} MHz / 2 (add + max)",
+                     "launch_us": avg_launch * 1e6},
+        "e2e": {"value": world * len(SEMIRINGS) * OPS_PER_GEMM / e2e_s / 1e9, "unit": "G semiring-ops/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "workloads": workloads,
+        "peaks_source": pk["source"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-ising", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -146,6 +146,9 @@ def _spec_shape(spec: str, shapes):
     for op, shp in zip(lhs.split(","), shapes):
         for ch, s in zip(op, shp):
             sizes.setdefault(ch, s)
+    missing = [ch for ch in out if ch not in sizes]
+    if missing:
+        raise TropicalError(-6, f"output label(s) {''.join(missing)} appear in no operand of '{spec}'")
     return [sizes[ch] for ch in out]
 
 

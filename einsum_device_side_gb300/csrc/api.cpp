@@ -581,6 +581,22 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         bool inGm = std::find(Gm.begin(), Gm.end(), l) != Gm.end();
         bool inGn = std::find(Gn.begin(), Gn.end(), l) != Gn.end();
         if (inGm || inGn || osize[i] == 1) continue;
+        // merge with the previous batch axis when every tensor's strides chain
+        if (g.nb > 0) {
+            int q = g.nb - 1;
+            int a = find_label(A, l), b = find_label(B, l), o = inO(l);
+            int64_t sz = a >= 0 ? A.size[a] : B.size[b];
+            int64_t sa = a >= 0 ? A.stride[a] : 0, sb = b >= 0 ? B.stride[b] : 0;
+            if (g.sAb[q] == sa * sz && g.sBb[q] == sb * sz && g.sCb[q] == ostride[o] * sz &&
+                g.sIb[q] == astride[o] * sz) {
+                g.bsize[q] *= sz;
+                g.sAb[q] = sa;
+                g.sBb[q] = sb;
+                g.sCb[q] = ostride[o];
+                g.sIb[q] = astride[o];
+                continue;
+            }
+        }
         TROP_TRY(add_batch(l));
     }
     if (text) {

@@ -91,7 +91,12 @@ __device__ __forceinline__ void batch_offsets(const Batch& bt, uint32_t b, int64
 // ------------------------------------------------------------------ tiled kernel
 constexpr int BM = 64, BN = 64, BK = 16, TM = 8, TN = 8;
 constexpr int TTHREADS = (BM / TM) * (BN / TN);  // 64
-constexpr int APAD = 2;                          // float2 pad per A row (keeps 16-byte alignment)
+constexpr int APAD = 4;                          // float pad per transposed A row (keeps 16-byte rows)
+#ifndef TROP_ARG_CHUNK
+#define TROP_ARG_CHUNK 8
+#endif
+constexpr int CH = TROP_ARG_CHUNK;               // k per argmax chunk (divides BK)
+static_assert(BK % CH == 0 && CH % 2 == 0, "chunk must divide the k-tile and hold whole k pairs");
 
 struct TiledParams {
     int M, N, K;
@@ -103,20 +108,37 @@ struct TiledParams {
     uint32_t nbatch;
     Batch bt;
     int vecA, vecB;  // 16-byte loads allowed (alignment of every row start)
+    int vecC, vecI;  // 16-byte stores allowed (unit column stride, aligned rows)
 };
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes)
+{
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::); }
+
+// rows / columns of the 8x8 outputs a thread owns: two groups of 4, half a tile apart
+__device__ __forceinline__ int row_of(int tm, int i) { return i < 4 ? tm * 4 + i : BM / 2 + tm * 4 + (i - 4); }
+__device__ __forceinline__ int col_of(int tn, int j) { return j < 4 ? tn * 4 + j : BN / 2 + tn * 4 + (j - 4); }
+
+// ARG: besides C, writes into I the chunk (+1) that holds each output's first
+// maximum, or 0 when no product beat the semiring zero; k_argmax_resolve then
+// replaces the chunk by the exact index.
 template <int SR, bool ARG>
 __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 {
     using O = Ops<SR>;
-    __shared__ __align__(16) float2 As[2][BK][BM + APAD];
+    __shared__ __align__(16) float As[2][BK][BM + APAD];  // A transposed: As[k][m]
     __shared__ __align__(16) float Bs[2][BK][BN];
-    __shared__ int32_t sid[ARG ? TM * TN : 1][ARG ? TTHREADS : 1];
+    __shared__ uint16_t sid[ARG ? TM * TN : 1][ARG ? TTHREADS : 1];
 
     const int tid = threadIdx.x;
     const int tm = tid / (BN / TN), tn = tid % (BN / TN);
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
     const int nkt = (p.K + BK - 1) / BK;
+    const float zero = O::zero();
 
     for (uint32_t b = blockIdx.z; b < p.nbatch; b += gridDim.z) {
         int64_t oa, ob, oc, oi;
@@ -128,8 +150,8 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
         const int la_m = tid / 4, la_k = (tid % 4) * 4;
         const int lb_k = tid / 16, lb_n = (tid % 16) * 4;
 
-        float4 ra[4], rb[4];
-        auto load_tile = [&](int kt) {
+        float4 ra[4];
+        auto load_a = [&](int kt) {
             const int k0 = kt * BK;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -140,35 +162,40 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
                 } else {
                     float v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = (m < p.M && k + q < p.K) ? __ldg(src + q) : O::zero();
+                    for (int q = 0; q < 4; ++q) v[q] = (m < p.M && k + q < p.K) ? __ldg(src + q) : zero;
                     ra[r] = make_float4(v[0], v[1], v[2], v[3]);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int k = k0 + lb_k + 4 * r, n = n0 + lb_n;
-                const float* src = B + (int64_t)k * p.sBk + n;
-                if (k < p.K && n + 3 < p.N && p.vecB) {
-                    rb[r] = __ldg(reinterpret_cast<const float4*>(src));
-                } else {
-                    float v[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = (k < p.K && n + q < p.N) ? __ldg(src + q) : O::bpad();
-                    rb[r] = make_float4(v[0], v[1], v[2], v[3]);
-                }
-            }
         };
-        auto store_tile = [&](int buf) {
+        auto store_a = [&](int buf) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int m = la_m + 16 * r;
-                As[buf][la_k + 0][m] = make_float2(ra[r].x, ra[r].x);
-                As[buf][la_k + 1][m] = make_float2(ra[r].y, ra[r].y);
-                As[buf][la_k + 2][m] = make_float2(ra[r].z, ra[r].z);
-                As[buf][la_k + 3][m] = make_float2(ra[r].w, ra[r].w);
+                As[buf][la_k + 0][m] = ra[r].x;
+                As[buf][la_k + 1][m] = ra[r].y;
+                As[buf][la_k + 2][m] = ra[r].z;
+                As[buf][la_k + 3][m] = ra[r].w;
             }
+        };
+        // B rows of a k-tile: cp.async with zero fill outside [0,K) x [0,N) (the K-tail pad of B is 0,
+        // and zero (x) 0 is the semiring zero, so padded products never win)
+        auto issue_b = [&](int kt, int buf) {
+            const int k0 = kt * BK;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) *reinterpret_cast<float4*>(&Bs[buf][lb_k + 4 * r][lb_n]) = rb[r];
+            for (int r = 0; r < 4; ++r) {
+                const int kk = lb_k + 4 * r, k = k0 + kk, n = n0 + lb_n;
+                float* dst = &Bs[buf][kk][lb_n];
+                if (p.vecB) {
+                    const int valid = (k < p.K) ? max(0, min(4, p.N - n)) : 0;
+                    const float* src = valid ? B + (int64_t)k * p.sBk + n : B;
+                    cp_async16(dst, src, valid * 4);
+                } else {
+                    const float* src = B + (int64_t)k * p.sBk + n;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = (k < p.K && n + q < p.N) ? __ldg(src + q) : 0.0f;
+                }
+            }
+            cp_async_commit();
         };
 
         float best[TM][TN];
@@ -176,113 +203,304 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) best[i][j] = O::zero();
-        if (ARG) {
-#pragma unroll
-            for (int q = 0; q < TM * TN; ++q) sid[q][tid] = 0;
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) snap[ARG ? i : 0][ARG ? j : 0] = O::zero();
-        }
+            for (int j = 0; j < TN; ++j) {
+                best[i][j] = zero;
+                if (ARG) snap[ARG ? i : 0][ARG ? j : 0] = zero;
+            }
 
-        load_tile(0);
-        store_tile(0);
+        issue_b(0, 0);
+        load_a(0);
+        store_a(0);
+        cp_async_wait_all();
         __syncthreads();
         for (int kt = 0; kt < nkt; ++kt) {
             const int buf = kt & 1;
-            if (kt + 1 < nkt) load_tile(kt + 1);
+            if (kt + 1 < nkt) {
+                issue_b(kt + 1, buf ^ 1);
+                load_a(kt + 1);
+            }
 #pragma unroll
             for (int kk = 0; kk < BK; kk += 2) {
-                float2 a0[TM], a1[TM];
-                float2 b0[TN / 2], b1[TN / 2];
+                float a0[TM], a1[TM], b0[TN], b1[TN];
                 {
-                    const float4* pa0 = reinterpret_cast<const float4*>(&As[buf][kk][tm * 4]);
-                    const float4* pa0h = reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + tm * 4]);
-                    const float4* pa1 = reinterpret_cast<const float4*>(&As[buf][kk + 1][tm * 4]);
-                    const float4* pa1h = reinterpret_cast<const float4*>(&As[buf][kk + 1][BM / 2 + tm * 4]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float4 x = pa0[h], y = pa0h[h], z = pa1[h], w = pa1h[h];
-                        a0[2 * h] = make_float2(x.x, x.y);
-                        a0[2 * h + 1] = make_float2(x.z, x.w);
-                        a0[4 + 2 * h] = make_float2(y.x, y.y);
-                        a0[4 + 2 * h + 1] = make_float2(y.z, y.w);
-                        a1[2 * h] = make_float2(z.x, z.y);
-                        a1[2 * h + 1] = make_float2(z.z, z.w);
-                        a1[4 + 2 * h] = make_float2(w.x, w.y);
-                        a1[4 + 2 * h + 1] = make_float2(w.z, w.w);
-                    }
-                    float4 u = *reinterpret_cast<const float4*>(&Bs[buf][kk][tn * 4]);
-                    float4 v = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tn * 4]);
-                    float4 s = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][tn * 4]);
-                    float4 t = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][BN / 2 + tn * 4]);
-                    b0[0] = make_float2(u.x, u.y);
-                    b0[1] = make_float2(u.z, u.w);
-                    b0[2] = make_float2(v.x, v.y);
-                    b0[3] = make_float2(v.z, v.w);
-                    b1[0] = make_float2(s.x, s.y);
-                    b1[1] = make_float2(s.z, s.w);
-                    b1[2] = make_float2(t.x, t.y);
-                    b1[3] = make_float2(t.z, t.w);
+                    const float4 x = *reinterpret_cast<const float4*>(&As[buf][kk][tm * 4]);
+                    const float4 y = *reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + tm * 4]);
+                    const float4 x1 = *reinterpret_cast<const float4*>(&As[buf][kk + 1][tm * 4]);
+                    const float4 y1 = *reinterpret_cast<const float4*>(&As[buf][kk + 1][BM / 2 + tm * 4]);
+                    const float4 u = *reinterpret_cast<const float4*>(&Bs[buf][kk][tn * 4]);
+                    const float4 v = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tn * 4]);
+                    const float4 u1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][tn * 4]);
+                    const float4 v1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][BN / 2 + tn * 4]);
+                    a0[0] = x.x; a0[1] = x.y; a0[2] = x.z; a0[3] = x.w;
+                    a0[4] = y.x; a0[5] = y.y; a0[6] = y.z; a0[7] = y.w;
+                    a1[0] = x1.x; a1[1] = x1.y; a1[2] = x1.z; a1[3] = x1.w;
+                    a1[4] = y1.x; a1[5] = y1.y; a1[6] = y1.z; a1[7] = y1.w;
+                    b0[0] = u.x; b0[1] = u.y; b0[2] = u.z; b0[3] = u.w;
+                    b0[4] = v.x; b0[5] = v.y; b0[6] = v.z; b0[7] = v.w;
+                    b1[0] = u1.x; b1[1] = u1.y; b1[2] = u1.z; b1[3] = u1.w;
+                    b1[4] = v1.x; b1[5] = v1.y; b1[6] = v1.z; b1[7] = v1.w;
                 }
 #pragma unroll
                 for (int i = 0; i < TM; ++i)
 #pragma unroll
-                    for (int jp = 0; jp < TN / 2; ++jp) {
-                        float2 t0 = O::mul2(a0[i], b0[jp]);
-                        float2 t1 = O::mul2(a1[i], b1[jp]);
-                        best[i][2 * jp] = O::fold3(best[i][2 * jp], t0.x, t1.x);
-                        best[i][2 * jp + 1] = O::fold3(best[i][2 * jp + 1], t0.y, t1.y);
+                    for (int j = 0; j < TN; j += 2) {
+                        const float2 t0 = O::mul2(make_float2(a0[i], a0[i]), make_float2(b0[j], b0[j + 1]));
+                        const float2 t1 = O::mul2(make_float2(a1[i], a1[i]), make_float2(b1[j], b1[j + 1]));
+                        best[i][j] = O::fold3(best[i][j], t0.x, t1.x);
+                        best[i][j + 1] = O::fold3(best[i][j + 1], t0.y, t1.y);
                     }
-            }
-            if (ARG) {
+                if (ARG && (kk + 2) % CH == 0) {
+                    // end of a chunk: a strict improvement over the chunk-start value marks it
+                    const uint16_t chunk = (uint16_t)((kt * BK + kk + 2) / CH - 1);
 #pragma unroll
-                for (int i = 0; i < TM; ++i)
+                    for (int i = 0; i < TM; ++i)
 #pragma unroll
-                    for (int j = 0; j < TN; ++j) {
-                        if (O::better(best[i][j], snap[ARG ? i : 0][ARG ? j : 0])) sid[i * TN + j][tid] = kt;
-                        snap[ARG ? i : 0][ARG ? j : 0] = best[i][j];
-                    }
+                        for (int j = 0; j < TN; ++j) {
+                            float& s = snap[ARG ? i : 0][ARG ? j : 0];
+                            if (O::better(best[i][j], s)) sid[i * TN + j][tid] = chunk;
+                            s = best[i][j];
+                        }
+                }
             }
-            if (kt + 1 < nkt) {
-                __syncthreads();
-                store_tile(buf ^ 1);
-                __syncthreads();
-            }
+            if (kt + 1 < nkt) store_a(buf ^ 1);
+            cp_async_wait_all();
+            __syncthreads();
         }
 
-        // ---------------- epilogue: resolve argmax inside the winning chunk, store
-        const float zero = O::zero();
+        // ---------------- store values (and chunk + 1) through the output strides
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
-            const int m = m0 + (i < 4 ? tm * 4 + i : BM / 2 + tm * 4 + (i - 4));
+            const int m = m0 + row_of(tm, i);
             if (m >= p.M) continue;
             float* crow = p.C + oc + (int64_t)m * p.sCm;
             int32_t* irow = ARG ? p.I + oi + (int64_t)m * p.sIm : nullptr;
+            int32_t code[TN];
+            if (ARG) {
 #pragma unroll
-            for (int j = 0; j < TN; ++j) {
-                const int n = n0 + (j < 4 ? tn * 4 + j : BN / 2 + tn * 4 + (j - 4));
-                if (n >= p.N) continue;
-                const float v = best[i][j];
-                crow[(int64_t)n * p.sCn] = v;
-                if (ARG) {
-                    int32_t idx = 0;
-                    if (v != zero) {
-                        const int k0 = sid[i * TN + j][tid] * BK;
-                        const int k1 = min(k0 + BK, p.K);
-                        const float* arow = A + (int64_t)m * p.sAm;
-                        const float* bcol = B + n;
-                        idx = k0;
-                        for (int k = k0; k < k1; ++k) {
-                            if (O::mul(__ldg(arow + k), __ldg(bcol + (int64_t)k * p.sBk)) == v) {
-                                idx = k;
-                                break;
-                            }
-                        }
-                    }
-                    irow[(int64_t)n * p.sIn] = idx;
+                for (int j = 0; j < TN; ++j) code[j] = best[i][j] != zero ? (int32_t)sid[i * TN + j][tid] + 1 : 0;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = n0 + (h ? BN / 2 : 0) + tn * 4;
+                if (p.vecC && n + 3 < p.N) {
+                    *reinterpret_cast<float4*>(crow + n) =
+                        make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (n + q < p.N) crow[(int64_t)(n + q) * p.sCn] = best[i][4 * h + q];
                 }
+                if (ARG) {
+                    if (p.vecI && n + 3 < p.N) {
+                        *reinterpret_cast<int4*>(irow + n) =
+                            make_int4(code[4 * h], code[4 * h + 1], code[4 * h + 2], code[4 * h + 3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (n + q < p.N) irow[(int64_t)(n + q) * p.sIn] = code[4 * h + q];
+                    }
+                }
+            }
+        }
+        // no barrier needed: the next batch iteration starts by writing stage 0, which every
+        // thread finished reading before the last loop barrier
+    }
+}
+
+// ------------------------------------------------------------------ argmax resolve
+// One CTA per 64x64 output tile.  The tile's values and chunk codes are loaded
+// into shared memory once; then, for every group of RG consecutive chunks that
+// holds a winner, the A rows and B columns of that group are staged into
+// shared memory and each winner's 16 products are recomputed to find the
+// first one equal to the value.  Every access after the two tile loads is to
+// shared memory.
+#ifndef TROP_RESOLVE_GK
+#define TROP_RESOLVE_GK 128
+#endif
+constexpr int RTHREADS = 256, RGK = TROP_RESOLVE_GK, RG = RGK / CH;  // k per staged group
+constexpr int RMAXG = 1024;                            // groups tracked by the bit set (K <= 65536)
+
+struct ResolveSmem {
+    float Ct[BM][BN + 1];
+    int32_t It[BM][BN + 1];
+    float EA[BM][RGK + 4];
+    float EB[RGK][BN];
+    uint16_t lst[BM * BN];
+    uint32_t gbits[RMAXG / 32];
+    int nlist;
+};
+constexpr size_t SMEM_RESOLVE = sizeof(ResolveSmem);
+
+template <int SR>
+__global__ void __launch_bounds__(RTHREADS) k_argmax_resolve(TiledParams p)
+{
+    using O = Ops<SR>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ResolveSmem& S = *reinterpret_cast<ResolveSmem*>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int nch = (p.K + CH - 1) / CH;
+    const int ngr = (nch + RG - 1) / RG;
+    // my 16 tile entries: rows (tid/16) + 16*r, columns (tid%16)*4 + j; entry q = 4r + j.
+    // Consecutive lanes cover consecutive columns, so every tile load/store is coalesced.
+    const int rr = tid / 16, cc = (tid % 16) * 4;
+    for (uint32_t b = blockIdx.z; b < p.nbatch; b += gridDim.z) {
+        int64_t oa, ob, oc, oi;
+        batch_offsets(p.bt, b, oa, ob, oc, oi);
+        const float* __restrict__ A = p.A + oa;
+        const float* __restrict__ B = p.B + ob;
+        if (tid < RMAXG / 32) S.gbits[tid] = 0;
+        int code[16];
+        uint64_t gm = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = rr + 16 * r, m = m0 + row;
+            const float* crow = p.C + oc + (int64_t)m * p.sCm;
+            const int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+            const int n = n0 + cc;
+            float cv[4];
+            int iv[4];
+            if (m < p.M && n + 3 < p.N && p.vecC && p.vecI) {
+                const float4 c4 = *reinterpret_cast<const float4*>(crow + n);
+                const int4 i4 = *reinterpret_cast<const int4*>(irow + n);
+                cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
+                iv[0] = i4.x; iv[1] = i4.y; iv[2] = i4.z; iv[3] = i4.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = m < p.M && n + j < p.N;
+                    cv[j] = in ? crow[(int64_t)(n + j) * p.sCn] : 0.0f;
+                    iv[j] = in ? irow[(int64_t)(n + j) * p.sIn] : 0;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                code[4 * r + j] = iv[j];
+                S.Ct[row][cc + j] = cv[j];
+                S.It[row][cc + j] = iv[j];
+                if (iv[j] > 0) {
+                    const int g = (iv[j] - 1) / RG;
+                    if (ngr <= 64) gm |= 1ull << g;
+                }
+            }
+        }
+        __syncthreads();  // gbits cleared before anyone sets a bit
+        if (ngr <= 64) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) gm |= __shfl_xor_sync(0xffffffffu, gm, o);
+            if (lane == 0 && gm) {
+                atomicOr(&S.gbits[0], (uint32_t)gm);
+                atomicOr(&S.gbits[1], (uint32_t)(gm >> 32));
+            }
+        } else if (ngr <= RMAXG) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (code[q] > 0) {
+                    const int g = (code[q] - 1) / RG;
+                    atomicOr(&S.gbits[g >> 5], 1u << (g & 31));
+                }
+        }
+        __syncthreads();
+        if (ngr <= RMAXG) {
+            for (int g = 0; g < ngr; ++g) {
+                if (!((S.gbits[g >> 5] >> (g & 31)) & 1u)) continue;
+                const int k0 = g * RGK;
+                if (tid == 0) S.nlist = 0;
+                // stage A rows (64 x 64 k) and B rows (64 k x 64 n), zero outside the operands
+                for (int e = tid; e < BM * RGK / 4; e += RTHREADS) {
+                    const int m = e / (RGK / 4), kq = (e % (RGK / 4)) * 4, gmr = m0 + m, gk = k0 + kq;
+                    float* dst = &S.EA[m][kq];
+                    if (p.vecA) {
+                        const int valid = gmr < p.M ? max(0, min(4, p.K - gk)) : 0;
+                        cp_async16(dst, valid ? A + (int64_t)gmr * p.sAm + gk : A, valid * 4);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = (gmr < p.M && gk + q < p.K) ? __ldg(A + (int64_t)gmr * p.sAm + gk + q) : 0.0f;
+                    }
+                }
+                for (int e = tid; e < RGK * BN / 4; e += RTHREADS) {
+                    const int kk = e / (BN / 4), nq = (e % (BN / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
+                    float* dst = &S.EB[kk][nq];
+                    if (p.vecB) {
+                        const int valid = gk < p.K ? max(0, min(4, p.N - gn)) : 0;
+                        cp_async16(dst, valid ? B + (int64_t)gk * p.sBk + gn : B, valid * 4);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = (gk < p.K && gn + q < p.N) ? __ldg(B + (int64_t)gk * p.sBk + gn + q) : 0.0f;
+                    }
+                }
+                cp_async_commit();
+                __syncthreads();  // nlist reset visible
+                // compact this group's winners (codes kept in registers: shared ones get overwritten)
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const bool mine = code[q] > 0 && (code[q] - 1) / RG == g;
+                    const unsigned bal = __ballot_sync(0xffffffffu, mine);
+                    int base = 0;
+                    if (lane == 0 && bal) base = atomicAdd(&S.nlist, __popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (mine)
+                        S.lst[base + __popc(bal & ((1u << lane) - 1u))] =
+                            (uint16_t)((rr + 16 * (q / 4)) * BN + cc + (q % 4));
+                }
+                cp_async_wait_all();
+                __syncthreads();
+                const int cnt = S.nlist;
+                for (int e = tid; e < cnt; e += RTHREADS) {
+                    const int pk = S.lst[e], r = pk / BN, c = pk % BN;
+                    const int chunk = S.It[r][c] - 1;
+                    const float target = S.Ct[r][c];
+                    const int kl = (chunk - g * RG) * CH;
+                    const int kmax = min(CH, p.K - chunk * CH);
+                    float av[CH];
+#pragma unroll
+                    for (int kk = 0; kk < CH; kk += 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(&S.EA[r][kl + kk]);
+                        av[kk] = x.x;
+                        av[kk + 1] = x.y;
+                        av[kk + 2] = x.z;
+                        av[kk + 3] = x.w;
+                    }
+                    int idx = 0;
+#pragma unroll
+                    for (int kk = CH - 1; kk >= 0; --kk)
+                        if (kk < kmax && O::mul(av[kk], S.EB[kl + kk][c]) == target) idx = kk;
+                    S.It[r][c] = chunk * CH + idx;
+                }
+                __syncthreads();
+            }
+        } else {
+            // very long contractions: search each winning chunk in global memory
+#pragma unroll 1
+            for (int q = 0; q < 16; ++q) {
+                const int r = rr + 16 * (q / 4), c = cc + (q % 4), m = m0 + r;
+                const int cd = S.It[r][c];
+                if (cd <= 0) continue;
+                const int chunk = cd - 1, k0 = chunk * CH, k1 = min(k0 + CH, p.K);
+                const float* arow = A + (int64_t)m * p.sAm;
+                const float* bcol = B + n0 + c;
+                const float target = S.Ct[r][c];
+                int idx = k0;
+                for (int k = k1 - 1; k >= k0; --k)
+                    if (O::mul(__ldg(arow + k), __ldg(bcol + (int64_t)k * p.sBk)) == target) idx = k;
+                S.It[r][c] = idx;
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = rr + 16 * r, m = m0 + row, n = n0 + cc;
+            if (m >= p.M) continue;
+            int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+            if (n + 3 < p.N && p.vecI) {
+                *reinterpret_cast<int4*>(irow + n) =
+                    make_int4(S.It[row][cc], S.It[row][cc + 1], S.It[row][cc + 2], S.It[row][cc + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (n + j < p.N) irow[(int64_t)(n + j) * p.sIn] = S.It[row][cc + j];
             }
         }
         __syncthreads();
@@ -472,16 +690,27 @@ int run_tiled(const GemmDesc& g, cudaStream_t s)
     p.nbatch = (uint32_t)nbatch;
     bool va = ((uintptr_t)g.A % 16) == 0 && g.sAm % 4 == 0;
     bool vb = ((uintptr_t)g.B % 16) == 0 && g.sBk % 4 == 0;
+    bool vc = ((uintptr_t)g.C % 16) == 0 && g.sCm % 4 == 0 && g.sCn == 1;
+    bool vi = ARG && ((uintptr_t)g.I % 16) == 0 && g.sIm % 4 == 0 && g.sIn == 1;
     for (int d = 0; d < p.bt.nb; ++d) {
         va = va && p.bt.sA[d] % 4 == 0;
         vb = vb && p.bt.sB[d] % 4 == 0;
+        vc = vc && p.bt.sC[d] % 4 == 0;
+        vi = vi && p.bt.sI[d] % 4 == 0;
     }
     p.vecA = va;
     p.vecB = vb;
+    p.vecC = vc;
+    p.vecI = vi;
     dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM),
               (unsigned)(nbatch < 65535 ? nbatch : 65535));
     k_gemm_tiled<SR, ARG><<<grid, TTHREADS, 0, s>>>(p);
-    return check_launch("k_gemm_tiled");
+    TROP_TRY(check_launch("k_gemm_tiled"));
+    if (ARG) {
+        k_argmax_resolve<SR><<<grid, RTHREADS, SMEM_RESOLVE, s>>>(p);
+        TROP_TRY(check_launch("k_argmax_resolve"));
+    }
+    return TROP_OK;
 }
 
 template <int SR, bool ARG>
@@ -590,17 +819,20 @@ Route choose(const GemmDesc& g, bool& swap)
     int64_t nbatch = 1;
     for (int d = 0; d < g.nb; ++d) nbatch *= g.bsize[d];
     const bool fits32 = g.M < (1 << 30) && g.N < (1 << 30) && g.K < (1 << 30) && nbatch < (int64_t(1) << 31);
-    const bool big = g.M >= 16 && g.N >= 16 && g.K >= 8;
+    // the argmax epilogue keeps chunk numbers in 16 bits
+    const bool big = g.M >= 16 && g.N >= 16 && g.K >= 8 && (!g.I || g.K <= (int64_t)CH * 65535);
+    const bool grid_ok = (g.M + BM - 1) / BM <= 65535 && (g.N + BN - 1) / BN <= 65535;
+    const bool grid_ok_t = (g.N + BM - 1) / BM <= 65535 && (g.M + BN - 1) / BN <= 65535;
     if (fits32 && big) {
-        if (g.sAk == 1 && g.sBn == 1) return R_TILED;
-        if (g.sBk == 1 && g.sAm == 1) {
+        if (g.sAk == 1 && g.sBn == 1 && grid_ok) return R_TILED;
+        if (g.sBk == 1 && g.sAm == 1 && grid_ok_t) {
             swap = true;
             return R_TILED;
         }
     }
     if (fits32 && g.K <= 64) {
-        if (g.M <= MAXM_STREAM && nbatch * ((g.N + 3) / 4) < (int64_t(1) << 31) && g.M <= g.N) return R_STREAM;
-        if (g.N <= MAXM_STREAM && nbatch * ((g.M + 3) / 4) < (int64_t(1) << 31)) {
+        if (g.M <= MAXM_STREAM && nbatch * g.N < (int64_t(1) << 31) && g.M <= g.N) return R_STREAM;
+        if (g.N <= MAXM_STREAM && nbatch * g.M < (int64_t(1) << 31)) {
             swap = true;
             return R_STREAM;
         }
@@ -648,6 +880,14 @@ int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name)
 int register_gemm_kernels()
 {
     cudaFuncAttributes a;
+    {
+        const void* kr[] = {(const void*)k_argmax_resolve<TROP_MAXPLUS>, (const void*)k_argmax_resolve<TROP_MINPLUS>,
+                            (const void*)k_argmax_resolve<TROP_MAXTIMES>};
+        for (const void* k : kr) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_RESOLVE);
+            if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (argmax resolve smem)");
+        }
+    }
     const void* ks[] = {
         (const void*)k_gemm_tiled<TROP_MAXPLUS, true>,  (const void*)k_gemm_tiled<TROP_MINPLUS, true>,
         (const void*)k_gemm_tiled<TROP_MAXTIMES, true>, (const void*)k_gemm_tiled<TROP_MAXPLUS, false>,

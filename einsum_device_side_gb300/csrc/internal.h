@@ -11,7 +11,7 @@
 namespace trop {
 
 constexpr int MAXR = TROP_MAX_RANK;
-constexpr int MAXB = 12;  // batch dims a GEMM launch can carry
+constexpr int MAXB = 16;  // batch dims a GEMM launch can carry (after merging)
 
 // ---------------------------------------------------------------- errors
 int set_error(int code, const char* fmt, ...);

@@ -1,0 +1,141 @@
+"""GPU parity: strided-batched tropical GEMM with argmax vs the CPU oracle.
+
+Values and argmax must be bit-identical (every tropical product rounds once,
+max/min are exact, ties go to the smallest k).  Calls go through the C ABI
+(tropical_gemm_strided_batched_argmax) via the ctypes binding.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+SR = (0, 1, 2)
+
+
+@pytest.fixture(scope="module")
+def trop():
+    import einsum_device_side_gb300 as t
+    t.load()
+    return t
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _check(trop, a, b, sr, a_dev=None, b_dev=None):
+    a_dev = _dev(a) if a_dev is None else a_dev
+    b_dev = _dev(b) if b_dev is None else b_dev
+    c, i = trop.gemm(a_dev, b_dev, sr)
+    rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+    c, i = c.cpu().numpy(), i.cpu().numpy()
+    assert c.tobytes() == rc.tobytes(), f"values differ at {np.argwhere(c != rc)[:5]}"
+    np.testing.assert_array_equal(i, ri)
+
+
+@pytest.mark.parametrize("sr", SR)
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 64, 64, 64), (3, 70, 45, 37), (2, 130, 129, 70),
+                                   (1, 200, 65, 257), (4, 17, 300, 16), (2, 5, 7, 3), (1, 64, 64, 1)])
+def test_gemm_matches_oracle(trop, sr, shape):
+    bt, m, n, k = shape
+    a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+    _check(trop, a, b, sr)
+
+
+@pytest.mark.parametrize("sr", SR)
+def test_gemm_integer_ties(trop, sr):
+    # small integers force ties between different k: argmax must pick the first
+    a = synth.uniform_int(11, (2, 96, 80), -3, 3).astype(np.float32)
+    b = synth.uniform_int(12, (2, 80, 72), -3, 3).astype(np.float32)
+    if sr == 2:
+        a, b = np.abs(a), np.abs(b)
+    _check(trop, a, b, sr)
+
+
+def test_gemm64_workload_and_transpose_pair(trop):
+    a, b = synth.gemm64_inputs()
+    c, i = trop.gemm(_dev(a), _dev(b), 0)
+    rc, ri = oracle.gemm(a, b, 0)
+    np.testing.assert_array_equal(c.cpu().numpy(), rc)
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
+    ct, it = trop.permute_pair(c[0], i[0], "ij->ji")
+    np.testing.assert_array_equal(ct.cpu().numpy(), rc[0].T)
+    np.testing.assert_array_equal(it.cpu().numpy(), ri[0].T)
+
+
+@pytest.mark.parametrize("layout", ["NT", "TN", "TT"])
+def test_gemm_transposed_layouts(trop, layout):
+    a, b = synth.gemm_batched_inputs(0, batch=2, m=96, n=80, k=50)
+    ad, bd = _dev(a), _dev(b)
+    if layout[0] == "T":
+        ad = _dev(np.ascontiguousarray(np.swapaxes(a, 1, 2))).transpose(1, 2)
+    if layout[1] == "T":
+        bd = _dev(np.ascontiguousarray(np.swapaxes(b, 1, 2))).transpose(1, 2)
+    _check(trop, a, b, 0, ad, bd)
+
+
+def test_gemm_broadcast_batch_and_strided_output(trop):
+    a, b = synth.gemm_batched_inputs(1, batch=3, m=40, n=33, k=21)
+    b1 = b[:1]
+    bd = _dev(b1).expand(3, 21, 33)
+    out = torch.empty((3, 33, 40), dtype=torch.float32, device="cuda").transpose(1, 2)
+    am = torch.empty((3, 33, 40), dtype=torch.int32, device="cuda").transpose(1, 2)
+    c, i = trop.gemm(_dev(a), bd, 1, out=out, out_argmax=am)
+    rc, ri = oracle.gemm(a, np.broadcast_to(b1, (3, 21, 33)), 1)
+    np.testing.assert_array_equal(c.cpu().numpy(), rc)
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
+
+
+@pytest.mark.parametrize("sr", SR)
+def test_gemm_empty_contraction(trop, sr):
+    a = torch.empty((2, 5, 0), device="cuda")
+    b = torch.empty((2, 0, 7), device="cuda")
+    c, i = trop.gemm(a, b, sr)
+    zero = {0: -np.inf, 1: np.inf, 2: 0.0}[sr]
+    assert (c.cpu().numpy() == np.float32(zero)).all() and (i.cpu().numpy() == 0).all()
+    c, i = trop.gemm(torch.empty((2, 0, 3), device="cuda"), torch.empty((2, 3, 7), device="cuda"), sr)
+    assert c.shape == (2, 0, 7)
+
+
+def test_gemm_without_argmax_matches(trop):
+    a, b = synth.gemm_batched_inputs(0, batch=2, m=70, n=90, k=45)
+    c = trop.gemm(_dev(a), _dev(b), 0, argmax=False)
+    rc, _ = oracle.gemm(a, b, 0)
+    np.testing.assert_array_equal(c.cpu().numpy(), rc)
+
+
+def test_identity_and_infinities(trop):
+    rng = np.random.default_rng(3)
+    a = rng.integers(-5, 6, size=(1, 70, 66)).astype(np.float32)
+    eye = np.full((1, 66, 66), -np.inf, dtype=np.float32)
+    eye[0, np.arange(66), np.arange(66)] = 0
+    _check(trop, a, eye, 0)
+
+
+@pytest.mark.parametrize("sr", SR)
+def test_full_size_batched_workload_sampled(trop, sr):
+    """batch 64 x 256^3 exactly as benchmarked: sampled outputs vs the oracle,
+    and an every-output certificate (A[m,I] (x) B[I,n] == C)."""
+    a, b = synth.gemm_batched_inputs(sr)
+    ad, bd = _dev(a), _dev(b)
+    c, i = trop.gemm(ad, bd, sr)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(100 + sr)
+    samples = rng.choice(c.numel(), size=20000, replace=False).astype(np.int64)
+    samples[:3] = [0, c.numel() - 1, 12345]
+    rc, ri = oracle.gemm(a, b, sr, samples=samples, nthreads=0)
+    cf, if_ = c.reshape(-1).cpu().numpy(), i.reshape(-1).cpu().numpy()
+    np.testing.assert_array_equal(cf[samples], rc)
+    np.testing.assert_array_equal(if_[samples], ri)
+    # certificate on every output (torch float32 add/mul round once as well)
+    idx = i.long()
+    a_sel = torch.gather(ad, 2, idx)                                 # A[b, m, I[b,m,n]]
+    b_sel = torch.gather(bd, 1, idx)                                 # B[b, I[b,m,n], n]
+    t = a_sel * b_sel if sr == 2 else a_sel + b_sel
+    assert torch.equal(t, c)
+    assert (i >= 0).all() and (i < 256).all()
