@@ -83,6 +83,7 @@ def load(path: str | None = None):
         "tropical_init": (I, [I]),
         "tropical_permute_trace": (I, [TP, ctypes.c_char_p, I, TP, P, P]),
         "tropical_permute_pair": (I, [TP, TP, ctypes.c_char_p, TP, TP, P]),
+        "tropical_permute_trace_noalloc": (I, [TP, ctypes.c_char_p, I, TP, P, P]),
         "tropical_gemm_strided_batched_argmax": (I, [I, I, I64, I64, I64, I64, P, I64, I64, I64, P, I64, I64, I64,
                                                      P, I64, I64, I64, P, P]),
         "tropical_einsum_pairwise": (I, [ctypes.c_char_p, TP, TP, I, TP, P, P]),
@@ -168,6 +169,20 @@ def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Ten
     _check(lib.tropical_permute_trace(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
                                       am.data_ptr() if am is not None and am.numel() else None, _stream(stream)))
     return (out, am) if am is not None else out
+
+
+def permute_trace_noalloc(x: torch.Tensor, spec: str, semiring="maxplus", *, out: torch.Tensor,
+                          argmax: torch.Tensor | None = None, stream=None):
+    """Like permute_trace, but the library allocates nothing: for callers that
+    cannot let it allocate device memory.  ``out`` (and ``argmax``, if wanted)
+    must be given; split reductions use the library's fixed scratch, so calls
+    must not overlap on the GPU."""
+    lib = load()
+    dx, do = tensor_desc(x), tensor_desc(out)
+    _check(lib.tropical_permute_trace_noalloc(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
+                                              argmax.data_ptr() if argmax is not None and argmax.numel() else None,
+                                              _stream(stream)))
+    return (out, argmax) if argmax is not None else out
 
 
 def permute_pair(val: torch.Tensor, arg: torch.Tensor, spec: str, out_val=None, out_arg=None, stream=None):

@@ -92,6 +92,11 @@ struct ReduceDesc {
 };
 int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* argmax,
                   const ReduceDesc& d, cudaStream_t s);
+// The same reduction with its split partials in caller-provided scratch (no allocation).
+int launch_reduce_scratch(int semiring, int dtype, const void* in, void* out, int32_t* argmax,
+                          const ReduceDesc& d, void* scratch, size_t scratch_bytes, cudaStream_t s);
+// Fixed scratch of noalloc.cu: its device address on the current device (looked up once per device).
+int noalloc_scratch(void** ptr, size_t* bytes);
 
 // Strided-batched tropical GEMM with a multi-dimensional batch.
 struct GemmDesc {

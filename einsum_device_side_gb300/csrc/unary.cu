@@ -671,6 +671,85 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
     return rc;
 }
 
+// Same reduction as launch_reduce_typed, but the partial results of a split
+// reduction go to caller-provided scratch instead of pool workspace; fails
+// when they would not fit.  Nothing is allocated.
+template <int SR, typename T>
+int launch_reduce_scratch_typed(const void* in_, void* out_, int32_t* arg, const ReduceDesc& d, void* scratch,
+                                size_t scratch_bytes, cudaStream_t s, const DeviceInfo* dev)
+{
+    const T* in = static_cast<const T*>(in_);
+    T* out = static_cast<T*>(out_);
+    RedParams p{};
+    p.n_out = 1;
+    p.out_rank = 0;
+    for (int i = 0; i < d.out_rank; ++i) {
+        if (d.out_size[i] == 0) return TROP_OK;
+        if (d.out_size[i] == 1) continue;
+        int k = p.out_rank++;
+        p.out_size[k] = d.out_size[i];
+        p.out_s_in[k] = d.out_s_in[i];
+        p.out_s_out[k] = d.out_s_out[i];
+        p.out_s_arg[k] = d.out_s_arg[i];
+        p.n_out *= d.out_size[i];
+    }
+    p.R = 1;
+    p.red_rank = 0;
+    for (int i = 0; i < d.red_rank; ++i) {
+        p.R *= d.red_size[i];
+        if (d.red_size[i] == 1) continue;
+        int q = p.red_rank - 1;
+        if (q >= 0 && p.red_s_in[q] == d.red_s_in[i] * d.red_size[i]) {
+            p.red_size[q] *= d.red_size[i];
+            p.red_s_in[q] = d.red_s_in[i];
+            continue;
+        }
+        p.red_size[p.red_rank] = d.red_size[i];
+        p.red_s_in[p.red_rank] = d.red_s_in[i];
+        ++p.red_rank;
+    }
+    if (p.red_rank == 0) {
+        p.red_rank = 1;
+        p.red_size[0] = 1;
+        p.red_s_in[0] = 0;
+    }
+    const int64_t threads_wanted = (int64_t)dev->sm_count * 1024;
+    if (p.R <= 64 || p.n_out >= threads_wanted) {
+        int g = grid_for(p.n_out, NT, dev->sm_count);
+        k_reduce_thread<SR, T><<<g, NT, 0, s>>>(in, out, arg, p);
+        return check_launch("k_reduce_thread");
+    }
+    const int64_t blocks_wanted = (int64_t)dev->sm_count * 8;
+    int64_t nsplit = (blocks_wanted + p.n_out - 1) / p.n_out;
+    int64_t max_split = (p.R + 2047) / 2048;
+    if (nsplit > max_split) nsplit = max_split;
+    if (nsplit < 1) nsplit = 1;
+    p.nsplit = nsplit;
+    p.chunk = (p.R + nsplit - 1) / nsplit;
+    T* part_v = nullptr;
+    int64_t* part_i = nullptr;
+    if (nsplit > 1) {
+        const size_t nb = (size_t)(p.n_out * nsplit);
+        const size_t need = nb * (sizeof(T) + sizeof(int64_t));
+        if (!scratch || need > scratch_bytes)
+            return set_error(TROP_ERR_UNSUPPORTED,
+                             "reduction needs %zu bytes of scratch for %lld partial results; the fixed scratch "
+                             "holds %zu bytes",
+                             need, (long long)nb, scratch_bytes);
+        part_i = static_cast<int64_t*>(scratch);
+        part_v = reinterpret_cast<T*>(part_i + nb);
+    }
+    int g = grid_for(p.n_out * nsplit, 1, dev->sm_count, 16);
+    k_reduce_block<SR, T><<<g, NT, 0, s>>>(in, out, arg, part_v, part_i, p);
+    int rc = check_launch("k_reduce_block");
+    if (rc == TROP_OK && nsplit > 1) {
+        int g2 = grid_for(p.n_out, NT, dev->sm_count);
+        k_reduce_combine<SR, T><<<g2, NT, 0, s>>>(out, arg, part_v, part_i, p);
+        rc = check_launch("k_reduce_combine");
+    }
+    return rc;
+}
+
 }  // namespace
 
 int launch_gather(const void* in, void* out, int elem_bytes, const int32_t* in2, int32_t* out2,
@@ -701,6 +780,30 @@ int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* a
     default: break;
     }
 #undef TROP_RED
+    return set_error(TROP_ERR_DTYPE, "reduce: unsupported semiring %d / dtype %d", semiring, dtype);
+}
+
+int launch_reduce_scratch(int semiring, int dtype, const void* in, void* out, int32_t* argmax, const ReduceDesc& d,
+                          void* scratch, size_t scratch_bytes, cudaStream_t s)
+{
+    const DeviceInfo* dev = nullptr;
+    TROP_TRY(ensure_device(&dev));
+#define TROP_RED_S(SR)                                                                                          \
+    case SR:                                                                                                    \
+        if (dtype == TROP_F32)                                                                                  \
+            return launch_reduce_scratch_typed<SR, float>(in, out, argmax, d, scratch, scratch_bytes, s, dev);   \
+        if (dtype == TROP_I32)                                                                                  \
+            return launch_reduce_scratch_typed<SR, int32_t>(in, out, argmax, d, scratch, scratch_bytes, s, dev); \
+        if (dtype == TROP_I64)                                                                                  \
+            return launch_reduce_scratch_typed<SR, int64_t>(in, out, argmax, d, scratch, scratch_bytes, s, dev); \
+        break;
+    switch (semiring) {
+        TROP_RED_S(TROP_MAXPLUS)
+        TROP_RED_S(TROP_MINPLUS)
+        TROP_RED_S(TROP_MAXTIMES)
+    default: break;
+    }
+#undef TROP_RED_S
     return set_error(TROP_ERR_DTYPE, "reduce: unsupported semiring %d / dtype %d", semiring, dtype);
 }
 

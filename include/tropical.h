@@ -148,6 +148,25 @@ int tropical_init(int device);
 int tropical_permute_trace(const trop_tensor* in, const char* spec, int semiring,
                            const trop_tensor* out, int32_t* argmax, void* stream);
 
+/* Allocation-free variant of tropical_permute_trace (no counterpart on the
+ * pages this library follows; it exists for callers of this library that
+ * cannot allocate device memory: hosts that own every device allocation,
+ * loops that cannot absorb an allocation's implicit synchronisation, or
+ * processes whose device memory is already handed to their own allocator).
+ * Same arguments, results and errors as tropical_permute_trace.  A split
+ * reduction keeps its partial results in one fixed 256 KiB device array
+ * compiled into the library (resident on every GPU that loads it) instead of
+ * pool workspace; no call allocates or frees memory.  Requests whose
+ * partials need more than 256 KiB fail with TROP_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array: calls whose kernels overlap on
+ * the GPU (other streams, other host threads) race on it, so serialise them.
+ * Nothing in it needs to start at zero: each call writes every partial it
+ * reads. */
+int tropical_permute_trace_noalloc(const trop_tensor* in, const char* spec, int semiring,
+                                   const trop_tensor* out, int32_t* argmax, void* stream);
+
 /* Output permute of a result and its argmax through ONE index mapping
  * [I52 "Resolved design for step 3": the float result and the argmax must be
  * permuted with bit-for-bit identical index mappings].  spec is a pure
