@@ -308,202 +308,133 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 }
 
 // ------------------------------------------------------------------ argmax resolve
-// One CTA per 64x64 output tile.  The tile's values and chunk codes are loaded
-// into shared memory once; then, for every group of RG consecutive chunks that
-// holds a winner, the A rows and B columns of that group are staged into
-// shared memory and each winner's 16 products are recomputed to find the
-// first one equal to the value.  Every access after the two tile loads is to
-// shared memory.
-#ifndef TROP_RESOLVE_GK
-#define TROP_RESOLVE_GK 128
-#endif
-constexpr int RTHREADS = 256, RGK = TROP_RESOLVE_GK, RG = RGK / CH;  // k per staged group
-constexpr int RMAXG = 1024;                            // groups tracked by the bit set (K <= 65536)
-
-struct ResolveSmem {
-    float Ct[BM][BN + 1];
-    int32_t It[BM][BN + 1];
-    float EA[BM][RGK + 4];
-    float EB[RGK][BN];
-    uint16_t lst[BM * BN];
-    uint32_t gbits[RMAXG / 32];
-    int nlist;
-};
-constexpr size_t SMEM_RESOLVE = sizeof(ResolveSmem);
+// One CTA (256 threads) per 64x64 output tile.  Each thread holds 16 outputs of
+// the tile (4 rows x 4 consecutive columns) in registers: value and chunk
+// code.  B's rows are staged into shared memory 256 k at a time; for each of
+// its outputs whose chunk lies in the staged group a thread recomputes the
+// chunk's CH products -- A's contiguous row segment through L1, B's column
+// from shared memory -- and keeps the first k whose product equals the value.
+// Results go back from registers with coalesced stores.
+constexpr int RTHREADS = 256, RGK = 256;
+constexpr size_t SMEM_RESOLVE = sizeof(float) * RGK * BN;  // 64 KiB
 
 template <int SR>
-__global__ void __launch_bounds__(RTHREADS) k_argmax_resolve(TiledParams p)
+__global__ void __launch_bounds__(RTHREADS, 2) k_argmax_resolve(TiledParams p)
 {
     using O = Ops<SR>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    ResolveSmem& S = *reinterpret_cast<ResolveSmem*>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31;
+    float(*EB)[BN] = reinterpret_cast<float(*)[BN]>(smem_raw);
+    const int tid = threadIdx.x;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-    const int nch = (p.K + CH - 1) / CH;
-    const int ngr = (nch + RG - 1) / RG;
-    // my 16 tile entries: rows (tid/16) + 16*r, columns (tid%16)*4 + j; entry q = 4r + j.
-    // Consecutive lanes cover consecutive columns, so every tile load/store is coalesced.
+    const int ngr = (p.K + RGK - 1) / RGK;
+    // my outputs: rows rr + 16*r (r < 4), columns cc .. cc+3
     const int rr = tid / 16, cc = (tid % 16) * 4;
     for (uint32_t b = blockIdx.z; b < p.nbatch; b += gridDim.z) {
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
         const float* __restrict__ A = p.A + oa;
         const float* __restrict__ B = p.B + ob;
-        if (tid < RMAXG / 32) S.gbits[tid] = 0;
-        int code[16];
-        uint64_t gm = 0;
+        float val[4][4];
+        int code[4][4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int row = rr + 16 * r, m = m0 + row;
+            const int m = m0 + rr + 16 * r, n = n0 + cc;
             const float* crow = p.C + oc + (int64_t)m * p.sCm;
             const int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
-            const int n = n0 + cc;
-            float cv[4];
-            int iv[4];
             if (m < p.M && n + 3 < p.N && p.vecC && p.vecI) {
                 const float4 c4 = *reinterpret_cast<const float4*>(crow + n);
                 const int4 i4 = *reinterpret_cast<const int4*>(irow + n);
-                cv[0] = c4.x; cv[1] = c4.y; cv[2] = c4.z; cv[3] = c4.w;
-                iv[0] = i4.x; iv[1] = i4.y; iv[2] = i4.z; iv[3] = i4.w;
+                val[r][0] = c4.x; val[r][1] = c4.y; val[r][2] = c4.z; val[r][3] = c4.w;
+                code[r][0] = i4.x; code[r][1] = i4.y; code[r][2] = i4.z; code[r][3] = i4.w;
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const bool in = m < p.M && n + j < p.N;
-                    cv[j] = in ? crow[(int64_t)(n + j) * p.sCn] : 0.0f;
-                    iv[j] = in ? irow[(int64_t)(n + j) * p.sIn] : 0;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                code[4 * r + j] = iv[j];
-                S.Ct[row][cc + j] = cv[j];
-                S.It[row][cc + j] = iv[j];
-                if (iv[j] > 0) {
-                    const int g = (iv[j] - 1) / RG;
-                    if (ngr <= 64) gm |= 1ull << g;
+                    val[r][j] = in ? crow[(int64_t)(n + j) * p.sCn] : 0.0f;
+                    code[r][j] = in ? irow[(int64_t)(n + j) * p.sIn] : 0;
                 }
             }
         }
-        __syncthreads();  // gbits cleared before anyone sets a bit
-        if (ngr <= 64) {
+        int res[4][4];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) gm |= __shfl_xor_sync(0xffffffffu, gm, o);
-            if (lane == 0 && gm) {
-                atomicOr(&S.gbits[0], (uint32_t)gm);
-                atomicOr(&S.gbits[1], (uint32_t)(gm >> 32));
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) res[r][j] = 0;  // code 0: nothing beat the zero, argmax 0
+        for (int g = 0; g < ngr; ++g) {
+            const int k0 = g * RGK;
+            const int kn = min(RGK, p.K - k0);
+            bool any = false;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int ch = code[r][j] - 1;
+                    any |= ch >= 0 && ch * CH >= k0 && ch * CH < k0 + RGK;
+                }
+            if (!__syncthreads_or(any)) continue;
+            // stage B rows k0 .. k0+kn of this tile's columns (zero outside the operand)
+            for (int e = tid; e < kn * (BN / 4); e += RTHREADS) {
+                const int kk = e / (BN / 4), nq = (e % (BN / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
+                float* dst = &EB[kk][nq];
+                if (p.vecB) {
+                    const int valid = max(0, min(4, p.N - gn));
+                    cp_async16(dst, valid ? B + (int64_t)gk * p.sBk + gn : B, valid * 4);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = (gn + q < p.N) ? __ldg(B + (int64_t)gk * p.sBk + gn + q) : 0.0f;
+                }
             }
-        } else if (ngr <= RMAXG) {
+            cp_async_commit();
+            cp_async_wait_all();
+            __syncthreads();
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                if (code[q] > 0) {
-                    const int g = (code[q] - 1) / RG;
-                    atomicOr(&S.gbits[g >> 5], 1u << (g & 31));
-                }
-        }
-        __syncthreads();
-        if (ngr <= RMAXG) {
-            for (int g = 0; g < ngr; ++g) {
-                if (!((S.gbits[g >> 5] >> (g & 31)) & 1u)) continue;
-                const int k0 = g * RGK;
-                if (tid == 0) S.nlist = 0;
-                // stage A rows (64 x 64 k) and B rows (64 k x 64 n), zero outside the operands
-                for (int e = tid; e < BM * RGK / 4; e += RTHREADS) {
-                    const int m = e / (RGK / 4), kq = (e % (RGK / 4)) * 4, gmr = m0 + m, gk = k0 + kq;
-                    float* dst = &S.EA[m][kq];
-                    if (p.vecA) {
-                        const int valid = gmr < p.M ? max(0, min(4, p.K - gk)) : 0;
-                        cp_async16(dst, valid ? A + (int64_t)gmr * p.sAm + gk : A, valid * 4);
-                    } else {
+            for (int r = 0; r < 4; ++r) {
+                const int m = m0 + rr + 16 * r;
+                const float* arow = A + (int64_t)m * p.sAm;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = (gmr < p.M && gk + q < p.K) ? __ldg(A + (int64_t)gmr * p.sAm + gk + q) : 0.0f;
-                    }
-                }
-                for (int e = tid; e < RGK * BN / 4; e += RTHREADS) {
-                    const int kk = e / (BN / 4), nq = (e % (BN / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
-                    float* dst = &S.EB[kk][nq];
-                    if (p.vecB) {
-                        const int valid = gk < p.K ? max(0, min(4, p.N - gn)) : 0;
-                        cp_async16(dst, valid ? B + (int64_t)gk * p.sBk + gn : B, valid * 4);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = (gk < p.K && gn + q < p.N) ? __ldg(B + (int64_t)gk * p.sBk + gn + q) : 0.0f;
-                    }
-                }
-                cp_async_commit();
-                __syncthreads();  // nlist reset visible
-                // compact this group's winners (codes kept in registers: shared ones get overwritten)
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const bool mine = code[q] > 0 && (code[q] - 1) / RG == g;
-                    const unsigned bal = __ballot_sync(0xffffffffu, mine);
-                    int base = 0;
-                    if (lane == 0 && bal) base = atomicAdd(&S.nlist, __popc(bal));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    if (mine)
-                        S.lst[base + __popc(bal & ((1u << lane) - 1u))] =
-                            (uint16_t)((rr + 16 * (q / 4)) * BN + cc + (q % 4));
-                }
-                cp_async_wait_all();
-                __syncthreads();
-                const int cnt = S.nlist;
-                for (int e = tid; e < cnt; e += RTHREADS) {
-                    const int pk = S.lst[e], r = pk / BN, c = pk % BN;
-                    const int chunk = S.It[r][c] - 1;
-                    const float target = S.Ct[r][c];
-                    const int kl = (chunk - g * RG) * CH;
-                    const int kmax = min(CH, p.K - chunk * CH);
+                for (int j = 0; j < 4; ++j) {
+                    const int ch = code[r][j] - 1;
+                    if (ch < 0 || ch * CH < k0 || ch * CH >= k0 + RGK) continue;
+                    const int ka = ch * CH, kl = ka - k0, c = cc + j;
+                    const int kmax = min(CH, p.K - ka);
                     float av[CH];
+                    if (p.vecA && kmax == CH) {
 #pragma unroll
-                    for (int kk = 0; kk < CH; kk += 4) {
-                        const float4 x = *reinterpret_cast<const float4*>(&S.EA[r][kl + kk]);
-                        av[kk] = x.x;
-                        av[kk + 1] = x.y;
-                        av[kk + 2] = x.z;
-                        av[kk + 3] = x.w;
+                        for (int kk = 0; kk < CH; kk += 4) {
+                            const float4 x = __ldg(reinterpret_cast<const float4*>(arow + ka + kk));
+                            av[kk] = x.x;
+                            av[kk + 1] = x.y;
+                            av[kk + 2] = x.z;
+                            av[kk + 3] = x.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < CH; ++kk) av[kk] = kk < kmax ? __ldg(arow + ka + kk) : 0.0f;
                     }
+                    const float target = val[r][j];
                     int idx = 0;
 #pragma unroll
                     for (int kk = CH - 1; kk >= 0; --kk)
-                        if (kk < kmax && O::mul(av[kk], S.EB[kl + kk][c]) == target) idx = kk;
-                    S.It[r][c] = chunk * CH + idx;
+                        if (kk < kmax && O::mul(av[kk], EB[kl + kk][c]) == target) idx = kk;
+                    res[r][j] = ka + idx;
                 }
-                __syncthreads();
             }
-        } else {
-            // very long contractions: search each winning chunk in global memory
-#pragma unroll 1
-            for (int q = 0; q < 16; ++q) {
-                const int r = rr + 16 * (q / 4), c = cc + (q % 4), m = m0 + r;
-                const int cd = S.It[r][c];
-                if (cd <= 0) continue;
-                const int chunk = cd - 1, k0 = chunk * CH, k1 = min(k0 + CH, p.K);
-                const float* arow = A + (int64_t)m * p.sAm;
-                const float* bcol = B + n0 + c;
-                const float target = S.Ct[r][c];
-                int idx = k0;
-                for (int k = k1 - 1; k >= k0; --k)
-                    if (O::mul(__ldg(arow + k), __ldg(bcol + (int64_t)k * p.sBk)) == target) idx = k;
-                S.It[r][c] = idx;
-            }
-            __syncthreads();
+            __syncthreads();  // before the next group overwrites the staged rows
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int row = rr + 16 * r, m = m0 + row, n = n0 + cc;
+            const int m = m0 + rr + 16 * r, n = n0 + cc;
             if (m >= p.M) continue;
             int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
             if (n + 3 < p.N && p.vecI) {
-                *reinterpret_cast<int4*>(irow + n) =
-                    make_int4(S.It[row][cc], S.It[row][cc + 1], S.It[row][cc + 2], S.It[row][cc + 3]);
+                *reinterpret_cast<int4*>(irow + n) = make_int4(res[r][0], res[r][1], res[r][2], res[r][3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (n + j < p.N) irow[(int64_t)(n + j) * p.sIn] = S.It[row][cc + j];
+                    if (n + j < p.N) irow[(int64_t)(n + j) * p.sIn] = res[r][j];
             }
         }
-        __syncthreads();
     }
 }
 
@@ -523,7 +454,7 @@ struct StreamParams {
     Batch bt;
 };
 
-template <int SR, bool ARG, int VEC>
+template <int SR, bool ARG, int VEC, int MAXM>
 __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
 {
     using O = Ops<SR>;
@@ -532,10 +463,10 @@ __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
         const int n = (int)(e - b * p.nvec) * VEC;
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
-        float best[MAXM_STREAM][VEC];
-        int32_t idx[MAXM_STREAM][VEC];
+        float best[MAXM][VEC];
+        int32_t idx[MAXM][VEC];
 #pragma unroll
-        for (int m = 0; m < MAXM_STREAM; ++m)
+        for (int m = 0; m < MAXM; ++m)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 best[m][v] = O::zero();
@@ -556,7 +487,7 @@ __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
                 for (int v = 0; v < VEC; ++v) bv[v] = __ldg(Bb + (int64_t)k * p.sBk + (int64_t)v * p.sBn);
             }
 #pragma unroll
-            for (int m = 0; m < MAXM_STREAM; ++m) {
+            for (int m = 0; m < MAXM; ++m) {
                 if (m < p.M) {
                     const float a = __ldg(Ab + (int64_t)m * p.sAm + (int64_t)k * p.sAk);
 #pragma unroll
@@ -571,7 +502,7 @@ __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
             }
         }
 #pragma unroll
-        for (int m = 0; m < MAXM_STREAM; ++m) {
+        for (int m = 0; m < MAXM; ++m) {
             if (m < p.M) {
                 float* cp = p.C + oc + (int64_t)m * p.sCm + (int64_t)n * p.sCn;
                 int32_t* ip = ARG ? p.I + oi + (int64_t)m * p.sIm + (int64_t)n * p.sIn : nullptr;
@@ -746,8 +677,17 @@ int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     int64_t blocks = ((int64_t)p.total + 255) / 256;
     int64_t cap = (int64_t)dev->sm_count * 16;
     int grid = (int)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
-    if (vec) k_gemm_stream<SR, ARG, 4><<<grid, 256, 0, s>>>(p);
-    else k_gemm_stream<SR, ARG, 1><<<grid, 256, 0, s>>>(p);
+    // register arrays sized to the rows actually present keep occupancy high
+    if (g.M <= 2) {
+        if (vec) k_gemm_stream<SR, ARG, 4, 2><<<grid, 256, 0, s>>>(p);
+        else k_gemm_stream<SR, ARG, 1, 2><<<grid, 256, 0, s>>>(p);
+    } else if (g.M <= 4) {
+        if (vec) k_gemm_stream<SR, ARG, 4, 4><<<grid, 256, 0, s>>>(p);
+        else k_gemm_stream<SR, ARG, 1, 4><<<grid, 256, 0, s>>>(p);
+    } else {
+        if (vec) k_gemm_stream<SR, ARG, 4, MAXM_STREAM><<<grid, 256, 0, s>>>(p);
+        else k_gemm_stream<SR, ARG, 1, MAXM_STREAM><<<grid, 256, 0, s>>>(p);
+    }
     return check_launch("k_gemm_stream");
 }
 
@@ -891,7 +831,7 @@ int register_gemm_kernels()
     const void* ks[] = {
         (const void*)k_gemm_tiled<TROP_MAXPLUS, true>,  (const void*)k_gemm_tiled<TROP_MINPLUS, true>,
         (const void*)k_gemm_tiled<TROP_MAXTIMES, true>, (const void*)k_gemm_tiled<TROP_MAXPLUS, false>,
-        (const void*)k_gemm_stream<TROP_MAXPLUS, true, 4>, (const void*)k_gemm_stream<TROP_MAXPLUS, true, 1>,
+        (const void*)k_gemm_stream<TROP_MAXPLUS, true, 4, 2>, (const void*)k_gemm_stream<TROP_MAXPLUS, true, 1, 2>,
         (const void*)k_gemm_generic<TROP_MAXPLUS, true>,
     };
     for (const void* k : ks) {

@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 
 #include "internal.h"
@@ -119,9 +120,12 @@ __global__ void k_copy_rows(const T* __restrict__ in, T* __restrict__ out, const
 // ------------------------------------------------------------------ transpose
 // Tile over two axis chains: GI = input-fastest chain (contiguous in the
 // input), GJ = output-fastest chain (contiguous in the output).  A tile is TI
-// consecutive GI indices x TJ consecutive GJ indices.
+// consecutive GI indices x TJ consecutive GJ indices with TI * TJ = TILE
+// elements; the shape adapts when one chain is short (e.g. 16 x 256 when the
+// input's fastest axis has 16 elements), so every tile stays full.
 struct TransParams {
     uint32_t nI, nJ;          // flattened chain extents
+    uint32_t TI, TJ;          // tile shape
     uint32_t tilesI, tilesJ;  // tiles along each chain
     uint32_t tiles;           // tilesI * tilesJ * rest count
     FastDiv div_tilesI, div_tilesJ;
@@ -135,8 +139,9 @@ struct TransParams {
 
 template <int T_BYTES>
 struct TileCfg {
-    static constexpr int TI = T_BYTES == 8 ? 32 : 64;
-    static constexpr int TJ = T_BYTES == 8 ? 32 : 64;
+    static constexpr int TILE = T_BYTES == 8 ? 2048 : 4096;  // elements per tile
+    static constexpr int TJMAX = 512;
+    static constexpr int TIMAX = 64;
 };
 
 template <typename T, bool PAIR>
@@ -144,14 +149,14 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                                                   const int32_t* __restrict__ in2, int32_t* __restrict__ out2,
                                                   TransParams p)
 {
-    constexpr int TI = TileCfg<sizeof(T)>::TI;
-    constexpr int TJ = TileCfg<sizeof(T)>::TJ;
+    using Cfg = TileCfg<sizeof(T)>;
     constexpr int W = 16 / sizeof(T);
-    __shared__ T tile[TJ][TI + 1];
-    __shared__ int32_t tile2[PAIR ? TJ : 1][PAIR ? TI + 1 : 1];
-    __shared__ int64_t row_in[TJ], row_in2[TJ];    // input offset of GJ index (tile row)
-    __shared__ int64_t row_out[TI], row_out2[TI];  // output offset of GI index (tile column)
+    __shared__ T tile[Cfg::TILE + Cfg::TJMAX];                         // rows of TI + 1
+    __shared__ int32_t tile2[PAIR ? Cfg::TILE + Cfg::TJMAX : 1];
+    __shared__ int64_t row_in[Cfg::TJMAX], row_in2[PAIR ? Cfg::TJMAX : 1];  // input offset of a GJ index
+    __shared__ int64_t row_out[Cfg::TIMAX], row_out2[PAIR ? Cfg::TIMAX : 1];  // output offset of a GI index
     __shared__ int64_t base[4];
+    const int TI = (int)p.TI, TJ = (int)p.TJ, LD = TI + 1;
 
     for (uint32_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
         uint32_t q1 = fdiv(t, p.div_tilesI);
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                     off2 += (int64_t)c * p.gj_s_in2[d];
                 }
                 row_in[x] = off;
-                row_in2[x] = off2;
+                if (PAIR) row_in2[PAIR ? x : 0] = off2;
             } else {
                 int y = x - TJ;
                 uint32_t i = i0 + y, rem = i < p.nI ? i : 0;
@@ -193,43 +198,45 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                     off2 += (int64_t)c * p.gi_s_out2[d];
                 }
                 row_out[y] = off;
-                row_out2[y] = off2;
+                if (PAIR) row_out2[PAIR ? y : 0] = off2;
             }
         }
         __syncthreads();
         const int64_t bin = base[0], bout = base[1], bin2 = base[2], bout2 = base[3];
-        const bool fullI = i0 + TI <= p.nI, fullJ = j0 + TJ <= p.nJ;
+        const bool fullI = i0 + TI <= p.nI;
         // load: rows = GJ index (strided in the input), columns = GI index (contiguous)
         if (fullI && p.vec_in) {
             using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
-            for (int e = threadIdx.x; e < TJ * (TI / W); e += NT) {
-                int r = e / (TI / W), c = (e - r * (TI / W)) * W;
-                if (!fullJ && j0 + r >= p.nJ) continue;
+            const int vpr = TI / W;  // vectors per row
+            for (int e = threadIdx.x; e < TJ * vpr; e += NT) {
+                const int r = e / vpr, c = (e - r * vpr) * W;
+                if (j0 + r >= p.nJ) continue;
                 V v = __ldg(reinterpret_cast<const V*>(in + bin + row_in[r] + i0 + c));
                 const T* pv = reinterpret_cast<const T*>(&v);
 #pragma unroll
-                for (int q = 0; q < W; ++q) tile[r][c + q] = pv[q];
+                for (int q = 0; q < W; ++q) tile[r * LD + c + q] = pv[q];
                 if (PAIR) {
 #pragma unroll
-                    for (int q = 0; q < W; ++q) tile2[r][c + q] = __ldg(in2 + bin2 + row_in2[r] + i0 + c + q);
+                    for (int q = 0; q < W; ++q)
+                        tile2[PAIR ? r * LD + c + q : 0] = __ldg(in2 + bin2 + row_in2[PAIR ? r : 0] + i0 + c + q);
                 }
             }
         } else {
             for (int e = threadIdx.x; e < TJ * TI; e += NT) {
-                int r = e / TI, c = e - r * TI;
+                const int r = e / TI, c = e - r * TI;
                 if (j0 + r < p.nJ && i0 + c < p.nI) {
-                    tile[r][c] = __ldg(in + bin + row_in[r] + i0 + c);
-                    if (PAIR) tile2[r][c] = __ldg(in2 + bin2 + row_in2[r] + i0 + c);
+                    tile[r * LD + c] = __ldg(in + bin + row_in[r] + i0 + c);
+                    if (PAIR) tile2[PAIR ? r * LD + c : 0] = __ldg(in2 + bin2 + row_in2[PAIR ? r : 0] + i0 + c);
                 }
             }
         }
         __syncthreads();
         // store: rows = GI index (strided in the output), columns = GJ index (contiguous)
         for (int e = threadIdx.x; e < TJ * TI; e += NT) {
-            int r = e / TJ, c = e - r * TJ;
+            const int r = e / TJ, c = e - r * TJ;
             if (i0 + r < p.nI && j0 + c < p.nJ) {
-                out[bout + row_out[r] + j0 + c] = tile[c][r];
-                if (PAIR) out2[bout2 + row_out2[r] + j0 + c] = tile2[c][r];
+                out[bout + row_out[r] + j0 + c] = tile[c * LD + r];
+                if (PAIR) out2[bout2 + row_out2[PAIR ? r : 0] + j0 + c] = tile2[PAIR ? c * LD + r : 0];
             }
         }
         __syncthreads();
@@ -503,7 +510,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
         if (d.s_in[i] == 1) din = i;
     if (d.rank >= 2 && small_idx && same_map && d.s_out[last] == 1 && din >= 0 && din != last) {
         // ---- tiled transpose over two axis chains
-        constexpr int TI = TileCfg<sizeof(T)>::TI;
+        constexpr int CHAIN_I = TileCfg<sizeof(T)>::TIMAX, CHAIN_J = TileCfg<sizeof(T)>::TJMAX;
         TransParams p{};
         int used = 0;
         // output-fastest chain
@@ -515,7 +522,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
                 gj[ngj++] = cur;
                 used |= 1 << cur;
                 nJ *= d.size[cur];
-                if (nJ >= TI) break;
+                if (nJ >= CHAIN_J) break;
                 int nxt = -1;
                 for (int i = 0; i < d.rank; ++i)
                     if (!(used & (1 << i)) && i != din && d.s_out[i] == nJ) nxt = i;
@@ -531,7 +538,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
                 gi[ngi++] = cur;
                 used |= 1 << cur;
                 nI *= d.size[cur];
-                if (nI >= TI) break;
+                if (nI >= CHAIN_I) break;
                 int nxt = -1;
                 for (int i = 0; i < d.rank; ++i)
                     if (!(used & (1 << i)) && d.s_in[i] == nI) nxt = i;
@@ -557,18 +564,32 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
         int64_t nrest = 1;
         for (int i = 0; i < d.rank; ++i)
             if (!(used & (1 << i))) nrest *= d.size[i];
-        constexpr int TJ = TileCfg<sizeof(T)>::TJ;
+        using Cfg = TileCfg<sizeof(T)>;
+        auto pow2ceil = [](int64_t v) {
+            int64_t r = 1;
+            while (r < v) r <<= 1;
+            return r;
+        };
+        // tile: TI x TJ = TILE elements, fitted to short chains
+        int64_t ti_ = std::min<int64_t>(Cfg::TIMAX, std::max<int64_t>(4, pow2ceil(nI)));
+        int64_t tj_ = std::min<int64_t>(Cfg::TJMAX, Cfg::TILE / ti_);
+        if (pow2ceil(nJ) < tj_) {
+            tj_ = std::max<int64_t>(4, pow2ceil(nJ));
+            ti_ = std::min<int64_t>(Cfg::TIMAX, std::max<int64_t>(4, std::min<int64_t>(pow2ceil(nI), Cfg::TILE / tj_)));
+        }
+        p.TI = (uint32_t)ti_;
+        p.TJ = (uint32_t)tj_;
         p.nI = (uint32_t)nI;
         p.nJ = (uint32_t)nJ;
-        p.tilesI = (uint32_t)((nI + TI - 1) / TI);
-        p.tilesJ = (uint32_t)((nJ + TJ - 1) / TJ);
+        p.tilesI = (uint32_t)((nI + ti_ - 1) / ti_);
+        p.tilesJ = (uint32_t)((nJ + tj_ - 1) / tj_);
         int64_t tiles = (int64_t)p.tilesI * p.tilesJ * nrest;
         if (tiles < (int64_t(1) << 31)) {
             p.tiles = (uint32_t)tiles;
             p.div_tilesI = make_fastdiv(p.tilesI);
             p.div_tilesJ = make_fastdiv(p.tilesJ);
             constexpr int W = 16 / sizeof(T);
-            bool vec = ((uintptr_t)in % 16) == 0 && (nI % W) == 0;
+            bool vec = ((uintptr_t)in % 16) == 0 && (nI % W) == 0 && (p.TI % W) == 0;
             for (int i = 0; i < d.rank; ++i)
                 if (i != din) vec = vec && (d.s_in[i] % W) == 0;
             p.vec_in = vec ? 1 : 0;
