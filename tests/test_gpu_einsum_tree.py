@@ -209,3 +209,17 @@ def test_spec_and_shape_errors(trop):
     with pytest.raises(trop.TropicalError) as e:
         trop.permute_trace(torch.zeros((2, 3), device="cuda"), "ii->i")
     assert e.value.name == "SHAPE"
+
+
+def test_ising_workload_24x24_full_size(trop):
+    """The benchmarked 24x24 instance: value and back-tracked configuration
+    bitwise against the oracle's site-by-site elimination (OpenMP)."""
+    from einsum_device_side_gb300 import ising
+    jh, jv = synth.ising_couplings()
+    w, spins, am = ising.ground_state(jh, jv)
+    del am
+    torch.cuda.empty_cache()
+    wo, so = oracle.ising_ground(jh, jv, 24, 24, nthreads=0)
+    assert w == wo
+    np.testing.assert_array_equal(spins, so)
+    assert oracle.ising_energy(jh, jv, spins) == -w
