@@ -119,21 +119,24 @@ __global__ void k_copy_rows(const T* __restrict__ in, T* __restrict__ out, const
 
 // ------------------------------------------------------------------ transpose
 // Tile over two axis chains: GI = input-fastest chain (contiguous in the
-// input), GJ = output-fastest chain (contiguous in the output).  A tile is TI
-// consecutive GI indices x TJ consecutive GJ indices with TI * TJ = TILE
-// elements; the shape adapts when one chain is short (e.g. 16 x 256 when the
-// input's fastest axis has 16 elements), so every tile stays full.
+// input), GJ = output-fastest chain (contiguous in the output), and TB
+// consecutive indices of the remaining axes.  A tile is TB x TJ x TI = TILE
+// elements (powers of two); its shape adapts when a chain is short (16 x 256
+// when the input's fastest axis has 16 elements; TB > 1 stacks several
+// outer-axis slices when both chains are short), so every tile stays full.
 struct TransParams {
-    uint32_t nI, nJ;          // flattened chain extents
-    uint32_t TI, TJ;          // tile shape
-    uint32_t tilesI, tilesJ;  // tiles along each chain
-    uint32_t tiles;           // tilesI * tilesJ * rest count
+    uint32_t nI, nJ, nR;         // flattened chain extents, remaining-axes count
+    uint32_t TI, TJ, TB;         // tile shape (powers of two)
+    uint32_t lTI, lTJ, lTB;      // their log2
+    uint32_t tilesI, tilesJ, tilesR;
+    uint32_t tiles;              // tilesI * tilesJ * tilesR
     FastDiv div_tilesI, div_tilesJ;
     int gi_rank, gj_rank;
     FastDiv gi_div[4], gj_div[4];
     int64_t gi_s_out[4], gi_s_out2[4];  // output strides of GI axes (last = fastest in input)
     int64_t gj_s_in[4], gj_s_in2[4];    // input strides of GJ axes (last = fastest in output)
     int vec_in;                          // input rows 16-byte aligned for vector loads
+    int vec_out;                         // output rows 16-byte aligned for vector stores
     RestDims rest;
 };
 
@@ -142,6 +145,7 @@ struct TileCfg {
     static constexpr int TILE = T_BYTES == 8 ? 2048 : 4096;  // elements per tile
     static constexpr int TJMAX = 512;
     static constexpr int TIMAX = 64;
+    static constexpr int TBMAX = 64;
 };
 
 template <typename T, bool PAIR>
@@ -150,30 +154,26 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                                                   TransParams p)
 {
     using Cfg = TileCfg<sizeof(T)>;
+    using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
     constexpr int W = 16 / sizeof(T);
-    __shared__ T tile[Cfg::TILE + Cfg::TJMAX];                         // rows of TI + 1
-    __shared__ int32_t tile2[PAIR ? Cfg::TILE + Cfg::TJMAX : 1];
-    __shared__ int64_t row_in[Cfg::TJMAX], row_in2[PAIR ? Cfg::TJMAX : 1];  // input offset of a GJ index
-    __shared__ int64_t row_out[Cfg::TIMAX], row_out2[PAIR ? Cfg::TIMAX : 1];  // output offset of a GI index
-    __shared__ int64_t base[4];
-    const int TI = (int)p.TI, TJ = (int)p.TJ, LD = TI + 1;
+    constexpr int VPT = Cfg::TILE / W / NT;  // vectors per thread in a full tile
+    __shared__ T tile[Cfg::TILE + Cfg::TILE / 4];  // TB*TJ rows of TI+1 (TI >= 4)
+    __shared__ int32_t tile2[PAIR ? Cfg::TILE + Cfg::TILE / 4 : 1];
+    __shared__ int64_t row_in[Cfg::TJMAX], row_in2[PAIR ? Cfg::TJMAX : 1];     // input offset of a GJ index
+    __shared__ int64_t row_out[Cfg::TIMAX], row_out2[PAIR ? Cfg::TIMAX : 1];   // output offset of a GI index
+    __shared__ int64_t bin_s[Cfg::TBMAX], bout_s[Cfg::TBMAX];                   // offsets of the TB outer slices
+    __shared__ int64_t bin2_s[PAIR ? Cfg::TBMAX : 1], bout2_s[PAIR ? Cfg::TBMAX : 1];
+    const int TI = (int)p.TI, TJ = (int)p.TJ, TB = (int)p.TB, LD = TI + 1;
+    const int lTI = (int)p.lTI, lTJ = (int)p.lTJ;
 
     for (uint32_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-        uint32_t q1 = fdiv(t, p.div_tilesI);
-        uint32_t ti = t - q1 * p.tilesI;
-        uint32_t q2 = fdiv(q1, p.div_tilesJ);
-        uint32_t tj = q1 - q2 * p.tilesJ;
-        uint32_t rest = q2;
+        const uint32_t q1 = fdiv(t, p.div_tilesI);
+        const uint32_t ti = t - q1 * p.tilesI;
+        const uint32_t q2 = fdiv(q1, p.div_tilesJ);
+        const uint32_t tj = q1 - q2 * p.tilesJ;
+        const uint32_t r0 = q2 << p.lTB;
         const uint32_t i0 = ti * TI, j0 = tj * TJ;
-        if (threadIdx.x == 0) {
-            int64_t a, b, c, d;
-            decode_rest(p.rest, rest, a, b, c, d);
-            base[0] = a;
-            base[1] = b;
-            base[2] = c;
-            base[3] = d;
-        }
-        for (int x = threadIdx.x; x < TJ + TI; x += NT) {
+        for (int x = threadIdx.x; x < TJ + TI + TB; x += NT) {
             if (x < TJ) {
                 uint32_t j = j0 + x, rem = j < p.nJ ? j : 0;
                 int64_t off = 0, off2 = 0;
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                 }
                 row_in[x] = off;
                 if (PAIR) row_in2[PAIR ? x : 0] = off2;
-            } else {
+            } else if (x < TJ + TI) {
                 int y = x - TJ;
                 uint32_t i = i0 + y, rem = i < p.nI ? i : 0;
                 int64_t off = 0, off2 = 0;
@@ -199,44 +199,75 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                 }
                 row_out[y] = off;
                 if (PAIR) row_out2[PAIR ? y : 0] = off2;
+            } else {
+                const int b = x - TJ - TI;
+                const uint32_t rr = r0 + b;
+                int64_t a, bb, c, d;
+                decode_rest(p.rest, rr < p.nR ? rr : 0, a, bb, c, d);
+                bin_s[b] = a;
+                bout_s[b] = bb;
+                if (PAIR) {
+                    bin2_s[PAIR ? b : 0] = c;
+                    bout2_s[PAIR ? b : 0] = d;
+                }
             }
         }
         __syncthreads();
-        const int64_t bin = base[0], bout = base[1], bin2 = base[2], bout2 = base[3];
-        const bool fullI = i0 + TI <= p.nI;
-        // load: rows = GJ index (strided in the input), columns = GI index (contiguous)
-        if (fullI && p.vec_in) {
-            using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
-            const int vpr = TI / W;  // vectors per row
-            for (int e = threadIdx.x; e < TJ * vpr; e += NT) {
-                const int r = e / vpr, c = (e - r * vpr) * W;
-                if (j0 + r >= p.nJ) continue;
-                V v = __ldg(reinterpret_cast<const V*>(in + bin + row_in[r] + i0 + c));
-                const T* pv = reinterpret_cast<const T*>(&v);
+        const bool full = i0 + TI <= p.nI && j0 + TJ <= p.nJ && r0 + TB <= p.nR;
+        const int lvi = lTI - (W == 4 ? 2 : 1);  // log2 of vectors per input row
+        // load: rows = (slice, GJ index) (strided in the input), columns = GI index (contiguous)
+        if (!PAIR && full && p.vec_in && TI >= W && (TB << (lTJ + lTI)) == Cfg::TILE) {
+            V v[VPT];
 #pragma unroll
-                for (int q = 0; q < W; ++q) tile[r * LD + c + q] = pv[q];
-                if (PAIR) {
+            for (int u = 0; u < VPT; ++u) {  // all loads in flight before any shared store
+                const int e = threadIdx.x + u * NT;
+                const int c = (e & ((1 << lvi) - 1)) * W, rj = e >> lvi;
+                const int r = rj & (TJ - 1), b = rj >> lTJ;
+                v[u] = __ldg(reinterpret_cast<const V*>(in + bin_s[b] + row_in[r] + i0 + c));
+            }
 #pragma unroll
-                    for (int q = 0; q < W; ++q)
-                        tile2[PAIR ? r * LD + c + q : 0] = __ldg(in2 + bin2 + row_in2[PAIR ? r : 0] + i0 + c + q);
-                }
+            for (int u = 0; u < VPT; ++u) {
+                const int e = threadIdx.x + u * NT;
+                const int c = (e & ((1 << lvi) - 1)) * W, rj = e >> lvi;
+                const T* pv = reinterpret_cast<const T*>(&v[u]);
+#pragma unroll
+                for (int q = 0; q < W; ++q) tile[rj * LD + c + q] = pv[q];
             }
         } else {
-            for (int e = threadIdx.x; e < TJ * TI; e += NT) {
-                const int r = e / TI, c = e - r * TI;
-                if (j0 + r < p.nJ && i0 + c < p.nI) {
-                    tile[r * LD + c] = __ldg(in + bin + row_in[r] + i0 + c);
-                    if (PAIR) tile2[PAIR ? r * LD + c : 0] = __ldg(in2 + bin2 + row_in2[PAIR ? r : 0] + i0 + c);
+            for (int e = threadIdx.x; e < TB * TJ * TI; e += NT) {
+                const int c = e & (TI - 1), rj = e >> lTI;
+                const int r = rj & (TJ - 1), b = rj >> lTJ;
+                if (r0 + b < p.nR && j0 + r < p.nJ && i0 + c < p.nI) {
+                    tile[rj * LD + c] = __ldg(in + bin_s[b] + row_in[r] + i0 + c);
+                    if (PAIR)
+                        tile2[PAIR ? rj * LD + c : 0] =
+                            __ldg(in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c);
                 }
             }
         }
         __syncthreads();
-        // store: rows = GI index (strided in the output), columns = GJ index (contiguous)
-        for (int e = threadIdx.x; e < TJ * TI; e += NT) {
-            const int r = e / TJ, c = e - r * TJ;
-            if (i0 + r < p.nI && j0 + c < p.nJ) {
-                out[bout + row_out[r] + j0 + c] = tile[c * LD + r];
-                if (PAIR) out2[bout2 + row_out2[PAIR ? r : 0] + j0 + c] = tile2[PAIR ? c * LD + r : 0];
+        // store: rows = (slice, GI index) (strided in the output), columns = GJ index (contiguous)
+        if (!PAIR && full && p.vec_out && TJ >= W) {
+            const int lvj = lTJ - (W == 4 ? 2 : 1);
+            for (int e = threadIdx.x; e < (TB * TI) << lvj; e += NT) {
+                const int c = (e & ((1 << lvj) - 1)) * W, ri = e >> lvj;
+                const int r = ri & (TI - 1), b = ri >> lTI;
+                V v;
+                T* pv = reinterpret_cast<T*>(&v);
+#pragma unroll
+                for (int q = 0; q < W; ++q) pv[q] = tile[((b << lTJ) + c + q) * LD + r];
+                *reinterpret_cast<V*>(out + bout_s[b] + row_out[r] + j0 + c) = v;
+            }
+        } else {
+            for (int e = threadIdx.x; e < TB * TJ * TI; e += NT) {
+                const int c = e & (TJ - 1), ri = e >> lTJ;
+                const int r = ri & (TI - 1), b = ri >> lTI;
+                if (r0 + b < p.nR && i0 + r < p.nI && j0 + c < p.nJ) {
+                    out[bout_s[b] + row_out[r] + j0 + c] = tile[((b << lTJ) + c) * LD + r];
+                    if (PAIR)
+                        out2[bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c] =
+                            tile2[PAIR ? ((b << lTJ) + c) * LD + r : 0];
+                }
             }
         }
         __syncthreads();
@@ -577,13 +608,25 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             tj_ = std::max<int64_t>(4, pow2ceil(nJ));
             ti_ = std::min<int64_t>(Cfg::TIMAX, std::max<int64_t>(4, std::min<int64_t>(pow2ceil(nI), Cfg::TILE / tj_)));
         }
+        // stack outer slices when both chains are short
+        int64_t tb_ = 1;
+        while (tb_ * 2 * ti_ * tj_ <= Cfg::TILE && tb_ * 2 <= Cfg::TBMAX && tb_ < nrest) tb_ *= 2;
         p.TI = (uint32_t)ti_;
         p.TJ = (uint32_t)tj_;
+        p.TB = (uint32_t)tb_;
+        p.lTI = 0;
+        while ((1u << p.lTI) < p.TI) ++p.lTI;
+        p.lTJ = 0;
+        while ((1u << p.lTJ) < p.TJ) ++p.lTJ;
+        p.lTB = 0;
+        while ((1u << p.lTB) < p.TB) ++p.lTB;
         p.nI = (uint32_t)nI;
         p.nJ = (uint32_t)nJ;
+        p.nR = (uint32_t)nrest;
         p.tilesI = (uint32_t)((nI + ti_ - 1) / ti_);
         p.tilesJ = (uint32_t)((nJ + tj_ - 1) / tj_);
-        int64_t tiles = (int64_t)p.tilesI * p.tilesJ * nrest;
+        p.tilesR = (uint32_t)((nrest + tb_ - 1) / tb_);
+        int64_t tiles = (int64_t)p.tilesI * p.tilesJ * p.tilesR;
         if (tiles < (int64_t(1) << 31)) {
             p.tiles = (uint32_t)tiles;
             p.div_tilesI = make_fastdiv(p.tilesI);
@@ -593,7 +636,12 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             for (int i = 0; i < d.rank; ++i)
                 if (i != din) vec = vec && (d.s_in[i] % W) == 0;
             p.vec_in = vec ? 1 : 0;
-            int g = grid_for(tiles, 1, dev->sm_count, 16);
+            // vector stores: output rows start 16-byte aligned (every stride but the GJ chain's unit one)
+            bool vo = ((uintptr_t)out % 16) == 0 && (nJ % W) == 0;
+            for (int i = 0; i < d.rank; ++i)
+                if (i != last) vo = vo && (d.s_out[i] % W) == 0;
+            p.vec_out = vo ? 1 : 0;
+            const int g = (int)std::min<int64_t>(tiles, (int64_t)dev->sm_count * 64);
             if (pair) k_transpose<T, true><<<g, NT, 0, s>>>(in, out, in2, out2, p);
             else k_transpose<T, false><<<g, NT, 0, s>>>(in, out, in2, out2, p);
             return check_launch("k_transpose");
