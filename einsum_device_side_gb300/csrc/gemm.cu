@@ -392,32 +392,42 @@ __global__ void __launch_bounds__(RTHREADS, 2) k_argmax_resolve(TiledParams p)
             for (int r = 0; r < 4; ++r) {
                 const int m = m0 + rr + 16 * r;
                 const float* arow = A + (int64_t)m * p.sAm;
+                // the four columns' A segments: all loads in flight before any search
+                float av[4][CH];
+                int ka[4];
+                bool live[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int ch = code[r][j] - 1;
-                    if (ch < 0 || ch * CH < k0 || ch * CH >= k0 + RGK) continue;
-                    const int ka = ch * CH, kl = ka - k0, c = cc + j;
-                    const int kmax = min(CH, p.K - ka);
-                    float av[CH];
+                    live[j] = ch >= 0 && ch * CH >= k0 && ch * CH < k0 + RGK;
+                    ka[j] = live[j] ? ch * CH : 0;
+                    const float* src = live[j] ? arow + ka[j] : A;
+                    const int kmax = live[j] ? min(CH, p.K - ka[j]) : 0;
                     if (p.vecA && kmax == CH) {
 #pragma unroll
                         for (int kk = 0; kk < CH; kk += 4) {
-                            const float4 x = __ldg(reinterpret_cast<const float4*>(arow + ka + kk));
-                            av[kk] = x.x;
-                            av[kk + 1] = x.y;
-                            av[kk + 2] = x.z;
-                            av[kk + 3] = x.w;
+                            const float4 x = __ldg(reinterpret_cast<const float4*>(src + kk));
+                            av[j][kk] = x.x;
+                            av[j][kk + 1] = x.y;
+                            av[j][kk + 2] = x.z;
+                            av[j][kk + 3] = x.w;
                         }
                     } else {
 #pragma unroll
-                        for (int kk = 0; kk < CH; ++kk) av[kk] = kk < kmax ? __ldg(arow + ka + kk) : 0.0f;
+                        for (int kk = 0; kk < CH; ++kk) av[j][kk] = kk < kmax ? __ldg(src + kk) : 0.0f;
                     }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (!live[j]) continue;
+                    const int kl = ka[j] - k0, c = cc + j;
+                    const int kmax = min(CH, p.K - ka[j]);
                     const float target = val[r][j];
                     int idx = 0;
 #pragma unroll
                     for (int kk = CH - 1; kk >= 0; --kk)
-                        if (kk < kmax && O::mul(av[kk], EB[kl + kk][c]) == target) idx = kk;
-                    res[r][j] = ka + idx;
+                        if (kk < kmax && O::mul(av[j][kk], EB[kl + kk][c]) == target) idx = kk;
+                    res[r][j] = ka[j] + idx;
                 }
             }
             __syncthreads();  // before the next group overwrites the staged rows
