@@ -32,6 +32,8 @@
 //   k_gemm_generic anything else: one thread per output, sequential k.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -91,13 +93,28 @@ __device__ __forceinline__ void batch_offsets(const Batch& bt, uint32_t b, int64
 // ------------------------------------------------------------------ tiled kernel
 constexpr int BM = 64, BN = 64, BK = 16, TM = 8, TN = 8;
 constexpr int TTHREADS = (BM / TM) * (BN / TN);  // 64
+constexpr int TILE_ELEMS = BM * BN;
 constexpr int APAD = 4;                          // float pad per transposed A row (keeps 16-byte rows)
 #ifndef TROP_ARG_CHUNK
 #define TROP_ARG_CHUNK 8
 #endif
 constexpr int CH = TROP_ARG_CHUNK;               // k per argmax chunk (divides BK)
 static_assert(BK % CH == 0 && CH % 2 == 0, "chunk must divide the k-tile and hold whole k pairs");
+static_assert((BK / CH) % 2 == 0, "an even number of chunks per k-tile (the accumulator sets alternate)");
 
+// Tile schedule.  Tiles are numbered t = (b * tiles_m + mt) * tiles_n + nt.  CTA t < T_dp
+// computes tile t over the whole contraction.  When the last tiles would only part-fill a
+// wave of resident CTAs, those R tiles are cut along k instead: their U = R * nkt k-tiles
+// ("units", tile-major) are dealt out L at a time to the CTAs after the data-parallel ones,
+// so the tail keeps every SM busy (the stream-K decomposition of Osama et al., "Stream-K:
+// Work-centric Parallel Decomposition for Dense Matrix-Matrix Multiplication on the GPU",
+// PPoPP 2023).  With L <= nkt the units of one CTA touch at most two tiles; the piece of a
+// tile it computes (a "segment") goes to workspace slot [j][0] for the tile its range starts
+// in and [j][1] for the next.  A tile's segments come from CTAs ua / L .. (ua + nkt - 1) / L,
+// ua being its first unit; the first of them used slot 1 if its range began in the tile
+// before.  Merging segments in k order, a later one winning only when strictly better,
+// reproduces the single pass exactly: (+) is exact, and the strict compare keeps the
+// first k that reaches the result.
 struct TiledParams {
     int M, N, K;
     const float* A;
@@ -109,7 +126,32 @@ struct TiledParams {
     Batch bt;
     int vecA, vecB;  // 16-byte loads allowed (alignment of every row start)
     int vecC, vecI;  // 16-byte stores allowed (unit column stride, aligned rows)
+    uint32_t tiles_m, tiles_n, nkt;
+    FastDiv div_tm, div_tn, div_nkt, div_L;
+    uint32_t T_dp;     // data-parallel tiles: 0 .. T_dp-1
+    uint32_t L, U;     // stream-K: k-tiles per CTA, k-tiles in all (0: no stream-K tiles)
+    float* seg_v;      // [G_sk][2][BM*BN] segment values
+    uint16_t* seg_c;   // [G_sk][2][BM*BN] chunk + 1 of each segment's first maximum, 0 if none (ARG)
+    uint32_t* sk_cnt;  // [R] arrival tickets of the stream-K tiles (zero before and after a launch)
+    uint64_t r_units;  // rows walked by the resolve pass: nbatch * tiles_n * M
 };
+
+__device__ __forceinline__ void tile_coord(const TiledParams& p, uint32_t t, uint32_t& b, int& m0, int& n0)
+{
+    const uint32_t q = fdiv(t, p.div_tn);
+    b = fdiv(q, p.div_tm);
+    m0 = (int)(q - b * p.tiles_m) * BM;
+    n0 = (int)(t - q * p.tiles_n) * BN;
+}
+
+// the CTAs holding the segments of stream-K tile tl, and the slot the first one used
+__device__ __forceinline__ void sk_segments(const TiledParams& p, uint32_t tl, uint32_t& j0, uint32_t& j1, int& slot0)
+{
+    const uint32_t ua = tl * p.nkt;
+    j0 = fdiv(ua, p.div_L);
+    j1 = fdiv(ua + p.nkt - 1, p.div_L);
+    slot0 = j0 * p.L < ua ? 1 : 0;
+}
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes)
 {
@@ -121,11 +163,92 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // rows / columns of the 8x8 outputs a thread owns: two groups of 4, half a tile apart
 __device__ __forceinline__ int row_of(int tm, int i) { return i < 4 ? tm * 4 + i : BM / 2 + tm * 4 + (i - 4); }
-__device__ __forceinline__ int col_of(int tn, int j) { return j < 4 ? tn * 4 + j : BN / 2 + tn * 4 + (j - 4); }
 
-// ARG: besides C, writes into I the chunk (+1) that holds each output's first
-// maximum, or 0 when no product beat the semiring zero; k_argmax_resolve then
-// replaces the chunk by the exact index.
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start once every CTA of the kernel before it has signalled (or exited); it must
+// wait before touching that kernel's results.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_signal() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Merge the segments of stream-K tile tl in k order (a later one wins only when strictly
+// better) and store the tile through C's strides; with ARG also -(chunk + 1), or 0, into I.
+// The segments of other CTAs are read through L2 (ld.global.cg): they were written by
+// other SMs during this launch.
+constexpr int MERGE_RUNS = TILE_ELEMS / 4 / TTHREADS;  // runs of 4 columns per thread
+constexpr int MERGE_BATCH = 8;                          // runs whose loads are in flight together
+
+template <int SR, bool ARG>
+__device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int m0, int n0, int64_t oc,
+                                         int64_t oi, int tid)
+{
+    using O = Ops<SR>;
+    uint32_t j0, j1;
+    int slot0;
+    sk_segments(p, tl, j0, j1, slot0);
+#pragma unroll 1
+    for (int q0 = 0; q0 < MERGE_RUNS; q0 += MERGE_BATCH) {
+        float v[MERGE_BATCH][4];
+        int cd[MERGE_BATCH][4];
+#pragma unroll
+        for (int q = 0; q < MERGE_BATCH; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                v[q][x] = O::zero();
+                cd[q][x] = 0;
+            }
+        for (uint32_t jj = j0; jj <= j1; ++jj) {
+            const size_t base = ((size_t)jj * 2 + (jj == j0 ? slot0 : 0)) * TILE_ELEMS;
+            float4 sv[MERGE_BATCH];
+            uint2 sc[MERGE_BATCH];
+#pragma unroll
+            for (int q = 0; q < MERGE_BATCH; ++q) {
+                const int e = ((q0 + q) * TTHREADS + tid) * 4;
+                sv[q] = __ldcg(reinterpret_cast<const float4*>(p.seg_v + base + e));
+                if (ARG) sc[q] = __ldcg(reinterpret_cast<const uint2*>(p.seg_c + base + e));
+            }
+#pragma unroll
+            for (int q = 0; q < MERGE_BATCH; ++q) {
+                const float s4[4] = {sv[q].x, sv[q].y, sv[q].z, sv[q].w};
+                const int c4[4] = {ARG ? (int)(sc[q].x & 0xffffu) : 0, ARG ? (int)(sc[q].x >> 16) : 0,
+                                   ARG ? (int)(sc[q].y & 0xffffu) : 0, ARG ? (int)(sc[q].y >> 16) : 0};
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    if (O::better(s4[x], v[q][x])) {
+                        v[q][x] = s4[x];
+                        cd[q][x] = c4[x];
+                    }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < MERGE_BATCH; ++q) {
+            const int e = ((q0 + q) * TTHREADS + tid) * 4;
+            const int m = m0 + e / BN, n = n0 + e % BN;
+            if (m >= p.M) continue;
+            float* crow = p.C + oc + (int64_t)m * p.sCm;
+            if (p.vecC && n + 3 < p.N) {
+                *reinterpret_cast<float4*>(crow + n) = make_float4(v[q][0], v[q][1], v[q][2], v[q][3]);
+            } else {
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    if (n + x < p.N) crow[(int64_t)(n + x) * p.sCn] = v[q][x];
+            }
+            if (ARG) {
+                int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+                if (p.vecI && n + 3 < p.N) {
+                    *reinterpret_cast<int4*>(irow + n) = make_int4(-cd[q][0], -cd[q][1], -cd[q][2], -cd[q][3]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        if (n + x < p.N) irow[(int64_t)(n + x) * p.sIn] = -cd[q][x];
+                }
+            }
+        }
+    }
+}
+
+// ARG: besides C, writes into I the chunk that holds each output's first maximum as
+// -(chunk + 1), or 0 when no product beat the semiring zero; k_argmax_resolve then
+// replaces the chunk by the exact index.  Stream-K segments go to the workspace instead.
 template <int SR, bool ARG>
 __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 {
@@ -134,13 +257,36 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
     __shared__ __align__(16) float Bs[2][BK][BN];
     __shared__ uint16_t sid[ARG ? TM * TN : 1][ARG ? TTHREADS : 1];
 
+    __shared__ int s_last;
+
+    pdl_signal();  // the resolve pass may start filling SMs as this grid drains
     const int tid = threadIdx.x;
     const int tm = tid / (BN / TN), tn = tid % (BN / TN);
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-    const int nkt = (p.K + BK - 1) / BK;
     const float zero = O::zero();
+    const bool sk = blockIdx.x >= p.T_dp;
+    const uint32_t j = sk ? blockIdx.x - p.T_dp : 0;
+    uint32_t u = sk ? j * p.L : 0;
+    const uint32_t ue = sk ? min(p.U, u + p.L) : 0;
 
-    for (uint32_t b = blockIdx.z; b < p.nbatch; b += gridDim.z) {
+    for (int pass = 0; pass < 2; ++pass) {
+        uint32_t t;
+        int kt0, kt1;
+        if (!sk) {
+            if (pass) break;
+            t = blockIdx.x;
+            kt0 = 0;
+            kt1 = (int)p.nkt;
+        } else {
+            if (u >= ue) break;
+            const uint32_t tl = fdiv(u, p.div_nkt);
+            kt0 = (int)(u - tl * p.nkt);
+            kt1 = (int)min(p.nkt, (uint32_t)kt0 + (ue - u));
+            u += (uint32_t)(kt1 - kt0);
+            t = p.T_dp + tl;
+        }
+        uint32_t b;
+        int m0, n0;
+        tile_coord(p, t, b, m0, n0);
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
         const float* __restrict__ A = p.A + oa;
@@ -199,23 +345,22 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
         };
 
         float best[TM][TN];
-        float snap[ARG ? TM : 1][ARG ? TN : 1];
+        float snap[ARG ? TM : 1][ARG ? TN : 1];  // the second accumulator set (ARG)
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) {
-                best[i][j] = zero;
-                if (ARG) snap[ARG ? i : 0][ARG ? j : 0] = zero;
-            }
+            for (int jj = 0; jj < TN; ++jj) best[i][jj] = zero;
 
-        issue_b(0, 0);
-        load_a(0);
+        // the stage buffers are free here: every thread passed the last loop barrier of the
+        // previous pass after its final reads
+        issue_b(kt0, 0);
+        load_a(kt0);
         store_a(0);
         cp_async_wait_all();
         __syncthreads();
-        for (int kt = 0; kt < nkt; ++kt) {
-            const int buf = kt & 1;
-            if (kt + 1 < nkt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
+            const int buf = (kt - kt0) & 1;
+            if (kt + 1 < kt1) {
                 issue_b(kt + 1, buf ^ 1);
                 load_a(kt + 1);
             }
@@ -227,7 +372,7 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
                     const float4 y = *reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + tm * 4]);
                     const float4 x1 = *reinterpret_cast<const float4*>(&As[buf][kk + 1][tm * 4]);
                     const float4 y1 = *reinterpret_cast<const float4*>(&As[buf][kk + 1][BM / 2 + tm * 4]);
-                    const float4 u = *reinterpret_cast<const float4*>(&Bs[buf][kk][tn * 4]);
+                    const float4 uu = *reinterpret_cast<const float4*>(&Bs[buf][kk][tn * 4]);
                     const float4 v = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tn * 4]);
                     const float4 u1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][tn * 4]);
                     const float4 v1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][BN / 2 + tn * 4]);
@@ -235,88 +380,228 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
                     a0[4] = y.x; a0[5] = y.y; a0[6] = y.z; a0[7] = y.w;
                     a1[0] = x1.x; a1[1] = x1.y; a1[2] = x1.z; a1[3] = x1.w;
                     a1[4] = y1.x; a1[5] = y1.y; a1[6] = y1.z; a1[7] = y1.w;
-                    b0[0] = u.x; b0[1] = u.y; b0[2] = u.z; b0[3] = u.w;
+                    b0[0] = uu.x; b0[1] = uu.y; b0[2] = uu.z; b0[3] = uu.w;
                     b0[4] = v.x; b0[5] = v.y; b0[6] = v.z; b0[7] = v.w;
                     b1[0] = u1.x; b1[1] = u1.y; b1[2] = u1.z; b1[3] = u1.w;
                     b1[4] = v1.x; b1[5] = v1.y; b1[6] = v1.z; b1[7] = v1.w;
                 }
-#pragma unroll
-                for (int i = 0; i < TM; ++i)
-#pragma unroll
-                    for (int j = 0; j < TN; j += 2) {
-                        const float2 t0 = O::mul2(make_float2(a0[i], a0[i]), make_float2(b0[j], b0[j + 1]));
-                        const float2 t1 = O::mul2(make_float2(a1[i], a1[i]), make_float2(b1[j], b1[j + 1]));
-                        best[i][j] = O::fold3(best[i][j], t0.x, t1.x);
-                        best[i][j + 1] = O::fold3(best[i][j + 1], t0.y, t1.y);
-                    }
-                if (ARG && (kk + 2) % CH == 0) {
-                    // end of a chunk: a strict improvement over the chunk-start value marks it
-                    const uint16_t chunk = (uint16_t)((kt * BK + kk + 2) / CH - 1);
+                if constexpr (!ARG) {
 #pragma unroll
                     for (int i = 0; i < TM; ++i)
 #pragma unroll
-                        for (int j = 0; j < TN; ++j) {
-                            float& s = snap[ARG ? i : 0][ARG ? j : 0];
-                            if (O::better(best[i][j], s)) sid[i * TN + j][tid] = chunk;
-                            s = best[i][j];
+                        for (int jj = 0; jj < TN; jj += 2) {
+                            const float2 t0 = O::mul2(make_float2(a0[i], a0[i]), make_float2(b0[jj], b0[jj + 1]));
+                            const float2 t1 = O::mul2(make_float2(a1[i], a1[i]), make_float2(b1[jj], b1[jj + 1]));
+                            best[i][jj] = O::fold3(best[i][jj], t0.x, t1.x);
+                            best[i][jj + 1] = O::fold3(best[i][jj + 1], t0.y, t1.y);
                         }
+                } else {
+                    // The two accumulator sets swap roles every chunk: the first fold of a chunk
+                    // reads the running result from one set and writes the other, so at the
+                    // chunk's end the set it came from still holds the chunk-start value to
+                    // compare against -- no snapshot copy.  Chunks per k-tile are even, so the
+                    // running result is back in `best` at every k-tile boundary.
+                    const bool odd = ((kk / CH) & 1) != 0;
+                    const bool first = (kk % CH) == 0;
+                    float(&src_)[TM][TN] = odd ? snap : best;
+                    float(&dst_)[TM][TN] = odd ? best : snap;
+#pragma unroll
+                    for (int i = 0; i < TM; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < TN; jj += 2) {
+                            const float2 t0 = O::mul2(make_float2(a0[i], a0[i]), make_float2(b0[jj], b0[jj + 1]));
+                            const float2 t1 = O::mul2(make_float2(a1[i], a1[i]), make_float2(b1[jj], b1[jj + 1]));
+                            dst_[i][jj] = O::fold3(first ? src_[i][jj] : dst_[i][jj], t0.x, t1.x);
+                            dst_[i][jj + 1] = O::fold3(first ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y, t1.y);
+                        }
+                    if ((kk + 2) % CH == 0) {
+                        // end of a chunk: a strict improvement over the chunk-start value marks it
+                        const uint16_t chunk = (uint16_t)((kt * BK + kk + 2) / CH - 1);
+#pragma unroll
+                        for (int i = 0; i < TM; ++i)
+#pragma unroll
+                            for (int jj = 0; jj < TN; ++jj)
+                                if (O::better(dst_[i][jj], src_[i][jj])) sid[i * TN + jj][tid] = chunk;
+                    }
                 }
             }
-            if (kt + 1 < nkt) store_a(buf ^ 1);
+            if (kt + 1 < kt1) store_a(buf ^ 1);
             cp_async_wait_all();
             __syncthreads();
         }
 
-        // ---------------- store values (and chunk + 1) through the output strides
+        if (!sk) {
+            // ---------------- store values (and -(chunk + 1)) through the output strides
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int m = m0 + row_of(tm, i);
-            if (m >= p.M) continue;
-            float* crow = p.C + oc + (int64_t)m * p.sCm;
-            int32_t* irow = ARG ? p.I + oi + (int64_t)m * p.sIm : nullptr;
-            int32_t code[TN];
-            if (ARG) {
-#pragma unroll
-                for (int j = 0; j < TN; ++j) code[j] = best[i][j] != zero ? (int32_t)sid[i * TN + j][tid] + 1 : 0;
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int n = n0 + (h ? BN / 2 : 0) + tn * 4;
-                if (p.vecC && n + 3 < p.N) {
-                    *reinterpret_cast<float4*>(crow + n) =
-                        make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (n + q < p.N) crow[(int64_t)(n + q) * p.sCn] = best[i][4 * h + q];
-                }
+            for (int i = 0; i < TM; ++i) {
+                const int m = m0 + row_of(tm, i);
+                if (m >= p.M) continue;
+                float* crow = p.C + oc + (int64_t)m * p.sCm;
+                int32_t* irow = ARG ? p.I + oi + (int64_t)m * p.sIm : nullptr;
+                int32_t code[TN];
                 if (ARG) {
-                    if (p.vecI && n + 3 < p.N) {
-                        *reinterpret_cast<int4*>(irow + n) =
-                            make_int4(code[4 * h], code[4 * h + 1], code[4 * h + 2], code[4 * h + 3]);
+#pragma unroll
+                    for (int jj = 0; jj < TN; ++jj)
+                        code[jj] = best[i][jj] != zero ? -((int32_t)sid[i * TN + jj][tid] + 1) : 0;
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = n0 + (h ? BN / 2 : 0) + tn * 4;
+                    if (p.vecC && n + 3 < p.N) {
+                        *reinterpret_cast<float4*>(crow + n) =
+                            make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
                     } else {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            if (n + q < p.N) irow[(int64_t)(n + q) * p.sIn] = code[4 * h + q];
+                            if (n + q < p.N) crow[(int64_t)(n + q) * p.sCn] = best[i][4 * h + q];
+                    }
+                    if (ARG) {
+                        if (p.vecI && n + 3 < p.N) {
+                            *reinterpret_cast<int4*>(irow + n) =
+                                make_int4(code[4 * h], code[4 * h + 1], code[4 * h + 2], code[4 * h + 3]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (n + q < p.N) irow[(int64_t)(n + q) * p.sIn] = code[4 * h + q];
+                        }
                     }
                 }
             }
+        } else {
+            // ---------------- stream-K segment: the whole 64x64 tile, row-major, to workspace
+            float* sv = p.seg_v + ((size_t)j * 2 + pass) * TILE_ELEMS;
+            uint16_t* sc = ARG ? p.seg_c + ((size_t)j * 2 + pass) * TILE_ELEMS : nullptr;
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const int r = row_of(tm, i);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = (h ? BN / 2 : 0) + tn * 4;
+                    *reinterpret_cast<float4*>(sv + r * BN + c) =
+                        make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
+                    if (ARG) {
+                        uint32_t cd[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            cd[q] = best[i][4 * h + q] != zero ? (uint32_t)sid[i * TN + 4 * h + q][tid] + 1u : 0u;
+                        *reinterpret_cast<uint2*>(sc + r * BN + c) = make_uint2(cd[0] | (cd[1] << 16), cd[2] | (cd[3] << 16));
+                    }
+                }
+            }
+            // arrival ticket: the last CTA to finish a segment of this tile merges them
+            const uint32_t tl = t - p.T_dp;
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t j0, j1;
+                int slot0;
+                sk_segments(p, tl, j0, j1, slot0);
+                const bool last = atomicAdd(&p.sk_cnt[tl], 1u) == j1 - j0;
+                if (last) p.sk_cnt[tl] = 0;  // zero again for the next launch on this stream
+                s_last = last;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                sk_merge<SR, ARG>(p, tl, m0, n0, oc, oi, tid);
+            }
         }
-        // no barrier needed: the next batch iteration starts by writing stage 0, which every
-        // thread finished reading before the last loop barrier
     }
 }
 
 // ------------------------------------------------------------------ argmax resolve
-// One CTA (256 threads) per 64x64 output tile.  Each thread holds 16 outputs of
-// the tile (4 rows x 4 consecutive columns) in registers: value and chunk
-// code.  B's rows are staged into shared memory 256 k at a time; for each of
-// its outputs whose chunk lies in the staged group a thread recomputes the
-// chunk's CH products -- A's contiguous row segment through L1, B's column
-// from shared memory -- and keeps the first k whose product equals the value.
-// Results go back from registers with coalesced stores.
-constexpr int RTHREADS = 256, RGK = 256;
+// Replaces each pending chunk by the exact first index.  The CTAs split the rows of all
+// 64-column panels (batch, column tile) evenly.  For each panel a CTA stages B's rows for
+// those columns into shared memory, RGK rows at a time; warp w then takes rows in steps of
+// RR, lane l owning columns l and l + 32 -- so the staged reads B[k][n] of a warp hit 32
+// distinct banks whatever chunk each lane needs.  An output whose chunk lies in the staged
+// group recomputes that chunk's CH products, A's contiguous segment coming through L1, and
+// keeps the first k whose product equals the value.  The (C, I) loads of a warp's next row
+// step are issued before the current step's search.  Launched as a programmatic dependent
+// of the GEMM, a CTA stages its first B rows before waiting for the GEMM's results.
+constexpr int RTHREADS = 256, RWARPS = RTHREADS / 32, RGK = 256;
+constexpr int RR = CH <= 8 ? 4 : 2;  // rows per warp step: RR x 2 outputs per lane
 constexpr size_t SMEM_RESOLVE = sizeof(float) * RGK * BN;  // 64 KiB
+static_assert(RGK % CH == 0, "a chunk never straddles two staged groups");
+
+// The rows mb .. me-1 of one staged group, for the common layout: C and I with unit column
+// stride, every chunk whole (K a multiple of CH) and A's segments 16-byte aligned.  Branch
+// free per output: a dead output (no pending chunk in this group) loads A's first segment,
+// searches B's first staged rows and stores nothing.
+template <int SR>
+__device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const float (*EB)[BN],
+                                                  const float* __restrict__ A, const float* __restrict__ Cb,
+                                                  int32_t* __restrict__ Ib, int n0, int mb, int me, int k0,
+                                                  int kn, int warp, int lane)
+{
+    using O = Ops<SR>;
+    const bool col0 = n0 + lane < p.N, col1 = n0 + 32 + lane < p.N;
+    const float* __restrict__ cb = Cb + n0 + lane;
+    int32_t* __restrict__ ib = Ib + n0 + lane;
+    float nval[RR][2];
+    int32_t ncode[RR][2];
+    auto load_step = [&](int ms) {
+#pragma unroll
+        for (int r = 0; r < RR; ++r) {
+            const int m = ms + r;
+            const float* cr = cb + (int64_t)m * p.sCm;
+            const int32_t* ir = ib + (int64_t)m * p.sIm;
+            const bool ok0 = m < me && col0, ok1 = m < me && col1;
+            nval[r][0] = ok0 ? cr[0] : 0.0f;
+            nval[r][1] = ok1 ? cr[32] : 0.0f;
+            ncode[r][0] = ok0 ? ir[0] : 0;
+            ncode[r][1] = ok1 ? ir[32] : 0;
+        }
+    };
+    int ms = mb + warp * RR;
+    if (ms < me) load_step(ms);
+    for (; ms < me; ms += RWARPS * RR) {
+        float val[RR][2];
+        int ka[RR][2];
+        bool live[RR][2];
+#pragma unroll
+        for (int r = 0; r < RR; ++r)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                val[r][h] = nval[r][h];
+                const int kc = (-ncode[r][h] - 1) * CH;
+                live[r][h] = ncode[r][h] < 0 && kc >= k0 && kc < k0 + kn;
+                ka[r][h] = live[r][h] ? kc : k0;
+            }
+        if (ms + RWARPS * RR < me) load_step(ms + RWARPS * RR);
+        float av[RR][2][CH];
+#pragma unroll
+        for (int r = 0; r < RR; ++r) {
+            // a row past me (end of the range) reads row mb instead: always inside A
+            const float* arow = A + (int64_t)(ms + r < me ? ms + r : mb) * p.sAm;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int kk = 0; kk < CH; kk += 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(arow + ka[r][h] + kk));
+                    av[r][h][kk] = x.x;
+                    av[r][h][kk + 1] = x.y;
+                    av[r][h][kk + 2] = x.z;
+                    av[r][h][kk + 3] = x.w;
+                }
+        }
+#pragma unroll
+        for (int r = 0; r < RR; ++r)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float* eb = &EB[ka[r][h] - k0][h * 32 + lane];
+                int idx = 0;
+#pragma unroll
+                for (int kk = CH - 2; kk >= 0; kk -= 2) {
+                    const float2 t = O::mul2(make_float2(av[r][h][kk], av[r][h][kk + 1]),
+                                             make_float2(eb[kk * BN], eb[(kk + 1) * BN]));
+                    idx = t.y == val[r][h] ? kk + 1 : idx;
+                    idx = t.x == val[r][h] ? kk : idx;
+                }
+                if (live[r][h]) ib[(int64_t)(ms + r) * p.sIm + h * 32] = ka[r][h] + idx;
+            }
+    }
+}
 
 template <int SR>
 __global__ void __launch_bounds__(RTHREADS, 2) k_argmax_resolve(TiledParams p)
@@ -324,55 +609,40 @@ __global__ void __launch_bounds__(RTHREADS, 2) k_argmax_resolve(TiledParams p)
     using O = Ops<SR>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float(*EB)[BN] = reinterpret_cast<float(*)[BN]>(smem_raw);
-    const int tid = threadIdx.x;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint64_t ubeg = (uint64_t)blockIdx.x * p.r_units / gridDim.x;
+    const uint64_t uend = (uint64_t)(blockIdx.x + 1) * p.r_units / gridDim.x;
     const int ngr = (p.K + RGK - 1) / RGK;
-    // my outputs: rows rr + 16*r (r < 4), columns cc .. cc+3
-    const int rr = tid / 16, cc = (tid % 16) * 4;
-    for (uint32_t b = blockIdx.z; b < p.nbatch; b += gridDim.z) {
+    // common layout: unit column strides, whole chunks, 16-byte aligned A segments
+    const bool fast = p.vecA && p.K % CH == 0 && p.sCn == 1 && p.sIn == 1;
+    bool waited = false;
+    for (uint64_t u = ubeg; u < uend;) {
+        // rows mb .. me-1 of panel pn
+        const uint64_t pn = u / (uint64_t)p.M;
+        const int mb = (int)(u - pn * (uint64_t)p.M);
+        const int me = (int)min((uint64_t)p.M, (uint64_t)mb + (uend - u));
+        u += (uint64_t)(me - mb);
+        const uint32_t b = (uint32_t)(pn / p.tiles_n);
+        const int n0 = (int)(pn - (uint64_t)b * p.tiles_n) * BN;
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
         const float* __restrict__ A = p.A + oa;
         const float* __restrict__ B = p.B + ob;
-        float val[4][4];
-        int code[4][4];
+        const float* __restrict__ Cb = p.C + oc;
+        int32_t* __restrict__ Ib = p.I + oi;
+        bool colok[2];
+        int64_t offC[2], offI[2];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int m = m0 + rr + 16 * r, n = n0 + cc;
-            const float* crow = p.C + oc + (int64_t)m * p.sCm;
-            const int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
-            if (m < p.M && n + 3 < p.N && p.vecC && p.vecI) {
-                const float4 c4 = *reinterpret_cast<const float4*>(crow + n);
-                const int4 i4 = *reinterpret_cast<const int4*>(irow + n);
-                val[r][0] = c4.x; val[r][1] = c4.y; val[r][2] = c4.z; val[r][3] = c4.w;
-                code[r][0] = i4.x; code[r][1] = i4.y; code[r][2] = i4.z; code[r][3] = i4.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool in = m < p.M && n + j < p.N;
-                    val[r][j] = in ? crow[(int64_t)(n + j) * p.sCn] : 0.0f;
-                    code[r][j] = in ? irow[(int64_t)(n + j) * p.sIn] : 0;
-                }
-            }
+        for (int h = 0; h < 2; ++h) {
+            const int n = n0 + h * 32 + lane;
+            colok[h] = n < p.N;
+            offC[h] = (int64_t)n * p.sCn;
+            offI[h] = (int64_t)n * p.sIn;
         }
-        int res[4][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) res[r][j] = 0;  // code 0: nothing beat the zero, argmax 0
         for (int g = 0; g < ngr; ++g) {
             const int k0 = g * RGK;
             const int kn = min(RGK, p.K - k0);
-            bool any = false;
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int ch = code[r][j] - 1;
-                    any |= ch >= 0 && ch * CH >= k0 && ch * CH < k0 + RGK;
-                }
-            if (!__syncthreads_or(any)) continue;
-            // stage B rows k0 .. k0+kn of this tile's columns (zero outside the operand)
+            __syncthreads();  // every warp is done with the rows staged before
             for (int e = tid; e < kn * (BN / 4); e += RTHREADS) {
                 const int kk = e / (BN / 4), nq = (e % (BN / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
                 float* dst = &EB[kk][nq];
@@ -388,64 +658,73 @@ __global__ void __launch_bounds__(RTHREADS, 2) k_argmax_resolve(TiledParams p)
             cp_async_commit();
             cp_async_wait_all();
             __syncthreads();
+            if (!waited) {
+                pdl_wait();  // C and I come from the GEMM grid (B above is its input)
+                waited = true;
+            }
+
+            if (fast) {
+                resolve_rows_fast<SR>(p, EB, A, Cb, Ib, n0, mb, me, k0, kn, warp, lane);
+                continue;
+            }
+            float nval[RR][2];
+            int32_t ncode[RR][2];
+            auto load_step = [&](int ms) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int m = m0 + rr + 16 * r;
-                const float* arow = A + (int64_t)m * p.sAm;
-                // the four columns' A segments: all loads in flight before any search
-                float av[4][CH];
-                int ka[4];
-                bool live[4];
+                for (int r = 0; r < RR; ++r) {
+                    const int m = ms + r;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int ch = code[r][j] - 1;
-                    live[j] = ch >= 0 && ch * CH >= k0 && ch * CH < k0 + RGK;
-                    ka[j] = live[j] ? ch * CH : 0;
-                    const float* src = live[j] ? arow + ka[j] : A;
-                    const int kmax = live[j] ? min(CH, p.K - ka[j]) : 0;
-                    if (p.vecA && kmax == CH) {
+                    for (int h = 0; h < 2; ++h) {
+                        const bool in = m < me && colok[h];
+                        nval[r][h] = in ? Cb[(int64_t)m * p.sCm + offC[h]] : 0.0f;
+                        ncode[r][h] = in ? Ib[(int64_t)m * p.sIm + offI[h]] : 0;
+                    }
+                }
+            };
+            int ms = mb + warp * RR;
+            if (ms < me) load_step(ms);
+            for (; ms < me; ms += RWARPS * RR) {
+                float val[RR][2];
+                int ka[RR][2];  // first k of the pending chunk, or -1
 #pragma unroll
-                        for (int kk = 0; kk < CH; kk += 4) {
-                            const float4 x = __ldg(reinterpret_cast<const float4*>(src + kk));
-                            av[j][kk] = x.x;
-                            av[j][kk + 1] = x.y;
-                            av[j][kk + 2] = x.z;
-                            av[j][kk + 3] = x.w;
-                        }
-                    } else {
+                for (int r = 0; r < RR; ++r)
 #pragma unroll
-                        for (int kk = 0; kk < CH; ++kk) av[j][kk] = kk < kmax ? __ldg(src + kk) : 0.0f;
+                    for (int h = 0; h < 2; ++h) {
+                        val[r][h] = nval[r][h];
+                        const int kc = (-ncode[r][h] - 1) * CH;  // ncode < 0: chunk -ncode-1
+                        ka[r][h] = (ncode[r][h] < 0 && kc >= k0 && kc < k0 + kn) ? kc : -1;
+                    }
+                if (ms + RWARPS * RR < me) load_step(ms + RWARPS * RR);
+                float av[RR][2][CH];
+#pragma unroll
+                for (int r = 0; r < RR; ++r) {
+                    const float* arow = A + (int64_t)(ms + r) * p.sAm;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int kmax = ka[r][h] >= 0 ? min(CH, p.K - ka[r][h]) : 0;
+                        const float* src = arow + (ka[r][h] >= 0 ? ka[r][h] : 0);
+#pragma unroll
+                        for (int kk = 0; kk < CH; ++kk) av[r][h][kk] = kk < kmax ? __ldg(src + kk) : 0.0f;
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (!live[j]) continue;
-                    const int kl = ka[j] - k0, c = cc + j;
-                    const int kmax = min(CH, p.K - ka[j]);
-                    const float target = val[r][j];
-                    int idx = 0;
+                for (int r = 0; r < RR; ++r)
 #pragma unroll
-                    for (int kk = CH - 1; kk >= 0; --kk)
-                        if (kk < kmax && O::mul(av[j][kk], EB[kl + kk][c]) == target) idx = kk;
-                    res[r][j] = ka[j] + idx;
-                }
-            }
-            __syncthreads();  // before the next group overwrites the staged rows
-        }
+                    for (int h = 0; h < 2; ++h) {
+                        if (ka[r][h] < 0) continue;
+                        const int kl = ka[r][h] - k0, c = h * 32 + lane;
+                        const int kmax = min(CH, p.K - ka[r][h]);
+                        int idx = 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int m = m0 + rr + 16 * r, n = n0 + cc;
-            if (m >= p.M) continue;
-            int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
-            if (n + 3 < p.N && p.vecI) {
-                *reinterpret_cast<int4*>(irow + n) = make_int4(res[r][0], res[r][1], res[r][2], res[r][3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (n + j < p.N) irow[(int64_t)(n + j) * p.sIn] = res[r][j];
+                        for (int kk = CH - 1; kk >= 0; --kk)
+                            if (kk < kmax && O::mul(av[r][h][kk], EB[kl + kk][c]) == val[r][h]) idx = kk;
+                        Ib[(int64_t)(ms + r) * p.sIm + offI[h]] = ka[r][h] + idx;
+                    }
             }
         }
     }
+    // every CTA waits once, so this grid ends after the GEMM grid whatever its row range
+    if (!waited) pdl_wait();
 }
 
 // ------------------------------------------------------------------ stream kernel
@@ -609,9 +888,32 @@ Batch make_batch(const GemmDesc& g, int64_t& nbatch)
     return bt;
 }
 
-template <int SR, bool ARG>
-int run_tiled(const GemmDesc& g, cudaStream_t s)
+// Resident CTAs per SM of a kernel (looked up once per kernel).
+int resident_ctas(const void* fn, int threads, size_t smem, std::atomic<int>& cache)
 {
+    int occ = cache.load(std::memory_order_relaxed);
+    if (occ > 0) return occ;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, smem);
+    if (e != cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        occ = 1;
+    }
+    cache.store(occ, std::memory_order_relaxed);
+    return occ;
+}
+
+// Stream-K only when the last wave would run at most this full (percent); each stream-K
+// CTA gets at least SK_MIN_UNITS k-tiles (unless a tile has fewer) and a tile is cut into at
+// most SK_MAX_SEGS segments.
+#ifndef TROP_SK_MAX_FILL_PCT
+#define TROP_SK_MAX_FILL_PCT 85
+#endif
+constexpr uint64_t SK_MAX_FILL_PCT = TROP_SK_MAX_FILL_PCT, SK_MIN_UNITS = 4, SK_MAX_SEGS = 32;
+
+template <int SR, bool ARG>
+int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
+{
+    static std::atomic<int> occ_gemm{0}, occ_resolve{0};
     TiledParams p{};
     p.M = (int)g.M;
     p.N = (int)g.N;
@@ -643,15 +945,73 @@ int run_tiled(const GemmDesc& g, cudaStream_t s)
     p.vecB = vb;
     p.vecC = vc;
     p.vecI = vi;
-    dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM),
-              (unsigned)(nbatch < 65535 ? nbatch : 65535));
-    k_gemm_tiled<SR, ARG><<<grid, TTHREADS, 0, s>>>(p);
-    TROP_TRY(check_launch("k_gemm_tiled"));
-    if (ARG) {
-        k_argmax_resolve<SR><<<grid, RTHREADS, SMEM_RESOLVE, s>>>(p);
-        TROP_TRY(check_launch("k_argmax_resolve"));
+    p.tiles_m = (uint32_t)((g.M + BM - 1) / BM);
+    p.tiles_n = (uint32_t)((g.N + BN - 1) / BN);
+    p.nkt = (uint32_t)((g.K + BK - 1) / BK);
+    p.div_tm = make_fastdiv(p.tiles_m);
+    p.div_tn = make_fastdiv(p.tiles_n);
+    p.div_nkt = make_fastdiv(p.nkt);
+    const uint64_t T = (uint64_t)nbatch * p.tiles_m * p.tiles_n;  // < 2^31 (route check)
+
+    // ---- schedule: whole tiles for the full waves, stream-K for a thin last wave
+    const uint64_t G = (uint64_t)dev->sm_count *
+                       resident_ctas((const void*)k_gemm_tiled<SR, ARG>, TTHREADS, 0, occ_gemm);
+    const uint64_t R = T % G;
+    uint64_t G_sk = 0;
+    void* ws = nullptr;
+    // With argmax the merge of a split tile sits on the tail's critical path; measured on
+    // batched 256^3 problems it paid off only when the whole problem is under half a wave.
+    const bool sk_ok = !ARG || T * 2 <= G;
+    if (sk_ok && R > 0 && R * 100 <= G * SK_MAX_FILL_PCT && R * p.nkt < (uint64_t(1) << 31)) {
+        const uint64_t U = R * p.nkt;
+        // at least SK_MIN_UNITS k-tiles and at most SK_MAX_SEGS segments per tile; L <= nkt as R < G
+        const uint64_t L = std::max({(U + G - 1) / G, std::min<uint64_t>(SK_MIN_UNITS, p.nkt),
+                                     (p.nkt + SK_MAX_SEGS - 1) / SK_MAX_SEGS});
+        const uint64_t n_sk = (U + L - 1) / L;
+        if (n_sk > R) {
+            const size_t seg_elems = (size_t)n_sk * 2 * TILE_ELEMS;
+            uint32_t* cnt = nullptr;
+            if (stream_tickets(s, (size_t)R, &cnt) == TROP_OK &&
+                pool_alloc(seg_elems * (sizeof(float) + (ARG ? sizeof(uint16_t) : 0)), s, &ws) == TROP_OK) {
+                G_sk = n_sk;
+                p.L = (uint32_t)L;
+                p.U = (uint32_t)U;
+                p.div_L = make_fastdiv(p.L);
+                p.seg_v = static_cast<float*>(ws);
+                p.seg_c = ARG ? reinterpret_cast<uint16_t*>(p.seg_v + seg_elems) : nullptr;
+                p.sk_cnt = cnt;
+            } else {
+                clear_error();  // no workspace: whole tiles only
+                ws = nullptr;
+            }
+        }
     }
-    return TROP_OK;
+    p.T_dp = (uint32_t)(G_sk ? T - R : T);
+
+    k_gemm_tiled<SR, ARG><<<(unsigned)(p.T_dp + G_sk), TTHREADS, 0, s>>>(p);
+    int rc = check_launch("k_gemm_tiled");
+    if (rc == TROP_OK && ARG) {
+        p.r_units = (uint64_t)nbatch * p.tiles_n * (uint64_t)g.M;
+        const uint64_t slots = (uint64_t)dev->sm_count *
+                               resident_ctas((const void*)k_argmax_resolve<SR>, RTHREADS, SMEM_RESOLVE, occ_resolve);
+        const uint64_t want = (p.r_units + RWARPS * RR - 1) / (RWARPS * RR);
+        // programmatic dependent launch: its CTAs stage B while the GEMM drains
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)std::max<uint64_t>(1, std::min(slots, want)));
+        cfg.blockDim = dim3(RTHREADS);
+        cfg.dynamicSmemBytes = SMEM_RESOLVE;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, k_argmax_resolve<SR>, p);
+        if (e != cudaSuccess) rc = cuda_error(e, "k_argmax_resolve");
+        else rc = check_launch("k_argmax_resolve");
+    }
+    if (ws) pool_retire(ws, s);
+    return rc;
 }
 
 template <int SR, bool ARG>
@@ -771,8 +1131,10 @@ Route choose(const GemmDesc& g, bool& swap)
     const bool fits32 = g.M < (1 << 30) && g.N < (1 << 30) && g.K < (1 << 30) && nbatch < (int64_t(1) << 31);
     // the argmax epilogue keeps chunk numbers in 16 bits
     const bool big = g.M >= 16 && g.N >= 16 && g.K >= 8 && (!g.I || g.K <= (int64_t)CH * 65535);
-    const bool grid_ok = (g.M + BM - 1) / BM <= 65535 && (g.N + BN - 1) / BN <= 65535;
-    const bool grid_ok_t = (g.N + BM - 1) / BM <= 65535 && (g.M + BN - 1) / BN <= 65535;
+    // tiles in a 1-D grid, with room for the stream-K CTAs
+    const int64_t tiles = nbatch * ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+    const bool grid_ok = tiles < (int64_t(1) << 30);
+    const bool grid_ok_t = grid_ok;
     if (fits32 && big) {
         if (g.sAk == 1 && g.sBn == 1 && grid_ok) return R_TILED;
         if (g.sBk == 1 && g.sAm == 1 && grid_ok_t) {
@@ -799,7 +1161,7 @@ int run(const GemmDesc& g0, cudaStream_t s, const DeviceInfo* dev, const char** 
     switch (r) {
     case R_TILED:
         if (name) *name = "k_gemm_tiled";
-        return run_tiled<SR, ARG>(g, s);
+        return run_tiled<SR, ARG>(g, s, dev);
     case R_STREAM:
         if (name) *name = "k_gemm_stream";
         return run_stream<SR, ARG>(g, s, dev);

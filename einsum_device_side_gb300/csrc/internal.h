@@ -49,6 +49,9 @@ enum { ST_ALLOC, ST_HIT, ST_MALLOC, ST_RETIRED, ST_RELEASED, ST_EVWAIT, ST_LEAKE
 int pool_alloc(size_t bytes, cudaStream_t stream, void** out);
 void pool_retire(void* ptr, cudaStream_t stream);
 
+// Zeroed per-stream counters for atomic arrival tickets (the kernels reset them to zero).
+int stream_tickets(cudaStream_t s, size_t count, uint32_t** out);
+
 // ---------------------------------------------------------------- fast divmod
 // Unsigned 32-bit division by a runtime-invariant divisor with a
 // precomputed multiplier (Granlund & Montgomery, "Division by invariant

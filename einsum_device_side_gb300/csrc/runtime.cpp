@@ -369,6 +369,58 @@ extern "C" int tropical_init(int device)
     return rc;
 }
 
+// ------------------------------------------------------------------ per-stream tile tickets
+// One zeroed uint32 array per (device, stream) for kernels whose CTAs count arrivals on a
+// tile with atomics and leave every counter at zero when they end.  Launches on one stream
+// run in order, so an array is never shared by two running launches.  Created on first use
+// (zeroed on that stream, so it is ready before the launch that follows), replaced by a
+// larger one when a launch needs more (the old array is freed by tropical_release_pool).
+namespace {
+struct Tickets {
+    std::mutex mu;
+    std::map<std::pair<int, cudaStream_t>, std::pair<uint32_t*, size_t>> arrays;
+    std::vector<std::pair<int, uint32_t*>> retired;
+};
+Tickets& tickets()
+{
+    static Tickets* t = new Tickets();
+    return *t;
+}
+}  // namespace
+
+int trop::stream_tickets(cudaStream_t s, size_t count, uint32_t** out)
+{
+    *out = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    Tickets& T = tickets();
+    std::lock_guard<std::mutex> lk(T.mu);
+    auto key = std::make_pair(dev, s);
+    auto it = T.arrays.find(key);
+    if (it != T.arrays.end() && it->second.second >= count) {
+        *out = it->second.first;
+        return TROP_OK;
+    }
+    const size_t n = (count + 4095) / 4096 * 4096;
+    uint32_t* p = nullptr;
+    e = cudaMalloc(&p, n * sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_error(e, "cudaMalloc (tile tickets)");
+    e = cudaMemsetAsync(p, 0, n * sizeof(uint32_t), s);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_error(e, "cudaMemsetAsync (tile tickets)");
+    }
+    if (it != T.arrays.end()) {
+        T.retired.emplace_back(dev, it->second.first);
+        it->second = std::make_pair(p, n);
+    } else {
+        T.arrays.emplace(key, std::make_pair(p, n));
+    }
+    *out = p;
+    return TROP_OK;
+}
+
 extern "C" int tropical_sync_pool(void)
 {
     clear_error();
@@ -390,6 +442,21 @@ extern "C" int tropical_release_pool(void)
         cudaSetDevice(kv.second.device);
         cudaFree(kv.second.ptr);
         P.cached_bytes -= kv.second.bytes;
+    }
+    {
+        // tile tickets: every launch that used them has finished (the caller synchronised)
+        Tickets& T = tickets();
+        std::lock_guard<std::mutex> lt(T.mu);
+        for (auto& kv : T.arrays) {
+            cudaSetDevice(kv.first.first);
+            cudaFree(kv.second.first);
+        }
+        for (auto& r : T.retired) {
+            cudaSetDevice(r.first);
+            cudaFree(r.second);
+        }
+        T.arrays.clear();
+        T.retired.clear();
     }
     cudaSetDevice(cur);
     P.free_.clear();

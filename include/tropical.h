@@ -247,7 +247,8 @@ int tropical_tree_backtrack(int n_inputs, const trop_tensor* inputs, int n_nodes
  * synchronize() is a drain point].  The only call that may block the host. */
 int tropical_sync_pool(void);
 
-/* Drain, then free every cached workspace block (teardown). */
+/* Drain, then free every cached workspace block and the per-stream arrival
+ * counters of the GEMM's split tiles (teardown). */
 int tropical_release_pool(void);
 
 int tropical_stats(trop_stats* out);
