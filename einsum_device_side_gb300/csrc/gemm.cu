@@ -13,23 +13,27 @@
 // Both are exact per element, so the result does not depend on the order in
 // which k is visited.
 //
-// Argmax without a compare per term: k is walked in chunks of 16 (one
-// shared-memory stage).  At the end of a chunk each output compares its
-// running result with a snapshot taken at the chunk's start; a strict
-// improvement stores the chunk number.  Because the running result only
-// grows (shrinks for min-plus), the last improving chunk holds the first k
-// that reaches the final value, and an epilogue recomputes just that chunk's
-// 16 products to find it.  If nothing beat the semiring zero the argmax is 0,
-// which is what a strict left-to-right scan gives.
+// Argmax without a compare per term: k is walked in chunks of CH = 8.  At the
+// end of a chunk each output compares its running result with the value it
+// had at the chunk's start; a strict improvement records the chunk number.
+// Because the running result only grows (shrinks for min-plus), the last
+// improving chunk holds the first k that reaches the final value, and a
+// second pass (k_argmax_resolve) recomputes just that chunk's CH products to
+// find it.  If nothing beat the semiring zero the argmax is 0, which is what
+// a strict left-to-right scan gives.
 //
 // Kernels:
-//   k_gemm_tiled   64x64 output tile per 64-thread CTA, 8x8 per thread,
-//                  A staged transposed and duplicated ({a,a} pairs) so the
-//                  packed add needs no register shuffles; needs sAk == 1
-//                  and sBn == 1 (the planner permutes other layouts).
-//   k_gemm_stream  few rows (M <= 8) and a short contraction (K <= 64):
-//                  one thread per (batch, column vector), memory bound.
-//   k_gemm_generic anything else: one thread per output, sequential k.
+//   k_gemm_tiled     64x64 output tile per 64-thread CTA, 8x8 per thread, A
+//                    staged transposed so the packed add takes {a,a} pairs
+//                    built in registers; needs sAk == 1 and sBn == 1 (the
+//                    planner permutes other layouts).  A thin last wave is
+//                    cut along k (stream-K, see the schedule below).
+//   k_argmax_resolve chunk -> exact index, rows of all column panels split
+//                    evenly over resident CTAs; launched as a programmatic
+//                    dependent of k_gemm_tiled.
+//   k_gemm_stream    few rows (M <= 8) and a short contraction (K <= 64):
+//                    one thread per (batch, column vector), memory bound.
+//   k_gemm_generic   anything else: one thread per output, sequential k.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -100,7 +104,6 @@ constexpr int APAD = 4;                          // float pad per transposed A r
 #endif
 constexpr int CH = TROP_ARG_CHUNK;               // k per argmax chunk (divides BK)
 static_assert(BK % CH == 0 && CH % 2 == 0, "chunk must divide the k-tile and hold whole k pairs");
-static_assert((BK / CH) % 2 == 0, "an even number of chunks per k-tile (the accumulator sets alternate)");
 
 // Tile schedule.  Tiles are numbered t = (b * tiles_m + mt) * tiles_n + nt.  CTA t < T_dp
 // computes tile t over the whole contraction.  When the last tiles would only part-fill a
@@ -349,7 +352,10 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int jj = 0; jj < TN; ++jj) best[i][jj] = zero;
+            for (int jj = 0; jj < TN; ++jj) {
+                best[i][jj] = zero;
+                if constexpr (ARG) snap[i][jj] = zero;
+            }
 
         // the stage buffers are free here: every thread passed the last loop barrier of the
         // previous pass after its final reads
@@ -401,8 +407,10 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
                     // chunk's end the set it came from still holds the chunk-start value to
                     // compare against -- no snapshot copy.  Chunks per k-tile are even, so the
                     // running result is back in `best` at every k-tile boundary.
-                    const bool odd = ((kk / CH) & 1) != 0;
-                    const bool first = (kk % CH) == 0;
+                    // (an odd number of chunks per k-tile keeps one set and copies it instead)
+                    constexpr bool alternate = (BK / CH) % 2 == 0;
+                    const bool odd = !alternate || ((kk / CH) & 1) != 0;
+                    const bool first = alternate && (kk % CH) == 0;
                     float(&src_)[TM][TN] = odd ? snap : best;
                     float(&dst_)[TM][TN] = odd ? best : snap;
 #pragma unroll
@@ -420,8 +428,10 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 #pragma unroll
                         for (int i = 0; i < TM; ++i)
 #pragma unroll
-                            for (int jj = 0; jj < TN; ++jj)
+                            for (int jj = 0; jj < TN; ++jj) {
                                 if (O::better(dst_[i][jj], src_[i][jj])) sid[i * TN + jj][tid] = chunk;
+                                if (!alternate) src_[i][jj] = dst_[i][jj];
+                            }
                     }
                 }
             }
@@ -519,8 +529,14 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
 // keeps the first k whose product equals the value.  The (C, I) loads of a warp's next row
 // step are issued before the current step's search.  Launched as a programmatic dependent
 // of the GEMM, a CTA stages its first B rows before waiting for the GEMM's results.
+#ifndef TROP_RESOLVE_RR
+#define TROP_RESOLVE_RR 4
+#endif
+#ifndef TROP_RESOLVE_MINB
+#define TROP_RESOLVE_MINB 2
+#endif
 constexpr int RTHREADS = 256, RWARPS = RTHREADS / 32, RGK = 256;
-constexpr int RR = CH <= 8 ? 4 : 2;  // rows per warp step: RR x 2 outputs per lane
+constexpr int RR = CH <= 8 ? TROP_RESOLVE_RR : 2;  // rows per warp step: RR x 2 outputs per lane
 constexpr size_t SMEM_RESOLVE = sizeof(float) * RGK * BN;  // 64 KiB
 static_assert(RGK % CH == 0, "a chunk never straddles two staged groups");
 
@@ -604,7 +620,7 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
 }
 
 template <int SR>
-__global__ void __launch_bounds__(RTHREADS, 2) k_argmax_resolve(TiledParams p)
+__global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(TiledParams p)
 {
     using O = Ops<SR>;
     extern __shared__ __align__(16) unsigned char smem_raw[];

@@ -139,3 +139,76 @@ def test_full_size_batched_workload_sampled(trop, sr):
     t = a_sel * b_sel if sr == 2 else a_sel + b_sel
     assert torch.equal(t, c)
     assert (i >= 0).all() and (i < 256).all()
+
+
+# ---------------------------------------------------------------- split tiles (stream-K) and the resolve pass
+
+@pytest.mark.parametrize("sr", SR)
+@pytest.mark.parametrize("batch", [64, 128])
+def test_split_tail_plain_full_size_sampled(trop, sr, batch):
+    """Batched 256^3 without argmax: the last partial wave is cut along k and the
+    segments merged by the last CTA to finish; sampled outputs vs the oracle."""
+    a, b = synth.gemm_batched_inputs(sr, batch=batch)
+    c = trop.gemm(_dev(a), _dev(b), sr, argmax=False)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(200 + sr + batch)
+    samples = rng.choice(c.numel(), size=20000, replace=False).astype(np.int64)
+    # the last tiles are the split ones: sample all of the final 64x64 tile too
+    tail = (c.numel() - 1 - np.arange(64)[:, None] * 256 - np.arange(64)[None, :]).reshape(-1)
+    samples = np.unique(np.concatenate([samples, tail]))
+    rc, _ = oracle.gemm(a, b, sr, samples=samples, nthreads=0)
+    assert c.reshape(-1).cpu().numpy()[samples].tobytes() == rc.tobytes()
+
+
+@pytest.mark.parametrize("sr", SR)
+@pytest.mark.parametrize("shape", [(1, 64, 64, 4096), (2, 100, 70, 2000), (1, 130, 64, 2001), (3, 64, 200, 520)])
+def test_split_k_long_contraction(trop, sr, shape):
+    """Few tiles and a long contraction: every tile is cut into many k segments
+    (up to 32), and the argmax resolve walks several staged groups of B rows;
+    K = 2001 is not a whole number of argmax chunks (generic resolve path)."""
+    bt, m, n, k = shape
+    a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+    _check(trop, a, b, sr)
+    c = trop.gemm(_dev(a), _dev(b), sr, argmax=False)
+    rc, _ = oracle.gemm(a, b, sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == rc.tobytes()
+
+
+def test_split_k_strided_output(trop):
+    """Output and argmax through transposed views (non-unit column strides): the
+    merge stores and the generic resolve path."""
+    a, b = synth.gemm_batched_inputs(0, batch=2, m=96, n=80, k=1536)
+    ct = torch.empty((2, 80, 96), device="cuda")
+    it = torch.empty((2, 80, 96), dtype=torch.int32, device="cuda")
+    c, i = ct.transpose(1, 2), it.transpose(1, 2)
+    trop.gemm(_dev(a), _dev(b), 0, out=c, out_argmax=i)
+    rc, ri = oracle.gemm(a, b, 0, nthreads=0)
+    np.testing.assert_array_equal(c.cpu().numpy(), rc)
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
+
+
+def test_split_gemms_on_two_streams(trop):
+    """Split GEMMs running at once on two streams use separate arrival counters:
+    results equal the same calls made one after another."""
+    work = []
+    for s, (bt, m, n, k, arg) in enumerate([(64, 256, 256, 256, False), (1, 64, 128, 3072, True),
+                                           (64, 256, 256, 256, False), (2, 64, 64, 2048, True)]):
+        a, b = synth.gemm_batched_inputs(s % 3, batch=bt, m=m, n=n, k=k)
+        work.append((s % 3, _dev(a), _dev(b), arg))
+    ref = []
+    for sr, ad, bd, arg in work:
+        ref.append(trop.gemm(ad, bd, sr, argmax=arg))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for rep in range(3):
+        for j, (sr, ad, bd, arg) in enumerate(work):
+            with torch.cuda.stream(streams[j % 2]):
+                outs.append((j, trop.gemm(ad, bd, sr, argmax=arg)))
+    torch.cuda.synchronize()
+    for j, got in outs:
+        want = ref[j]
+        if work[j][3]:
+            assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
+        else:
+            assert torch.equal(got, want)
