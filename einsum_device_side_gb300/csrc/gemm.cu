@@ -95,8 +95,15 @@ __device__ __forceinline__ void batch_offsets(const Batch& bt, uint32_t b, int64
 }
 
 // ------------------------------------------------------------------ tiled kernel
-constexpr int BM = 64, BN = 64, BK = 16, TM = 8, TN = 8;
-constexpr int TTHREADS = (BM / TM) * (BN / TN);  // 64
+constexpr int BM = 64, BN = 64, BK = 16, TM = 8;
+// Outputs per thread: TM rows x TN columns.  Without argmax TN = 8 (64 threads per tile);
+// with argmax the two accumulator sets double the registers, so TN = 4 (128 threads per tile)
+// keeps a thread near 128 registers and gives each SM twice the warps to hide latency with.
+#ifndef TROP_ARG_TN
+#define TROP_ARG_TN 4
+#endif
+template <bool ARG> __host__ __device__ constexpr int tile_tn() { return ARG ? TROP_ARG_TN : 8; }
+template <int TN> __host__ __device__ constexpr int tile_threads() { return (BM / TM) * (BN / TN); }
 constexpr int TILE_ELEMS = BM * BN;
 constexpr int APAD = 4;                          // float pad per transposed A row (keeps 16-byte rows)
 #ifndef TROP_ARG_CHUNK
@@ -177,14 +184,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // better) and store the tile through C's strides; with ARG also -(chunk + 1), or 0, into I.
 // The segments of other CTAs are read through L2 (ld.global.cg): they were written by
 // other SMs during this launch.
-constexpr int MERGE_RUNS = TILE_ELEMS / 4 / TTHREADS;  // runs of 4 columns per thread
-constexpr int MERGE_BATCH = 8;                          // runs whose loads are in flight together
+constexpr int MERGE_BATCH = 8;  // runs of 4 columns whose loads are in flight together
 
-template <int SR, bool ARG>
+template <int SR, bool ARG, int THREADS>
 __device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int m0, int n0, int64_t oc,
                                          int64_t oi, int tid)
 {
     using O = Ops<SR>;
+    constexpr int MERGE_RUNS = TILE_ELEMS / 4 / THREADS;  // runs of 4 columns per thread
+    static_assert(MERGE_RUNS % MERGE_BATCH == 0, "whole batches of runs");
     uint32_t j0, j1;
     int slot0;
     sk_segments(p, tl, j0, j1, slot0);
@@ -205,7 +213,7 @@ __device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int 
             uint2 sc[MERGE_BATCH];
 #pragma unroll
             for (int q = 0; q < MERGE_BATCH; ++q) {
-                const int e = ((q0 + q) * TTHREADS + tid) * 4;
+                const int e = ((q0 + q) * THREADS + tid) * 4;
                 sv[q] = __ldcg(reinterpret_cast<const float4*>(p.seg_v + base + e));
                 if (ARG) sc[q] = __ldcg(reinterpret_cast<const uint2*>(p.seg_c + base + e));
             }
@@ -224,7 +232,7 @@ __device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int 
         }
 #pragma unroll
         for (int q = 0; q < MERGE_BATCH; ++q) {
-            const int e = ((q0 + q) * TTHREADS + tid) * 4;
+            const int e = ((q0 + q) * THREADS + tid) * 4;
             const int m = m0 + e / BN, n = n0 + e % BN;
             if (m >= p.M) continue;
             float* crow = p.C + oc + (int64_t)m * p.sCm;
@@ -252,13 +260,24 @@ __device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int 
 // ARG: besides C, writes into I the chunk that holds each output's first maximum as
 // -(chunk + 1), or 0 when no product beat the semiring zero; k_argmax_resolve then
 // replaces the chunk by the exact index.  Stream-K segments go to the workspace instead.
-template <int SR, bool ARG>
-__global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
+// resident CTAs per SM the register allocation must allow (measured best on GB300)
+#ifndef TROP_ARG_MINB
+#define TROP_ARG_MINB 3
+#endif
+#ifndef TROP_PLAIN_MINB
+#define TROP_PLAIN_MINB 1
+#endif
+template <int SR, bool ARG, int TN>
+__global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP_PLAIN_MINB) k_gemm_tiled(TiledParams p)
 {
     using O = Ops<SR>;
+    constexpr int THREADS = tile_threads<TN>();
+    constexpr int NG = TN / 4;             // groups of 4 columns per thread, half a tile apart
+    constexpr int NLA = BM * BK / 4 / THREADS, NLB = BK * BN / 4 / THREADS;  // float4 loads per k-tile
+    static_assert(TN == 4 || TN == 8, "4 or 8 columns per thread");
     __shared__ __align__(16) float As[2][BK][BM + APAD];  // A transposed: As[k][m]
     __shared__ __align__(16) float Bs[2][BK][BN];
-    __shared__ uint16_t sid[ARG ? TM * TN : 1][ARG ? TTHREADS : 1];
+    __shared__ uint16_t sid[ARG ? TM * TN : 1][ARG ? THREADS : 1];
 
     __shared__ int s_last;
 
@@ -295,16 +314,17 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
         const float* __restrict__ A = p.A + oa;
         const float* __restrict__ B = p.B + ob;
 
-        // loader roles: A: rows tid/4 + 16*r, k quad (tid%4)*4;  B: rows tid/16 + 4*r, n quad (tid%16)*4
+        // loader roles: A: rows tid/4 + (THREADS/4)*r, k quad (tid%4)*4;
+        //               B: rows tid/16 + (THREADS/16)*r, n quad (tid%16)*4
         const int la_m = tid / 4, la_k = (tid % 4) * 4;
         const int lb_k = tid / 16, lb_n = (tid % 16) * 4;
 
-        float4 ra[4];
+        float4 ra[NLA];
         auto load_a = [&](int kt) {
             const int k0 = kt * BK;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int m = m0 + la_m + 16 * r, k = k0 + la_k;
+            for (int r = 0; r < NLA; ++r) {
+                const int m = m0 + la_m + (THREADS / 4) * r, k = k0 + la_k;
                 const float* src = A + (int64_t)m * p.sAm + k;
                 if (m < p.M && k + 3 < p.K && p.vecA) {
                     ra[r] = __ldg(reinterpret_cast<const float4*>(src));
@@ -318,8 +338,8 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
         };
         auto store_a = [&](int buf) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int m = la_m + 16 * r;
+            for (int r = 0; r < NLA; ++r) {
+                const int m = la_m + (THREADS / 4) * r;
                 As[buf][la_k + 0][m] = ra[r].x;
                 As[buf][la_k + 1][m] = ra[r].y;
                 As[buf][la_k + 2][m] = ra[r].z;
@@ -331,8 +351,8 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
         auto issue_b = [&](int kt, int buf) {
             const int k0 = kt * BK;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int kk = lb_k + 4 * r, k = k0 + kk, n = n0 + lb_n;
+            for (int r = 0; r < NLB; ++r) {
+                const int kk = lb_k + (THREADS / 16) * r, k = k0 + kk, n = n0 + lb_n;
                 float* dst = &Bs[buf][kk][lb_n];
                 if (p.vecB) {
                     const int valid = (k < p.K) ? max(0, min(4, p.N - n)) : 0;
@@ -378,18 +398,17 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
                     const float4 y = *reinterpret_cast<const float4*>(&As[buf][kk][BM / 2 + tm * 4]);
                     const float4 x1 = *reinterpret_cast<const float4*>(&As[buf][kk + 1][tm * 4]);
                     const float4 y1 = *reinterpret_cast<const float4*>(&As[buf][kk + 1][BM / 2 + tm * 4]);
-                    const float4 uu = *reinterpret_cast<const float4*>(&Bs[buf][kk][tn * 4]);
-                    const float4 v = *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tn * 4]);
-                    const float4 u1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][tn * 4]);
-                    const float4 v1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][BN / 2 + tn * 4]);
                     a0[0] = x.x; a0[1] = x.y; a0[2] = x.z; a0[3] = x.w;
                     a0[4] = y.x; a0[5] = y.y; a0[6] = y.z; a0[7] = y.w;
                     a1[0] = x1.x; a1[1] = x1.y; a1[2] = x1.z; a1[3] = x1.w;
                     a1[4] = y1.x; a1[5] = y1.y; a1[6] = y1.z; a1[7] = y1.w;
-                    b0[0] = uu.x; b0[1] = uu.y; b0[2] = uu.z; b0[3] = uu.w;
-                    b0[4] = v.x; b0[5] = v.y; b0[6] = v.z; b0[7] = v.w;
-                    b1[0] = u1.x; b1[1] = u1.y; b1[2] = u1.z; b1[3] = u1.w;
-                    b1[4] = v1.x; b1[5] = v1.y; b1[6] = v1.z; b1[7] = v1.w;
+#pragma unroll
+                    for (int h = 0; h < NG; ++h) {
+                        const float4 uu = *reinterpret_cast<const float4*>(&Bs[buf][kk][h * (BN / 2) + tn * 4]);
+                        const float4 u1 = *reinterpret_cast<const float4*>(&Bs[buf][kk + 1][h * (BN / 2) + tn * 4]);
+                        b0[4 * h] = uu.x; b0[4 * h + 1] = uu.y; b0[4 * h + 2] = uu.z; b0[4 * h + 3] = uu.w;
+                        b1[4 * h] = u1.x; b1[4 * h + 1] = u1.y; b1[4 * h + 2] = u1.z; b1[4 * h + 3] = u1.w;
+                    }
                 }
                 if constexpr (!ARG) {
 #pragma unroll
@@ -455,8 +474,8 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
                         code[jj] = best[i][jj] != zero ? -((int32_t)sid[i * TN + jj][tid] + 1) : 0;
                 }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = n0 + (h ? BN / 2 : 0) + tn * 4;
+                for (int h = 0; h < NG; ++h) {
+                    const int n = n0 + h * (BN / 2) + tn * 4;
                     if (p.vecC && n + 3 < p.N) {
                         *reinterpret_cast<float4*>(crow + n) =
                             make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
@@ -485,8 +504,8 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
             for (int i = 0; i < TM; ++i) {
                 const int r = row_of(tm, i);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = (h ? BN / 2 : 0) + tn * 4;
+                for (int h = 0; h < NG; ++h) {
+                    const int c = h * (BN / 2) + tn * 4;
                     *reinterpret_cast<float4*>(sv + r * BN + c) =
                         make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
                     if (ARG) {
@@ -513,7 +532,7 @@ __global__ void __launch_bounds__(TTHREADS) k_gemm_tiled(TiledParams p)
             __syncthreads();
             if (s_last) {
                 __threadfence();
-                sk_merge<SR, ARG>(p, tl, m0, n0, oc, oi, tid);
+                sk_merge<SR, ARG, THREADS>(p, tl, m0, n0, oc, oi, tid);
             }
         }
     }
@@ -970,8 +989,9 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     const uint64_t T = (uint64_t)nbatch * p.tiles_m * p.tiles_n;  // < 2^31 (route check)
 
     // ---- schedule: whole tiles for the full waves, stream-K for a thin last wave
+    constexpr int TN = tile_tn<ARG>(), THREADS = tile_threads<TN>();
     const uint64_t G = (uint64_t)dev->sm_count *
-                       resident_ctas((const void*)k_gemm_tiled<SR, ARG>, TTHREADS, 0, occ_gemm);
+                       resident_ctas((const void*)k_gemm_tiled<SR, ARG, TN>, THREADS, 0, occ_gemm);
     const uint64_t R = T % G;
     uint64_t G_sk = 0;
     void* ws = nullptr;
@@ -1004,7 +1024,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     }
     p.T_dp = (uint32_t)(G_sk ? T - R : T);
 
-    k_gemm_tiled<SR, ARG><<<(unsigned)(p.T_dp + G_sk), TTHREADS, 0, s>>>(p);
+    k_gemm_tiled<SR, ARG, TN><<<(unsigned)(p.T_dp + G_sk), THREADS, 0, s>>>(p);
     int rc = check_launch("k_gemm_tiled");
     if (rc == TROP_OK && ARG) {
         p.r_units = (uint64_t)nbatch * p.tiles_n * (uint64_t)g.M;
@@ -1217,8 +1237,8 @@ int register_gemm_kernels()
         }
     }
     const void* ks[] = {
-        (const void*)k_gemm_tiled<TROP_MAXPLUS, true>,  (const void*)k_gemm_tiled<TROP_MINPLUS, true>,
-        (const void*)k_gemm_tiled<TROP_MAXTIMES, true>, (const void*)k_gemm_tiled<TROP_MAXPLUS, false>,
+        (const void*)k_gemm_tiled<TROP_MAXPLUS, true, tile_tn<true>()>,  (const void*)k_gemm_tiled<TROP_MINPLUS, true, tile_tn<true>()>,
+        (const void*)k_gemm_tiled<TROP_MAXTIMES, true, tile_tn<true>()>, (const void*)k_gemm_tiled<TROP_MAXPLUS, false, tile_tn<false>()>,
         (const void*)k_gemm_stream<TROP_MAXPLUS, true, 4, 2>, (const void*)k_gemm_stream<TROP_MAXPLUS, true, 1, 2>,
         (const void*)k_gemm_generic<TROP_MAXPLUS, true>,
     };
