@@ -212,3 +212,23 @@ def test_split_gemms_on_two_streams(trop):
             assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
         else:
             assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("sr", SR)
+def test_whole_tiles_long_contraction_sampled(trop, sr):
+    """Enough whole tiles that none is split, with K > 4096 (too many k-tiles to
+    resolve the argmax inside the tile): chunk codes go through the separate
+    resolve pass.  Sampled outputs vs the oracle, plus a certificate on all."""
+    a, b = synth.gemm_batched_inputs(sr, batch=60, m=128, n=128, k=4200)
+    ad, bd = _dev(a), _dev(b)
+    c, i = trop.gemm(ad, bd, sr)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(300 + sr)
+    samples = rng.choice(c.numel(), size=4000, replace=False).astype(np.int64)
+    rc, ri = oracle.gemm(a, b, sr, samples=samples, nthreads=0)
+    np.testing.assert_array_equal(c.reshape(-1).cpu().numpy()[samples], rc)
+    np.testing.assert_array_equal(i.reshape(-1).cpu().numpy()[samples], ri)
+    idx = i.long()
+    t = torch.gather(ad, 2, idx) * torch.gather(bd, 1, idx) if sr == 2 else \
+        torch.gather(ad, 2, idx) + torch.gather(bd, 1, idx)
+    assert torch.equal(t, c)
