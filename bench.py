@@ -385,7 +385,7 @@ def run_gpu(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": region_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "strided-batched tropical GEMM + int32 argmax, batch 64 x M=N=K=256, "
-                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 launches",
+                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 GEMM calls (k_gemm_tiled + k_argmax_resolve each)",
                    "parallelism": f"replicas x{world}",
                    "l2": f"{N_SETS} rotated input sets (288 MiB of operands) so each step reads cold inputs"},
         "roofline": {"bound": "alu", "kernel": "k_gemm_tiled+k_argmax_resolve (one tropical GEMM call)",
