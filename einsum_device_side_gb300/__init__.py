@@ -120,24 +120,49 @@ def _sr(semiring) -> int:
     return int(semiring)
 
 
-def _stream(stream=None) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream
+# the current stream's raw handle without building a Stream object (a few us per call)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream=None, like: torch.Tensor | None = None) -> int:
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        dev = like.get_device() if like is not None and like.is_cuda else torch.cuda.current_device()
+        return _raw_stream(dev)
+    return torch.cuda.current_stream().cuda_stream
+
+
+_desc_cache: dict = {}
 
 
 def tensor_desc(t: torch.Tensor) -> TropTensor:
-    if t.dtype not in _DTYPES:
+    """The C descriptor of a tensor.  A descriptor is a pure function of (data
+    pointer, dtype, shape, strides), so repeated calls on the same tensors reuse
+    one (bounded cache; the C side only reads it)."""
+    key = (t.data_ptr(), t.dtype, t.shape, t.stride())
+    d = _desc_cache.get(key)
+    if d is None:
+        if len(_desc_cache) >= 512:
+            _desc_cache.clear()
+        d = _desc_cache[key] = _make_desc(t)
+    return d
+
+
+def _make_desc(t: torch.Tensor) -> TropTensor:
+    code = _DTYPES.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    if t.dim() > MAX_RANK:
+    n = t.dim()
+    if n > MAX_RANK:
         raise ValueError("rank above 32")
     d = TropTensor()
     d.data = t.data_ptr() if t.numel() > 0 else None
-    d.dtype = _DTYPES[t.dtype]
-    d.rank = t.dim()
-    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
-        d.shape[i] = s
-        d.stride[i] = st
+    d.dtype = code
+    d.rank = n
+    if n:
+        d.shape[:n] = t.shape
+        d.stride[:n] = t.stride()
     return d
 
 
@@ -167,7 +192,7 @@ def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Ten
         am = torch.empty(out.shape, dtype=torch.int32, device=x.device)
     dx, do = tensor_desc(x), tensor_desc(out)
     _check(lib.tropical_permute_trace(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
-                                      am.data_ptr() if am is not None and am.numel() else None, _stream(stream)))
+                                      am.data_ptr() if am is not None and am.numel() else None, _stream(stream, x)))
     return (out, am) if am is not None else out
 
 
@@ -181,7 +206,7 @@ def permute_trace_noalloc(x: torch.Tensor, spec: str, semiring="maxplus", *, out
     dx, do = tensor_desc(x), tensor_desc(out)
     _check(lib.tropical_permute_trace_noalloc(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
                                               argmax.data_ptr() if argmax is not None and argmax.numel() else None,
-                                              _stream(stream)))
+                                              _stream(stream, x)))
     return (out, argmax) if argmax is not None else out
 
 
@@ -195,7 +220,7 @@ def permute_pair(val: torch.Tensor, arg: torch.Tensor, spec: str, out_val=None, 
         out_arg = torch.empty(shape, dtype=torch.int32, device=val.device)
     a, b, c, d = tensor_desc(val), tensor_desc(arg), tensor_desc(out_val), tensor_desc(out_arg)
     _check(lib.tropical_permute_pair(ctypes.byref(a), ctypes.byref(b), spec.encode(), ctypes.byref(c),
-                                     ctypes.byref(d), _stream(stream)))
+                                     ctypes.byref(d), _stream(stream, val)))
     return out_val, out_arg
 
 
@@ -229,7 +254,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
         A.data_ptr() if A.numel() else None, A.stride(0), A.stride(1), A.stride(2),
         B.data_ptr() if B.numel() else None, B.stride(0), B.stride(1), B.stride(2),
         out.data_ptr() if out.numel() else None, out.stride(0), out.stride(1), out.stride(2),
-        am.data_ptr() if am is not None and am.numel() else None, _stream(stream)))
+        am.data_ptr() if am is not None and am.numel() else None, _stream(stream, out)))
     return (out, am) if argmax else out
 
 
@@ -246,7 +271,7 @@ def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argm
     a, b, o = tensor_desc(A), tensor_desc(B), tensor_desc(out)
     _check(lib.tropical_einsum_pairwise(spec.encode(), ctypes.byref(a), ctypes.byref(b), _sr(semiring),
                                         ctypes.byref(o), am.data_ptr() if am is not None and am.numel() else None,
-                                        _stream(stream)))
+                                        _stream(stream, out)))
     return (out, am) if argmax else out
 
 
@@ -283,7 +308,7 @@ def contract_tree(inputs, nodes, semiring="maxplus", out: torch.Tensor | None = 
                                                for t in node_argmax])
     o = tensor_desc(out)
     _check(lib.tropical_contract_tree(len(inputs), descs, len(nodes), table.arr, _sr(semiring), ctypes.byref(o),
-                                      ams, _stream(stream)))
+                                      ams, _stream(stream, out)))
     return out
 
 
@@ -300,7 +325,7 @@ def tree_backtrack(inputs, nodes, node_argmax, n_labels: int, root_index: int = 
     ams = (ctypes.c_void_p * len(nodes))(*[(t.data_ptr() if t is not None and t.numel() else None)
                                            for t in node_argmax])
     _check(lib.tropical_tree_backtrack(len(inputs), descs, len(nodes), table.arr, ams, root_index, n_labels,
-                                       assignment.data_ptr(), _stream(stream)))
+                                       assignment.data_ptr(), _stream(stream, assignment)))
     return assignment
 
 

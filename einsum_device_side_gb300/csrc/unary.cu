@@ -137,8 +137,21 @@ struct TransParams {
     int64_t gj_s_in[4], gj_s_in2[4];    // input strides of GJ axes (last = fastest in output)
     int vec_in;                          // input rows 16-byte aligned for vector loads
     int vec_out;                         // output rows 16-byte aligned for vector stores
+    int sw;                              // shared-memory swizzle step (see tile_pos)
     RestDims rest;
 };
+
+// Shared-memory slot of tile element (x, c): x = slice * TJ + GJ index, in [0, L) with
+// L = TB * TJ; c = GI index.  The tile is held transposed, in rows of L elements per GI
+// index, and a row's x is XOR-ed with a multiple of the vector width W below 32 that grows
+// with c / W.  The loader's scalar stores -- lanes spread over W-wide runs of c and over
+// consecutive x -- then land in distinct banks, and the storer's W-wide reads along x stay
+// contiguous and 16-byte aligned.
+template <int W>
+__device__ __forceinline__ int tile_pos(int x, int c, int L, int sw)
+{
+    return c * L + (x ^ (((c / W) * sw) & 31 & (L - 1)));
+}
 
 template <int T_BYTES>
 struct TileCfg {
@@ -148,8 +161,18 @@ struct TileCfg {
     static constexpr int TBMAX = 64;
 };
 
+// Residency of the transpose, which is bound by load latency: registers capped for 6 CTAs
+// (48 warps) per SM and a shared-memory carveout that fits them while leaving L1 room for
+// the loads in flight (measured on GB300: a 16^6 f32 'abcdef->afbcde' took 31.4 us at
+// 4 CTAs/SM, 25.1 us here; the maximum carveout starved L1 and doubled the time).
+#ifndef TROP_TRANSPOSE_MINB
+#define TROP_TRANSPOSE_MINB 6
+#endif
+#ifndef TROP_TRANSPOSE_CARVEOUT
+#define TROP_TRANSPOSE_CARVEOUT 60
+#endif
 template <typename T, bool PAIR>
-__global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* __restrict__ out,
+__global__ void __launch_bounds__(NT, TROP_TRANSPOSE_MINB) k_transpose(const T* __restrict__ in, T* __restrict__ out,
                                                   const int32_t* __restrict__ in2, int32_t* __restrict__ out2,
                                                   TransParams p)
 {
@@ -157,13 +180,13 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
     using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
     constexpr int W = 16 / sizeof(T);
     constexpr int VPT = Cfg::TILE / W / NT;  // vectors per thread in a full tile
-    __shared__ T tile[Cfg::TILE + Cfg::TILE / 4];  // TB*TJ rows of TI+1 (TI >= 4)
-    __shared__ int32_t tile2[PAIR ? Cfg::TILE + Cfg::TILE / 4 : 1];
+    __shared__ __align__(16) T tile[Cfg::TILE];  // TI rows of L = TB*TJ, swizzled (tile_pos)
+    __shared__ int32_t tile2[PAIR ? Cfg::TILE : 1];
     __shared__ int64_t row_in[Cfg::TJMAX], row_in2[PAIR ? Cfg::TJMAX : 1];     // input offset of a GJ index
     __shared__ int64_t row_out[Cfg::TIMAX], row_out2[PAIR ? Cfg::TIMAX : 1];   // output offset of a GI index
     __shared__ int64_t bin_s[Cfg::TBMAX], bout_s[Cfg::TBMAX];                   // offsets of the TB outer slices
     __shared__ int64_t bin2_s[PAIR ? Cfg::TBMAX : 1], bout2_s[PAIR ? Cfg::TBMAX : 1];
-    const int TI = (int)p.TI, TJ = (int)p.TJ, TB = (int)p.TB, LD = TI + 1;
+    const int TI = (int)p.TI, TJ = (int)p.TJ, TB = (int)p.TB, L = TB * TJ, sw = p.sw;
     const int lTI = (int)p.lTI, lTJ = (int)p.lTJ;
 
     for (uint32_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
@@ -231,16 +254,16 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                 const int c = (e & ((1 << lvi) - 1)) * W, rj = e >> lvi;
                 const T* pv = reinterpret_cast<const T*>(&v[u]);
 #pragma unroll
-                for (int q = 0; q < W; ++q) tile[rj * LD + c + q] = pv[q];
+                for (int q = 0; q < W; ++q) tile[tile_pos<W>(rj, c + q, L, sw)] = pv[q];
             }
         } else {
             for (int e = threadIdx.x; e < TB * TJ * TI; e += NT) {
                 const int c = e & (TI - 1), rj = e >> lTI;
                 const int r = rj & (TJ - 1), b = rj >> lTJ;
                 if (r0 + b < p.nR && j0 + r < p.nJ && i0 + c < p.nI) {
-                    tile[rj * LD + c] = __ldg(in + bin_s[b] + row_in[r] + i0 + c);
+                    tile[tile_pos<W>(rj, c, L, sw)] = __ldg(in + bin_s[b] + row_in[r] + i0 + c);
                     if (PAIR)
-                        tile2[PAIR ? rj * LD + c : 0] =
+                        tile2[PAIR ? tile_pos<W>(rj, c, L, sw) : 0] =
                             __ldg(in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c);
                 }
             }
@@ -252,10 +275,7 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
             for (int e = threadIdx.x; e < (TB * TI) << lvj; e += NT) {
                 const int c = (e & ((1 << lvj) - 1)) * W, ri = e >> lvj;
                 const int r = ri & (TI - 1), b = ri >> lTI;
-                V v;
-                T* pv = reinterpret_cast<T*>(&v);
-#pragma unroll
-                for (int q = 0; q < W; ++q) pv[q] = tile[((b << lTJ) + c + q) * LD + r];
+                const V v = *reinterpret_cast<const V*>(&tile[tile_pos<W>((b << lTJ) + c, r, L, sw)]);
                 *reinterpret_cast<V*>(out + bout_s[b] + row_out[r] + j0 + c) = v;
             }
         } else {
@@ -263,10 +283,10 @@ __global__ void __launch_bounds__(NT) k_transpose(const T* __restrict__ in, T* _
                 const int c = e & (TJ - 1), ri = e >> lTJ;
                 const int r = ri & (TI - 1), b = ri >> lTI;
                 if (r0 + b < p.nR && i0 + r < p.nI && j0 + c < p.nJ) {
-                    out[bout_s[b] + row_out[r] + j0 + c] = tile[((b << lTJ) + c) * LD + r];
+                    out[bout_s[b] + row_out[r] + j0 + c] = tile[tile_pos<W>((b << lTJ) + c, r, L, sw)];
                     if (PAIR)
                         out2[bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c] =
-                            tile2[PAIR ? ((b << lTJ) + c) * LD + r : 0];
+                            tile2[PAIR ? tile_pos<W>((b << lTJ) + c, r, L, sw) : 0];
                 }
             }
         }
@@ -641,6 +661,9 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             for (int i = 0; i < d.rank; ++i)
                 if (i != last) vo = vo && (d.s_out[i] % W) == 0;
             p.vec_out = vo ? 1 : 0;
+            // swizzle step: the x values one warp's loads cover (32 lanes over TI / W vectors per row),
+            // at least W so the storer's W-wide runs stay whole
+            p.sw = (int)std::max<int64_t>(W, (int64_t)32 * W / ti_);
             const int g = (int)std::min<int64_t>(tiles, (int64_t)dev->sm_count * 64);
             if (pair) k_transpose<T, true><<<g, NT, 0, s>>>(in, out, in2, out2, p);
             else k_transpose<T, false><<<g, NT, 0, s>>>(in, out, in2, out2, p);
@@ -894,6 +917,13 @@ int register_unary_kernels()
     for (const void* k : ks) {
         cudaError_t e = cudaFuncGetAttributes(&a, k);
         if (e != cudaSuccess) return cuda_error(e, "cudaFuncGetAttributes (unary kernels)");
+    }
+    // shared-memory carveout of the transpose (see TROP_TRANSPOSE_CARVEOUT)
+    const void* kt[] = {(const void*)k_transpose<int32_t, false>, (const void*)k_transpose<int64_t, false>,
+                        (const void*)k_transpose<int32_t, true>, (const void*)k_transpose<int64_t, true>};
+    for (const void* k : kt) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, TROP_TRANSPOSE_CARVEOUT);
+        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (transpose carveout)");
     }
     return TROP_OK;
 }
