@@ -1188,6 +1188,67 @@ Route choose(const GemmDesc& g, bool& swap)
     return R_GENERIC;
 }
 
+// The tiled kernel writes 4-column runs of an output row; when the output's column stride is
+// not 1 (a transposed or permuted output) those become scattered 4-byte stores, and the argmax
+// pass reads them back the same way.  Such a product goes to a contiguous pool buffer first and
+// is then moved, value and argmax through one index mapping, by the tiled transpose.
+template <int SR, bool ARG>
+int run_tiled_staged(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
+{
+    int64_t nbatch = 1;
+    for (int d = 0; d < g.nb; ++d) nbatch *= g.bsize[d];
+    const size_t elems = (size_t)nbatch * (size_t)g.M * (size_t)g.N;
+    void* ws = nullptr;
+    if (pool_alloc(elems * (sizeof(float) + (ARG ? sizeof(int32_t) : 0)), s, &ws) != TROP_OK) {
+        clear_error();
+        return run_tiled<SR, ARG>(g, s, dev);  // no workspace: write through the strides
+    }
+    GemmDesc t = g;
+    t.C = static_cast<float*>(ws);
+    t.I = ARG ? reinterpret_cast<int32_t*>(t.C + elems) : nullptr;
+    t.sCm = t.sIm = g.N;
+    t.sCn = t.sIn = 1;
+    GatherDesc gd{};
+    gd.rank = g.nb + 2;
+    int64_t st = g.M * g.N;
+    for (int d = g.nb - 1; d >= 0; --d) {
+        t.sCb[d] = t.sIb[d] = st;
+        gd.size[d] = g.bsize[d];
+        gd.s_in[d] = gd.s_in2[d] = st;
+        gd.s_out[d] = g.sCb[d];
+        gd.s_out2[d] = g.sIb[d];
+        st *= g.bsize[d];
+    }
+    const int m = g.nb, n = g.nb + 1;
+    gd.size[m] = g.M;
+    gd.size[n] = g.N;
+    gd.s_in[m] = gd.s_in2[m] = g.N;
+    gd.s_in[n] = gd.s_in2[n] = 1;
+    gd.s_out[m] = g.sCm;
+    gd.s_out[n] = g.sCn;
+    gd.s_out2[m] = g.sIm;
+    gd.s_out2[n] = g.sIn;
+    {
+        // axes in the output's order (slowest first), as the gather planner expects
+        GatherDesc o = gd;
+        int idx[MAXR];
+        for (int i = 0; i < gd.rank; ++i) idx[i] = i;
+        std::stable_sort(idx, idx + gd.rank, [&](int x, int y) { return gd.s_out[x] > gd.s_out[y]; });
+        for (int i = 0; i < gd.rank; ++i) {
+            o.size[i] = gd.size[idx[i]];
+            o.s_in[i] = gd.s_in[idx[i]];
+            o.s_out[i] = gd.s_out[idx[i]];
+            o.s_in2[i] = gd.s_in2[idx[i]];
+            o.s_out2[i] = gd.s_out2[idx[i]];
+        }
+        gd = o;
+    }
+    int rc = run_tiled<SR, ARG>(t, s, dev);
+    if (rc == TROP_OK) rc = launch_gather(t.C, g.C, (int)sizeof(float), t.I, g.I, gd, s);
+    pool_retire(ws, s);
+    return rc;
+}
+
 template <int SR, bool ARG>
 int run(const GemmDesc& g0, cudaStream_t s, const DeviceInfo* dev, const char** name)
 {
@@ -1197,6 +1258,7 @@ int run(const GemmDesc& g0, cudaStream_t s, const DeviceInfo* dev, const char** 
     switch (r) {
     case R_TILED:
         if (name) *name = "k_gemm_tiled";
+        if (g.sCn != 1 || (ARG && g.sIn != 1)) return run_tiled_staged<SR, ARG>(g, s, dev);
         return run_tiled<SR, ARG>(g, s, dev);
     case R_STREAM:
         if (name) *name = "k_gemm_stream";

@@ -172,7 +172,7 @@ struct TileCfg {
 #define TROP_TRANSPOSE_CARVEOUT 60
 #endif
 template <typename T, bool PAIR>
-__global__ void __launch_bounds__(NT, TROP_TRANSPOSE_MINB) k_transpose(const T* __restrict__ in, T* __restrict__ out,
+__global__ void __launch_bounds__(NT, PAIR ? 3 : TROP_TRANSPOSE_MINB) k_transpose(const T* __restrict__ in, T* __restrict__ out,
                                                   const int32_t* __restrict__ in2, int32_t* __restrict__ out2,
                                                   TransParams p)
 {
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(NT, TROP_TRANSPOSE_MINB) k_transpose(const T* 
     constexpr int W = 16 / sizeof(T);
     constexpr int VPT = Cfg::TILE / W / NT;  // vectors per thread in a full tile
     __shared__ __align__(16) T tile[Cfg::TILE];  // TI rows of L = TB*TJ, swizzled (tile_pos)
-    __shared__ int32_t tile2[PAIR ? Cfg::TILE : 1];
+    __shared__ __align__(16) int32_t tile2[PAIR ? Cfg::TILE : 1];
     __shared__ int64_t row_in[Cfg::TJMAX], row_in2[PAIR ? Cfg::TJMAX : 1];     // input offset of a GJ index
     __shared__ int64_t row_out[Cfg::TIMAX], row_out2[PAIR ? Cfg::TIMAX : 1];   // output offset of a GI index
     __shared__ int64_t bin_s[Cfg::TBMAX], bout_s[Cfg::TBMAX];                   // offsets of the TB outer slices
@@ -239,14 +239,20 @@ __global__ void __launch_bounds__(NT, TROP_TRANSPOSE_MINB) k_transpose(const T* 
         const bool full = i0 + TI <= p.nI && j0 + TJ <= p.nJ && r0 + TB <= p.nR;
         const int lvi = lTI - (W == 4 ? 2 : 1);  // log2 of vectors per input row
         // load: rows = (slice, GJ index) (strided in the input), columns = GI index (contiguous)
-        if (!PAIR && full && p.vec_in && TI >= W && (TB << (lTJ + lTI)) == Cfg::TILE) {
+        // (the int32 companion of a pair rides in the same vectors when T is 4 bytes wide)
+        constexpr bool VPAIR = !PAIR || sizeof(T) == 4;
+        if (VPAIR && full && p.vec_in && TI >= W && (TB << (lTJ + lTI)) == Cfg::TILE) {
             V v[VPT];
+            int4 v2[PAIR ? VPT : 1];
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {  // all loads in flight before any shared store
                 const int e = threadIdx.x + u * NT;
                 const int c = (e & ((1 << lvi) - 1)) * W, rj = e >> lvi;
                 const int r = rj & (TJ - 1), b = rj >> lTJ;
                 v[u] = __ldg(reinterpret_cast<const V*>(in + bin_s[b] + row_in[r] + i0 + c));
+                if (PAIR)
+                    v2[PAIR ? u : 0] = __ldg(reinterpret_cast<const int4*>(
+                        in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c));
             }
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
@@ -255,6 +261,11 @@ __global__ void __launch_bounds__(NT, TROP_TRANSPOSE_MINB) k_transpose(const T* 
                 const T* pv = reinterpret_cast<const T*>(&v[u]);
 #pragma unroll
                 for (int q = 0; q < W; ++q) tile[tile_pos<W>(rj, c + q, L, sw)] = pv[q];
+                if (PAIR) {
+                    const int32_t* pv2 = reinterpret_cast<const int32_t*>(&v2[PAIR ? u : 0]);
+#pragma unroll
+                    for (int q = 0; q < W; ++q) tile2[PAIR ? tile_pos<W>(rj, c + q, L, sw) : 0] = pv2[q];
+                }
             }
         } else {
             for (int e = threadIdx.x; e < TB * TJ * TI; e += NT) {
@@ -270,13 +281,17 @@ __global__ void __launch_bounds__(NT, TROP_TRANSPOSE_MINB) k_transpose(const T* 
         }
         __syncthreads();
         // store: rows = (slice, GI index) (strided in the output), columns = GJ index (contiguous)
-        if (!PAIR && full && p.vec_out && TJ >= W) {
+        if (VPAIR && full && p.vec_out && TJ >= W) {
             const int lvj = lTJ - (W == 4 ? 2 : 1);
             for (int e = threadIdx.x; e < (TB * TI) << lvj; e += NT) {
                 const int c = (e & ((1 << lvj) - 1)) * W, ri = e >> lvj;
                 const int r = ri & (TI - 1), b = ri >> lTI;
-                const V v = *reinterpret_cast<const V*>(&tile[tile_pos<W>((b << lTJ) + c, r, L, sw)]);
+                const int at = tile_pos<W>((b << lTJ) + c, r, L, sw);
+                const V v = *reinterpret_cast<const V*>(&tile[at]);
                 *reinterpret_cast<V*>(out + bout_s[b] + row_out[r] + j0 + c) = v;
+                if (PAIR)
+                    *reinterpret_cast<int4*>(out2 + bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c) =
+                        *reinterpret_cast<const int4*>(&tile2[PAIR ? at : 0]);
             }
         } else {
             for (int e = threadIdx.x; e < TB * TJ * TI; e += NT) {
@@ -652,12 +667,13 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             p.div_tilesI = make_fastdiv(p.tilesI);
             p.div_tilesJ = make_fastdiv(p.tilesJ);
             constexpr int W = 16 / sizeof(T);
-            bool vec = ((uintptr_t)in % 16) == 0 && (nI % W) == 0 && (p.TI % W) == 0;
+            bool vec = ((uintptr_t)in % 16) == 0 && (nI % W) == 0 && (p.TI % W) == 0 &&
+                       (!pair || ((uintptr_t)in2 % 16) == 0);
             for (int i = 0; i < d.rank; ++i)
                 if (i != din) vec = vec && (d.s_in[i] % W) == 0;
             p.vec_in = vec ? 1 : 0;
             // vector stores: output rows start 16-byte aligned (every stride but the GJ chain's unit one)
-            bool vo = ((uintptr_t)out % 16) == 0 && (nJ % W) == 0;
+            bool vo = ((uintptr_t)out % 16) == 0 && (nJ % W) == 0 && (!pair || ((uintptr_t)out2 % 16) == 0);
             for (int i = 0; i < d.rank; ++i)
                 if (i != last) vo = vo && (d.s_out[i] % W) == 0;
             p.vec_out = vo ? 1 : 0;
