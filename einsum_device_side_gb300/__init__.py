@@ -14,6 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 __all__ = [
@@ -143,7 +144,7 @@ def tensor_desc(t: torch.Tensor) -> TropTensor:
     key = (t.data_ptr(), t.dtype, t.shape, t.stride())
     d = _desc_cache.get(key)
     if d is None:
-        if len(_desc_cache) >= 512:
+        if len(_desc_cache) >= 4096:
             _desc_cache.clear()
         d = _desc_cache[key] = _make_desc(t)
     return d
@@ -275,21 +276,44 @@ def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argm
     return (out, am) if argmax else out
 
 
+_NODE_DTYPE = np.dtype({"names": ["lhs", "rhs", "n_lhs", "n_rhs", "n_out", "lhs_labels", "rhs_labels", "out_labels"],
+                        "formats": ["<i4"] * 5 + ["<u8"] * 3,
+                        "offsets": [TropNode.lhs.offset, TropNode.rhs.offset, TropNode.n_lhs.offset,
+                                    TropNode.n_rhs.offset, TropNode.n_out.offset, TropNode.lhs_labels.offset,
+                                    TropNode.rhs_labels.offset, TropNode.out_labels.offset],
+                        "itemsize": ctypes.sizeof(TropNode)})
+
+
 class _NodeTable:
-    """Keeps the ctypes arrays of a node list alive for one call."""
+    """The trop_node array of a node list, built in one pass: every label list
+    lives in one int32 array and the nodes point into it.  Keeps both alive for
+    one call."""
 
     def __init__(self, nodes):
-        self.keep = []
-        self.arr = (TropNode * len(nodes))()
-        for j, (lhs, rhs, ll, rl, ol) in enumerate(nodes):
-            n = self.arr[j]
-            n.lhs, n.rhs = lhs, (-1 if rhs is None else rhs)
-            for attr, cnt, labs in (("lhs_labels", "n_lhs", ll), ("rhs_labels", "n_rhs", rl or []),
-                                    ("out_labels", "n_out", ol)):
-                buf = (ctypes.c_int32 * max(1, len(labs)))(*labs)
-                self.keep.append(buf)
-                setattr(n, attr, ctypes.cast(buf, ctypes.POINTER(ctypes.c_int32)))
-                setattr(n, cnt, len(labs))
+        lh, rh, nl, nr, no, labs = [], [], [], [], [], []
+        for lhs, rhs, ll, rl, ol in nodes:
+            rl = rl or ()
+            lh.append(lhs)
+            rh.append(-1 if rhs is None else rhs)
+            nl.append(len(ll))
+            nr.append(len(rl))
+            no.append(len(ol))
+            labs.extend(ll)
+            labs.extend(rl)
+            labs.extend(ol)
+        labs.append(0)  # every pointer, even of an empty list, stays inside the array
+        self.labels = np.asarray(labs, dtype=np.int32)
+        nl, nr, no = (np.asarray(v, dtype=np.int64) for v in (nl, nr, no))
+        start = np.zeros(len(nodes), dtype=np.int64)
+        np.cumsum((nl + nr + no)[:-1], out=start[1:])
+        base = self.labels.ctypes.data
+        t = np.zeros(len(nodes), dtype=_NODE_DTYPE)
+        t["lhs"], t["rhs"], t["n_lhs"], t["n_rhs"], t["n_out"] = lh, rh, nl, nr, no
+        t["lhs_labels"] = base + 4 * start
+        t["rhs_labels"] = base + 4 * (start + nl)
+        t["out_labels"] = base + 4 * (start + nl + nr)
+        self.table = t
+        self.arr = t.ctypes.data_as(ctypes.POINTER(TropNode))
 
 
 def contract_tree(inputs, nodes, semiring="maxplus", out: torch.Tensor | None = None, node_argmax=None,
