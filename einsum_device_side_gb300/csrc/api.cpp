@@ -601,9 +601,11 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
     }
     if (text) {
         char buf[512];
-        snprintf(buf, sizeof buf, "%sgemm M=%lld N=%lld K=%lld batch_axes=%d sAm=%lld sAk=%lld sBk=%lld sBn=%lld sCm=%lld sCn=%lld",
+        char route[96];
+        describe_gemm(g, route, sizeof route);
+        snprintf(buf, sizeof buf, "%sgemm M=%lld N=%lld K=%lld batch_axes=%d sAm=%lld sAk=%lld sBk=%lld sBn=%lld sCm=%lld sCn=%lld%s",
                  desc.c_str(), (long long)g.M, (long long)g.N, (long long)g.K, g.nb, (long long)g.sAm,
-                 (long long)g.sAk, (long long)g.sBk, (long long)g.sBn, (long long)g.sCm, (long long)g.sCn);
+                 (long long)g.sAk, (long long)g.sBk, (long long)g.sBn, (long long)g.sCm, (long long)g.sCn, route);
         *text = buf;
     }
     if (dry) return TROP_OK;

@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 
 #include "internal.h"
 
@@ -1050,6 +1051,17 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     return rc;
 }
 
+// 16-byte vectors along n for the stream kernel: every row of B, C (and I) aligned
+bool stream_vec(const GemmDesc& g, bool arg)
+{
+    bool vec = g.N % 4 == 0 && g.sBn == 1 && g.sCn == 1 && (!arg || g.sIn == 1) && ((uintptr_t)g.B % 16) == 0 &&
+               ((uintptr_t)g.C % 16) == 0 && (!arg || ((uintptr_t)g.I % 16) == 0) && g.sBk % 4 == 0 &&
+               g.sCm % 4 == 0 && (!arg || g.sIm % 4 == 0);
+    for (int d = 0; d < g.nb; ++d)
+        if (g.bsize[d] != 1) vec = vec && g.sBb[d] % 4 == 0 && g.sCb[d] % 4 == 0 && (!arg || g.sIb[d] % 4 == 0);
+    return vec;
+}
+
 template <int SR, bool ARG>
 int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 {
@@ -1071,11 +1083,7 @@ int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.sIn = g.sIn;
     int64_t nbatch = 1;
     p.bt = make_batch(g, nbatch);
-    bool vec = g.N % 4 == 0 && g.sBn == 1 && g.sCn == 1 && (!ARG || g.sIn == 1) && ((uintptr_t)g.B % 16) == 0 &&
-               ((uintptr_t)g.C % 16) == 0 && (!ARG || ((uintptr_t)g.I % 16) == 0) && g.sBk % 4 == 0 &&
-               g.sCm % 4 == 0 && (!ARG || g.sIm % 4 == 0);
-    for (int d = 0; d < p.bt.nb; ++d)
-        vec = vec && p.bt.sB[d] % 4 == 0 && p.bt.sC[d] % 4 == 0 && (!ARG || p.bt.sI[d] % 4 == 0);
+    const bool vec = stream_vec(g, ARG);
     const int VEC = vec ? 4 : 1;
     p.nvec = (uint32_t)(g.N / VEC);
     p.div_nvec = make_fastdiv(p.nvec);
@@ -1270,6 +1278,28 @@ int run(const GemmDesc& g0, cudaStream_t s, const DeviceInfo* dev, const char** 
 }
 
 }  // namespace
+
+void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
+{
+    // a description is about layouts: take every pointer as 256-byte aligned
+    GemmDesc g0 = g1;
+    const uintptr_t aligned = 256;
+    g0.A = reinterpret_cast<const float*>(aligned);
+    g0.B = reinterpret_cast<const float*>(aligned);
+    g0.C = reinterpret_cast<float*>(aligned);
+    if (g1.I) g0.I = reinterpret_cast<int32_t*>(aligned);
+    bool swap = false;
+    const Route r = choose(g0, swap);
+    const GemmDesc g = swap ? swapped(g0) : g0;
+    const bool arg = g.I != nullptr;
+    if (r == R_TILED)
+        snprintf(buf, n, " route=tiled%s%s", swap ? " swap" : "",
+                 (g.sCn != 1 || (arg && g.sIn != 1)) ? " staged" : "");
+    else if (r == R_STREAM)
+        snprintf(buf, n, " route=stream%s vec=%d", swap ? " swap" : "", stream_vec(g, arg) ? 4 : 1);
+    else
+        snprintf(buf, n, " route=generic");
+}
 
 int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name)
 {

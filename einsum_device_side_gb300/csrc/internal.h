@@ -115,6 +115,8 @@ struct GemmDesc {
     int64_t sAb[MAXB], sBb[MAXB], sCb[MAXB], sIb[MAXB];
 };
 int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name);
+// The route launch_gemm takes for g (kernel, operand swap, vector width, staging) as text.
+void describe_gemm(const GemmDesc& g, char* buf, size_t n);
 
 // Tree back-tracking (backtrack.cu).
 struct BtNode {

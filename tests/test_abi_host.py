@@ -66,11 +66,23 @@ def test_planner_lowering(trop, spec, sa, sb, expect):
     assert text.startswith(expect), text
 
 
-def test_planner_contiguous_output_needs_no_output_permute(trop):
-    # the GEMM writes through the output strides: a transposed output costs nothing extra
+def test_planner_transposed_output_is_staged_not_permuted(trop):
+    # the planner does not permute for a transposed output; the GEMM dispatcher
+    # writes the tiled product to a contiguous buffer and transposes it once
     st_a, st_b = _desc("bmk,bkn->bnm", [2, 64, 32], [2, 32, 48])
     text = trop.plan_describe("bmk,bkn->bnm", [2, 64, 32], st_a, [2, 32, 48], st_b)
-    assert "perm" not in text and "sCm=1" in text
+    assert "perm" not in text and "sCm=1" in text and "route=tiled staged" in text
+
+
+@pytest.mark.parametrize("spec,sa,sb,route", [
+    ("bmk,bkn->bmn", [64, 256, 256], [64, 256, 256], "route=tiled"),
+    ("alub,lun->alnb", [8, 2, 2, 16], [2, 2, 2], "route=stream"),
+    ("ij,jk->ik", [5, 300], [300, 7], "route=generic"),
+])
+def test_planner_reports_the_gemm_route(trop, spec, sa, sb, route):
+    st_a, st_b = _desc(spec, sa, sb)
+    text = trop.plan_describe(spec, sa, st_a, sb, st_b)
+    assert route in text, text
 
 
 @pytest.mark.parametrize("spec,err", [
