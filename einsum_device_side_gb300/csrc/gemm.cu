@@ -555,63 +555,82 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
 #ifndef TROP_RESOLVE_MINB
 #define TROP_RESOLVE_MINB 2
 #endif
-constexpr int RTHREADS = 256, RWARPS = RTHREADS / 32, RGK = 256;
+constexpr int RTHREADS = 256, RWARPS = RTHREADS / 32, RGK = 256;  // B rows staged per group (64 columns)
 constexpr int RR = CH <= 8 ? TROP_RESOLVE_RR : 2;  // rows per warp step: RR x 2 outputs per lane
 constexpr size_t SMEM_RESOLVE = sizeof(float) * RGK * BN;  // 64 KiB
 static_assert(RGK % CH == 0, "a chunk never straddles two staged groups");
 
-// The rows mb .. me-1 of one staged group, for the common layout: C and I with unit column
-// stride, every chunk whole (K a multiple of CH) and A's segments 16-byte aligned.  Branch
-// free per output: a dead output (no pending chunk in this group) loads A's first segment,
-// searches B's first staged rows and stores nothing.
-template <int SR>
-__device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const float (*EB)[BN],
+// The rows mb .. me-1 of one staged group of a PW-column panel, for the common layout: C
+// and I with unit column stride, every chunk whole (K a multiple of CH) and A's segments
+// 16-byte aligned.  A lane owns NCOL columns (l, l + 32 for PW = 64) of RSUB interleaved rows
+// (lanes l and l + PW for PW = 16) per row slot, RRP row slots per step.  Branch free per
+// output: a dead output (no pending chunk in this group) loads A's first segment, searches
+// the first staged rows and stores nothing.
+template <int PW>
+struct PanelShape {
+    static constexpr int NCOL = PW >= 64 ? PW / 32 : 1;  // columns per lane
+    static constexpr int RSUB = PW >= 32 ? 1 : 32 / PW;  // rows sharing a row slot
+    static constexpr int RRP = PW >= 64 ? RR : 2 * RR;   // row slots per lane and step
+    static constexpr int ROWS = RRP * RSUB;              // rows per warp step
+    static constexpr int GK = (int)(SMEM_RESOLVE / sizeof(float)) / PW;  // B rows per staged group
+};
+
+template <int SR, int PW>
+__device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const float* __restrict__ EB,
                                                   const float* __restrict__ A, const float* __restrict__ Cb,
                                                   int32_t* __restrict__ Ib, int n0, int mb, int me, int k0,
                                                   int kn, int warp, int lane)
 {
     using O = Ops<SR>;
-    const bool col0 = n0 + lane < p.N, col1 = n0 + 32 + lane < p.N;
-    const float* __restrict__ cb = Cb + n0 + lane;
-    int32_t* __restrict__ ib = Ib + n0 + lane;
-    float nval[RR][2];
-    int32_t ncode[RR][2];
+    using S = PanelShape<PW>;
+    constexpr int NCOL = S::NCOL, RSUB = S::RSUB, RRP = S::RRP, ROWS = S::ROWS;
+    const int cl = PW >= 32 ? lane : lane % PW;  // column (of the first column group)
+    const int rs = PW >= 32 ? 0 : lane / PW;     // row within a row slot
+    bool colok[NCOL];
+#pragma unroll
+    for (int h = 0; h < NCOL; ++h) colok[h] = n0 + h * 32 + cl < p.N;
+    const float* __restrict__ cb = Cb + n0 + cl;
+    int32_t* __restrict__ ib = Ib + n0 + cl;
+    float nval[RRP][NCOL];
+    int32_t ncode[RRP][NCOL];
     auto load_step = [&](int ms) {
 #pragma unroll
-        for (int r = 0; r < RR; ++r) {
-            const int m = ms + r;
+        for (int r = 0; r < RRP; ++r) {
+            const int m = ms + r * RSUB + rs;
             const float* cr = cb + (int64_t)m * p.sCm;
             const int32_t* ir = ib + (int64_t)m * p.sIm;
-            const bool ok0 = m < me && col0, ok1 = m < me && col1;
-            nval[r][0] = ok0 ? cr[0] : 0.0f;
-            nval[r][1] = ok1 ? cr[32] : 0.0f;
-            ncode[r][0] = ok0 ? ir[0] : 0;
-            ncode[r][1] = ok1 ? ir[32] : 0;
+#pragma unroll
+            for (int h = 0; h < NCOL; ++h) {
+                const bool ok = m < me && colok[h];
+                nval[r][h] = ok ? cr[h * 32] : 0.0f;
+                ncode[r][h] = ok ? ir[h * 32] : 0;
+            }
         }
     };
-    int ms = mb + warp * RR;
+    int ms = mb + warp * ROWS;
     if (ms < me) load_step(ms);
-    for (; ms < me; ms += RWARPS * RR) {
-        float val[RR][2];
-        int ka[RR][2];
-        bool live[RR][2];
+    for (; ms < me; ms += RWARPS * ROWS) {
+        float val[RRP][NCOL];
+        int ka[RRP][NCOL];
+        bool live[RRP][NCOL];
 #pragma unroll
-        for (int r = 0; r < RR; ++r)
+        for (int r = 0; r < RRP; ++r)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NCOL; ++h) {
                 val[r][h] = nval[r][h];
                 const int kc = (-ncode[r][h] - 1) * CH;
                 live[r][h] = ncode[r][h] < 0 && kc >= k0 && kc < k0 + kn;
                 ka[r][h] = live[r][h] ? kc : k0;
             }
-        if (ms + RWARPS * RR < me) load_step(ms + RWARPS * RR);
-        float av[RR][2][CH];
+        if (ms + RWARPS * ROWS < me) load_step(ms + RWARPS * ROWS);
+        float av[RRP][NCOL][CH];
 #pragma unroll
-        for (int r = 0; r < RR; ++r) {
+        for (int r = 0; r < RRP; ++r) {
+            const int m = ms + r * RSUB + rs;
             // a row past me (end of the range) reads row mb instead: always inside A
-            const float* arow = A + (int64_t)(ms + r < me ? ms + r : mb) * p.sAm;
+            const float* arow = A + (int64_t)(m < me ? m : mb) * p.sAm;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < NCOL; ++h)
 #pragma unroll
                 for (int kk = 0; kk < CH; kk += 4) {
                     const float4 x = __ldg(reinterpret_cast<const float4*>(arow + ka[r][h] + kk));
@@ -622,33 +641,40 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
                 }
         }
 #pragma unroll
-        for (int r = 0; r < RR; ++r)
+        for (int r = 0; r < RRP; ++r)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float* eb = &EB[ka[r][h] - k0][h * 32 + lane];
+            for (int h = 0; h < NCOL; ++h) {
+                const float* eb = EB + (ka[r][h] - k0) * PW + h * 32 + cl;
                 int idx = 0;
 #pragma unroll
                 for (int kk = CH - 2; kk >= 0; kk -= 2) {
                     const float2 t = O::mul2(make_float2(av[r][h][kk], av[r][h][kk + 1]),
-                                             make_float2(eb[kk * BN], eb[(kk + 1) * BN]));
+                                             make_float2(eb[kk * PW], eb[(kk + 1) * PW]));
                     idx = t.y == val[r][h] ? kk + 1 : idx;
                     idx = t.x == val[r][h] ? kk : idx;
                 }
-                if (live[r][h]) ib[(int64_t)(ms + r) * p.sIm + h * 32] = ka[r][h] + idx;
+                if (live[r][h]) ib[(int64_t)(ms + r * RSUB + rs) * p.sIm + h * 32] = ka[r][h] + idx;
             }
     }
 }
 
-template <int SR>
+// PW: columns per panel.  A narrower panel stages more B rows in the same 64 KiB (GK = 256,
+// 512, 1024 for PW = 64, 32, 16), so a long contraction needs fewer passes over the rows;
+// only the common layout (resolve_rows_fast) runs with PW < 64.
+template <int SR, int PW>
 __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(TiledParams p)
 {
     using O = Ops<SR>;
+    constexpr int GK = PanelShape<PW>::GK;
+    static_assert(GK % CH == 0, "a chunk never straddles two staged groups");
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float(*EB)[BN] = reinterpret_cast<float(*)[BN]>(smem_raw);
+    float* EBf = reinterpret_cast<float*>(smem_raw);
+    float(*EB)[BN] = reinterpret_cast<float(*)[BN]>(smem_raw);  // the PW = 64 view
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t ubeg = (uint64_t)blockIdx.x * p.r_units / gridDim.x;
     const uint64_t uend = (uint64_t)(blockIdx.x + 1) * p.r_units / gridDim.x;
-    const int ngr = (p.K + RGK - 1) / RGK;
+    const int ngr = (p.K + GK - 1) / GK;
+    const uint32_t npan = (uint32_t)((p.N + PW - 1) / PW);  // panels per batch
     // common layout: unit column strides, whole chunks, 16-byte aligned A segments
     const bool fast = p.vecA && p.K % CH == 0 && p.sCn == 1 && p.sIn == 1;
     bool waited = false;
@@ -658,8 +684,8 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
         const int mb = (int)(u - pn * (uint64_t)p.M);
         const int me = (int)min((uint64_t)p.M, (uint64_t)mb + (uend - u));
         u += (uint64_t)(me - mb);
-        const uint32_t b = (uint32_t)(pn / p.tiles_n);
-        const int n0 = (int)(pn - (uint64_t)b * p.tiles_n) * BN;
+        const uint32_t b = (uint32_t)(pn / npan);
+        const int n0 = (int)(pn - (uint64_t)b * npan) * PW;
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
         const float* __restrict__ A = p.A + oa;
@@ -676,12 +702,12 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
             offI[h] = (int64_t)n * p.sIn;
         }
         for (int g = 0; g < ngr; ++g) {
-            const int k0 = g * RGK;
-            const int kn = min(RGK, p.K - k0);
+            const int k0 = g * GK;
+            const int kn = min(GK, p.K - k0);
             __syncthreads();  // every warp is done with the rows staged before
-            for (int e = tid; e < kn * (BN / 4); e += RTHREADS) {
-                const int kk = e / (BN / 4), nq = (e % (BN / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
-                float* dst = &EB[kk][nq];
+            for (int e = tid; e < kn * (PW / 4); e += RTHREADS) {
+                const int kk = e / (PW / 4), nq = (e % (PW / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
+                float* dst = EBf + kk * PW + nq;
                 if (p.vecB) {
                     const int valid = max(0, min(4, p.N - gn));
                     cp_async16(dst, valid ? B + (int64_t)gk * p.sBk + gn : B, valid * 4);
@@ -700,9 +726,10 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
             }
 
             if (fast) {
-                resolve_rows_fast<SR>(p, EB, A, Cb, Ib, n0, mb, me, k0, kn, warp, lane);
+                resolve_rows_fast<SR, PW>(p, EBf, A, Cb, Ib, n0, mb, me, k0, kn, warp, lane);
                 continue;
             }
+            if constexpr (PW != BN) continue;  // (the host sends other layouts to PW = 64)
             float nval[RR][2];
             int32_t ncode[RR][2];
             auto load_step = [&](int ms) {
@@ -938,6 +965,43 @@ int resident_ctas(const void* fn, int threads, size_t smem, std::atomic<int>& ca
     return occ;
 }
 
+template <int SR, int PW>
+int launch_resolve_pw(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t s, const DeviceInfo* dev)
+{
+    static std::atomic<int> occ{0};
+    const uint64_t npan = (uint64_t)((p.N + PW - 1) / PW);
+    p.r_units = (uint64_t)nbatch * npan * (uint64_t)M;
+    const uint64_t slots =
+        (uint64_t)dev->sm_count * resident_ctas((const void*)k_argmax_resolve<SR, PW>, RTHREADS, SMEM_RESOLVE, occ);
+    const uint64_t per_cta = (uint64_t)RWARPS * PanelShape<PW>::ROWS;
+    const uint64_t want = (p.r_units + per_cta - 1) / per_cta;
+    // programmatic dependent launch: its CTAs stage B while the GEMM drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::max<uint64_t>(1, std::min(slots, want)));
+    cfg.blockDim = dim3(RTHREADS);
+    cfg.dynamicSmemBytes = SMEM_RESOLVE;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_argmax_resolve<SR, PW>, p);
+    if (e != cudaSuccess) return cuda_error(e, "k_argmax_resolve");
+    return check_launch("k_argmax_resolve");
+}
+
+// Panel width of the resolve pass: the widest whose staged group covers K (fewest passes over
+// the rows), 64 columns for layouts outside the common one.
+template <int SR>
+int launch_resolve(TiledParams& p, const GemmDesc& g, int64_t nbatch, cudaStream_t s, const DeviceInfo* dev)
+{
+    const bool fast = p.vecA && p.K % CH == 0 && p.sCn == 1 && p.sIn == 1;
+    if (!fast || p.K <= PanelShape<64>::GK) return launch_resolve_pw<SR, 64>(p, g.M, nbatch, s, dev);
+    if (p.K <= PanelShape<32>::GK) return launch_resolve_pw<SR, 32>(p, g.M, nbatch, s, dev);
+    return launch_resolve_pw<SR, 16>(p, g.M, nbatch, s, dev);
+}
+
 // Stream-K only when the last wave would run at most this full (percent); each stream-K
 // CTA gets at least SK_MIN_UNITS k-tiles (unless a tile has fewer) and a tile is cut into at
 // most SK_MAX_SEGS segments.
@@ -949,7 +1013,7 @@ constexpr uint64_t SK_MAX_FILL_PCT = TROP_SK_MAX_FILL_PCT, SK_MIN_UNITS = 4, SK_
 template <int SR, bool ARG>
 int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 {
-    static std::atomic<int> occ_gemm{0}, occ_resolve{0};
+    static std::atomic<int> occ_gemm{0};
     TiledParams p{};
     p.M = (int)g.M;
     p.N = (int)g.N;
@@ -1027,26 +1091,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 
     k_gemm_tiled<SR, ARG, TN><<<(unsigned)(p.T_dp + G_sk), THREADS, 0, s>>>(p);
     int rc = check_launch("k_gemm_tiled");
-    if (rc == TROP_OK && ARG) {
-        p.r_units = (uint64_t)nbatch * p.tiles_n * (uint64_t)g.M;
-        const uint64_t slots = (uint64_t)dev->sm_count *
-                               resident_ctas((const void*)k_argmax_resolve<SR>, RTHREADS, SMEM_RESOLVE, occ_resolve);
-        const uint64_t want = (p.r_units + RWARPS * RR - 1) / (RWARPS * RR);
-        // programmatic dependent launch: its CTAs stage B while the GEMM drains
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)std::max<uint64_t>(1, std::min(slots, want)));
-        cfg.blockDim = dim3(RTHREADS);
-        cfg.dynamicSmemBytes = SMEM_RESOLVE;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, k_argmax_resolve<SR>, p);
-        if (e != cudaSuccess) rc = cuda_error(e, "k_argmax_resolve");
-        else rc = check_launch("k_argmax_resolve");
-    }
+    if (rc == TROP_OK && ARG) rc = launch_resolve<SR>(p, g, nbatch, s, dev);
     if (ws) pool_retire(ws, s);
     return rc;
 }
@@ -1321,8 +1366,12 @@ int register_gemm_kernels()
 {
     cudaFuncAttributes a;
     {
-        const void* kr[] = {(const void*)k_argmax_resolve<TROP_MAXPLUS>, (const void*)k_argmax_resolve<TROP_MINPLUS>,
-                            (const void*)k_argmax_resolve<TROP_MAXTIMES>};
+        const void* kr[] = {
+            (const void*)k_argmax_resolve<TROP_MAXPLUS, 64>,  (const void*)k_argmax_resolve<TROP_MINPLUS, 64>,
+            (const void*)k_argmax_resolve<TROP_MAXTIMES, 64>, (const void*)k_argmax_resolve<TROP_MAXPLUS, 32>,
+            (const void*)k_argmax_resolve<TROP_MINPLUS, 32>,  (const void*)k_argmax_resolve<TROP_MAXTIMES, 32>,
+            (const void*)k_argmax_resolve<TROP_MAXPLUS, 16>,  (const void*)k_argmax_resolve<TROP_MINPLUS, 16>,
+            (const void*)k_argmax_resolve<TROP_MAXTIMES, 16>};
         for (const void* k : kr) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_RESOLVE);
             if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (argmax resolve smem)");

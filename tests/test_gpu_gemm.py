@@ -40,7 +40,8 @@ def _check(trop, a, b, sr, a_dev=None, b_dev=None):
 
 @pytest.mark.parametrize("sr", SR)
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 64, 64, 64), (3, 70, 45, 37), (2, 130, 129, 70),
-                                   (1, 200, 65, 257), (4, 17, 300, 16), (2, 5, 7, 3), (1, 64, 64, 1)])
+                                   (1, 200, 65, 257), (4, 17, 300, 16), (2, 5, 7, 3), (1, 64, 64, 1),
+                                   (2, 96, 80, 384), (1, 70, 130, 512), (1, 66, 40, 1032)])
 def test_gemm_matches_oracle(trop, sr, shape):
     bt, m, n, k = shape
     a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
