@@ -241,12 +241,18 @@ def secondary(trop, torch, pk, reps=20):
 
     for dt in ("f32", "i32"):
         x, perm = synth.permute_inputs(dt)
-        xd = torch.from_numpy(x).cuda()
         src = "abcdef"
         spec = src + "->" + "".join(src[p] for p in perm)
-        y = torch.empty([16] * 6, dtype=xd.dtype, device="cuda")
-        t = timed(lambda: trop.permute_trace(xd, spec, out=y), reps)
-        tg = graph_timed(lambda: trop.permute_trace(xd, spec, out=y))
+        # three input/output pairs (384 MiB) rotated so each call reads and writes past the L2
+        xs = [torch.from_numpy(x).cuda() for _ in range(3)]
+        ys = [torch.empty([16] * 6, dtype=xs[0].dtype, device="cuda") for _ in range(3)]
+        rot = [0]
+
+        def perm_call():
+            i = rot[0] = (rot[0] + 1) % 3
+            trop.permute_trace(xs[i], spec, out=ys[i])
+        t = timed(perm_call, reps)
+        tg = graph_timed(perm_call, calls=21)
         gbs = 2 * x.nbytes / t / 1e9
         out[f"permute_16^6_{dt}"] = {"spec": spec, "GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "us": t * 1e6,
                                     "us_device": None if tg is None else tg * 1e6,
@@ -261,7 +267,30 @@ def secondary(trop, torch, pk, reps=20):
                               "us_device": None if tg is None else tg * 1e6,
                               "GB/s_device": None if tg is None else moved / tg / 1e9,
                               "note": "us: one API call (host bound at 4 MiB); us_device: per call inside a "
-                                      "replayed CUDA graph of 20 calls"}
+                                      "replayed CUDA graph of 20 calls; permutes rotate 3 buffer pairs (384 MiB)"}
+    # the '->jk' variant of the trace: (+)-reduction over the diagonal label as well
+    yj = torch.empty((64, 64), device="cuda")
+    t = timed(lambda: trop.permute_trace(tr, "iijk->jk", out=yj), reps)
+    tg = graph_timed(lambda: trop.permute_trace(tr, "iijk->jk", out=yj))
+    moved = 128 * 64 * 64 * 4 + 64 * 64 * 4
+    out["trace_iijk->jk"] = {"us": t * 1e6, "us_device": None if tg is None else tg * 1e6,
+                             "GB/s_device": None if tg is None else moved / tg / 1e9,
+                             "frac_hbm_device": None if tg is None else moved / tg / 1e9 / pk["hbm_gbs"]}
+    # 64^3 max-plus GEMM with argmax (integer entries, ties), then a transpose of value and argmax
+    a64, b64 = synth.gemm64_inputs()
+    a64d, b64d = torch.from_numpy(a64).cuda(), torch.from_numpy(b64).cuda()
+    c64 = torch.empty((1, 64, 64), device="cuda")
+    i64 = torch.empty((1, 64, 64), dtype=torch.int32, device="cuda")
+    ct = torch.empty((1, 64, 64), device="cuda")
+    it = torch.empty((1, 64, 64), dtype=torch.int32, device="cuda")
+
+    def c1():
+        trop.gemm(a64d, b64d, 0, out=c64, out_argmax=i64)
+        trop.permute_pair(c64, i64, "bmn->bnm", out_val=ct, out_arg=it)
+    t = timed(c1, reps)
+    tg = graph_timed(c1)
+    out["gemm64_argmax_transpose"] = {"us": t * 1e6, "us_device": None if tg is None else tg * 1e6,
+                                      "G semiring-ops/s_device": None if tg is None else 64 ** 3 / tg / 1e9}
     A, B = synth.einsum_inputs()
     Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     o = torch.empty((16, 512, 512), device="cuda")

@@ -445,6 +445,59 @@ __global__ void __launch_bounds__(NT) k_reduce_block(const T* __restrict__ in, T
     }
 }
 
+// 32 consecutive outputs along the fastest output axis (unit stride in the input, so a slice's
+// loads are coalesced) x RS slices of the reduced range per CTA: lane x of slice y takes
+// r = y, y + RS, ...  The slices' partial (value, first index) pairs are merged in shared
+// memory, a better value or an equal one with a smaller index winning: the strict
+// left-to-right result.
+template <int SR, typename T, int RS>
+__global__ void __launch_bounds__(32 * RS) k_reduce_tile(const T* __restrict__ in, T* __restrict__ out,
+                                                        int32_t* __restrict__ arg, RedParams p)
+{
+    using S = Semi<SR, T>;
+    __shared__ T sv[RS][32];
+    __shared__ int64_t si[RS][32];
+    const int x = threadIdx.x & 31, y = threadIdx.x >> 5;
+    const int64_t inner = p.out_size[p.out_rank - 1];
+    const int64_t per_row = (inner + 31) / 32;
+    const int64_t groups = p.n_out / inner * per_row;
+    for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
+        const int64_t row = g / per_row, c = (g - row * per_row) * 32 + x;
+        const bool valid = c < inner;
+        int64_t oi = 0, oo = 0, oa = 0;
+        if (valid) out_offsets(p, row * inner + c, oi, oo, oa);
+        T best = S::zero();
+        int64_t idx = NO_INDEX;
+        if (valid) {
+#pragma unroll 4
+            for (int64_t r = y; r < p.R; r += RS) {
+                const T v = __ldg(in + oi + red_offset(p, r));
+                if (S::better(v, best)) {
+                    best = v;
+                    idx = r;
+                }
+            }
+        }
+        sv[y][x] = best;
+        si[y][x] = idx;
+        __syncthreads();
+        if (y == 0 && valid) {
+#pragma unroll
+            for (int q = 1; q < RS; ++q) {
+                const T v = sv[q][x];
+                const int64_t i = si[q][x];
+                if (S::better(v, best) || (v == best && i < idx)) {
+                    best = v;
+                    idx = i;
+                }
+            }
+            out[oo] = best;
+            if (arg) arg[oa] = idx == NO_INDEX ? 0 : (int32_t)idx;
+        }
+        __syncthreads();
+    }
+}
+
 // combine the chunks of each output in chunk order (strict: earliest wins)
 template <int SR, typename T>
 __global__ void k_reduce_combine(T* __restrict__ out, int32_t* __restrict__ arg, const T* __restrict__ part_v,
@@ -750,6 +803,15 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
         k_reduce_thread<SR, T><<<g, NT, 0, s>>>(in, out, arg, p);
         return check_launch("k_reduce_thread");
     }
+    if (p.out_rank >= 1 && p.out_s_in[p.out_rank - 1] == 1 && p.R <= (int64_t(1) << 24)) {
+        // outputs contiguous in the input: coalesced slices, no workspace
+        const int64_t inner = p.out_size[p.out_rank - 1];
+        const int64_t groups = p.n_out / inner * ((inner + 31) / 32);
+        const int g = (int)std::min<int64_t>(std::max<int64_t>(groups, 1), (int64_t)dev->sm_count * 16);
+        if (p.R >= 64) k_reduce_tile<SR, T, 32><<<g, 32 * 32, 0, s>>>(in, out, arg, p);
+        else k_reduce_tile<SR, T, 8><<<g, 32 * 8, 0, s>>>(in, out, arg, p);
+        return check_launch("k_reduce_tile");
+    }
     // split each output's reduced range so that enough blocks exist
     const int64_t blocks_wanted = (int64_t)dev->sm_count * 8;
     int64_t nsplit = (blocks_wanted + p.n_out - 1) / p.n_out;
@@ -826,6 +888,15 @@ int launch_reduce_scratch_typed(const void* in_, void* out_, int32_t* arg, const
         int g = grid_for(p.n_out, NT, dev->sm_count);
         k_reduce_thread<SR, T><<<g, NT, 0, s>>>(in, out, arg, p);
         return check_launch("k_reduce_thread");
+    }
+    if (p.out_rank >= 1 && p.out_s_in[p.out_rank - 1] == 1 && p.R <= (int64_t(1) << 24)) {
+        // outputs contiguous in the input: coalesced slices, no workspace
+        const int64_t inner = p.out_size[p.out_rank - 1];
+        const int64_t groups = p.n_out / inner * ((inner + 31) / 32);
+        const int g = (int)std::min<int64_t>(std::max<int64_t>(groups, 1), (int64_t)dev->sm_count * 16);
+        if (p.R >= 64) k_reduce_tile<SR, T, 32><<<g, 32 * 32, 0, s>>>(in, out, arg, p);
+        else k_reduce_tile<SR, T, 8><<<g, 32 * 8, 0, s>>>(in, out, arg, p);
+        return check_launch("k_reduce_tile");
     }
     const int64_t blocks_wanted = (int64_t)dev->sm_count * 8;
     int64_t nsplit = (blocks_wanted + p.n_out - 1) / p.n_out;
@@ -928,6 +999,7 @@ int register_unary_kernels()
         (const void*)k_transpose<int32_t, false>, (const void*)k_transpose<int64_t, false>,
         (const void*)k_transpose<int32_t, true>, (const void*)k_transpose<int64_t, true>,
         (const void*)k_reduce_thread<TROP_MAXPLUS, float>, (const void*)k_reduce_block<TROP_MAXPLUS, float>,
+        (const void*)k_reduce_tile<TROP_MAXPLUS, float, 8>, (const void*)k_reduce_tile<TROP_MAXPLUS, float, 32>,
         (const void*)k_reduce_combine<TROP_MAXPLUS, float>,
     };
     for (const void* k : ks) {

@@ -121,3 +121,21 @@ def test_permute_pair_one_mapping(trop):
     gd = _dev(np.ascontiguousarray(np.transpose(g, (1, 0, 2)))).permute(1, 0, 2)
     ov, og = trop.permute_pair(_dev(v), gd, "abc->cab")
     np.testing.assert_array_equal(og.cpu().numpy(), np.transpose(g, (2, 0, 1)))
+
+
+@pytest.mark.parametrize("sr", [0, 1, 2])
+@pytest.mark.parametrize("dtype", ["f32", "i32", "i64"])
+@pytest.mark.parametrize("spec,shape", [("ijk->k", (300, 5, 70)), ("ij->j", (100, 33)), ("iijk->jk", (128, 128, 3, 40))])
+def test_reduce_over_slices_with_ties(trop, sr, dtype, spec, shape):
+    """Reductions whose outputs are contiguous in the input run as coalesced
+    slices merged in shared memory; small integer ranges force ties, so the
+    merge must keep the first index."""
+    lo = 0 if sr == 2 else -3
+    if dtype == "f32":
+        x = synth.uniform_int(41, shape, lo, 3).astype(np.float32)
+    else:
+        x = synth.uniform_int(42, shape, lo, 3, NP[dtype])
+    y, a = trop.permute_trace(_dev(x), spec, sr, argmax=True)
+    ref, refa = oracle.einsum(spec, x, semiring=sr, nthreads=0)
+    assert y.cpu().numpy().tobytes() == ref.tobytes()
+    np.testing.assert_array_equal(a.cpu().numpy(), refa)
