@@ -69,6 +69,9 @@ def _load():
             lib.oracle_ising_ground.restype = ctypes.c_int
             lib.oracle_ising_ground.argtypes = [ctypes.c_int, ctypes.c_int, i8p, i8p, i64p, i8p,
                                                 ctypes.c_int]
+            I64 = ctypes.c_int64
+            lib.oracle_gemm_backward.restype = ctypes.c_int
+            lib.oracle_gemm_backward.argtypes = [ctypes.c_int, I64, I64, I64, I64] + [P, I64, I64, I64] * 6
             _lib = lib
     return _lib
 
@@ -153,6 +156,33 @@ def gemm(a: np.ndarray, b: np.ndarray, semiring: int = MAXPLUS, samples=None, nt
     """Batched tropical GEMM C[b,m,n] = (+)_k A[b,m,k] (x) B[b,k,n] with argmax k
     (the einsum 'bmk,bkn->bmn'); accepts strided numpy views."""
     return einsum("bmk,bkn->bmn", a, b, semiring, samples=samples, nthreads=nthreads)
+
+
+def gemm_backward(a: np.ndarray, b: np.ndarray, dc: np.ndarray, argmax: np.ndarray, semiring: int = MAXPLUS,
+                  want_a: bool = True, want_b: bool = True):
+    """Gradient of C[b,m,n] = (+)_k A[b,m,k] (x) B[b,k,n] with respect to A and B,
+    routed through the forward argmax (see oracle.c, oracle_gemm_backward).
+    Returns (dA, dB); either is None when not wanted."""
+    lib = _load()
+    a = np.asarray(a, dtype=np.float32)
+    b = np.asarray(b, dtype=np.float32)
+    dc = np.asarray(dc, dtype=np.float32)
+    argmax = np.asarray(argmax, dtype=np.int32)
+    nb, m, k = a.shape
+    n = b.shape[2]
+    assert b.shape == (nb, k, n) and dc.shape == (nb, m, n) and argmax.shape == (nb, m, n)
+    da = np.empty((nb, m, k), dtype=np.float32) if want_a else None
+    db = np.empty((nb, k, n), dtype=np.float32) if want_b else None
+
+    def ptr_st(x):
+        if x is None:
+            return [None, 0, 0, 0]
+        s = [st // x.itemsize for st in x.strides]
+        return [x.ctypes.data, s[0], s[1], s[2]]
+    rc = lib.oracle_gemm_backward(int(semiring), nb, m, n, k, *ptr_st(a), *ptr_st(b), *ptr_st(dc),
+                                  *ptr_st(argmax), *ptr_st(da), *ptr_st(db))
+    assert rc == 0
+    return da, db
 
 
 def _i8(x):

@@ -30,6 +30,24 @@
  *        max-times: (+) = max, (x) = *, zero = 0   (nonnegative domain)
  *    For i32/i64 (unary only) the zero is the type's min / max / 0.
  *
+ *  - oracle_gemm_backward: the gradient of the batched tropical GEMM with
+ *    respect to A and B, given dC and the forward argmax ("winner routing").
+ *      * omeinsum-rs issue #52, "Acceptance criteria": forward, backward and
+ *        argmax must stay consistent with the CPU path.
+ *      * tropical-gemm PR #35, review of python/tropical_gemm/pytorch.py: the
+ *        batched autograd functions route the gradient through the argmax
+ *        with scatter_add.
+ *      * rustytorch commit "ops::index": scatter-add walks the adjoint of the
+ *        selection, deterministic with duplicate indices.
+ *    Each output (b,m,n) sends dC[b,m,n] to k = I[b,m,n]:
+ *        dA[b,m,k] += dC[b,m,n]            dB[b,k,n] += dC[b,m,n]
+ *    for max-plus / min-plus, where d(a+b)/da = d(a+b)/db = 1, and
+ *        dA[b,m,k] += dC[b,m,n] * B[b,k,n] dB[b,k,n] += dC[b,m,n] * A[b,m,k]
+ *    for max-times.  Every output routes to its argmax, including the
+ *    convention 0 when nothing beat the zero; an index outside [0,K) routes
+ *    nowhere.  The sums run in increasing n (dA) and increasing m (dB), each
+ *    product and each addition rounding once in binary32.
+ *
  *  - oracle_ising_ground / oracle_ising_brute / oracle_ising_energy: the
  *    spin-glass workload that the contraction-tree executor is measured on.
  *    The pages do not describe it; the elimination order (row-major, one
@@ -278,6 +296,49 @@ int oracle_einsum(int sr, int dtype,
  * Spin x in {0,1} <-> s = 2x - 1.  Jh[r*(C-1)+c] couples (r,c)-(r,c+1),
  * Jv[r*C+c] couples (r,c)-(r+1,c).  W = max over spins of sum J s_i s_j;
  * the ground energy of H = -sum J s_i s_j is E0 = -W.                       */
+
+/* Gradient of C = A (x) B (batched tropical GEMM) with respect to A and B
+ * given dC and the forward argmax I (see the file header).  Strides in
+ * elements; dA / dB may be NULL (not wanted); A / B are read only for
+ * max-times.  Returns 0. */
+int oracle_gemm_backward(int sr, int64_t batch, int64_t M, int64_t N, int64_t K,
+                         const float* A, int64_t sAb, int64_t sAm, int64_t sAk,
+                         const float* B, int64_t sBb, int64_t sBk, int64_t sBn,
+                         const float* dC, int64_t sCb, int64_t sCm, int64_t sCn,
+                         const int32_t* I, int64_t sIb, int64_t sIm, int64_t sIn,
+                         float* dA, int64_t sdAb, int64_t sdAm, int64_t sdAk,
+                         float* dB, int64_t sdBb, int64_t sdBk, int64_t sdBn)
+{
+    if (dA) {
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t m = 0; m < M; ++m) {
+                for (int64_t k = 0; k < K; ++k) dA[b * sdAb + m * sdAm + k * sdAk] = 0.0f;
+                for (int64_t n = 0; n < N; ++n) {
+                    int64_t k = I[b * sIb + m * sIm + n * sIn];
+                    if (k < 0 || k >= K) continue;
+                    float g = dC[b * sCb + m * sCm + n * sCn];
+                    if (sr == SR_MAXTIMES) g = g * B[b * sBb + k * sBk + n * sBn];
+                    float* t = &dA[b * sdAb + m * sdAm + k * sdAk];
+                    *t = *t + g;
+                }
+            }
+    }
+    if (dB) {
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t n = 0; n < N; ++n) {
+                for (int64_t k = 0; k < K; ++k) dB[b * sdBb + k * sdBk + n * sdBn] = 0.0f;
+                for (int64_t m = 0; m < M; ++m) {
+                    int64_t k = I[b * sIb + m * sIm + n * sIn];
+                    if (k < 0 || k >= K) continue;
+                    float g = dC[b * sCb + m * sCm + n * sCn];
+                    if (sr == SR_MAXTIMES) g = g * A[b * sAb + m * sAm + k * sAk];
+                    float* t = &dB[b * sdBb + k * sdBk + n * sdBn];
+                    *t = *t + g;
+                }
+            }
+    }
+    return 0;
+}
 
 static int spin_of(int x) { return 2 * x - 1; }
 
