@@ -291,6 +291,18 @@ def secondary(trop, torch, pk, reps=20):
     tg = graph_timed(c1)
     out["gemm64_argmax_transpose"] = {"us": t * 1e6, "us_device": None if tg is None else tg * 1e6,
                                       "G semiring-ops/s_device": None if tg is None else 64 ** 3 / tg / 1e9}
+    # backward of the batched GEMM (winner routing): dA and dB of the batch-64 256^3 max-plus call
+    ga, gb = synth.gemm_batched_inputs(0)
+    gad, gbd = torch.from_numpy(ga).cuda(), torch.from_numpy(gb).cuda()
+    _, gi = trop.gemm(gad, gbd, 0)
+    gdc = torch.from_numpy(synth.uniform_f32(711, tuple(gi.shape), -1.0, 1.0)).cuda()
+    gda = torch.empty_like(gad)
+    gdb = torch.empty_like(gbd)
+    t = timed(lambda: trop.gemm_backward(gad, gbd, gdc, gi, 0, out_a=gda, out_b=gdb), reps)
+    moved = 2 * (gi.numel() * 4 + gdc.numel() * 4) + gda.numel() * 4 + gdb.numel() * 4
+    out["gemm_backward_b64x256"] = {"us": t * 1e6, "GB/s": moved / t / 1e9, "frac_hbm": moved / t / 1e9 / pk["hbm_gbs"],
+                                    "note": "dA and dB of one max-plus call; bytes = argmax and dC read once per "
+                                            "gradient + both gradients written"}
     A, B = synth.einsum_inputs()
     Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     o = torch.empty((16, 512, 512), device="cuda")

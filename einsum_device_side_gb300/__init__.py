@@ -88,6 +88,8 @@ def load(path: str | None = None):
         "tropical_gemm_strided_batched_argmax": (I, [I, I, I64, I64, I64, I64, P, I64, I64, I64, P, I64, I64, I64,
                                                      P, I64, I64, I64, P, P]),
         "tropical_einsum_pairwise": (I, [ctypes.c_char_p, TP, TP, I, TP, P, P]),
+        "tropical_gemm_backward": (I, [I, I64, I64, I64, I64, P, I64, I64, I64, P, I64, I64, I64,
+                                       P, I64, I64, I64, P, P, I64, I64, I64, P, I64, I64, I64, P]),
         "tropical_contract_tree": (I, [I, TP, I, ctypes.POINTER(TropNode), I, TP, ctypes.POINTER(P), P]),
         "tropical_tree_backtrack": (I, [I, TP, I, ctypes.POINTER(TropNode), ctypes.POINTER(P), I64, I, P, P]),
         "tropical_sync_pool": (I, []),
@@ -257,6 +259,36 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
         out.data_ptr() if out.numel() else None, out.stride(0), out.stride(1), out.stride(2),
         am.data_ptr() if am is not None and am.numel() else None, _stream(stream, out)))
     return (out, am) if argmax else out
+
+
+def gemm_backward(A: torch.Tensor, B: torch.Tensor, dC: torch.Tensor, argmax: torch.Tensor, semiring="maxplus",
+                  want_a: bool = True, want_b: bool = True, out_a=None, out_b=None, stream=None):
+    """Gradient of the strided-batched tropical GEMM C = A (x) B with respect to A
+    and B, routed through the forward argmax (dA: [batch, M, K], dB: [batch, K,
+    N]).  Returns (dA, dB); an unwanted one is None."""
+    lib = load()
+    if A.dim() == 2:
+        A = A.unsqueeze(0)
+    if B.dim() == 2:
+        B = B.unsqueeze(0)
+    if dC.dim() == 2:
+        dC, argmax = dC.unsqueeze(0), argmax.unsqueeze(0)
+    batch, M, N = dC.shape
+    K = A.shape[2]
+    if A.shape[0] != batch:
+        A = A.expand(batch, *A.shape[1:])
+    if B.shape[0] != batch:
+        B = B.expand(batch, *B.shape[1:])
+    if argmax.shape != dC.shape or argmax.stride() != dC.stride():
+        raise ValueError("argmax must have the shape and strides of dC")
+    da = (out_a if out_a is not None else torch.empty((batch, M, K), device=dC.device)) if want_a else None
+    db = (out_b if out_b is not None else torch.empty((batch, K, N), device=dC.device)) if want_b else None
+    ptr = lambda t: t.data_ptr() if t is not None and t.numel() else None  # noqa: E731
+    st = lambda t: tuple(t.stride()) if t is not None else (0, 0, 0)  # noqa: E731
+    _check(lib.tropical_gemm_backward(
+        _sr(semiring), batch, M, N, K, ptr(A), *st(A), ptr(B), *st(B), ptr(dC), *st(dC), ptr(argmax),
+        ptr(da), *st(da), ptr(db), *st(db), _stream(stream, dC)))
+    return da, db
 
 
 def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = True, out=None,

@@ -23,6 +23,7 @@ namespace trop {
 
 int register_unary_kernels();
 int register_gemm_kernels();
+int register_backward_kernels();
 int register_backtrack_kernels();
 int launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s);
 
@@ -30,6 +31,7 @@ int register_kernels_for_device()
 {
     TROP_TRY(register_unary_kernels());
     TROP_TRY(register_gemm_kernels());
+    TROP_TRY(register_backward_kernels());
     TROP_TRY(register_backtrack_kernels());
     return TROP_OK;
 }
@@ -804,6 +806,36 @@ extern "C" int tropical_gemm_strided_batched_argmax(int semiring, int dtype, int
         g.sAk = g.sBk = 0;
     }
     return launch_gemm(g, (cudaStream_t)stream, nullptr);
+}
+
+extern "C" int tropical_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int64_t K, const float* A,
+                                      int64_t sAb, int64_t sAm, int64_t sAk, const float* B, int64_t sBb, int64_t sBk,
+                                      int64_t sBn, const float* dC, int64_t sCb, int64_t sCm, int64_t sCn,
+                                      const int32_t* argmax, float* dA, int64_t sdAb, int64_t sdAm, int64_t sdAk,
+                                      float* dB, int64_t sdBb, int64_t sdBk, int64_t sdBn, void* stream)
+{
+    clear_error();
+    if (semiring < 0 || semiring > 2) return set_error(TROP_ERR_INVALID_ARG, "unknown semiring %d", semiring);
+    if (batch < 0 || M < 0 || N < 0 || K < 0) return set_error(TROP_ERR_INVALID_ARG, "negative extent");
+    if (K > INT32_MAX) return set_error(TROP_ERR_OVERFLOW, "K = %lld exceeds the int32 argmax range", (long long)K);
+    const bool wantA = dA && M > 0 && K > 0, wantB = dB && N > 0 && K > 0;
+    if (batch == 0 || (!wantA && !wantB)) return TROP_OK;
+    TROP_TRY(ensure_device(nullptr));
+    if (wantA) TROP_TRY(check_device_pointer(dA, "dA"));
+    if (wantB) TROP_TRY(check_device_pointer(dB, "dB"));
+    const bool walks = (wantA && N > 0) || (wantB && M > 0);  // anything routes at all
+    if (walks) {
+        TROP_TRY(check_device_pointer(dC, "dC"));
+        TROP_TRY(check_device_pointer(argmax, "argmax"));
+        if (semiring == TROP_MAXTIMES) {
+            if (wantA) TROP_TRY(check_device_pointer(B, "B"));
+            if (wantB) TROP_TRY(check_device_pointer(A, "A"));
+        }
+    }
+    const int64_t sA[3] = {sAb, sAm, sAk}, sB[3] = {sBb, sBk, sBn}, sC[3] = {sCb, sCm, sCn};
+    const int64_t sdA[3] = {sdAb, sdAm, sdAk}, sdB[3] = {sdBb, sdBk, sdBn};
+    return launch_gemm_backward(semiring, batch, M, N, K, A, sA, B, sB, dC, sC, argmax, wantA ? dA : nullptr, sdA,
+                                wantB ? dB : nullptr, sdB, (cudaStream_t)stream);
 }
 
 extern "C" int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, const trop_tensor* B, int semiring,

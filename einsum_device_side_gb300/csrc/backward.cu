@@ -1,0 +1,246 @@
+// backward.cu -- gradient of the strided-batched tropical GEMM, routed through
+// the forward argmax ("winner routing").
+//
+// dA[b,m,k] = sum over n (increasing) with I[b,m,n] == k of g,
+// dB[b,k,n] = sum over m (increasing) with I[b,m,n] == k of g,
+// g = dC (max-plus, min-plus) or dC times the other operand (max-times).
+// (omeinsum-rs issue #52 "Acceptance criteria": forward, backward and argmax
+// consistent with the CPU path; tropical-gemm PR #35: the batched autograd
+// functions send the gradient through the argmax with a scatter-add; the
+// rustytorch commit's ops::index: a scatter-add over the adjoint of the
+// selection, deterministic with duplicate indices and free of atomics.)
+//
+// The adjoint needs no sort: each output line (a row of dA, a column of dB) is
+// walked in increasing order by the lanes that own its bins, one lane per
+// (line, bin range), adding into bins of its own in shared memory -- every bin
+// has one writer adding in the stated order, so every sum is the sequential
+// one, bit for bit.  A CTA takes 32 lines; its 8 warps split a span of 256
+// bins (32 per lane) and all walk the same staged block (32 lines x 32 steps of
+// argmax and dC), which the CTA loads coalesced along whichever index is
+// contiguous and double buffers.  Longer contractions repeat the walk per
+// 256-bin span.  dA and dB are two jobs of one launch (blockIdx.y).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace trop {
+namespace {
+
+#ifndef TROP_ROUTE_WARPS
+#define TROP_ROUTE_WARPS 4
+#endif
+constexpr int BW_WARPS = TROP_ROUTE_WARPS, BW_THREADS = BW_WARPS * 32;
+constexpr int BW_SPAN = 256;                // bins a CTA covers per walk
+constexpr int BW_KL = BW_SPAN / BW_WARPS;   // bins per lane
+constexpr int BW_LD = 33;                   // padded rows: [bin][line] and [line][step]
+constexpr int BW_BLK = 32 * BW_LD;          // one staged 32 x 32 block
+constexpr size_t BW_SMEM = sizeof(float) * (BW_WARPS * BW_KL * BW_LD + 4 * BW_BLK) + 2 * 32 * sizeof(int64_t);
+
+// One gradient: owners (b, x), x < X, each walking s < S.
+//   index and dC of (b, x, s):     I[b*sIb + x*sIx + s*sIs], G[b*sGb + x*sGx + s*sGs]
+//   other operand of (b, k, s):    P[b*sPb + k*sPk + s*sPs]        (max-times)
+//   gradient element (b, x, k):    O[b*sOb + x*sOx + k*sOk]
+struct RouteJob {
+    int64_t X, S;
+    const int32_t* I;
+    int64_t sIb, sIx, sIs;
+    const float* G;
+    int64_t sGb, sGx, sGs;
+    const float* P;
+    int64_t sPb, sPk, sPs;
+    float* O;
+    int64_t sOb, sOx, sOk;
+};
+
+struct RouteParams {
+    int64_t nbatch, K;
+    RouteJob job[2];
+    int njobs;
+};
+
+template <bool MUL>
+__global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
+{
+    extern __shared__ __align__(16) float smem_all[];
+    if ((int)blockIdx.y >= p.njobs) return;
+    const RouteJob& j = p.job[blockIdx.y];
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    float* bins = smem_all + w * BW_KL * BW_LD;                      // this warp's [bin][line]
+    int* tk = reinterpret_cast<int*>(smem_all + BW_WARPS * BW_KL * BW_LD);  // [2][line][step]
+    float* tg = smem_all + BW_WARPS * BW_KL * BW_LD + 2 * BW_BLK;          // [2][line][step]
+    int64_t* line_i = reinterpret_cast<int64_t*>(smem_all + BW_WARPS * BW_KL * BW_LD + 4 * BW_BLK);  // [32]
+    int64_t* line_p = line_i + 32;                                   // [32] batch offset of P per line
+    const int64_t lines = p.nbatch * j.X;
+    // contiguous walk: a warp's loads cover 32 steps of one line; else 32 lines of one step
+    const bool along_walk = j.sIs == 1 && j.sIx != 1;
+    for (int64_t base = (int64_t)blockIdx.x * 32; base < lines; base += (int64_t)gridDim.x * 32) {
+        __syncthreads();  // the previous group's readers of the tables are done
+        if (tid < 32) {
+            const int64_t o = base + tid;
+            const int64_t b = o < lines ? o / j.X : 0, x = o < lines ? o - b * j.X : 0;
+            // offset of the line in argmax and dC (the entry point gives both dC's strides)
+            line_i[tid] = o < lines ? b * j.sIb + x * j.sIx : -1;
+            line_p[tid] = b * j.sPb;
+        }
+        __syncthreads();
+        // a block moves in two halves: its loads go to registers before the current block's walk,
+        // the shared stores after it, so the walk hides the load latency
+        constexpr int PER = 1024 / BW_THREADS;
+        int rk[PER];
+        float rg[PER];
+        auto fetch = [&](int64_t s0) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = tid + i * BW_THREADS;
+                const int r = along_walk ? e >> 5 : e & 31, t = along_walk ? e & 31 : e >> 5;
+                const int64_t off = line_i[r], s = s0 + t;
+                const bool in = off >= 0 && s < j.S;
+                rk[i] = in ? __ldg(j.I + off + s * j.sIs) : -1;
+                rg[i] = in ? __ldg(j.G + off + s * j.sGs) : 0.0f;
+            }
+        };
+        auto put = [&](int q) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = tid + i * BW_THREADS;
+                const int r = along_walk ? e >> 5 : e & 31, t = along_walk ? e & 31 : e >> 5;
+                tk[q * BW_BLK + r * BW_LD + t] = rk[i];
+                tg[q * BW_BLK + r * BW_LD + t] = rg[i];
+            }
+        };
+        const bool valid = line_i[l] >= 0;
+        const float* Pl = MUL ? j.P + line_p[l] : nullptr;
+        for (int64_t kc = 0; kc < p.K; kc += BW_SPAN) {
+            __syncthreads();  // the previous span's stores and walks are done with bins and stages
+            const int64_t klo = kc + (int64_t)w * BW_KL;  // this lane's bins: [klo, klo + kl)
+            const int klo32 = (int)klo;                    // K < 2^31: every index fits 32 bits
+            const unsigned kl = (unsigned)max((int64_t)0, min((int64_t)BW_KL, p.K - klo));
+#pragma unroll
+            for (int kk = 0; kk < BW_KL; ++kk) bins[kk * BW_LD + l] = 0.0f;
+            int q = 0;
+            fetch(0);
+            put(0);
+            for (int64_t s0 = 0; s0 < j.S; s0 += 32) {
+                __syncthreads();  // block s0 staged; the other buffer's readers are done
+                const bool more = s0 + 32 < j.S;
+                if (more) fetch(s0 + 32);
+                const int* mk = tk + q * BW_BLK + l * BW_LD;
+                const float* mg = tg + q * BW_BLK + l * BW_LD;
+                // a step is this lane's when its bin lies in [klo, klo + kl): one unsigned compare
+                if (MUL) {
+                    // the other operand's terms of the block: loads in flight together, then applied in order
+                    float pv[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const unsigned d = (unsigned)(mk[t] - klo32);
+                        pv[t] = d < kl ? __ldg(Pl + (int64_t)mk[t] * j.sPk + (s0 + t) * j.sPs) : 0.0f;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const unsigned d = (unsigned)(mk[t] - klo32);
+                        if (d < kl) {
+                            float* dst = &bins[d * BW_LD + l];
+                            *dst = __fadd_rn(*dst, __fmul_rn(mg[t], pv[t]));
+                        }
+                    }
+                } else {
+#pragma unroll 8
+                    for (int t = 0; t < 32; ++t) {
+                        const unsigned d = (unsigned)(mk[t] - klo32);
+                        if (d < kl) {
+                            float* dst = &bins[d * BW_LD + l];
+                            *dst = __fadd_rn(*dst, mg[t]);
+                        }
+                    }
+                }
+                if (more) put(q ^ 1);
+                q ^= 1;
+            }
+            __syncwarp();
+            const int kt = (int)max((int64_t)0, min((int64_t)BW_KL, p.K - klo));
+            if (j.sOk == 1) {
+                // lanes along k: line r, 32 consecutive bins per store
+                for (int r = 0; r < 32; ++r) {
+                    const int64_t orr = base + r;
+                    if (orr >= lines) break;
+                    const int64_t br = orr / j.X, xr = orr - br * j.X;
+                    float* Or = j.O + br * j.sOb + xr * j.sOx + klo;
+                    for (int kk = l; kk < kt; kk += 32) Or[kk] = bins[kk * BW_LD + r];
+                }
+            } else if (valid) {
+                // lanes along the lines (consecutive x when sOx == 1)
+                const int64_t o = base + l, b = o / j.X, x = o - b * j.X;
+                float* Or = j.O + b * j.sOb + x * j.sOx + klo * j.sOk;
+                for (int kk = 0; kk < kt; ++kk) Or[kk * j.sOk] = bins[kk * BW_LD + l];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int64_t K, const float* A,
+                         const int64_t* sA, const float* B, const int64_t* sB, const float* dC, const int64_t* sC,
+                         const int32_t* I, float* dA, const int64_t* sdA, float* dB, const int64_t* sdB,
+                         cudaStream_t s)
+{
+    const DeviceInfo* dev = nullptr;
+    TROP_TRY(ensure_device(&dev));
+    RouteParams p{};
+    p.nbatch = batch;
+    p.K = K;
+    if (dA) {
+        // owners: rows (b, m); walk n; other operand B[b,k,n]
+        RouteJob& j = p.job[p.njobs++];
+        j.X = M;
+        j.S = N;
+        j.I = I;
+        j.sIb = sC[0], j.sIx = sC[1], j.sIs = sC[2];
+        j.G = dC;
+        j.sGb = sC[0], j.sGx = sC[1], j.sGs = sC[2];
+        j.P = B;
+        j.sPb = sB[0], j.sPk = sB[1], j.sPs = sB[2];
+        j.O = dA;
+        j.sOb = sdA[0], j.sOx = sdA[1], j.sOk = sdA[2];
+    }
+    if (dB) {
+        // owners: columns (b, n); walk m; other operand A[b,m,k]
+        RouteJob& j = p.job[p.njobs++];
+        j.X = N;
+        j.S = M;
+        j.I = I;
+        j.sIb = sC[0], j.sIx = sC[2], j.sIs = sC[1];
+        j.G = dC;
+        j.sGb = sC[0], j.sGx = sC[2], j.sGs = sC[1];
+        j.P = A;
+        j.sPb = sA[0], j.sPk = sA[2], j.sPs = sA[1];
+        j.O = dB;
+        j.sOb = sdB[0], j.sOx = sdB[2], j.sOk = sdB[1];
+    }
+    if (p.njobs == 0 || batch == 0 || K == 0) return TROP_OK;
+    int64_t ctas = 1;
+    for (int q = 0; q < p.njobs; ++q) ctas = std::max(ctas, (batch * p.job[q].X + 31) / 32);
+    const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)dev->sm_count * 16));
+    const dim3 grid(gx, (unsigned)p.njobs);
+    if (semiring == TROP_MAXTIMES) k_winner_route<true><<<grid, BW_THREADS, BW_SMEM, s>>>(p);
+    else k_winner_route<false><<<grid, BW_THREADS, BW_SMEM, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "k_winner_route");
+    count_launches(1);
+    return TROP_OK;
+}
+
+int register_backward_kernels()
+{
+    const void* ks[] = {(const void*)k_winner_route<true>, (const void*)k_winner_route<false>};
+    for (const void* k : ks) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BW_SMEM);
+        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (winner route smem)");
+    }
+    return TROP_OK;
+}
+
+}  // namespace trop

@@ -118,6 +118,13 @@ int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name);
 // The route launch_gemm takes for g (kernel, operand swap, vector width, staging) as text.
 void describe_gemm(const GemmDesc& g, char* buf, size_t n);
 
+// Gradient of the tropical GEMM routed through its argmax (backward.cu).  Strides are
+// {batch, row, column} of each 3-d operand; dA / dB nullable.
+int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int64_t K, const float* A,
+                         const int64_t* sA, const float* B, const int64_t* sB, const float* dC, const int64_t* sC,
+                         const int32_t* I, float* dA, const int64_t* sdA, float* dB, const int64_t* sdB,
+                         cudaStream_t s);
+
 // Tree back-tracking (backtrack.cu).
 struct BtNode {
     const int32_t* argmax;  // nullable

@@ -20,6 +20,10 @@
  *         output": Summary (batched max-plus / min-plus / maxmul f32 kernels
  *         with argmax; rejecting host memory; zero-sized dimension guards;
  *         same-device validation).
+ *  [RT]   rustytorch commit adding native CUDA gather / scatter-add
+ *         (ops::index): scatter-add over the adjoint of the selection, with
+ *         no atomics and deterministic results with duplicate indices; the
+ *         adjoint identity test.
  *  [WR]   tenferro-rs design note "cuTENSOR workspace retirement without a
  *         stream barrier": Proposal (event on the owning stream + retirement
  *         queue) and "Open decisions" 1-2 (drain before allocation, bound 16,
@@ -191,6 +195,33 @@ int tropical_gemm_strided_batched_argmax(int semiring, int dtype,
                                          const void* B, int64_t sBb, int64_t sBk, int64_t sBn,
                                          void* C, int64_t sCb, int64_t sCm, int64_t sCn,
                                          int32_t* argmax, void* stream);
+
+/* Backward of the strided-batched tropical GEMM: the gradient routed through
+ * the forward argmax ("winner routing") [I52 "Acceptance criteria": forward,
+ * backward and argmax consistent with the CPU path; PR35: the batched
+ * autograd functions send the gradient through the argmax with a
+ * scatter-add; RT: scatter-add over the adjoint, deterministic, no atomics].
+ * Given dC and argmax I of a forward call (I uses dC's strides):
+ *   dA[b,m,k] = sum over n in increasing order with I[b,m,n] == k of g
+ *   dB[b,k,n] = sum over m in increasing order with I[b,m,n] == k of g
+ * where g = dC[b,m,n] for max-plus / min-plus, and for max-times
+ * g = dC[b,m,n] * B[b,k,n] in dA and g = dC[b,m,n] * A[b,m,k] in dB.  Every
+ * output routes to its argmax (including 0 when nothing beat the zero); an
+ * index outside [0,K) routes nowhere.  Each product and each addition rounds
+ * once in binary32, in the order stated, so results are bit-reproducible.
+ * dA and dB are written entirely (zero where nothing routes); either may be
+ * NULL (not wanted).  A and B are read only for max-times (may be NULL
+ * otherwise).  All pointers are device memory, f32 except the int32 argmax;
+ * the caller owns every buffer.  Strides in elements, any sign-free layout.
+ * Errors: INVALID_ARG (negative extent, missing pointer), OVERFLOW
+ *         (K > INT32_MAX), HOST_POINTER, DEVICE_MISMATCH, CUDA. */
+int tropical_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int64_t K,
+                           const float* A, int64_t sAb, int64_t sAm, int64_t sAk,
+                           const float* B, int64_t sBb, int64_t sBk, int64_t sBn,
+                           const float* dC, int64_t sCb, int64_t sCm, int64_t sCn,
+                           const int32_t* argmax,
+                           float* dA, int64_t sdAb, int64_t sdAm, int64_t sdAk,
+                           float* dB, int64_t sdBb, int64_t sdBk, int64_t sdBn, void* stream);
 
 /* Pairwise tropical einsum [I52 Summary and "Resolved design for step 3";
  * PR35 Summary]:  spec "zacd,zdce->zea" over letters a-z A-Z.
