@@ -291,6 +291,31 @@ def gemm_backward(A: torch.Tensor, B: torch.Tensor, dC: torch.Tensor, argmax: to
     return da, db
 
 
+class TropicalGemm(torch.autograd.Function):
+    """Autograd over the batched tropical GEMM: forward = gemm (value and argmax),
+    backward = gemm_backward through the saved argmax (winner routing).
+    ``TropicalGemm.apply(A, B, semiring)`` returns C; the argmax stays saved."""
+
+    @staticmethod
+    def forward(ctx, A, B, semiring="maxplus"):
+        C, I = gemm(A, B, semiring)
+        ctx.semiring = semiring
+        ctx.save_for_backward(A, B, I)
+        ctx.mark_non_differentiable(I)
+        return C
+
+    @staticmethod
+    def backward(ctx, dC):
+        A, B, I = ctx.saved_tensors
+        dA, dB = gemm_backward(A, B, dC.contiguous(), I, ctx.semiring,
+                               want_a=ctx.needs_input_grad[0], want_b=ctx.needs_input_grad[1])
+        if dA is not None and A.dim() == 2:
+            dA = dA[0]
+        if dB is not None and B.dim() == 2:
+            dB = dB[0]
+        return dA, dB, None
+
+
 def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = True, out=None,
            out_argmax=None, stream=None):
     """Pairwise tropical einsum, e.g. ``einsum('zacd,zdce->zea', A, B)``.

@@ -95,3 +95,17 @@ def test_backward_empty_extents_zero_the_gradient(trop):
                                 torch.empty((2, 3, 0), dtype=torch.int32, device="cuda"), 0)
     assert da.shape == (2, 3, 4) and (da.cpu().numpy() == 0).all()
     assert db.shape == (2, 4, 0)
+
+
+@pytest.mark.parametrize("sr", SR)
+def test_autograd_function_routes_through_the_argmax(trop, sr):
+    a, b, dc, _ = _case(sr, 2, 30, 20, 50, seed=9)
+    ta = _dev(a).requires_grad_(True)
+    tb = _dev(b).requires_grad_(True)
+    c = trop.TropicalGemm.apply(ta, tb, sr)
+    rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+    np.testing.assert_array_equal(c.detach().cpu().numpy(), rc)
+    c.backward(_dev(dc))
+    ra, rb = oracle.gemm_backward(a, b, dc, ri, sr)
+    assert ta.grad.cpu().numpy().tobytes() == ra.tobytes()
+    assert tb.grad.cpu().numpy().tobytes() == rb.tobytes()
