@@ -81,7 +81,7 @@ def _arr(ctype, values):
     return (ctype * max(1, len(values)))(*values)
 
 
-_DTYPES = {np.dtype(np.float32): 0, np.dtype(np.int32): 1, np.dtype(np.int64): 2}
+_DTYPES = {np.dtype(np.float32): 0, np.dtype(np.int32): 1, np.dtype(np.int64): 2, np.dtype(np.float64): 3}
 
 
 def parse_spec(spec: str):

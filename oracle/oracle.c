@@ -29,6 +29,9 @@
  *        min-plus : (+) = min, (x) = +, zero = +inf
  *        max-times: (+) = max, (x) = *, zero = 0   (nonnegative domain)
  *    For i32/i64 (unary only) the zero is the type's min / max / 0.
+ *    f64 (unary and pairwise) is the same definition in binary64: the
+ *    tropical-gemm PR #35 "CPU Dtype Handling" commit supports f32 and f64
+ *    ("no more silent precision loss"); each product rounds once in binary64.
  *
  *  - oracle_gemm_backward: the gradient of the batched tropical GEMM with
  *    respect to A and B, given dC and the forward argmax ("winner routing").
@@ -70,7 +73,7 @@
 #endif
 
 enum { SR_MAXPLUS = 0, SR_MINPLUS = 1, SR_MAXTIMES = 2 };
-enum { DT_F32 = 0, DT_I32 = 1, DT_I64 = 2 };
+enum { DT_F32 = 0, DT_I32 = 1, DT_I64 = 2, DT_F64 = 3 };
 enum { OK = 0, E_ARG = -1, E_SHAPE = -2, E_DTYPE = -3, E_NOMEM = -4 };
 
 #define MAXLAB 64
@@ -92,6 +95,24 @@ static float f32_otimes(int sr, float a, float b)
 }
 
 static int f32_better(int sr, float t, float best)
+{
+    return sr == SR_MINPLUS ? (t < best) : (t > best);
+}
+
+static double f64_zero(int sr)
+{
+    if (sr == SR_MAXPLUS) return -INFINITY;
+    if (sr == SR_MINPLUS) return INFINITY;
+    return 0.0;
+}
+
+static double f64_otimes(int sr, double a, double b)
+{
+    /* one binary64 operation */
+    return sr == SR_MAXTIMES ? a * b : a + b;
+}
+
+static int f64_better(int sr, double t, double best)
 {
     return sr == SR_MINPLUS ? (t < best) : (t > best);
 }
@@ -182,9 +203,9 @@ int oracle_einsum(int sr, int dtype,
                   const int64_t* samples, int64_t nsamples, int nthreads)
 {
     if (sr < 0 || sr > 2 || nA < 0 || nA > MAXLAB || nO < 0 || nO > MAXLAB || nB > MAXLAB) return E_ARG;
-    if (dtype < 0 || dtype > 2) return E_DTYPE;
+    if (dtype < 0 || dtype > 3) return E_DTYPE;
     const int pairwise = nB >= 0;
-    if (pairwise && dtype != DT_F32) return E_DTYPE;
+    if (pairwise && dtype != DT_F32 && dtype != DT_F64) return E_DTYPE;
 
     labels_t t;
     t.n = 0;
@@ -270,6 +291,32 @@ int oracle_einsum(int sr, int dtype,
                 } while (odometer_next(K, nK, t.size, val));
             }
             ((float*)out)[w] = best;
+        } else if (dtype == DT_F64) {
+            double best = f64_zero(sr);
+            int64_t k = 0;
+            if (nK_assign > 0) {
+                for (int i = 0; i < nK; ++i) val[K[i]] = 0;
+                do {
+                    double v;
+                    if (!pairwise) {
+                        v = ((const double*)A)[offset_of(nA, idA, stA, val)];
+                    } else {
+                        v = f64_zero(sr);
+                        if (nR_assign > 0) {
+                            for (int i = 0; i < nR; ++i) val[R[i]] = 0;
+                            do {
+                                double a = ((const double*)A)[offset_of(nA, idA, stA, val)];
+                                double b = ((const double*)B)[offset_of(nB, idB, stB, val)];
+                                double p = f64_otimes(sr, a, b);
+                                if (f64_better(sr, p, v)) v = p;
+                            } while (odometer_next(R, nR, t.size, val));
+                        }
+                    }
+                    if (f64_better(sr, v, best)) { best = v; idx = (int32_t)k; }
+                    ++k;
+                } while (odometer_next(K, nK, t.size, val));
+            }
+            ((double*)out)[w] = best;
         } else {
             int64_t best = i64_zero(sr, dtype);
             int64_t k = 0;
