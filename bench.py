@@ -40,6 +40,7 @@ OPS_PER_GEMM = GEMM_B * GEMM_M * GEMM_N * GEMM_K
 SEMIRINGS = (0, 1, 2)
 METRIC = "tropical GEMM G semiring-ops/s (% of FP32 ALU peak); permute/trace GB/s (% HBM)"
 N_SETS = 3  # independent input sets rotated across steps: 288 MiB of inputs > 129 MB L2
+F64_TFLOPS_NOMINAL = 1.25  # GB300 binary64 rate, nominal (no measured figure for this pipe)
 
 
 def gemm_traffic():
@@ -303,6 +304,18 @@ def secondary(trop, torch, pk, reps=20):
     out["gemm_backward_b64x256"] = {"us": t * 1e6, "GB/s": moved / t / 1e9, "frac_hbm": moved / t / 1e9 / pk["hbm_gbs"],
                                     "note": "dA and dB of one max-plus call; bytes = argmax and dC read once per "
                                             "gradient + both gradients written"}
+    # the same batched GEMM in binary64 (max-plus with argmax): one double add per semiring op
+    fa, fb = synth.gemm_batched_inputs(0, dtype="f64")
+    fad, fbd = torch.from_numpy(fa).cuda(), torch.from_numpy(fb).cuda()
+    fc = torch.empty((64, 256, 256), dtype=torch.float64, device="cuda")
+    fi = torch.empty((64, 256, 256), dtype=torch.int32, device="cuda")
+    t = timed(lambda: trop.gemm(fad, fbd, 0, out=fc, out_argmax=fi), max(3, reps // 4))
+    ops = 64 * 256 ** 3
+    f64_peak = F64_TFLOPS_NOMINAL * 1e12 / 2
+    out["gemm_f64_b64x256"] = {"us": t * 1e6, "G semiring-ops/s": ops / t / 1e9,
+                               "frac_f64_nominal": ops / t / f64_peak,
+                               "note": "peak = nominal binary64 rate (%.2f TFLOP/s, an FMA counted as 2) / 2 = "
+                                       "one double add per semiring op" % F64_TFLOPS_NOMINAL}
     A, B = synth.einsum_inputs()
     Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     o = torch.empty((16, 512, 512), device="cuda")

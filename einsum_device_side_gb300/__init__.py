@@ -26,7 +26,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtropical_gb300.so")
 SEMIRINGS = {"maxplus": 0, "minplus": 1, "maxtimes": 2}
-_DTYPES = {torch.float32: 0, torch.int32: 1, torch.int64: 2}
+_DTYPES = {torch.float32: 0, torch.int32: 1, torch.int64: 2, torch.float64: 3}
 MAX_RANK = 32
 
 ERRORS = {
@@ -245,15 +245,19 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
     N = B.shape[2]
     if B.shape[1] != K:
         raise ValueError("inner extents differ")
+    if A.dtype not in (torch.float32, torch.float64) or B.dtype != A.dtype:
+        raise TypeError(f"gemm needs two float32 or two float64 operands, got {A.dtype} and {B.dtype}")
     if out is None:
-        out = torch.empty((batch, M, N), dtype=torch.float32, device=A.device)
+        out = torch.empty((batch, M, N), dtype=A.dtype, device=A.device)
+    elif out.dtype != A.dtype:
+        raise TypeError(f"out is {out.dtype}, operands are {A.dtype}")
     am = None
     if argmax:
         am = out_argmax if out_argmax is not None else torch.empty((batch, M, N), dtype=torch.int32, device=A.device)
         if am.stride() != out.stride():
             raise ValueError("argmax must have the strides of out")
     _check(lib.tropical_gemm_strided_batched_argmax(
-        _sr(semiring), 0, batch, M, N, K,
+        _sr(semiring), _DTYPES[A.dtype], batch, M, N, K,
         A.data_ptr() if A.numel() else None, A.stride(0), A.stride(1), A.stride(2),
         B.data_ptr() if B.numel() else None, B.stride(0), B.stride(1), B.stride(2),
         out.data_ptr() if out.numel() else None, out.stride(0), out.stride(1), out.stride(2),
@@ -322,7 +326,7 @@ def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argm
     Returns (out, argmax) or out."""
     lib = load()
     if out is None:
-        out = torch.empty(_spec_shape(spec, [A.shape, B.shape]), dtype=torch.float32, device=A.device)
+        out = torch.empty(_spec_shape(spec, [A.shape, B.shape]), dtype=A.dtype, device=A.device)
     am = None
     if argmax:
         am = out_argmax if out_argmax is not None else torch.empty(out.shape, dtype=torch.int32, device=A.device)

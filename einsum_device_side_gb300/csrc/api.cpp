@@ -24,6 +24,7 @@ namespace trop {
 int register_unary_kernels();
 int register_gemm_kernels();
 int register_backward_kernels();
+int register_gemm64_kernels();
 int register_backtrack_kernels();
 int launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s);
 
@@ -32,6 +33,7 @@ int register_kernels_for_device()
     TROP_TRY(register_unary_kernels());
     TROP_TRY(register_gemm_kernels());
     TROP_TRY(register_backward_kernels());
+    TROP_TRY(register_gemm64_kernels());
     TROP_TRY(register_backtrack_kernels());
     return TROP_OK;
 }
@@ -378,11 +380,11 @@ std::vector<int32_t> pick_group(const std::vector<int32_t>& cands, const View& v
     return g;
 }
 
-int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t* lo, int ro, float* out,
+int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t* lo, int ro, void* out,
                           const int64_t* ostride, int32_t* argmax, cudaStream_t s, bool dry, std::string* text)
 {
-    if (A0.dtype != TROP_F32 || B0.dtype != TROP_F32)
-        return set_error(TROP_ERR_DTYPE, "pairwise tropical einsum needs f32 operands");
+    if ((A0.dtype != TROP_F32 && A0.dtype != TROP_F64) || B0.dtype != A0.dtype)
+        return set_error(TROP_ERR_DTYPE, "pairwise tropical einsum needs two f32 or two f64 operands");
     View A, B;
     TROP_TRY(unique_view(A0, A));
     TROP_TRY(unique_view(B0, B));
@@ -546,11 +548,12 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
 
     GemmDesc g{};
     g.semiring = sr;
+    g.dtype = A0.dtype;
     g.M = group_sizes(Gm, A);
     g.N = group_sizes(Gn, B);
     g.K = group_sizes(Lk, A);
-    g.A = static_cast<const float*>(A.data);
-    g.B = static_cast<const float*>(B.data);
+    g.A = A.data;
+    g.B = B.data;
     g.C = out;
     g.I = argmax;
     g.sAk = sAk;
@@ -767,7 +770,7 @@ extern "C" int tropical_gemm_strided_batched_argmax(int semiring, int dtype, int
 {
     clear_error();
     if (semiring < 0 || semiring > 2) return set_error(TROP_ERR_INVALID_ARG, "unknown semiring %d", semiring);
-    if (dtype != TROP_F32) return set_error(TROP_ERR_DTYPE, "tropical GEMM supports f32 only");
+    if (dtype != TROP_F32 && dtype != TROP_F64) return set_error(TROP_ERR_DTYPE, "tropical GEMM supports f32 and f64");
     if (batch < 0 || M < 0 || N < 0 || K < 0) return set_error(TROP_ERR_INVALID_ARG, "negative extent");
     if (argmax && K - 1 > INT32_MAX)
         return set_error(TROP_ERR_OVERFLOW, "K = %lld does not fit an int32 argmax", (long long)K);
@@ -781,12 +784,13 @@ extern "C" int tropical_gemm_strided_batched_argmax(int semiring, int dtype, int
     if (argmax) TROP_TRY(check_device_pointer(argmax, "argmax"));
     GemmDesc g{};
     g.semiring = semiring;
+    g.dtype = dtype;
     g.M = M;
     g.N = N;
     g.K = K;
-    g.A = static_cast<const float*>(A);
-    g.B = static_cast<const float*>(B);
-    g.C = static_cast<float*>(C);
+    g.A = A;
+    g.B = B;
+    g.C = C;
     g.I = argmax;
     g.sAm = sAm;
     g.sAk = sAk;
@@ -853,7 +857,9 @@ extern "C" int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, 
     TROP_TRY(tensor_labels_check(A, ra, "A"));
     TROP_TRY(tensor_labels_check(B, rb, "B"));
     TROP_TRY(tensor_labels_check(out, ro, "out"));
-    if (out->dtype != TROP_F32) return set_error(TROP_ERR_DTYPE, "out must be f32");
+    if (out->dtype != TROP_F32 && out->dtype != TROP_F64) return set_error(TROP_ERR_DTYPE, "out must be f32 or f64");
+    if (A->dtype != out->dtype || B->dtype != out->dtype)
+        return set_error(TROP_ERR_DTYPE, "A, B and out must share one dtype");
     TROP_TRY(ensure_device(nullptr));
     // output extents must match the operands
     View vA = view_of(A, la), vB = view_of(B, lb);
@@ -870,7 +876,7 @@ extern "C" int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, 
         n_out *= out->shape[i];
     }
     if (argmax && n_out > 0) TROP_TRY(check_device_pointer(argmax, "argmax"));
-    return plan_and_run_pairwise(semiring, vA, vB, lo, ro, static_cast<float*>(out->data), out->stride, argmax,
+    return plan_and_run_pairwise(semiring, vA, vB, lo, ro, out->data, out->stride, argmax,
                                  (cudaStream_t)stream, false, nullptr);
 }
 
@@ -925,7 +931,8 @@ struct NodeShape {
 };
 
 int node_operand(int id, int n_inputs, const trop_tensor* inputs, const std::vector<NodeShape>& shapes,
-                 const std::vector<void*>& inter, int nlab, const int32_t* labs, View& v, const char* name)
+                 const std::vector<void*>& inter, int nlab, const int32_t* labs, int dtype, View& v,
+                 const char* name)
 {
     if (id < n_inputs) {
         const trop_tensor* t = &inputs[id];
@@ -939,7 +946,7 @@ int node_operand(int id, int n_inputs, const trop_tensor* inputs, const std::vec
                              nlab);
         v = View{};
         v.data = inter[id - n_inputs];
-        v.dtype = TROP_F32;
+        v.dtype = dtype;
         v.rank = nlab;
         for (int i = 0; i < nlab; ++i) {
             v.lab[i] = labs[i];
@@ -964,7 +971,8 @@ int tree_shapes(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop
         const int nops = nd.rhs < 0 ? 1 : 2;
         if (nd.n_out < 0 || nd.n_out > MAXR || (nd.n_out > 0 && !nd.out_labels))
             return set_error(TROP_ERR_INVALID_ARG, "node %d: bad output labels", j);
-        if (nops == 2 && dtype != TROP_F32) return set_error(TROP_ERR_DTYPE, "node %d: binary nodes need f32", j);
+        if (nops == 2 && dtype != TROP_F32 && dtype != TROP_F64)
+            return set_error(TROP_ERR_DTYPE, "node %d: binary nodes need f32 or f64", j);
         int32_t all_lab[2 * MAXR];
         int64_t all_size[2 * MAXR];
         int nall = 0;
@@ -1069,9 +1077,9 @@ extern "C" int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, i
         }
         int32_t* am = node_argmax ? node_argmax[j] : nullptr;
         View a{}, b{};
-        rc = node_operand(nd.lhs, n_inputs, inputs, shapes, inter, nd.n_lhs, nd.lhs_labels, a, "lhs");
+        rc = node_operand(nd.lhs, n_inputs, inputs, shapes, inter, nd.n_lhs, nd.lhs_labels, out->dtype, a, "lhs");
         if (rc == TROP_OK && nd.rhs >= 0)
-            rc = node_operand(nd.rhs, n_inputs, inputs, shapes, inter, nd.n_rhs, nd.rhs_labels, b, "rhs");
+            rc = node_operand(nd.rhs, n_inputs, inputs, shapes, inter, nd.n_rhs, nd.rhs_labels, out->dtype, b, "rhs");
         if (rc != TROP_OK) break;
         if (nd.rhs < 0) {
             a.dtype = out->dtype;
@@ -1079,7 +1087,7 @@ extern "C" int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, i
             rc = plan_unary(a, nd.out_labels, nd.n_out, up);
             if (rc == TROP_OK) rc = exec_unary(semiring, up, nd.n_out, dst, ostride, am, s);
         } else {
-            rc = plan_and_run_pairwise(semiring, a, b, nd.out_labels, nd.n_out, static_cast<float*>(dst), ostride, am,
+            rc = plan_and_run_pairwise(semiring, a, b, nd.out_labels, nd.n_out, dst, ostride, am,
                                        s, false, nullptr);
         }
         // retire intermediates whose last consumer is this node

@@ -1018,9 +1018,9 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
-    p.A = g.A;
-    p.B = g.B;
-    p.C = g.C;
+    p.A = static_cast<const float*>(g.A);
+    p.B = static_cast<const float*>(g.B);
+    p.C = static_cast<float*>(g.C);
     p.I = g.I;
     p.sAm = g.sAm;
     p.sBk = g.sBk;
@@ -1114,9 +1114,9 @@ int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
-    p.A = g.A;
-    p.B = g.B;
-    p.C = g.C;
+    p.A = static_cast<const float*>(g.A);
+    p.B = static_cast<const float*>(g.B);
+    p.C = static_cast<float*>(g.C);
     p.I = g.I;
     p.sAm = g.sAm;
     p.sAk = g.sAk;
@@ -1157,9 +1157,9 @@ int run_generic(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.M = g.M;
     p.N = g.N;
     p.K = g.K;
-    p.A = g.A;
-    p.B = g.B;
-    p.C = g.C;
+    p.A = static_cast<const float*>(g.A);
+    p.B = static_cast<const float*>(g.B);
+    p.C = static_cast<float*>(g.C);
     p.I = g.I;
     p.sAm = g.sAm;
     p.sAk = g.sAk;
@@ -1257,8 +1257,8 @@ int run_tiled_staged(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
         return run_tiled<SR, ARG>(g, s, dev);  // no workspace: write through the strides
     }
     GemmDesc t = g;
-    t.C = static_cast<float*>(ws);
-    t.I = ARG ? reinterpret_cast<int32_t*>(t.C + elems) : nullptr;
+    t.C = ws;
+    t.I = ARG ? reinterpret_cast<int32_t*>(static_cast<float*>(ws) + elems) : nullptr;
     t.sCm = t.sIm = g.N;
     t.sCn = t.sIn = 1;
     GatherDesc gd{};
@@ -1329,10 +1329,14 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
     // a description is about layouts: take every pointer as 256-byte aligned
     GemmDesc g0 = g1;
     const uintptr_t aligned = 256;
-    g0.A = reinterpret_cast<const float*>(aligned);
-    g0.B = reinterpret_cast<const float*>(aligned);
-    g0.C = reinterpret_cast<float*>(aligned);
+    g0.A = reinterpret_cast<const void*>(aligned);
+    g0.B = reinterpret_cast<const void*>(aligned);
+    g0.C = reinterpret_cast<void*>(aligned);
     if (g1.I) g0.I = reinterpret_cast<int32_t*>(aligned);
+    if (g1.dtype == TROP_F64) {
+        snprintf(buf, n, " route=tiled_f64");
+        return;
+    }
     bool swap = false;
     const Route r = choose(g0, swap);
     const GemmDesc g = swap ? swapped(g0) : g0;
@@ -1353,6 +1357,11 @@ int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name)
     if (g.M == 0 || g.N == 0) return TROP_OK;
     for (int d = 0; d < g.nb; ++d)
         if (g.bsize[d] == 0) return TROP_OK;
+    if (g.dtype == TROP_F64) {
+        if (kernel_name) *kernel_name = "k_gemm_tiled_f64";
+        return launch_gemm_f64(g, s);
+    }
+    if (g.dtype != TROP_F32) return set_error(TROP_ERR_DTYPE, "tropical GEMM: unsupported dtype %d", g.dtype);
     const bool arg = g.I != nullptr;
     switch (g.semiring) {
     case TROP_MAXPLUS: return arg ? run<TROP_MAXPLUS, true>(g, s, dev, kernel_name) : run<TROP_MAXPLUS, false>(g, s, dev, kernel_name);

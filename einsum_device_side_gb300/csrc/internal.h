@@ -104,10 +104,11 @@ int noalloc_scratch(void** ptr, size_t* bytes);
 // Strided-batched tropical GEMM with a multi-dimensional batch.
 struct GemmDesc {
     int semiring;
+    int dtype;  // TROP_F32 (gemm.cu) or TROP_F64 (gemm64.cu); A, B and C share it
     int64_t M, N, K;
-    const float* A;
-    const float* B;
-    float* C;
+    const void* A;
+    const void* B;
+    void* C;
     int32_t* I;  // nullable
     int64_t sAm, sAk, sBk, sBn, sCm, sCn, sIm, sIn;
     int nb;
@@ -115,6 +116,8 @@ struct GemmDesc {
     int64_t sAb[MAXB], sBb[MAXB], sCb[MAXB], sIb[MAXB];
 };
 int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name);
+// The binary64 GEMM (gemm64.cu); launch_gemm forwards TROP_F64 descriptors here.
+int launch_gemm_f64(const GemmDesc& g, cudaStream_t s);
 // The route launch_gemm takes for g (kernel, operand swap, vector width, staging) as text.
 void describe_gemm(const GemmDesc& g, char* buf, size_t n);
 

@@ -60,6 +60,7 @@ size_t dtype_bytes(int dtype)
     case TROP_F32: return 4;
     case TROP_I32: return 4;
     case TROP_I64: return 8;
+    case TROP_F64: return 8;
     default: return 0;
     }
 }

@@ -323,6 +323,18 @@ struct Semi<SR, int32_t> {
     __device__ static int32_t zero() { return SR == TROP_MAXPLUS ? INT32_MIN : SR == TROP_MINPLUS ? INT32_MAX : 0; }
     __device__ static bool better(int32_t a, int32_t b) { return SR == TROP_MINPLUS ? a < b : a > b; }
 };
+// binary64: compared through the order-preserving signed-integer image of the
+// double (integer lanes, not the narrow binary64 pipe); exact for non-NaN values
+template <int SR>
+struct Semi<SR, double> {
+    __device__ static double zero() { return SR == TROP_MAXPLUS ? -INFINITY : SR == TROP_MINPLUS ? INFINITY : 0.0; }
+    __device__ static long long key(double x)
+    {
+        const long long b = __double_as_longlong(x);
+        return b ^ (long long)((unsigned long long)(b >> 63) >> 1);
+    }
+    __device__ static bool better(double a, double b) { return SR == TROP_MINPLUS ? key(a) < key(b) : key(a) > key(b); }
+};
 template <int SR>
 struct Semi<SR, int64_t> {
     __device__ static int64_t zero() { return SR == TROP_MAXPLUS ? INT64_MIN : SR == TROP_MINPLUS ? INT64_MAX : 0; }
@@ -951,6 +963,7 @@ int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* a
         if (dtype == TROP_F32) return launch_reduce_typed<SR, float>(in, out, argmax, d, s, dev);   \
         if (dtype == TROP_I32) return launch_reduce_typed<SR, int32_t>(in, out, argmax, d, s, dev); \
         if (dtype == TROP_I64) return launch_reduce_typed<SR, int64_t>(in, out, argmax, d, s, dev); \
+        if (dtype == TROP_F64) return launch_reduce_typed<SR, double>(in, out, argmax, d, s, dev);  \
         break;
     switch (semiring) {
         TROP_RED(TROP_MAXPLUS)
@@ -975,6 +988,8 @@ int launch_reduce_scratch(int semiring, int dtype, const void* in, void* out, in
             return launch_reduce_scratch_typed<SR, int32_t>(in, out, argmax, d, scratch, scratch_bytes, s, dev); \
         if (dtype == TROP_I64)                                                                                  \
             return launch_reduce_scratch_typed<SR, int64_t>(in, out, argmax, d, scratch, scratch_bytes, s, dev); \
+        if (dtype == TROP_F64)                                                                                  \
+            return launch_reduce_scratch_typed<SR, double>(in, out, argmax, d, scratch, scratch_bytes, s, dev);  \
         break;
     switch (semiring) {
         TROP_RED_S(TROP_MAXPLUS)

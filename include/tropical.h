@@ -34,8 +34,11 @@
  *     TROP_MAXPLUS : a (+) b = max(a,b), a (x) b = a + b, zero = -inf
  *     TROP_MINPLUS : a (+) b = min(a,b), a (x) b = a + b, zero = +inf
  *     TROP_MAXTIMES: a (+) b = max(a,b), a (x) b = a * b, zero = 0
- * Each (x) rounds once in IEEE binary32 (round to nearest even, subnormals
- * kept); each (+) is exact, so results do not depend on evaluation order.
+ * Each (x) rounds once in the operands' IEEE format, binary32 (TROP_F32) or
+ * binary64 (TROP_F64) (round to nearest even, subnormals kept); each (+) is
+ * exact, so results do not depend on evaluation order.  f64 operands: I52
+ * "Resolved design for step 3" kernel (a) lists f32/f64 operands; PR35
+ * "Summary of latest fixes" handles f32 and f64 on its CPU path.
  * Argmax: the smallest contracted linear index that reaches the result; 0
  * when no term beats the semiring zero (e.g. an empty contraction).
  * Preconditions (not checked): no NaN; no -0.0; max-plus operands below
@@ -75,7 +78,7 @@ extern "C" {
 #define TROP_MAX_RANK 32
 
 typedef enum { TROP_MAXPLUS = 0, TROP_MINPLUS = 1, TROP_MAXTIMES = 2 } trop_semiring;
-typedef enum { TROP_F32 = 0, TROP_I32 = 1, TROP_I64 = 2 } trop_dtype;
+typedef enum { TROP_F32 = 0, TROP_I32 = 1, TROP_I64 = 2, TROP_F64 = 3 } trop_dtype;
 
 enum {
     TROP_OK = 0,
@@ -142,7 +145,7 @@ int tropical_init(int device);
  *   out[o] = (+) over the labels of `in` absent from the output of
  *   in[diagonal position], in the semiring `semiring`; with no such label
  *   this is a strided gather (any dtype; semiring only checked for range).
- * in, out:  same dtype (f32, i32 or i64); out.shape must equal the output
+ * in, out:  same dtype (f32, f64, i32 or i64); out.shape must equal the output
  *           label extents; out may be strided.
  * argmax:   nullable int32 buffer, contiguous row-major in out's shape: the
  *           row-major linear index over the reduced labels (first-appearance
@@ -175,7 +178,7 @@ int tropical_permute_trace_noalloc(const trop_tensor* in, const char* spec, int 
  * [I52 "Resolved design for step 3": the float result and the argmax must be
  * permuted with bit-for-bit identical index mappings].  spec is a pure
  * permutation "abc->cab" (no repeated or dropped label).  val_in/val_out are
- * f32, i32 or i64 of equal dtype; arg_in/arg_out are int32 tensors of the
+ * f32, f64, i32 or i64 of equal dtype; arg_in/arg_out are int32 tensors of the
  * same shapes as val_in/val_out (any strides).  One kernel launch moves both. */
 int tropical_permute_pair(const trop_tensor* val_in, const trop_tensor* arg_in, const char* spec,
                           const trop_tensor* val_out, const trop_tensor* arg_out, void* stream);
@@ -185,7 +188,8 @@ int tropical_permute_pair(const trop_tensor* val_in, const trop_tensor* arg_in, 
  *   C[b,m,n] = (+)_{k<K} A[b,m,k] (x) B[b,k,n]
  *   argmax[b,m,n] = smallest k reaching C[b,m,n] (0 if none beats zero).
  * Element (b,m,k) of A is A[b*sAb + m*sAm + k*sAk]; likewise B and C.
- * argmax (nullable, int32) uses C's strides.  dtype must be TROP_F32.
+ * argmax (nullable, int32) uses C's strides.  dtype: TROP_F32 or TROP_F64,
+ * shared by A, B and C (the pointers carry no type: the caller guarantees it).
  * Errors: INVALID_ARG (negative extent, null pointer with nonzero extent),
  *         DTYPE, OVERFLOW (K > INT32_MAX with argmax), HOST_POINTER,
  *         DEVICE_MISMATCH, CUDA. */
@@ -226,7 +230,7 @@ int tropical_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, in
 /* Pairwise tropical einsum [I52 Summary and "Resolved design for step 3";
  * PR35 Summary]:  spec "zacd,zdce->zea" over letters a-z A-Z.
  *   out[o] = (+) over all assignments of the labels absent from the output
- *            of A[..] (x) B[..]   (f32 only)
+ *            of A[..] (x) B[..]   (A, B and out all f32 or all f64)
  *   argmax[o] = row-major linear index over the CONTRACTED labels (present
  *            in both operands, absent from the output), ordered by first
  *            appearance in A's spec, of the smallest index reaching out[o].
@@ -253,7 +257,7 @@ int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, const trop_
  *   j receives node j's argmax (contiguous, node output shape), with the
  *   meaning of tropical_einsum_pairwise (binary) or tropical_permute_trace
  *   (unary).
- * All inputs must share out's dtype; binary nodes need f32.
+ * All inputs must share out's dtype; binary nodes need f32 or f64.
  * Errors: as the pairwise/unary calls, plus INVALID_ARG for bad operand ids.
  * Validation of the whole tree happens before the first launch. */
 int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, int n_nodes,

@@ -13,6 +13,10 @@ Recipes (one stream per tensor, ``seed = 0x7E570000 + 16 * workload + tensor``):
 * f32 uniform(a, b): ``a + (b - a) * (z >> 40) * 2**-24``.  For (a, b) = (-1, 1)
   and (0, 1) every value is exactly representable in binary32, and (-1, 1)
   never yields -0.0.
+* f64 uniform(a, b): ``a + (b - a) * (z >> 11) * 2**-53``.  For (-1, 1) and
+  (0, 1) every value is exactly representable in binary64 (and uses the whole
+  53-bit significand, so binary32 arithmetic would round differently); (-1, 1)
+  never yields -0.0.
 * integers uniform in [lo, hi]: ``lo + z % n`` with rejection of the top
   partial block (``z >= 2**64 - 2**64 % n``), consuming the stream in order.
 * axis permutations: Fisher-Yates, swapping position i with ``z % (i + 1)``
@@ -60,6 +64,13 @@ def uniform_f32(seed: int, shape, lo: float, hi: float) -> np.ndarray:
     u = (z >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
     x = lo + (hi - lo) * u
     return x.astype(np.float32).reshape(shape)
+
+
+def uniform_f64(seed: int, shape, lo: float, hi: float) -> np.ndarray:
+    n = int(np.prod(shape, dtype=np.int64))
+    z = splitmix64(seed, n)
+    u = (z >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return (lo + (hi - lo) * u).reshape(shape)
 
 
 def uniform_int(seed: int, shape, lo: int, hi: int, dtype=np.int32) -> np.ndarray:
@@ -119,11 +130,12 @@ def gemm64_inputs():
 SEMIRING_RANGES = {0: (-1.0, 1.0), 1: (-1.0, 1.0), 2: (0.0, 1.0)}
 
 
-def gemm_batched_inputs(semiring: int, batch=64, m=256, n=256, k=256):
+def gemm_batched_inputs(semiring: int, batch=64, m=256, n=256, k=256, dtype="f32"):
     lo, hi = SEMIRING_RANGES[semiring]
     s = W_GEMM_BATCHED
-    a = uniform_f32(seed_for(s, 2 * semiring), (batch, m, k), lo, hi)
-    b = uniform_f32(seed_for(s, 2 * semiring + 1), (batch, k, n), lo, hi)
+    draw = uniform_f64 if dtype == "f64" else uniform_f32
+    a = draw(seed_for(s, 2 * semiring), (batch, m, k), lo, hi)
+    b = draw(seed_for(s, 2 * semiring + 1), (batch, k, n), lo, hi)
     return a, b
 
 
