@@ -233,3 +233,59 @@ def test_whole_tiles_long_contraction_sampled(trop, sr):
     t = torch.gather(ad, 2, idx) * torch.gather(bd, 1, idx) if sr == 2 else \
         torch.gather(ad, 2, idx) + torch.gather(bd, 1, idx)
     assert torch.equal(t, c)
+
+
+def test_argmax_gemm_streams_and_graph_replay(trop):
+    """Whole-tile argmax GEMMs (value kernel + programmatic-dependent resolve
+    pass): results must not depend on the stream a call runs on, on the order
+    of problem sizes, or on replaying a captured CUDA graph with new inputs."""
+    cases = [(0, 64, 256, 256, 256), (1, 8, 192, 320, 300), (2, 30, 128, 128, 512), (0, 40, 70, 200, 96)]
+    work = []
+    for sr, bt, m, n, k in cases:
+        a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+        work.append((sr, _dev(a), _dev(b)))
+    ref = [trop.gemm(ad, bd, sr) for sr, ad, bd in work]
+    torch.cuda.synchronize()
+    for j, (sr, ad, bd) in enumerate(work[1:2] + work[3:4]):   # oracle pins for two of them
+        got = ref[1] if j == 0 else ref[3]
+        rc, ri = oracle.gemm(ad.cpu().numpy(), bd.cpu().numpy(), sr, nthreads=0)
+        np.testing.assert_array_equal(got[0].cpu().numpy(), rc)
+        np.testing.assert_array_equal(got[1].cpu().numpy(), ri)
+    # fresh streams, problem sizes interleaved
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    order = [3, 1, 2, 0, 0, 2, 1, 3]
+    outs = []
+    for rep in range(2):
+        for q, j in enumerate(order):
+            sr, ad, bd = work[j]
+            with torch.cuda.stream(streams[(q + rep) % 2]):
+                outs.append((j, trop.gemm(ad, bd, sr)))
+    torch.cuda.synchronize()
+    for j, got in outs:
+        assert torch.equal(got[0], ref[j][0]) and torch.equal(got[1], ref[j][1])
+    # graph replay with new inputs copied in between replays
+    sr, ad, bd = work[0]
+    a2, b2 = synth.gemm_batched_inputs(1, batch=64, m=256, n=256, k=256)
+    sets = [(ad, bd), (_dev(a2), _dev(b2))]
+    ref2 = trop.gemm(sets[1][0], sets[1][1], sr)
+    xa, xb = ad.clone(), bd.clone()
+    c = torch.empty_like(ref[0][0])
+    i = torch.empty_like(ref[0][1])
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        trop.gemm(xa, xb, sr, out=c, out_argmax=i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        trop.gemm(xa, xb, sr, out=c, out_argmax=i)
+    for rep in range(4):
+        src = sets[rep % 2]
+        want = ref[0] if rep % 2 == 0 else ref2
+        xa.copy_(src[0])
+        xb.copy_(src[1])
+        c.fill_(0)
+        i.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(c, want[0]) and torch.equal(i, want[1]), rep
