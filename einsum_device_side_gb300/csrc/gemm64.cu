@@ -32,6 +32,10 @@ namespace {
 
 constexpr int D_BM = 64, D_BN = 64, D_BK = 16, D_THREADS = 256;
 constexpr int D_LD = D_BM + 1;  // padded row (doubles) of the staged tiles
+// two CTAs per SM: sixteen warps to hide the shared-memory latency of the operand reads
+#ifndef TROP_F64_MINB
+#define TROP_F64_MINB 2
+#endif
 
 // order key: signed 64-bit integer that compares like the double (no NaN)
 __device__ __forceinline__ long long okey(double x)
@@ -68,7 +72,7 @@ struct Gemm64Params {
 };
 
 template <int SR, bool ARG>
-__global__ void __launch_bounds__(D_THREADS) k_gemm_tiled_f64(Gemm64Params p)
+__global__ void __launch_bounds__(D_THREADS, TROP_F64_MINB) k_gemm_tiled_f64(Gemm64Params p)
 {
     using O = Ops64<SR>;
     __shared__ double As[D_BK][D_LD];
