@@ -92,6 +92,11 @@ def load(path: str | None = None):
                                        P, I64, I64, I64, P, P, I64, I64, I64, P, I64, I64, I64, P]),
         "tropical_contract_tree": (I, [I, TP, I, ctypes.POINTER(TropNode), I, TP, ctypes.POINTER(P), P]),
         "tropical_tree_backtrack": (I, [I, TP, I, ctypes.POINTER(TropNode), ctypes.POINTER(P), I64, I, P, P]),
+        "tropical_tree_plan_create": (I, [I, TP, I, ctypes.POINTER(TropNode), I, TP, ctypes.POINTER(P),
+                                          ctypes.POINTER(P)]),
+        "tropical_tree_plan_run": (I, [P, P]),
+        "tropical_tree_plan_info": (I, [P, i64p, ctypes.POINTER(ctypes.c_size_t)]),
+        "tropical_tree_plan_destroy": (I, [P]),
         "tropical_sync_pool": (I, []),
         "tropical_release_pool": (I, []),
         "tropical_stats": (I, [ctypes.POINTER(TropStats)]),
@@ -395,6 +400,55 @@ def contract_tree(inputs, nodes, semiring="maxplus", out: torch.Tensor | None = 
     _check(lib.tropical_contract_tree(len(inputs), descs, len(nodes), table.arr, _sr(semiring), ctypes.byref(o),
                                       ams, _stream(stream, out)))
     return out
+
+
+class TreePlan:
+    """A contraction tree lowered once and captured as one CUDA graph
+    (tropical_tree_plan_*).  It binds the tensors given here: ``run()`` reads
+    the inputs' current contents and writes ``out`` and the node argmax
+    tensors, so refill inputs in place between runs.  The tensors are kept
+    referenced for the plan's lifetime."""
+
+    def __init__(self, inputs, nodes, semiring="maxplus", out: torch.Tensor | None = None, node_argmax=None):
+        lib = load()
+        self._keep = (list(inputs), out, None if node_argmax is None else list(node_argmax))
+        descs = (TropTensor * max(1, len(inputs)))(*[tensor_desc(t) for t in inputs])
+        table = _NodeTable(nodes)
+        ams = None
+        if node_argmax is not None:
+            ams = (ctypes.c_void_p * len(nodes))(*[(t.data_ptr() if t is not None and t.numel() else None)
+                                                   for t in node_argmax])
+        o = tensor_desc(out)
+        h = ctypes.c_void_p()
+        _check(lib.tropical_tree_plan_create(len(inputs), descs, len(nodes), table.arr, _sr(semiring),
+                                             ctypes.byref(o), ams, ctypes.byref(h)))
+        self._h = h
+        self.out = out
+        k, w = ctypes.c_int64(), ctypes.c_size_t()
+        _check(lib.tropical_tree_plan_info(h, ctypes.byref(k), ctypes.byref(w)))
+        self.kernels, self.workspace_bytes = int(k.value), int(w.value)
+
+    def run(self, stream=None):
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        _check(_lib.tropical_tree_plan_run(self._h, _stream(stream, self.out)))
+        return self.out
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            _check(_lib.tropical_tree_plan_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tree_plan(inputs, nodes, semiring="maxplus", out: torch.Tensor | None = None, node_argmax=None) -> TreePlan:
+    """Lower a contraction tree once and capture it as a CUDA graph; see TreePlan."""
+    return TreePlan(inputs, nodes, semiring, out, node_argmax)
 
 
 def tree_backtrack(inputs, nodes, node_argmax, n_labels: int, root_index: int = 0, assignment=None, stream=None):

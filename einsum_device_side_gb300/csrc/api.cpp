@@ -1028,10 +1028,11 @@ int tree_shapes(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop
 
 }  // namespace
 
-extern "C" int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop_node* nodes,
-                                      int semiring, const trop_tensor* out, int32_t* const* node_argmax, void* stream)
+namespace {
+
+int run_tree(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop_node* nodes, int semiring,
+             const trop_tensor* out, int32_t* const* node_argmax, cudaStream_t s)
 {
-    clear_error();
     if (semiring < 0 || semiring > 2) return set_error(TROP_ERR_INVALID_ARG, "unknown semiring %d", semiring);
     if (n_inputs < 0 || n_nodes < 1 || (n_inputs > 0 && !inputs) || !nodes)
         return set_error(TROP_ERR_INVALID_ARG, "empty tree or NULL arrays");
@@ -1055,7 +1056,6 @@ extern "C" int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, i
             for (int i = 0; i < shapes[j].rank; ++i) n *= shapes[j].size[i];
             if (node_argmax[j] && n > 0) TROP_TRY(check_device_pointer(node_argmax[j], "node_argmax"));
         }
-    cudaStream_t s = (cudaStream_t)stream;
     std::vector<void*> inter(n_nodes, nullptr);
     int rc = TROP_OK;
     for (int j = 0; j < n_nodes && rc == TROP_OK; ++j) {
@@ -1103,6 +1103,137 @@ extern "C" int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, i
     // intermediates nobody consumed (or left over after an error)
     for (int j = 0; j < n_nodes; ++j)
         if (inter[j]) pool_retire(inter[j], s);
+    return rc;
+}
+
+// Capture run_tree's launches on `ps` into a graph with `arena` serving every workspace request.
+int capture_tree(CaptureArena* arena, cudaStream_t ps, int n_inputs, const trop_tensor* inputs, int n_nodes,
+                 const trop_node* nodes, int semiring, const trop_tensor* out, int32_t* const* node_argmax,
+                 cudaGraph_t* graph)
+{
+    *graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(ps, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_error(e, "cudaStreamBeginCapture");
+    set_capture_arena(arena);
+    int rc = run_tree(n_inputs, inputs, n_nodes, nodes, semiring, out, node_argmax, ps);
+    set_capture_arena(nullptr);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(ps, &g);
+    if (rc != TROP_OK) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return rc;
+    }
+    if (e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return cuda_error(e, "cudaStreamEndCapture");
+    }
+    *graph = g;
+    return TROP_OK;
+}
+
+}  // namespace
+
+struct trop_tree_plan_s {
+    int device;
+    cudaGraphExec_t exec;
+    void* arena;
+    size_t arena_bytes;
+    int64_t launches;
+};
+
+extern "C" int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop_node* nodes,
+                                      int semiring, const trop_tensor* out, int32_t* const* node_argmax, void* stream)
+{
+    clear_error();
+    return run_tree(n_inputs, inputs, n_nodes, nodes, semiring, out, node_argmax, (cudaStream_t)stream);
+}
+
+extern "C" int tropical_tree_plan_create(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop_node* nodes,
+                                         int semiring, const trop_tensor* out, int32_t* const* node_argmax,
+                                         trop_tree_plan* plan)
+{
+    clear_error();
+    if (!plan) return set_error(TROP_ERR_INVALID_ARG, "NULL plan");
+    *plan = nullptr;
+    TROP_TRY(ensure_device(nullptr));  // module set-up stays outside the capture
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    cudaStream_t ps = nullptr;
+    e = cudaStreamCreateWithFlags(&ps, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_error(e, "cudaStreamCreateWithFlags");
+    // pass 1: the same lowering over a fake, aligned base measures the workspace high-water mark
+    CaptureArena measure;
+    measure.base = uintptr_t(1) << 40;
+    measure.measuring = true;
+    cudaGraph_t g = nullptr;
+    int rc = capture_tree(&measure, ps, n_inputs, inputs, n_nodes, nodes, semiring, out, node_argmax, &g);
+    if (g) cudaGraphDestroy(g);
+    g = nullptr;
+    void* mem = nullptr;
+    const size_t bytes = std::max<size_t>(measure.high, 256);
+    if (rc == TROP_OK) {
+        e = cudaMalloc(&mem, bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            rc = set_error(TROP_ERR_OOM, "plan workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+        }
+    }
+    // pass 2: real memory of that size; every block lands at the offset it had in pass 1
+    CaptureArena real;
+    real.base = reinterpret_cast<uintptr_t>(mem);
+    real.capacity = bytes;
+    if (rc == TROP_OK) rc = capture_tree(&real, ps, n_inputs, inputs, n_nodes, nodes, semiring, out, node_argmax, &g);
+    cudaGraphExec_t exec = nullptr;
+    if (rc == TROP_OK) {
+        e = cudaGraphInstantiate(&exec, g, 0);
+        if (e != cudaSuccess) rc = cuda_error(e, "cudaGraphInstantiate");
+    }
+    if (g) cudaGraphDestroy(g);
+    cudaStreamDestroy(ps);
+    if (rc != TROP_OK) {
+        if (mem) cudaFree(mem);
+        return rc;
+    }
+    *plan = new trop_tree_plan_s{dev, exec, mem, bytes, real.launches};
+    return TROP_OK;
+}
+
+extern "C" int tropical_tree_plan_run(trop_tree_plan plan, void* stream)
+{
+    clear_error();
+    if (!plan) return set_error(TROP_ERR_INVALID_ARG, "NULL plan");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev != plan->device)
+        return set_error(TROP_ERR_DEVICE_MISMATCH, "plan belongs to device %d, current device is %d", plan->device, dev);
+    e = cudaGraphLaunch(plan->exec, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
+    count_launches(plan->launches);
+    return TROP_OK;
+}
+
+extern "C" int tropical_tree_plan_info(trop_tree_plan plan, int64_t* kernels, size_t* workspace_bytes)
+{
+    clear_error();
+    if (!plan) return set_error(TROP_ERR_INVALID_ARG, "NULL plan");
+    if (kernels) *kernels = plan->launches;
+    if (workspace_bytes) *workspace_bytes = plan->arena_bytes;
+    return TROP_OK;
+}
+
+extern "C" int tropical_tree_plan_destroy(trop_tree_plan plan)
+{
+    clear_error();
+    if (!plan) return TROP_OK;
+    int rc = TROP_OK;
+    cudaError_t e = cudaGraphExecDestroy(plan->exec);
+    if (e != cudaSuccess) rc = cuda_error(e, "cudaGraphExecDestroy");
+    e = cudaFree(plan->arena);
+    if (e != cudaSuccess && rc == TROP_OK) rc = cuda_error(e, "cudaFree (plan workspace)");
+    delete plan;
     return rc;
 }
 

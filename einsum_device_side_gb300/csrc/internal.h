@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <map>
+
 #include "tropical.h"
 
 namespace trop {
@@ -51,6 +53,29 @@ void pool_retire(void* ptr, cudaStream_t stream);
 
 // Zeroed per-stream counters for atomic arrival tickets (the kernels reset them to zero).
 int stream_tickets(cudaStream_t s, size_t count, uint32_t** out);
+
+// ---------------------------------------------------------------- capture arena
+// While a CaptureArena is installed on the calling thread (tree plans capture their launches
+// into a CUDA graph, api.cpp), pool_alloc / pool_retire / stream_tickets take memory from it
+// instead of the pool, and count_launches counts into it.  Blocks are placed first fit at
+// 256-byte offsets from `base` and reused after release, so a capture's placement depends only
+// on its sequence of requests: a measuring pass over a fake base (capacity unbounded) finds
+// the high-water mark, and a second pass over real memory of that size places every block at
+// the same offset.  The graph runs its nodes in capture order, so a block released by one node
+// may serve a later node, as the pool does on one stream.
+struct CaptureArena {
+    uintptr_t base = 0;
+    size_t capacity = 0;
+    bool measuring = false;
+    size_t top = 0, high = 0;
+    int64_t launches = 0;
+    std::map<size_t, size_t> free_;  // offset -> length of free extents below top
+    std::map<size_t, size_t> used_;  // offset -> length of live blocks
+    int alloc(size_t bytes, void** out);
+    bool release(void* p);
+};
+void set_capture_arena(CaptureArena* a);
+CaptureArena* capture_arena();
 
 // ---------------------------------------------------------------- fast divmod
 // Unsigned 32-bit division by a runtime-invariant divisor with a

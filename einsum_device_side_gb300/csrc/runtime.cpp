@@ -18,7 +18,9 @@
 // the new work after the old (the usual stream-ordered caching rule).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
+#include <iterator>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -69,7 +71,15 @@ size_t dtype_bytes(int dtype)
 static std::atomic<int64_t> c_module_inits{0}, c_launches{0}, c_stream_syncs{0};
 static std::atomic<int64_t> c_pool[8];
 
-void count_launches(int64_t n) { c_launches += n; }
+static thread_local CaptureArena* t_arena = nullptr;
+void set_capture_arena(CaptureArena* a) { t_arena = a; }
+CaptureArena* capture_arena() { return t_arena; }
+
+void count_launches(int64_t n)
+{
+    if (t_arena) t_arena->launches += n;
+    else c_launches += n;
+}
 void count_module_init() { c_module_inits += 1; }
 void count_pool(int field, int64_t n) { c_pool[field] += n; }
 
@@ -253,8 +263,60 @@ size_t round_bytes(size_t n)
 
 }  // namespace
 
+int CaptureArena::alloc(size_t bytes, void** out)
+{
+    *out = nullptr;
+    const size_t want = (std::max<size_t>(bytes, 1) + 255) / 256 * 256;
+    size_t off = top;
+    for (auto it = free_.begin(); it != free_.end(); ++it) {
+        if (it->second < want) continue;
+        off = it->first;
+        const size_t rest = it->second - want;
+        free_.erase(it);
+        if (rest) free_.emplace(off + want, rest);
+        break;
+    }
+    if (off == top) {
+        if (!measuring && top + want > capacity)
+            return set_error(TROP_ERR_OOM, "capture arena exhausted (%zu + %zu > %zu bytes)", top, want, capacity);
+        top += want;
+        high = std::max(high, top);
+    }
+    used_.emplace(off, want);
+    *out = reinterpret_cast<void*>(base + off);
+    return TROP_OK;
+}
+
+bool CaptureArena::release(void* p)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if (a < base) return false;
+    auto it = used_.find(a - base);
+    if (it == used_.end()) return false;
+    size_t off = it->first, len = it->second;
+    used_.erase(it);
+    // coalesce with the free neighbours, then give the tail back to top
+    auto nx = free_.lower_bound(off);
+    if (nx != free_.end() && off + len == nx->first) {
+        len += nx->second;
+        nx = free_.erase(nx);
+    }
+    if (nx != free_.begin()) {
+        auto pv = std::prev(nx);
+        if (pv->first + pv->second == off) {
+            off = pv->first;
+            len += pv->second;
+            free_.erase(pv);
+        }
+    }
+    if (off + len == top) top = off;
+    else free_.emplace(off, len);
+    return true;
+}
+
 int pool_alloc(size_t bytes, cudaStream_t stream, void** out)
 {
+    if (t_arena) return t_arena->alloc(bytes, out);
     *out = nullptr;
     if (bytes == 0) bytes = 1;
     const size_t want = round_bytes(bytes);
@@ -319,6 +381,10 @@ int pool_alloc(size_t bytes, cudaStream_t stream, void** out)
 void pool_retire(void* ptr, cudaStream_t stream)
 {
     if (!ptr) return;
+    if (t_arena) {
+        t_arena->release(ptr);
+        return;
+    }
     Pool& P = pool();
     std::lock_guard<std::mutex> lk(P.mu);
     auto it = P.live_.find(ptr);
@@ -392,6 +458,17 @@ Tickets& tickets()
 int trop::stream_tickets(cudaStream_t s, size_t count, uint32_t** out)
 {
     *out = nullptr;
+    if (CaptureArena* a = capture_arena()) {
+        // captured: counters of the plan's own, zeroed by a memset node ahead of their kernel
+        void* p = nullptr;
+        TROP_TRY(a->alloc(count * sizeof(uint32_t), &p));
+        if (!a->measuring) {
+            cudaError_t e = cudaMemsetAsync(p, 0, count * sizeof(uint32_t), s);
+            if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync (captured tickets)");
+        }
+        *out = static_cast<uint32_t*>(p);
+        return TROP_OK;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");

@@ -69,6 +69,7 @@
 #ifndef TROPICAL_GB300_H
 #define TROPICAL_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -263,6 +264,45 @@ int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, const trop_
 int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, int n_nodes,
                            const trop_node* nodes, int semiring, const trop_tensor* out,
                            int32_t* const* node_argmax, void* stream);
+
+/* Tree plans: a contraction tree lowered once and replayed as one CUDA graph.
+ * [WR "Result": with the stream barriers gone, per-kernel launch latency is
+ * the remaining gap; WR "Problem": the cuTENSOR path caches its plans per
+ * contraction; I52 "Proposed plan" step 1: build the GPU context and module
+ * once instead of per contraction.]
+ *
+ * tropical_tree_plan_create validates and lowers the tree exactly as
+ * tropical_contract_tree does, then captures the resulting launches into a
+ * CUDA graph.  The plan binds the buffers passed here: every run reads the
+ * current contents of `inputs` and writes `out` and the non-NULL
+ * `node_argmax` buffers, so callers refill inputs in place between runs.
+ * Intermediates and all internal workspace live in one device allocation
+ * owned by the plan (blocks reused along the tree as their last consumer
+ * passes, as the pool does); the shape, strides and dtypes fixed at creation
+ * decide every lowering choice, so a run does no host planning and no
+ * allocation.  Creation synchronises nothing but allocates (cudaMalloc).
+ * Errors of create: as tropical_contract_tree, plus OOM and CUDA (a capture
+ * or graph call failed); *plan is NULL on failure.
+ *
+ * tropical_tree_plan_run launches the graph on `stream` (asynchronous, like
+ * every call here).  Runs of one plan are ordered by CUDA (a graph cannot run
+ * concurrently with itself); callers that share a plan across host threads
+ * serialise their calls.  Errors: INVALID_ARG (NULL plan), DEVICE_MISMATCH
+ * (current device is not the plan's), CUDA.
+ *
+ * tropical_tree_plan_info reports the kernels one run launches and the bytes
+ * of the plan's workspace (either pointer may be NULL).
+ *
+ * tropical_tree_plan_destroy frees the graph and the workspace; call it once
+ * no run of the plan is pending (cudaFree waits for the device).  NULL is a
+ * no-op. */
+typedef struct trop_tree_plan_s* trop_tree_plan;
+int tropical_tree_plan_create(int n_inputs, const trop_tensor* inputs, int n_nodes,
+                              const trop_node* nodes, int semiring, const trop_tensor* out,
+                              int32_t* const* node_argmax, trop_tree_plan* plan);
+int tropical_tree_plan_run(trop_tree_plan plan, void* stream);
+int tropical_tree_plan_info(trop_tree_plan plan, int64_t* kernels, size_t* workspace_bytes);
+int tropical_tree_plan_destroy(trop_tree_plan plan);
 
 /* Argmax back-tracking through a contraction tree, on the device.  Given the
  * tree of tropical_contract_tree, every node's argmax buffer and the linear
