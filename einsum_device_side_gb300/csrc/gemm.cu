@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cstdint>
 #include <cstdio>
 
@@ -65,6 +66,10 @@ struct Ops {
         return SR == TROP_MAXTIMES ? __fmul2_rn(a, b) : __fadd2_rn(a, b);
     }
     __device__ __forceinline__ static bool better(float a, float b) { return SR == TROP_MINPLUS ? a < b : a > b; }
+    __device__ __forceinline__ static float fold2(float acc, float x)
+    {
+        return SR == TROP_MINPLUS ? fminf(acc, x) : fmaxf(acc, x);
+    }
     __device__ __forceinline__ static float fold3(float acc, float x, float y)
     {
         float r;
@@ -145,6 +150,14 @@ struct TiledParams {
     uint16_t* seg_c;   // [G_sk][2][BM*BN] chunk + 1 of each segment's first maximum, 0 if none (ARG)
     uint32_t* sk_cnt;  // [R] arrival tickets of the stream-K tiles (zero before and after a launch)
     uint64_t r_units;  // rows walked by the resolve pass: nbatch * tiles_n * M
+    int sAm32, sCm32, sIm32;  // the row strides as 32-bit values (short-K resolve only)
+    // resolve work split: CTA j walks rows [j * r_per + min(j, r_rem), + r_per + (j < r_rem));
+    // with r32 (r_units < 2^31) a row unit splits into (panel, row) and a panel into (batch,
+    // column panel) by the fast 32-bit divisions
+    uint64_t r_per;
+    uint32_t r_rem;
+    int r32;
+    FastDiv div_M, div_npan;
 };
 
 __device__ __forceinline__ void tile_coord(const TiledParams& p, uint32_t t, uint32_t& b, int& m0, int& n0)
@@ -180,6 +193,30 @@ __device__ __forceinline__ int row_of(int tm, int i) { return i < 4 ? tm * 4 + i
 // wait before touching that kernel's results.  Without the launch attribute both are no-ops.
 __device__ __forceinline__ void pdl_signal() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Rows of the resolve pass that this CTA walks, and the (batch, first column, row) of row
+// unit u (units run over the rows of every column panel of every batch).
+__device__ __forceinline__ void resolve_range(const TiledParams& p, uint64_t& ubeg, uint64_t& uend)
+{
+    const uint64_t j = blockIdx.x;
+    ubeg = j * p.r_per + min(j, (uint64_t)p.r_rem);
+    uend = ubeg + p.r_per + (j < p.r_rem ? 1 : 0);
+}
+__device__ __forceinline__ void resolve_unit(const TiledParams& p, uint64_t u, uint32_t npan, int pw, uint32_t& b,
+                                             int& n0, int& mb)
+{
+    if (p.r32) {
+        const uint32_t pn = fdiv((uint32_t)u, p.div_M);
+        mb = (int)((uint32_t)u - pn * (uint32_t)p.M);
+        b = fdiv(pn, p.div_npan);
+        n0 = (int)(pn - b * npan) * pw;
+    } else {
+        const uint64_t pn = u / (uint64_t)p.M;
+        mb = (int)(u - pn * (uint64_t)p.M);
+        b = (uint32_t)(pn / npan);
+        n0 = (int)(pn - (uint64_t)b * npan) * pw;
+    }
+}
 
 // Merge the segments of stream-K tile tl in k order (a later one wins only when strictly
 // better) and store the tile through C's strides; with ARG also -(chunk + 1), or 0, into I.
@@ -439,8 +476,13 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                         for (int jj = 0; jj < TN; jj += 2) {
                             const float2 t0 = O::mul2(make_float2(a0[i], a0[i]), make_float2(b0[jj], b0[jj + 1]));
                             const float2 t1 = O::mul2(make_float2(a1[i], a1[i]), make_float2(b1[jj], b1[jj + 1]));
+#ifdef TROP_FOLD2
+                            dst_[i][jj] = O::fold2(O::fold2(first ? src_[i][jj] : dst_[i][jj], t0.x), t1.x);
+                            dst_[i][jj + 1] = O::fold2(O::fold2(first ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y), t1.y);
+#else
                             dst_[i][jj] = O::fold3(first ? src_[i][jj] : dst_[i][jj], t0.x, t1.x);
                             dst_[i][jj + 1] = O::fold3(first ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y, t1.y);
+#endif
                         }
                     if ((kk + 2) % CH == 0) {
                         // end of a chunk: a strict improvement over the chunk-start value marks it
@@ -671,8 +713,8 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
     float* EBf = reinterpret_cast<float*>(smem_raw);
     float(*EB)[BN] = reinterpret_cast<float(*)[BN]>(smem_raw);  // the PW = 64 view
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint64_t ubeg = (uint64_t)blockIdx.x * p.r_units / gridDim.x;
-    const uint64_t uend = (uint64_t)(blockIdx.x + 1) * p.r_units / gridDim.x;
+    uint64_t ubeg, uend;
+    resolve_range(p, ubeg, uend);
     const int ngr = (p.K + GK - 1) / GK;
     const uint32_t npan = (uint32_t)((p.N + PW - 1) / PW);  // panels per batch
     // common layout: unit column strides, whole chunks, 16-byte aligned A segments
@@ -680,12 +722,11 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
     bool waited = false;
     for (uint64_t u = ubeg; u < uend;) {
         // rows mb .. me-1 of panel pn
-        const uint64_t pn = u / (uint64_t)p.M;
-        const int mb = (int)(u - pn * (uint64_t)p.M);
+        uint32_t b;
+        int n0, mb;
+        resolve_unit(p, u, npan, PW, b, n0, mb);
         const int me = (int)min((uint64_t)p.M, (uint64_t)mb + (uend - u));
         u += (uint64_t)(me - mb);
-        const uint32_t b = (uint32_t)(pn / npan);
-        const int n0 = (int)(pn - (uint64_t)b * npan) * PW;
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
         const float* __restrict__ A = p.A + oa;
@@ -784,6 +825,153 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
                         Ib[(int64_t)(ms + r) * p.sIm + offI[h]] = ka[r][h] + idx;
                     }
             }
+        }
+    }
+    // every CTA waits once, so this grid ends after the GEMM grid whatever its row range
+    if (!waited) pdl_wait();
+}
+
+// ------------------------------------------------------------------ argmax resolve, short K
+// The same replacement for contractions of at most 32 chunks (K <= 256) in the common layout
+// (unit column strides, whole chunks, 16-byte aligned A rows, row strides below 2^31).  A warp
+// takes one row of a 64-column panel per step.  Lane l loads chunk l of the row -- the warp
+// reads the row once, coalesced -- and an output whose pending chunk is c takes that chunk's
+// CH values of A from lane c by shuffles; B's rows sit in shared memory as in the general
+// pass (lane l owns columns l and l + 32, so the staged reads are free of bank conflicts).
+// No global load waits on another, so the next row's C, I and A are in flight while a row is
+// searched; the two rows in flight live in two register sets used in turn.
+#ifndef TROP_RESOLVE2_MINB
+#define TROP_RESOLVE2_MINB 3
+#endif
+constexpr int SHORT_K = 32 * CH;  // one chunk per lane
+static_assert(SHORT_K <= RGK, "the staged B rows cover a short contraction");
+static_assert(CH == 8, "the short resolve searches a chunk of 8 by halving");
+
+template <int SR>
+__global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve_rows(TiledParams p)
+{
+    using O = Ops<SR>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float* EB = reinterpret_cast<float*>(smem_raw);  // [K][BN]: the panel's rows of B
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t ubeg, uend;
+    resolve_range(p, ubeg, uend);
+    const uint32_t npan = (uint32_t)((p.N + BN - 1) / BN);
+    // lane l holds chunk l of every row; lanes past the last chunk read the last one (unused)
+    const int achunk = min(lane, p.K / CH - 1);
+    const int sA = p.sAm32, sC = p.sCm32, sI = p.sIm32;
+    bool waited = false;
+    for (uint64_t u = ubeg; u < uend;) {
+        // rows mb .. me-1 of panel pn
+        uint32_t b;
+        int n0, mb;
+        resolve_unit(p, u, npan, BN, b, n0, mb);
+        const int me = (int)min((uint64_t)p.M, (uint64_t)mb + (uend - u));
+        u += (uint64_t)(me - mb);
+        int64_t oa, ob, oc, oi;
+        batch_offsets(p.bt, b, oa, ob, oc, oi);
+        // loads are never predicated: a column past N reads column N - 1 and a row past the
+        // range reads its last row; neither is searched or stored
+        const int ncl = p.N - 1 - n0;
+        const int c0 = min(lane, ncl), c1 = min(lane + 32, ncl);
+        const float* __restrict__ Al = p.A + oa + achunk * CH;
+        const float* __restrict__ B = p.B + ob;
+        const float* __restrict__ Cb = p.C + oc + n0;
+        const int32_t* __restrict__ Ib = p.I + oi + n0;
+        int32_t* __restrict__ Il = p.I + oi + n0 + lane;
+
+        __syncthreads();  // every warp is done with the previous panel's rows
+        {
+            // thread -> column quad tid % 16 of rows tid / 16 + 16 i; zero fill past N
+            const int q = (tid % (BN / 4)) * 4, n = n0 + q;
+            const int valid = max(0, min(4, p.N - n));
+            const float* src = valid ? B + n : B;
+            const int64_t step = valid ? p.sBk * (RTHREADS / (BN / 4)) : 0;
+            src += valid ? (int64_t)(tid / (BN / 4)) * p.sBk : 0;
+            if (p.vecB) {  // 16-byte aligned rows of B
+                for (int k = tid / (BN / 4); k < p.K; k += RTHREADS / (BN / 4), src += step)
+                    cp_async16(EB + k * BN + q, src, valid * 4);
+                cp_async_commit();
+                cp_async_wait_all();
+            } else {
+                for (int k = tid / (BN / 4); k < p.K; k += RTHREADS / (BN / 4), src += step) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = e < valid ? __ldg(src + e) : 0.0f;
+                    *reinterpret_cast<float4*>(EB + k * BN + q) = make_float4(v[0], v[1], v[2], v[3]);
+                }
+            }
+        }
+        __syncthreads();
+        if (!waited) {
+            pdl_wait();  // C and I come from the GEMM grid (B above is its input)
+            waited = true;
+        }
+
+        const bool col0 = lane <= ncl, col1 = lane + 32 <= ncl;
+        // one row per warp step, two register sets used in turn (no copy between steps)
+        struct RowSet {
+            float v[2];
+            int32_t c[2];
+            float4 a[2];
+            bool ok[2];
+        };
+        auto load_row = [&](RowSet& s, int m) {
+            const bool rok = m < me;
+            const int mm = rok ? m : me - 1;
+            const float* cr = Cb + (int64_t)mm * sC;
+            const int32_t* ir = Ib + (int64_t)mm * sI;
+            const float* ar = Al + (int64_t)mm * sA;
+            s.v[0] = cr[c0];
+            s.v[1] = cr[c1];
+            s.c[0] = ir[c0];
+            s.c[1] = ir[c1];
+            s.a[0] = __ldg(reinterpret_cast<const float4*>(ar));
+            s.a[1] = __ldg(reinterpret_cast<const float4*>(ar + 4));
+            s.ok[0] = rok && col0;
+            s.ok[1] = rok && col1;
+        };
+        auto search_row = [&](const RowSet& s, int m) {
+            const float ar[CH] = {s.a[0].x, s.a[0].y, s.a[0].z, s.a[0].w, s.a[1].x, s.a[1].y, s.a[1].z, s.a[1].w};
+            int32_t* irow = Il + (int64_t)m * sI;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // code -(c + 1): chunk c pending; 0: final (nothing beat the zero)
+                const bool live = s.ok[h] && s.c[h] < 0;
+                const int c = live ? ~s.c[h] : 0;
+                const float v = s.v[h];
+                float a[CH];
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk) a[kk] = __shfl_sync(0xffffffffu, ar[kk], c);
+                const float* eb = EB + c * (CH * BN) + h * 32 + lane;
+                // every product of the chunk is at most v (at least v for min-plus) and one equals
+                // it, so the prefix (+) of the products first reaches v at the first such k:
+                // halve the range on the prefixes of 4 and then 2 products, then test one product
+                float t[CH];
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk) t[kk] = O::mul(a[kk], eb[kk * BN]);
+                const float p1 = O::fold3(t[0], t[1], t[1]);
+                const float p3 = O::fold3(p1, t[2], t[3]);
+                const float p5 = O::fold3(p3, t[4], t[5]);
+                const bool s2 = p3 != v;
+                const bool s1 = (s2 ? p5 : p1) != v;
+                const float x = s2 ? (s1 ? t[6] : t[4]) : (s1 ? t[2] : t[0]);
+                const int idx = (s2 ? 4 : 0) + (s1 ? 2 : 0) + (x != v ? 1 : 0);
+                if (live) irow[h * 32] = c * CH + idx;
+            }
+        };
+        constexpr int WSTEP = RWARPS;
+        int ms = mb + warp;
+        RowSet s0, s1;
+        if (ms < me) load_row(s0, ms);
+        while (ms < me) {
+            if (ms + WSTEP < me) load_row(s1, ms + WSTEP);
+            search_row(s0, ms);
+            ms += WSTEP;
+            if (ms >= me) break;
+            if (ms + WSTEP < me) load_row(s0, ms + WSTEP);
+            search_row(s1, ms);
+            ms += WSTEP;
         }
     }
     // every CTA waits once, so this grid ends after the GEMM grid whatever its row range
@@ -965,6 +1153,15 @@ int resident_ctas(const void* fn, int threads, size_t smem, std::atomic<int>& ca
     return occ;
 }
 
+void resolve_split(TiledParams& p, uint64_t grid, uint32_t npan)
+{
+    p.r_per = p.r_units / grid;
+    p.r_rem = (uint32_t)(p.r_units % grid);
+    p.r32 = p.r_units < (uint64_t(1) << 31);
+    p.div_M = make_fastdiv((uint32_t)p.M);
+    p.div_npan = make_fastdiv(npan);
+}
+
 template <int SR, int PW>
 int launch_resolve_pw(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t s, const DeviceInfo* dev)
 {
@@ -976,8 +1173,10 @@ int launch_resolve_pw(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t s,
     const uint64_t per_cta = (uint64_t)RWARPS * PanelShape<PW>::ROWS;
     const uint64_t want = (p.r_units + per_cta - 1) / per_cta;
     // programmatic dependent launch: its CTAs stage B while the GEMM drains
+    const uint64_t grid = std::max<uint64_t>(1, std::min(slots, want));
+    resolve_split(p, grid, (uint32_t)npan);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::max<uint64_t>(1, std::min(slots, want)));
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(RTHREADS);
     cfg.dynamicSmemBytes = SMEM_RESOLVE;
     cfg.stream = s;
@@ -994,9 +1193,39 @@ int launch_resolve_pw(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t s,
 // Panel width of the resolve pass: the widest whose staged group covers K (fewest passes over
 // the rows), 64 columns for layouts outside the common one.
 template <int SR>
+int launch_resolve_short(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t s, const DeviceInfo* dev)
+{
+    static std::atomic<int> occ{0};
+    const uint64_t npan = (uint64_t)((p.N + BN - 1) / BN);
+    p.r_units = (uint64_t)nbatch * npan * (uint64_t)M;
+    const uint64_t slots =
+        (uint64_t)dev->sm_count * resident_ctas((const void*)k_argmax_resolve_rows<SR>, RTHREADS, SMEM_RESOLVE, occ);
+    const uint64_t per_cta = (uint64_t)RWARPS;
+    const uint64_t want = (p.r_units + per_cta - 1) / per_cta;
+    const uint64_t grid = std::max<uint64_t>(1, std::min(slots, want));
+    resolve_split(p, grid, (uint32_t)npan);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(RTHREADS);
+    cfg.dynamicSmemBytes = sizeof(float) * (size_t)p.K * BN;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR>, p);
+    if (e != cudaSuccess) return cuda_error(e, "k_argmax_resolve_rows");
+    return check_launch("k_argmax_resolve_rows");
+}
+
+template <int SR>
 int launch_resolve(TiledParams& p, const GemmDesc& g, int64_t nbatch, cudaStream_t s, const DeviceInfo* dev)
 {
     const bool fast = p.vecA && p.K % CH == 0 && p.sCn == 1 && p.sIn == 1;
+    const auto fits32 = [](int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; };
+    if (fast && p.K >= CH && p.K <= SHORT_K && fits32(g.sAm) && fits32(g.sCm) && fits32(g.sIm))
+        return launch_resolve_short<SR>(p, g.M, nbatch, s, dev);
     if (!fast || p.K <= PanelShape<64>::GK) return launch_resolve_pw<SR, 64>(p, g.M, nbatch, s, dev);
     if (p.K <= PanelShape<32>::GK) return launch_resolve_pw<SR, 32>(p, g.M, nbatch, s, dev);
     return launch_resolve_pw<SR, 16>(p, g.M, nbatch, s, dev);
@@ -1028,6 +1257,9 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.sCn = g.sCn;
     p.sIm = g.sIm;
     p.sIn = g.sIn;
+    p.sAm32 = (int)g.sAm;
+    p.sCm32 = (int)g.sCm;
+    p.sIm32 = (int)g.sIm;
     int64_t nbatch = 1;
     p.bt = make_batch(g, nbatch);
     p.nbatch = (uint32_t)nbatch;
@@ -1380,7 +1612,8 @@ int register_gemm_kernels()
             (const void*)k_argmax_resolve<TROP_MAXTIMES, 64>, (const void*)k_argmax_resolve<TROP_MAXPLUS, 32>,
             (const void*)k_argmax_resolve<TROP_MINPLUS, 32>,  (const void*)k_argmax_resolve<TROP_MAXTIMES, 32>,
             (const void*)k_argmax_resolve<TROP_MAXPLUS, 16>,  (const void*)k_argmax_resolve<TROP_MINPLUS, 16>,
-            (const void*)k_argmax_resolve<TROP_MAXTIMES, 16>};
+            (const void*)k_argmax_resolve<TROP_MAXTIMES, 16>,  (const void*)k_argmax_resolve_rows<TROP_MAXPLUS>,
+            (const void*)k_argmax_resolve_rows<TROP_MINPLUS>,   (const void*)k_argmax_resolve_rows<TROP_MAXTIMES>};
         for (const void* k : kr) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_RESOLVE);
             if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (argmax resolve smem)");

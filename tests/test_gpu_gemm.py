@@ -289,3 +289,36 @@ def test_argmax_gemm_streams_and_graph_replay(trop):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(c, want[0]) and torch.equal(i, want[1]), rep
+
+
+# ---------------------------------------------------------------- short contractions (K <= 256, whole chunks)
+# These take the resolve pass that reads whole rows of A, one chunk per lane.
+
+@pytest.mark.parametrize("sr", SR)
+@pytest.mark.parametrize("shape", [(3, 70, 45, 40), (2, 130, 129, 248), (1, 33, 200, 256), (5, 64, 64, 8),
+                                   (2, 191, 67, 136)])
+def test_short_contraction_ragged(trop, sr, shape):
+    bt, m, n, k = shape
+    a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+    _check(trop, a, b, sr)
+
+
+@pytest.mark.parametrize("sr", SR)
+def test_short_contraction_padded_rows_and_ties(trop, sr):
+    """Integer entries (ties in every chunk), A and C/I rows padded past their extents,
+    B broadcast over the batch: values and argmax against the oracle on the logical views."""
+    bt, m, n, k = 3, 97, 75, 256
+    a = synth.uniform_int(21, (bt, m, k), -4, 4).astype(np.float32)
+    b = synth.uniform_int(22, (1, k, n), -4, 4).astype(np.float32)
+    if sr == 2:
+        a, b = np.abs(a), np.abs(b)
+    wide = torch.zeros((bt, m, k + 12), dtype=torch.float32, device="cuda")
+    wide[:, :, 4:4 + k] = _dev(a)
+    ad = wide[:, :, 4:4 + k]                       # row stride k + 12, 16-byte aligned rows
+    bd = _dev(b).expand(bt, k, n)
+    cw = torch.empty((bt, m, n + 9), dtype=torch.float32, device="cuda")
+    iw = torch.empty((bt, m, n + 9), dtype=torch.int32, device="cuda")
+    c, i = trop.gemm(ad, bd, sr, out=cw[:, :, :n], out_argmax=iw[:, :, :n])
+    rc, ri = oracle.gemm(a, np.broadcast_to(b, (bt, k, n)), sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == np.ascontiguousarray(rc).tobytes()
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
