@@ -106,6 +106,7 @@ def load(path: str | None = None):
         "tropical_plan_describe": (I, [ctypes.c_char_p, I, i64p, i64p, I, i64p, i64p, ctypes.c_char_p, I]),
         "tropical_debug_fail_next_event_records": (None, [I]),
         "tropical_set_pool_capacity": (None, [I]),
+        "tropical_device_wait_timeouts": (I, [ctypes.POINTER(ctypes.c_uint), I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -487,6 +488,13 @@ def sync_pool():
 def release_pool():
     lib = load()
     _check(lib.tropical_release_pool())
+
+
+def device_wait_timeouts(reset: bool = False) -> int:
+    """Kernel waits on the current device that gave up since load (blocks until idle)."""
+    n = ctypes.c_uint(0)
+    _check(load().tropical_device_wait_timeouts(ctypes.byref(n), int(bool(reset))))
+    return n.value
 
 
 def set_pool_capacity(n: int):

@@ -34,6 +34,7 @@
 //   k_gemm_stream    few rows (M <= 8) and a short contraction (K <= 64):
 //                    one thread per (batch, column vector), memory bound.
 //   k_gemm_generic   anything else: one thread per output, sequential k.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -66,10 +67,6 @@ struct Ops {
         return SR == TROP_MAXTIMES ? __fmul2_rn(a, b) : __fadd2_rn(a, b);
     }
     __device__ __forceinline__ static bool better(float a, float b) { return SR == TROP_MINPLUS ? a < b : a > b; }
-    __device__ __forceinline__ static float fold2(float acc, float x)
-    {
-        return SR == TROP_MINPLUS ? fminf(acc, x) : fmaxf(acc, x);
-    }
     __device__ __forceinline__ static float fold3(float acc, float x, float y)
     {
         float r;
@@ -476,13 +473,8 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                         for (int jj = 0; jj < TN; jj += 2) {
                             const float2 t0 = O::mul2(make_float2(a0[i], a0[i]), make_float2(b0[jj], b0[jj + 1]));
                             const float2 t1 = O::mul2(make_float2(a1[i], a1[i]), make_float2(b1[jj], b1[jj + 1]));
-#ifdef TROP_FOLD2
-                            dst_[i][jj] = O::fold2(O::fold2(first ? src_[i][jj] : dst_[i][jj], t0.x), t1.x);
-                            dst_[i][jj + 1] = O::fold2(O::fold2(first ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y), t1.y);
-#else
                             dst_[i][jj] = O::fold3(first ? src_[i][jj] : dst_[i][jj], t0.x, t1.x);
                             dst_[i][jj + 1] = O::fold3(first ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y, t1.y);
-#endif
                         }
                     if ((kk + 2) % CH == 0) {
                         // end of a chunk: a strict improvement over the chunk-start value marks it
@@ -577,6 +569,202 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                 __threadfence();
                 sk_merge<SR, ARG, THREADS>(p, tl, m0, n0, oc, oi, tid);
             }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ TMA-fed tiled kernel (argmax)
+// The tile, thread layout and chunked argmax of k_gemm_tiled<SR, true, 4> for the common case:
+// one batch axis, K a multiple of BK (every k-tile whole), 16-byte aligned rows and strides.
+// A's [BM x BK] box and B's [BK x BN] box arrive by TMA (cp.async.bulk.tensor) in a ring of
+// TMA_STAGES stages, each with an mbarrier that counts the bytes landed; one thread issues
+// the copies, so the loads cost the other threads no address arithmetic or bounds tests.  A
+// keeps its natural [m][k] layout: for every 4 k a thread reads its 4 B rows once (16 bytes
+// each) and then 4 k of each of its rows with one 16-byte load.  Rows or columns past M and
+// N arrive zero-filled and are never stored.
+#ifndef TROP_TMA_STAGES
+#define TROP_TMA_STAGES 3
+#endif
+#ifndef TROP_TMA_MINB
+#define TROP_TMA_MINB 4
+#endif
+constexpr int TMA_STAGES = TROP_TMA_STAGES;
+constexpr uint32_t TMA_STAGE_BYTES = (BM * BK + BK * BN) * sizeof(float);
+
+struct TmaMaps {
+    CUtensorMap a;  // A as [batch][M][K] (K fastest), box [1][BM][BK]
+    CUtensorMap b;  // B as [batch][K][N] (N fastest), box [1][BK][BN]
+};
+
+// bounded waits on this device that gave up (a copy that never landed); stays 0
+__device__ unsigned int g_wait_timeouts;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) { return (uint32_t)__cvta_generic_to_shared(ptr); }
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `parity` to complete; give up after about 0.2 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > 200000000ull) return false;
+    return true;
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int SR>
+__global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
+    k_gemm_tma(const __grid_constant__ TmaMaps maps, TiledParams p)
+{
+    using O = Ops<SR>;
+    constexpr int TN = 4, THREADS = tile_threads<TN>();
+    static_assert(BK % 4 == 0 && CH % 4 == 0 && (BK / CH) % 2 == 0, "k quads, an even number of chunks per k-tile");
+    __shared__ __align__(128) float As[TMA_STAGES][BM][BK];
+    __shared__ __align__(128) float Bs[TMA_STAGES][BK][BN];
+    __shared__ __align__(8) uint64_t full[TMA_STAGES];
+    __shared__ uint16_t sid[TM * TN][THREADS];
+    __shared__ int s_fail;
+
+    pdl_signal();  // the resolve pass may start filling SMs as this grid drains
+    const int tid = threadIdx.x;
+    const int tm = tid / (BN / TN), tn = tid % (BN / TN);
+    const float zero = O::zero();
+    uint32_t b;
+    int m0, n0;
+    tile_coord(p, blockIdx.x, b, m0, n0);
+    const int nkt = (int)p.nkt;
+    if (tid == 0) {
+        for (int s = 0; s < TMA_STAGES; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_fail = 0;
+    }
+    __syncthreads();
+    auto issue = [&](int kt) {
+        const int s = kt % TMA_STAGES;
+        mbar_expect_tx(&full[s], TMA_STAGE_BYTES);
+        tma_load_3d(&As[s][0][0], &maps.a, kt * BK, m0, (int)b, &full[s]);
+        tma_load_3d(&Bs[s][0][0], &maps.b, n0, kt * BK, (int)b, &full[s]);
+    };
+    if (tid == 0)
+        for (int kt = 0; kt < min(nkt, TMA_STAGES); ++kt) issue(kt);
+
+    float best[TM][TN], snap[TM][TN];  // two accumulator sets, roles swapped every chunk
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int jj = 0; jj < TN; ++jj) best[i][jj] = snap[i][jj] = zero;
+
+    for (int kt = 0; kt < nkt; ++kt) {
+        const int s = kt % TMA_STAGES;
+        if (!mbar_wait(&full[s], (uint32_t)(kt / TMA_STAGES) & 1u)) s_fail = 1;
+#pragma unroll
+        for (int kq = 0; kq < BK; kq += 4) {
+            // chunk parity and the first quad of a chunk are known at compile time (BK / CH even)
+            const bool odd = ((kq / CH) & 1) != 0;
+            const bool first = (kq % CH) == 0;
+            float(&src_)[TM][TN] = odd ? snap : best;
+            float(&dst_)[TM][TN] = odd ? best : snap;
+            float bq[4][TN];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float4 v = *reinterpret_cast<const float4*>(&Bs[s][kq + r][tn * 4]);
+                bq[r][0] = v.x; bq[r][1] = v.y; bq[r][2] = v.z; bq[r][3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const float4 a4 = *reinterpret_cast<const float4*>(&As[s][row_of(tm, i)][kq]);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int kp = 0; kp < 4; kp += 2) {
+                    const bool ff = first && kp == 0;
+#pragma unroll
+                    for (int jj = 0; jj < TN; jj += 2) {
+                        const float2 t0 = O::mul2(make_float2(av[kp], av[kp]), make_float2(bq[kp][jj], bq[kp][jj + 1]));
+                        const float2 t1 =
+                            O::mul2(make_float2(av[kp + 1], av[kp + 1]), make_float2(bq[kp + 1][jj], bq[kp + 1][jj + 1]));
+                        dst_[i][jj] = O::fold3(ff ? src_[i][jj] : dst_[i][jj], t0.x, t1.x);
+                        dst_[i][jj + 1] = O::fold3(ff ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y, t1.y);
+                    }
+                }
+            }
+            if ((kq + 4) % CH == 0) {
+                // end of a chunk: a strict improvement over the chunk-start value marks it
+                const uint16_t chunk = (uint16_t)((kt * BK + kq + 4) / CH - 1);
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < TN; ++jj)
+                        if (O::better(dst_[i][jj], src_[i][jj])) sid[i * TN + jj][tid] = chunk;
+            }
+        }
+        __syncthreads();  // every thread is done with stage s
+        if (s_fail) {
+            // a copy did not land in time: wait (bounded) for the copies still in flight, store nothing
+            if (tid == 0) {
+                atomicAdd(&g_wait_timeouts, 1u);
+                for (int k2 = kt; k2 < min(nkt, kt + TMA_STAGES); ++k2)
+                    mbar_wait(&full[k2 % TMA_STAGES], (uint32_t)(k2 / TMA_STAGES) & 1u);
+            }
+            return;
+        }
+        if (tid == 0 && kt + TMA_STAGES < nkt) issue(kt + TMA_STAGES);
+    }
+
+    // ---------------- store values and -(chunk + 1) (0: nothing beat the zero) through the strides
+    int64_t oa, ob, oc, oi;
+    batch_offsets(p.bt, b, oa, ob, oc, oi);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int m = m0 + row_of(tm, i);
+        if (m >= p.M) continue;
+        float* crow = p.C + oc + (int64_t)m * p.sCm;
+        int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+        int32_t code[TN];
+#pragma unroll
+        for (int jj = 0; jj < TN; ++jj) code[jj] = best[i][jj] != zero ? -((int32_t)sid[i * TN + jj][tid] + 1) : 0;
+        const int n = n0 + tn * 4;
+        if (p.vecC && n + 3 < p.N) {
+            *reinterpret_cast<float4*>(crow + n) = make_float4(best[i][0], best[i][1], best[i][2], best[i][3]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (n + q < p.N) crow[(int64_t)(n + q) * p.sCn] = best[i][q];
+        }
+        if (p.vecI && n + 3 < p.N) {
+            *reinterpret_cast<int4*>(irow + n) = make_int4(code[0], code[1], code[2], code[3]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (n + q < p.N) irow[(int64_t)(n + q) * p.sIn] = code[q];
         }
     }
 }
@@ -1231,6 +1419,49 @@ int launch_resolve(TiledParams& p, const GemmDesc& g, int64_t nbatch, cudaStream
     return launch_resolve_pw<SR, 16>(p, g.M, nbatch, s, dev);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once (no link against libcuda)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled()
+{
+    static std::atomic<int> state{0};  // 0: not looked up, 1: found, 2: unavailable
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    if (state.load(std::memory_order_acquire) == 0) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && ptr) {
+            fn.store(reinterpret_cast<EncodeTiledFn>(ptr), std::memory_order_relaxed);
+            state.store(1, std::memory_order_release);
+        } else {
+            cudaGetLastError();
+            state.store(2, std::memory_order_release);
+        }
+    }
+    return state.load(std::memory_order_acquire) == 1 ? fn.load(std::memory_order_relaxed) : nullptr;
+}
+
+// A 3-D tensor map of a row-major f32 operand [batch][rows][cols] (cols contiguous) with a
+// [1][box_rows][box_cols] box; false when TMA cannot describe it (the caller keeps the
+// cp.async kernel).  Strides in elements.
+bool make_map(CUtensorMap* map, const float* base, uint64_t cols, uint64_t rows, uint64_t batch, int64_t row_stride,
+              int64_t batch_stride, uint32_t box_cols, uint32_t box_rows)
+{
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    if (((uintptr_t)base % 16) != 0 || row_stride <= 0 || row_stride % 4 != 0) return false;
+    if (batch > 1 && (batch_stride <= 0 || batch_stride % 4 != 0)) return false;
+    const cuuint64_t dims[3] = {cols, rows, batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_stride * sizeof(float),
+                                   (cuuint64_t)(batch > 1 ? batch_stride : row_stride * (int64_t)rows) * sizeof(float)};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Stream-K only when the last wave would run at most this full (percent); each stream-K
 // CTA gets at least SK_MIN_UNITS k-tiles (unless a tile has fewer) and a tile is cut into at
 // most SK_MAX_SEGS segments.
@@ -1321,8 +1552,25 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     }
     p.T_dp = (uint32_t)(G_sk ? T - R : T);
 
-    k_gemm_tiled<SR, ARG, TN><<<(unsigned)(p.T_dp + G_sk), THREADS, 0, s>>>(p);
-    int rc = check_launch("k_gemm_tiled");
+    int rc = TROP_OK;
+    bool launched = false;
+    if constexpr (ARG) {
+        // whole tiles, one batch axis, whole k-tiles: operands by TMA
+        if (!G_sk && p.bt.nb <= 1 && g.K % BK == 0) {
+            TmaMaps maps;
+            const int64_t sAb = p.bt.nb ? p.bt.sA[0] : 0, sBb = p.bt.nb ? p.bt.sB[0] : 0;
+            if (make_map(&maps.a, p.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)nbatch, g.sAm, sAb, BK, BM) &&
+                make_map(&maps.b, p.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)nbatch, g.sBk, sBb, BN, BK)) {
+                k_gemm_tma<SR><<<(unsigned)T, tile_threads<4>(), 0, s>>>(maps, p);
+                rc = check_launch("k_gemm_tma");
+                launched = true;
+            }
+        }
+    }
+    if (!launched) {
+        k_gemm_tiled<SR, ARG, TN><<<(unsigned)(p.T_dp + G_sk), THREADS, 0, s>>>(p);
+        rc = check_launch("k_gemm_tiled");
+    }
     if (rc == TROP_OK && ARG) rc = launch_resolve<SR>(p, g, nbatch, s, dev);
     if (ws) pool_retire(ws, s);
     return rc;
@@ -1633,3 +1881,19 @@ int register_gemm_kernels()
 }
 
 }  // namespace trop
+
+extern "C" int tropical_device_wait_timeouts(unsigned int* count, int reset)
+{
+    using namespace trop;
+    if (!count) return set_error(TROP_ERR_INVALID_ARG, "count pointer is NULL");
+    const DeviceInfo* dev = nullptr;
+    TROP_TRY(ensure_device(&dev));
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned int));
+    if (e != cudaSuccess) return cuda_error(e, "reading the wait-timeout counter");
+    if (reset) {
+        const unsigned int z = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(unsigned int));
+        if (e != cudaSuccess) return cuda_error(e, "resetting the wait-timeout counter");
+    }
+    return TROP_OK;
+}

@@ -329,6 +329,15 @@ int tropical_release_pool(void);
 int tropical_stats(trop_stats* out);
 void tropical_reset_stats(void);
 
+/* Bounded waits inside kernels on the current device that gave up, since load
+ * or since the last reset.  The TMA-fed GEMM waits for each operand copy on an
+ * mbarrier for at most about 0.2 s; a CTA whose copy did not land by then
+ * counts one here and stores nothing (so a wrong result is never silent when
+ * this count is read).  Reads a device counter: blocks until the device is
+ * idle.  reset != 0 zeroes the counter after reading it.  Returns TROP_OK, or
+ * TROP_ERR_INVALID_ARG for a NULL count, or TROP_ERR_CUDA. */
+int tropical_device_wait_timeouts(unsigned int* count, int reset);
+
 /* Message of the last failure on this host thread ("" if none). */
 const char* tropical_last_error(void);
 

@@ -322,3 +322,12 @@ def test_short_contraction_padded_rows_and_ties(trop, sr):
     rc, ri = oracle.gemm(a, np.broadcast_to(b, (bt, k, n)), sr, nthreads=0)
     assert c.cpu().numpy().tobytes() == np.ascontiguousarray(rc).tobytes()
     np.testing.assert_array_equal(i.cpu().numpy(), ri)
+
+
+def test_tma_gemm_waits_never_gave_up(trop):
+    """Every operand copy of the TMA-fed GEMM landed within its bounded wait (the device
+    counter of given-up waits stays 0 after the full-size calls)."""
+    for sr in SR:
+        a, b = synth.gemm_batched_inputs(sr, batch=8)
+        trop.gemm(_dev(a), _dev(b), sr)
+    assert trop.device_wait_timeouts() == 0
