@@ -47,7 +47,7 @@ def gemm_traffic():
     """DRAM bytes of one tropical GEMM call from the committed ncu summary, or
     None when the kernel source changed since those counters were taken."""
     import hashlib
-    f = os.path.join(ROOT, "profiles", "k_gemm_tiled_traffic.txt")
+    f = os.path.join(ROOT, "profiles", "k_gemm_tma_traffic.txt")
     if not os.path.exists(f):
         return None
     kv = dict(line.split(": ", 1) for line in open(f).read().splitlines() if ": " in line)
@@ -492,10 +492,10 @@ def run_gpu(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": region_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "strided-batched tropical GEMM + int32 argmax, batch 64 x M=N=K=256, "
-                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 GEMM calls (k_gemm_tiled + k_argmax_resolve each)",
+                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 GEMM calls (k_gemm_tma + k_argmax_resolve_rows each)",
                    "parallelism": f"replicas x{world}",
                    "l2": f"{N_SETS} rotated input sets (288 MiB of operands) so each step reads cold inputs"},
-        "roofline": {"bound": "alu", "kernel": "k_gemm_tiled+k_argmax_resolve (one tropical GEMM call)",
+        "roofline": {"bound": "alu", "kernel": "k_gemm_tma+k_argmax_resolve_rows (one tropical GEMM call)",
                      "achieved": achieved, "peak": peak_ops / 1e9,
                      "unit": "G semiring-ops/s", "frac": achieved / (peak_ops / 1e9), "traffic": traffic,
                      "peak_def": f"{sms} SMs x 128 FP32 lanes x {pk['sm_max_mhz']:.0f} MHz / 2 (add + max)",
