@@ -654,7 +654,6 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
     __shared__ uint16_t sid[TM * TN][THREADS];
     __shared__ int s_fail;
 
-    pdl_signal();  // the resolve pass may start filling SMs as this grid drains
     const int tid = threadIdx.x;
     const int tm = tid / (BN / TN), tn = tid % (BN / TN);
     const float zero = O::zero();
@@ -668,6 +667,11 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
         s_fail = 0;
     }
     __syncthreads();
+    // Launched as a programmatic dependent of whatever precedes it on the stream: nothing in
+    // global memory is touched before that grid has completed (the wait), so the launch only
+    // hides its latency.  Then the resolve pass may start filling SMs as this grid drains.
+    pdl_wait();
+    pdl_signal();
     auto issue = [&](int kt) {
         const int s = kt % TMA_STAGES;
         mbar_expect_tx(&full[s], TMA_STAGE_BYTES);
@@ -894,6 +898,7 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
 template <int SR, int PW>
 __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(TiledParams p)
 {
+    pdl_signal();  // a programmatic dependent (the next GEMM) may take SMs as this grid drains
     using O = Ops<SR>;
     constexpr int GK = PanelShape<PW>::GK;
     static_assert(GK % CH == 0, "a chunk never straddles two staged groups");
@@ -1038,6 +1043,7 @@ static_assert(CH == 8, "the short resolve searches a chunk of 8 by halving");
 template <int SR>
 __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve_rows(TiledParams p)
 {
+    pdl_signal();  // a programmatic dependent (the next GEMM) may take SMs as this grid drains
     using O = Ops<SR>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float* EB = reinterpret_cast<float*>(smem_raw);  // [K][BN]: the panel's rows of B
@@ -1561,8 +1567,17 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
             const int64_t sAb = p.bt.nb ? p.bt.sA[0] : 0, sBb = p.bt.nb ? p.bt.sB[0] : 0;
             if (make_map(&maps.a, p.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)nbatch, g.sAm, sAb, BK, BM) &&
                 make_map(&maps.b, p.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)nbatch, g.sBk, sBb, BN, BK)) {
-                k_gemm_tma<SR><<<(unsigned)T, tile_threads<4>(), 0, s>>>(maps, p);
-                rc = check_launch("k_gemm_tma");
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3((unsigned)T);
+                cfg.blockDim = dim3(tile_threads<4>());
+                cfg.stream = s;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tma<SR>, maps, p);
+                rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma") : check_launch("k_gemm_tma");
                 launched = true;
             }
         }
