@@ -1347,6 +1347,27 @@ int resident_ctas(const void* fn, int threads, size_t smem, std::atomic<int>& ca
     return occ;
 }
 
+// The TMA-fed argmax kernel's layout conditions (the tensor maps may still refuse): one batch
+// axis, whole k-tiles, 16-byte aligned operands with row and batch strides in 16-byte units.
+bool tma_layout_ok(const GemmDesc& g, const Batch& bt, int64_t nbatch)
+{
+    if (!g.I || bt.nb > 1 || g.K % BK != 0) return false;
+    if ((uintptr_t)g.A % 16 || (uintptr_t)g.B % 16 || g.sAm <= 0 || g.sAm % 4 || g.sBk <= 0 || g.sBk % 4) return false;
+    if (nbatch > 1 && (bt.sA[0] <= 0 || bt.sA[0] % 4 || bt.sB[0] <= 0 || bt.sB[0] % 4)) return false;
+    return true;
+}
+
+// Which argmax resolve pass follows the TMA-fed or tiled argmax kernel: "rows" (K <= 256, whole
+// chunks, unit column strides, 32-bit row strides) or the panel pass of width 64 / 32 / 16.
+const char* resolve_kind(const GemmDesc& g, bool vecA)
+{
+    const bool fast = vecA && g.K % CH == 0 && g.sCn == 1 && g.sIn == 1;
+    const auto fits32 = [](int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; };
+    if (fast && g.K >= CH && g.K <= SHORT_K && fits32(g.sAm) && fits32(g.sCm) && fits32(g.sIm)) return "rows";
+    if (!fast || g.K <= PanelShape<64>::GK) return "panel64";
+    return g.K <= PanelShape<32>::GK ? "panel32" : "panel16";
+}
+
 void resolve_split(TiledParams& p, uint64_t grid, uint32_t npan)
 {
     p.r_per = p.r_units / grid;
@@ -1416,12 +1437,10 @@ int launch_resolve_short(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t
 template <int SR>
 int launch_resolve(TiledParams& p, const GemmDesc& g, int64_t nbatch, cudaStream_t s, const DeviceInfo* dev)
 {
-    const bool fast = p.vecA && p.K % CH == 0 && p.sCn == 1 && p.sIn == 1;
-    const auto fits32 = [](int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; };
-    if (fast && p.K >= CH && p.K <= SHORT_K && fits32(g.sAm) && fits32(g.sCm) && fits32(g.sIm))
-        return launch_resolve_short<SR>(p, g.M, nbatch, s, dev);
-    if (!fast || p.K <= PanelShape<64>::GK) return launch_resolve_pw<SR, 64>(p, g.M, nbatch, s, dev);
-    if (p.K <= PanelShape<32>::GK) return launch_resolve_pw<SR, 32>(p, g.M, nbatch, s, dev);
+    const char* kind = resolve_kind(g, p.vecA != 0);
+    if (kind[0] == 'r') return launch_resolve_short<SR>(p, g.M, nbatch, s, dev);
+    if (kind[5] == '6') return launch_resolve_pw<SR, 64>(p, g.M, nbatch, s, dev);
+    if (kind[5] == '3') return launch_resolve_pw<SR, 32>(p, g.M, nbatch, s, dev);
     return launch_resolve_pw<SR, 16>(p, g.M, nbatch, s, dev);
 }
 
@@ -1562,7 +1581,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     bool launched = false;
     if constexpr (ARG) {
         // whole tiles, one batch axis, whole k-tiles: operands by TMA
-        if (!G_sk && p.bt.nb <= 1 && g.K % BK == 0) {
+        if (!G_sk && tma_layout_ok(g, p.bt, nbatch)) {
             TmaMaps maps;
             const int64_t sAb = p.bt.nb ? p.bt.sA[0] : 0, sBb = p.bt.nb ? p.bt.sB[0] : 0;
             if (make_map(&maps.a, p.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)nbatch, g.sAm, sAb, BK, BM) &&
@@ -1836,9 +1855,25 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
     const Route r = choose(g0, swap);
     const GemmDesc g = swap ? swapped(g0) : g0;
     const bool arg = g.I != nullptr;
-    if (r == R_TILED)
-        snprintf(buf, n, " route=tiled%s%s", swap ? " swap" : "",
-                 (g.sCn != 1 || (arg && g.sIn != 1)) ? " staged" : "");
+    if (r == R_TILED) {
+        const bool staged = g.sCn != 1 || (arg && g.sIn != 1);
+        char extra[96] = "";
+        if (arg) {
+            // the staged product is contiguous: describe the kernels on that layout
+            GemmDesc gs = g;
+            if (staged) {
+                gs.sCn = gs.sIn = 1;
+                gs.sCm = gs.sIm = gs.N;
+            }
+            int64_t nbatch = 1;
+            const Batch bt = make_batch(gs, nbatch);
+            bool va = ((uintptr_t)gs.A % 16) == 0 && gs.sAm % 4 == 0;
+            for (int d = 0; d < bt.nb; ++d) va = va && bt.sA[d] % 4 == 0;
+            snprintf(extra, sizeof(extra), " kernel=%s resolve=%s", tma_layout_ok(gs, bt, nbatch) ? "tma" : "tiled",
+                     resolve_kind(gs, va));
+        }
+        snprintf(buf, n, " route=tiled%s%s%s", swap ? " swap" : "", staged ? " staged" : "", extra);
+    }
     else if (r == R_STREAM)
         snprintf(buf, n, " route=stream%s vec=%d", swap ? " swap" : "", stream_vec(g, arg) ? 4 : 1);
     else

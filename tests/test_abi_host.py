@@ -98,3 +98,35 @@ def test_planner_rejects_inconsistent_extents(trop):
     with pytest.raises(trop.TropicalError) as e:
         trop.plan_describe("ij,jk->ik", [2, 3], [3, 1], [4, 5], [5, 1])
     assert e.value.name == "SHAPE"
+
+
+def _contig(shape):
+    st, acc = [], 1
+    for d in reversed(shape):
+        st.append(acc)
+        acc *= d
+    return list(reversed(st))
+
+
+@pytest.mark.parametrize("k, kernel, resolve", [(256, "tma", "rows"), (64, "tma", "rows"), (16, "tma", "rows"),
+                                                (512, "tma", "panel32"), (1024, "tma", "panel16"),
+                                                (40, "tiled", "rows"), (72, "tiled", "rows"),
+                                                (257, "tiled", "panel64")])
+def test_describe_names_gemm_kernel_and_resolve(trop, k, kernel, resolve):
+    """The planner reports which argmax GEMM kernel and resolve pass a layout takes: the TMA-fed
+    kernel needs one batch axis, K a multiple of 16 and 16-byte row strides; the row resolve
+    needs K <= 256 in whole chunks of 8."""
+    sa, sb = [8, 128, k], [8, k, 128]
+    text = trop.plan_describe("zmk,zkn->zmn", sa, _contig(sa), sb, _contig(sb))
+    assert f"kernel={kernel}" in text and f"resolve={resolve}" in text, text
+
+
+def test_describe_tma_needs_aligned_rows_and_one_batch_axis(trop):
+    # rows of A 16 floats + 1 apart: not 16-byte aligned, so the cp.async kernel
+    text = trop.plan_describe("zmk,zkn->zmn", [4, 64, 16], [64 * 17, 17, 1], [4, 16, 64], [1024, 64, 1])
+    assert "kernel=tiled" in text, text
+    # two batch axes that do not merge into one: the cp.async kernel
+    sa, sb = [3, 5, 64, 32], [3, 5, 32, 64]
+    st_a = [5 * 64 * 32 + 64, 64 * 32, 32, 1]
+    text = trop.plan_describe("yzmk,yzkn->yzmn", sa, st_a, sb, _contig(sb))
+    assert "kernel=tiled" in text and "batch_axes=2" in text, text

@@ -331,3 +331,32 @@ def test_tma_gemm_waits_never_gave_up(trop):
         a, b = synth.gemm_batched_inputs(sr, batch=8)
         trop.gemm(_dev(a), _dev(b), sr)
     assert trop.device_wait_timeouts() == 0
+
+
+# ---------------------------------------------------------------- the TMA-fed kernel (one batch axis, K % 16 == 0)
+
+@pytest.mark.parametrize("sr", SR)
+@pytest.mark.parametrize("shape", [(3, 70, 44, 48), (2, 130, 132, 256), (1, 200, 68, 128), (2, 64, 64, 16),
+                                   (1, 33, 260, 512), (2, 65, 64, 1024)])
+def test_tma_path_integer_ties_padded_rows(trop, sr, shape):
+    """Small integers (ties between k in every chunk and across k-tiles), A's and the output's
+    rows padded past their extents, ragged M and N: values and argmax equal the oracle's.  The
+    planner confirms the layout takes the TMA-fed kernel (K = 512 and 1024 then take the panel
+    resolve, the others the row resolve)."""
+    bt, m, n, k = shape
+    a = synth.uniform_int(41, (bt, m, k), -4, 4).astype(np.float32)
+    b = synth.uniform_int(42, (bt, k, n), -4, 4).astype(np.float32)
+    if sr == 2:
+        a, b = np.abs(a), np.abs(b)
+    wide = torch.zeros((bt, m, k + 8), dtype=torch.float32, device="cuda")
+    wide[:, :, :k] = _dev(a)
+    ad = wide[:, :, :k]                                   # row stride k + 8 (16-byte rows)
+    bd = _dev(b)
+    desc = trop.plan_describe("zmk,zkn->zmn", list(ad.shape), list(ad.stride()), list(bd.shape), list(bd.stride()))
+    assert "kernel=tma" in desc, desc
+    cw = torch.empty((bt, m, n + 4), dtype=torch.float32, device="cuda")
+    iw = torch.empty((bt, m, n + 4), dtype=torch.int32, device="cuda")
+    c, i = trop.gemm(ad, bd, sr, out=cw[:, :, :n], out_argmax=iw[:, :, :n])
+    rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == np.ascontiguousarray(rc).tobytes()
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
