@@ -1186,6 +1186,11 @@ struct StreamParams {
     FastDiv div_nvec;
     uint32_t total;  // nbatch * nvec
     Batch bt;
+    // binner > 0: the innermost batch axis (binner entries) varies fastest across threads, for
+    // layouts where its strides are below the column stride (consecutive threads then touch
+    // consecutive memory); 0: the columns vary fastest
+    uint32_t binner;
+    FastDiv div_binner;
 };
 
 template <int SR, bool ARG, int VEC, int MAXM>
@@ -1193,8 +1198,17 @@ __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
 {
     using O = Ops<SR>;
     for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.total; e += gridDim.x * blockDim.x) {
-        const uint32_t b = fdiv(e, p.div_nvec);
-        const int n = (int)(e - b * p.nvec) * VEC;
+        uint32_t b;
+        int n;
+        if (p.binner) {
+            const uint32_t r = fdiv(e, p.div_binner);
+            const uint32_t q = fdiv(r, p.div_nvec);
+            n = (int)(r - q * p.nvec) * VEC;
+            b = q * p.binner + (e - r * p.binner);
+        } else {
+            b = fdiv(e, p.div_nvec);
+            n = (int)(e - b * p.nvec) * VEC;
+        }
         int64_t oa, ob, oc, oi;
         batch_offsets(p.bt, b, oa, ob, oc, oi);
         float best[MAXM][VEC];
@@ -1647,6 +1661,18 @@ int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.nvec = (uint32_t)(g.N / VEC);
     p.div_nvec = make_fastdiv(p.nvec);
     p.total = (uint32_t)(nbatch * p.nvec);
+    if (p.bt.nb > 0) {
+        // the batch index's fastest axis is the last one of the decomposition
+        const int d = p.bt.nb - 1;
+        const auto mag = [](int64_t v) { return v < 0 ? -v : v; };
+        const int64_t col = std::min(mag(g.sBn), mag(g.sCn)) * VEC;
+        int64_t bs = std::max(mag(p.bt.sB[d]), mag(p.bt.sC[d]));
+        if (ARG) bs = std::max(bs, mag(p.bt.sI[d]));
+        if (bs < col) {
+            p.binner = p.bt.div[d].d;
+            p.div_binner = p.bt.div[d];
+        }
+    }
     int64_t blocks = ((int64_t)p.total + 255) / 256;
     int64_t cap = (int64_t)dev->sm_count * 16;
     int grid = (int)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
