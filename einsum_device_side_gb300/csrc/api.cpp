@@ -1316,7 +1316,7 @@ extern "C" int tropical_tree_backtrack(int n_inputs, const trop_tensor* inputs, 
     int rc = e == cudaSuccess ? TROP_OK : cuda_error(e, "cudaMemcpyAsync (backtrack tables)");
     if (rc == TROP_OK)
         rc = launch_backtrack(static_cast<const BtNode*>(dev), n_nodes,
-                              reinterpret_cast<const int32_t*>(static_cast<char*>(dev) + off_labs),
+                              reinterpret_cast<const int32_t*>(static_cast<char*>(dev) + off_labs), (int)labs.size(),
                               reinterpret_cast<const int64_t*>(static_cast<char*>(dev) + off_sizes), root_index,
                               n_labels, assignment, s);
     pool_retire(dev, s);

@@ -6,7 +6,8 @@
 // the nodes from the root backwards, each node's output labels are already
 // known (its consumers come later in the node order), so one read of its
 // argmax fixes the labels it eliminated.  The walk is inherently sequential;
-// one device thread does it so that no argmax ever leaves device memory.
+// it runs on the device (one warp, or one thread for trees whose tables do not
+// fit in shared memory) so that no argmax ever leaves device memory.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -58,6 +59,90 @@ __global__ void k_backtrack(const BtNode* __restrict__ nodes, int n_nodes, const
     }
 }
 
+// The same walk with the node, label and extent tables and the assignment in shared memory (the
+// tables of a tree fit there when the tree has up to a few thousand nodes).  One warp walks:
+// lane i takes output label i of a node, a warp scan turns the extents into row-major strides
+// and a warp sum gives the node's argmax offset, so a node costs one read of its argmax.
+constexpr size_t BT_SMEM_MAX = 200 * 1024;
+__host__ __device__ constexpr size_t bt_align(size_t n) { return (n + 15) / 16 * 16; }
+__host__ __device__ inline size_t bt_smem_bytes(int n_nodes, int n_labs, int n_labels)
+{
+    return bt_align(sizeof(BtNode) * (size_t)n_nodes) + bt_align(sizeof(int64_t) * (size_t)n_labels) +
+           bt_align(sizeof(int32_t) * (size_t)n_labs) + sizeof(int32_t) * (size_t)n_labels;
+}
+
+__global__ void __launch_bounds__(256) k_backtrack_smem(const BtNode* __restrict__ nodes_g, int n_nodes,
+                                                        const int32_t* __restrict__ labs_g, int n_labs,
+                                                        const int64_t* __restrict__ sizes_g, int64_t root_index,
+                                                        int n_labels, int32_t* __restrict__ assign_g)
+{
+    extern __shared__ __align__(16) unsigned char bsm[];
+    BtNode* nodes = reinterpret_cast<BtNode*>(bsm);
+    int64_t* sizes = reinterpret_cast<int64_t*>(bsm + bt_align(sizeof(BtNode) * (size_t)n_nodes));
+    int32_t* labs = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(sizes) +
+                                               bt_align(sizeof(int64_t) * (size_t)n_labels));
+    int32_t* assign = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(labs) +
+                                                 bt_align(sizeof(int32_t) * (size_t)n_labs));
+    const int tid = threadIdx.x;
+    for (int i = tid; i < n_nodes; i += blockDim.x) nodes[i] = nodes_g[i];
+    for (int i = tid; i < n_labels; i += blockDim.x) {
+        sizes[i] = sizes_g[i];
+        assign[i] = -1;
+    }
+    for (int i = tid; i < n_labs; i += blockDim.x) labs[i] = labs_g[i];
+    __syncthreads();
+    if (tid >= 32) return;
+    const int lane = tid;
+    const unsigned full = 0xffffffffu;
+    if (lane == 0) {
+        // root output labels from root_index (row-major, last fastest)
+        const BtNode r = nodes[n_nodes - 1];
+        int64_t rem = root_index;
+        for (int i = r.n_out - 1; i >= 0; --i) {
+            const int32_t l = labs[r.lab_off + i];
+            const int64_t sz = sizes[l];
+            assign[l] = (int32_t)(rem % sz);
+            rem /= sz;
+        }
+    }
+    __syncwarp();
+    for (int j = n_nodes - 1; j >= 0; --j) {
+        const BtNode nd = nodes[j];
+        if (!nd.argmax || nd.n_k == 0) continue;
+        int64_t sz = 1;
+        int32_t v = 0;
+        if (lane < nd.n_out) {
+            const int32_t l = labs[nd.lab_off + lane];
+            sz = sizes[l];
+            v = assign[l];
+        }
+        if (__any_sync(full, v < 0)) continue;  // an output label no later node fixed
+        // inclusive suffix product of the extents, then shifted: the row-major stride of lane i
+        int64_t st = sz;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t t = __shfl_down_sync(full, st, d);
+            if (lane + d < 32) st *= t;
+        }
+        int64_t stride = __shfl_down_sync(full, st, 1);
+        if (lane == 31) stride = 1;
+        int64_t o = lane < nd.n_out ? (int64_t)v * stride : 0;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) o += __shfl_xor_sync(full, o, d);
+        if (lane == 0) {
+            int64_t a = nd.argmax[o];
+            for (int i = nd.n_k - 1; i >= 0; --i) {
+                const int32_t l = labs[nd.lab_off + nd.n_out + i];
+                const int64_t s = sizes[l];
+                assign[l] = (int32_t)(a % s);
+                a /= s;
+            }
+        }
+        __syncwarp();
+    }
+    for (int l = lane; l < n_labels; l += 32) assign_g[l] = assign[l];
+}
+
 __global__ void k_fill_i32(int32_t* __restrict__ p, int64_t n, int32_t v)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
@@ -66,10 +151,15 @@ __global__ void k_fill_i32(int32_t* __restrict__ p, int64_t n, int32_t v)
 
 }  // namespace
 
-int launch_backtrack(const BtNode* nodes_dev, int n_nodes, const int32_t* labels_dev, const int64_t* sizes_dev,
-                     int64_t root_index, int n_labels, int32_t* assignment, cudaStream_t s)
+int launch_backtrack(const BtNode* nodes_dev, int n_nodes, const int32_t* labels_dev, int n_labs,
+                     const int64_t* sizes_dev, int64_t root_index, int n_labels, int32_t* assignment, cudaStream_t s)
 {
-    k_backtrack<<<1, 256, 0, s>>>(nodes_dev, n_nodes, labels_dev, sizes_dev, root_index, n_labels, assignment);
+    const size_t smem = bt_smem_bytes(n_nodes, n_labs, n_labels);
+    if (smem <= BT_SMEM_MAX)
+        k_backtrack_smem<<<1, 256, smem, s>>>(nodes_dev, n_nodes, labels_dev, n_labs, sizes_dev, root_index, n_labels,
+                                              assignment);
+    else
+        k_backtrack<<<1, 256, 0, s>>>(nodes_dev, n_nodes, labels_dev, sizes_dev, root_index, n_labels, assignment);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "k_backtrack");
     count_launches(1);
@@ -92,7 +182,10 @@ int launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s)
 int register_backtrack_kernels()
 {
     cudaFuncAttributes a;
-    cudaError_t e = cudaFuncGetAttributes(&a, (const void*)k_backtrack);
+    cudaError_t e = cudaFuncSetAttribute((const void*)k_backtrack_smem, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)BT_SMEM_MAX);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (backtrack smem)");
+    e = cudaFuncGetAttributes(&a, (const void*)k_backtrack);
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, (const void*)k_fill_i32);
     if (e != cudaSuccess) return cuda_error(e, "cudaFuncGetAttributes (backtrack kernels)");
     return TROP_OK;

@@ -160,7 +160,7 @@ struct BtNode {
     int n_k;                // argmax labels (row-major, last fastest)
     int lab_off;            // offset into the label table: n_out out labels then n_k argmax labels
 };
-int launch_backtrack(const BtNode* nodes_dev, int n_nodes, const int32_t* labels_dev,
+int launch_backtrack(const BtNode* nodes_dev, int n_nodes, const int32_t* labels_dev, int n_labs,
                      const int64_t* sizes_dev, int64_t root_index, int n_labels,
                      int32_t* assignment, cudaStream_t s);
 
