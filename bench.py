@@ -43,16 +43,27 @@ N_SETS = 3  # independent input sets rotated across steps: 288 MiB of inputs > 1
 F64_TFLOPS_NOMINAL = 1.25  # GB300 binary64 rate, nominal (no measured figure for this pipe)
 
 
+def code_sha256(path):
+    """sha256 of a C/C++/CUDA source with its comments and whitespace removed: it changes when
+    the code changes, not when only its comments do."""
+    import hashlib
+    import re
+    src = open(path, encoding="utf-8").read()
+    # drop comments outside string and character literals
+    pat = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'', re.S)
+    src = pat.sub(lambda m: "" if m.group(0).startswith("/") else m.group(0), src)
+    return hashlib.sha256(re.sub(r"\s+", "", src).encode()).hexdigest()
+
+
 def gemm_traffic():
     """DRAM bytes of one tropical GEMM call from the committed ncu summary, or
-    None when the kernel source changed since those counters were taken."""
-    import hashlib
+    None when the GEMM source's code changed since those counters were taken."""
     f = os.path.join(ROOT, "profiles", "k_gemm_tma_traffic.txt")
     if not os.path.exists(f):
         return None
     kv = dict(line.split(": ", 1) for line in open(f).read().splitlines() if ": " in line)
-    src = open(os.path.join(ROOT, "einsum_device_side_gb300", "csrc", "gemm.cu"), "rb").read()
-    if hashlib.sha256(src).hexdigest() != kv.get("source_sha256"):
+    src = os.path.join(ROOT, "einsum_device_side_gb300", "csrc", "gemm.cu")
+    if code_sha256(src) != kv.get("source_code_sha256"):
         return None
     return int(kv["bytes_per_launch"])
 

@@ -23,14 +23,23 @@
 // a strict left-to-right scan gives.
 //
 // Kernels:
-//   k_gemm_tiled     64x64 output tile per 64-thread CTA, 8x8 per thread, A
-//                    staged transposed so the packed add takes {a,a} pairs
-//                    built in registers; needs sAk == 1 and sBn == 1 (the
-//                    planner permutes other layouts).  A thin last wave is
-//                    cut along k (stream-K, see the schedule below).
-//   k_argmax_resolve chunk -> exact index, rows of all column panels split
-//                    evenly over resident CTAs; launched as a programmatic
-//                    dependent of k_gemm_tiled.
+//   k_gemm_tma       the argmax GEMM for one batch axis, K a multiple of 16 and
+//                    16-byte rows: 64x64 tile per 128-thread CTA, 8x4 outputs
+//                    per thread, A and B boxes by TMA into a 3-stage mbarrier
+//                    ring, 4 CTAs per SM; a programmatic dependent of the
+//                    kernel before it.
+//   k_gemm_tiled     other layouts: 64x64 output tile, 8x8 per thread (8x4
+//                    with argmax), A staged transposed through registers and
+//                    B by cp.async; needs sAk == 1 and sBn == 1 (the planner
+//                    permutes other layouts).  A thin last wave is cut along k
+//                    (stream-K, see the schedule below).
+//   k_argmax_resolve_rows  chunk -> exact index for K <= 256: a warp reads a
+//                    row of A once, one chunk per lane, and outputs take their
+//                    chunk's values by shuffles.
+//   k_argmax_resolve chunk -> exact index for longer contractions or other
+//                    layouts, B staged per column panel.  Both resolve passes
+//                    split the rows of all column panels evenly over resident
+//                    CTAs and are programmatic dependents of the GEMM.
 //   k_gemm_stream    few rows (M <= 8) and a short contraction (K <= 64):
 //                    one thread per (batch, column vector), memory bound.
 //   k_gemm_generic   anything else: one thread per output, sequential k.
