@@ -197,8 +197,6 @@ __device__ __forceinline__ int row_of(int tm, int i) { return i < 4 ? tm * 4 + i
 // Programmatic dependent launch: a kernel launched with programmatic stream serialisation
 // may start once every CTA of the kernel before it has signalled (or exited); it must
 // wait before touching that kernel's results.  Without the launch attribute both are no-ops.
-__device__ __forceinline__ void pdl_signal() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Rows of the resolve pass that this CTA walks, and the (batch, first column, row) of row
 // unit u (units run over the rows of every column panel of every batch).
@@ -325,6 +323,7 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
 
     __shared__ int s_last;
 
+    pdl_wait();    // launched as a programmatic dependent: the grid before it has completed
     pdl_signal();  // the resolve pass may start filling SMs as this grid drains
     const int tid = threadIdx.x;
     const int tm = tid / (BN / TN), tn = tid % (BN / TN);
@@ -1206,6 +1205,8 @@ template <int SR, bool ARG, int VEC, int MAXM>
 __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
 {
     using O = Ops<SR>;
+    pdl_wait();
+    pdl_signal();
     for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.total; e += gridDim.x * blockDim.x) {
         uint32_t b;
         int n;
@@ -1297,6 +1298,8 @@ struct GenericParams {
 template <int SR, bool ARG>
 __global__ void k_gemm_generic(GenericParams p)
 {
+    pdl_wait();
+    pdl_signal();
     using O = Ops<SR>;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < p.total;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -1625,7 +1628,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
         }
     }
     if (!launched) {
-        k_gemm_tiled<SR, ARG, TN><<<(unsigned)(p.T_dp + G_sk), THREADS, 0, s>>>(p);
+        (void)launch_pdl(k_gemm_tiled<SR, ARG, TN>, dim3((unsigned)(p.T_dp + G_sk)), dim3(THREADS), 0, s, p);
         rc = check_launch("k_gemm_tiled");
     }
     if (rc == TROP_OK && ARG) rc = launch_resolve<SR>(p, g, nbatch, s, dev);
@@ -1687,14 +1690,14 @@ int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     int grid = (int)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
     // register arrays sized to the rows actually present keep occupancy high
     if (g.M <= 2) {
-        if (vec) k_gemm_stream<SR, ARG, 4, 2><<<grid, 256, 0, s>>>(p);
-        else k_gemm_stream<SR, ARG, 1, 2><<<grid, 256, 0, s>>>(p);
+        if (vec) (void)launch_pdl(k_gemm_stream<SR, ARG, 4, 2>, grid, 256, 0, s, p);
+        else (void)launch_pdl(k_gemm_stream<SR, ARG, 1, 2>, grid, 256, 0, s, p);
     } else if (g.M <= 4) {
-        if (vec) k_gemm_stream<SR, ARG, 4, 4><<<grid, 256, 0, s>>>(p);
-        else k_gemm_stream<SR, ARG, 1, 4><<<grid, 256, 0, s>>>(p);
+        if (vec) (void)launch_pdl(k_gemm_stream<SR, ARG, 4, 4>, grid, 256, 0, s, p);
+        else (void)launch_pdl(k_gemm_stream<SR, ARG, 1, 4>, grid, 256, 0, s, p);
     } else {
-        if (vec) k_gemm_stream<SR, ARG, 4, MAXM_STREAM><<<grid, 256, 0, s>>>(p);
-        else k_gemm_stream<SR, ARG, 1, MAXM_STREAM><<<grid, 256, 0, s>>>(p);
+        if (vec) (void)launch_pdl(k_gemm_stream<SR, ARG, 4, MAXM_STREAM>, grid, 256, 0, s, p);
+        else (void)launch_pdl(k_gemm_stream<SR, ARG, 1, MAXM_STREAM>, grid, 256, 0, s, p);
     }
     return check_launch("k_gemm_stream");
 }
@@ -1732,7 +1735,7 @@ int run_generic(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     int64_t blocks = (p.total + 255) / 256;
     int64_t cap = (int64_t)dev->sm_count * 16;
     int grid = (int)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
-    k_gemm_generic<SR, ARG><<<grid, 256, 0, s>>>(p);
+    (void)launch_pdl(k_gemm_generic<SR, ARG>, grid, 256, 0, s, p);
     return check_launch("k_gemm_generic");
 }
 

@@ -93,6 +93,34 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f)
 }
 #endif
 
+#ifdef __CUDACC__
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the grid
+// before it on the stream drains; it calls pdl_wait() before its first access to global
+// memory (which waits for that grid to complete and its writes to be visible) and then
+// pdl_signal(), which lets the grid after it start the same way.  Without the launch attribute
+// both are no-ops.  Every access therefore keeps plain stream order; only launch latency is
+// hidden.
+__device__ __forceinline__ void pdl_signal() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
+
 // ---------------------------------------------------------------- launches
 // Gather / permute over `rank` dims (output order, last fastest).  Optional
 // companion int32 tensor moved through the same index mapping.

@@ -71,6 +71,8 @@ template <typename T, bool PAIR>
 __global__ void k_gather(const T* __restrict__ in, T* __restrict__ out, const int32_t* __restrict__ in2,
                          int32_t* __restrict__ out2, GatherParams p)
 {
+    pdl_wait();
+    pdl_signal();
     for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < p.total;
          o += (int64_t)gridDim.x * blockDim.x) {
         int64_t rem = o, oi = 0, oo = 0, oi2 = 0, oo2 = 0;
@@ -102,6 +104,8 @@ template <typename T, typename V, bool PAIR>
 __global__ void k_copy_rows(const T* __restrict__ in, T* __restrict__ out, const int32_t* __restrict__ in2,
                             int32_t* __restrict__ out2, RowParams p)
 {
+    pdl_wait();
+    pdl_signal();
     constexpr int W = sizeof(V) / sizeof(T);
     for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.total; e += gridDim.x * blockDim.x) {
         uint32_t row = fdiv(e, p.divLv);
@@ -176,6 +180,8 @@ __global__ void __launch_bounds__(NT, PAIR ? 3 : TROP_TRANSPOSE_MINB) k_transpos
                                                   const int32_t* __restrict__ in2, int32_t* __restrict__ out2,
                                                   TransParams p)
 {
+    pdl_wait();
+    pdl_signal();
     using Cfg = TileCfg<sizeof(T)>;
     using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
     constexpr int W = 16 / sizeof(T);
@@ -383,6 +389,8 @@ template <int SR, typename T>
 __global__ void k_reduce_thread(const T* __restrict__ in, T* __restrict__ out, int32_t* __restrict__ arg,
                                 RedParams p)
 {
+    pdl_wait();
+    pdl_signal();
     using S = Semi<SR, T>;
     for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < p.n_out;
          o += (int64_t)gridDim.x * blockDim.x) {
@@ -409,6 +417,8 @@ __global__ void __launch_bounds__(NT) k_reduce_block(const T* __restrict__ in, T
                                                      int32_t* __restrict__ arg, T* __restrict__ part_v,
                                                      int64_t* __restrict__ part_i, RedParams p)
 {
+    pdl_wait();
+    pdl_signal();
     using S = Semi<SR, T>;
     __shared__ T sv[NT];
     __shared__ int64_t si[NT];
@@ -466,6 +476,8 @@ template <int SR, typename T, int RS>
 __global__ void __launch_bounds__(32 * RS) k_reduce_tile(const T* __restrict__ in, T* __restrict__ out,
                                                         int32_t* __restrict__ arg, RedParams p)
 {
+    pdl_wait();
+    pdl_signal();
     using S = Semi<SR, T>;
     __shared__ T sv[RS][32];
     __shared__ int64_t si[RS][32];
@@ -515,6 +527,8 @@ template <int SR, typename T>
 __global__ void k_reduce_combine(T* __restrict__ out, int32_t* __restrict__ arg, const T* __restrict__ part_v,
                                  const int64_t* __restrict__ part_i, RedParams p)
 {
+    pdl_wait();
+    pdl_signal();
     using S = Semi<SR, T>;
     for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < p.n_out;
          o += (int64_t)gridDim.x * blockDim.x) {
@@ -623,15 +637,15 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             p.divLv = make_fastdiv(p.Lv);
             using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
             int g = grid_for(p.total, NT, dev->sm_count);
-            if (pair) k_copy_rows<T, V, true><<<g, NT, 0, s>>>(in, out, in2, out2, p);
-            else k_copy_rows<T, V, false><<<g, NT, 0, s>>>(in, out, in2, out2, p);
+            if (pair) (void)launch_pdl(k_copy_rows<T, V, true>, g, NT, 0, s, in, out, in2, out2, p);
+            else (void)launch_pdl(k_copy_rows<T, V, false>, g, NT, 0, s, in, out, in2, out2, p);
         } else {
             p.Lv = p.L;
             p.total = (uint32_t)total;
             p.divLv = make_fastdiv(p.Lv);
             int g = grid_for(p.total, NT, dev->sm_count);
-            if (pair) k_copy_rows<T, T, true><<<g, NT, 0, s>>>(in, out, in2, out2, p);
-            else k_copy_rows<T, T, false><<<g, NT, 0, s>>>(in, out, in2, out2, p);
+            if (pair) (void)launch_pdl(k_copy_rows<T, T, true>, g, NT, 0, s, in, out, in2, out2, p);
+            else (void)launch_pdl(k_copy_rows<T, T, false>, g, NT, 0, s, in, out, in2, out2, p);
         }
         return check_launch("k_copy_rows");
     }
@@ -746,8 +760,8 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             // at least W so the storer's W-wide runs stay whole
             p.sw = (int)std::max<int64_t>(W, (int64_t)32 * W / ti_);
             const int g = (int)std::min<int64_t>(tiles, (int64_t)dev->sm_count * 64);
-            if (pair) k_transpose<T, true><<<g, NT, 0, s>>>(in, out, in2, out2, p);
-            else k_transpose<T, false><<<g, NT, 0, s>>>(in, out, in2, out2, p);
+            if (pair) (void)launch_pdl(k_transpose<T, true>, g, NT, 0, s, in, out, in2, out2, p);
+            else (void)launch_pdl(k_transpose<T, false>, g, NT, 0, s, in, out, in2, out2, p);
             return check_launch("k_transpose");
         }
     }
@@ -764,8 +778,8 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
         p.s_out2[i] = d.s_out2[i];
     }
     int g = grid_for(total, NT, dev->sm_count);
-    if (pair) k_gather<T, true><<<g, NT, 0, s>>>(in, out, in2, out2, p);
-    else k_gather<T, false><<<g, NT, 0, s>>>(in, out, in2, out2, p);
+    if (pair) (void)launch_pdl(k_gather<T, true>, g, NT, 0, s, in, out, in2, out2, p);
+    else (void)launch_pdl(k_gather<T, false>, g, NT, 0, s, in, out, in2, out2, p);
     return check_launch("k_gather");
 }
 
@@ -812,7 +826,7 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
     const int64_t threads_wanted = (int64_t)dev->sm_count * 1024;
     if (p.R <= 64 || p.n_out >= threads_wanted) {
         int g = grid_for(p.n_out, NT, dev->sm_count);
-        k_reduce_thread<SR, T><<<g, NT, 0, s>>>(in, out, arg, p);
+        (void)launch_pdl(k_reduce_thread<SR, T>, g, NT, 0, s, in, out, arg, p);
         return check_launch("k_reduce_thread");
     }
     if (p.out_rank >= 1 && p.out_s_in[p.out_rank - 1] == 1 && p.R <= (int64_t(1) << 24)) {
@@ -820,8 +834,8 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
         const int64_t inner = p.out_size[p.out_rank - 1];
         const int64_t groups = p.n_out / inner * ((inner + 31) / 32);
         const int g = (int)std::min<int64_t>(std::max<int64_t>(groups, 1), (int64_t)dev->sm_count * 16);
-        if (p.R >= 64) k_reduce_tile<SR, T, 32><<<g, 32 * 32, 0, s>>>(in, out, arg, p);
-        else k_reduce_tile<SR, T, 8><<<g, 32 * 8, 0, s>>>(in, out, arg, p);
+        if (p.R >= 64) (void)launch_pdl(k_reduce_tile<SR, T, 32>, g, 32 * 32, 0, s, in, out, arg, p);
+        else (void)launch_pdl(k_reduce_tile<SR, T, 8>, g, 32 * 8, 0, s, in, out, arg, p);
         return check_launch("k_reduce_tile");
     }
     // split each output's reduced range so that enough blocks exist
@@ -842,11 +856,11 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
         part_v = reinterpret_cast<T*>(part_i + nb);
     }
     int g = grid_for(p.n_out * nsplit, 1, dev->sm_count, 16);
-    k_reduce_block<SR, T><<<g, NT, 0, s>>>(in, out, arg, part_v, part_i, p);
+    (void)launch_pdl(k_reduce_block<SR, T>, g, NT, 0, s, in, out, arg, part_v, part_i, p);
     int rc = check_launch("k_reduce_block");
     if (rc == TROP_OK && nsplit > 1) {
         int g2 = grid_for(p.n_out, NT, dev->sm_count);
-        k_reduce_combine<SR, T><<<g2, NT, 0, s>>>(out, arg, part_v, part_i, p);
+        (void)launch_pdl(k_reduce_combine<SR, T>, g2, NT, 0, s, out, arg, part_v, part_i, p);
         rc = check_launch("k_reduce_combine");
     }
     if (ws) pool_retire(ws, s);
@@ -898,7 +912,7 @@ int launch_reduce_scratch_typed(const void* in_, void* out_, int32_t* arg, const
     const int64_t threads_wanted = (int64_t)dev->sm_count * 1024;
     if (p.R <= 64 || p.n_out >= threads_wanted) {
         int g = grid_for(p.n_out, NT, dev->sm_count);
-        k_reduce_thread<SR, T><<<g, NT, 0, s>>>(in, out, arg, p);
+        (void)launch_pdl(k_reduce_thread<SR, T>, g, NT, 0, s, in, out, arg, p);
         return check_launch("k_reduce_thread");
     }
     if (p.out_rank >= 1 && p.out_s_in[p.out_rank - 1] == 1 && p.R <= (int64_t(1) << 24)) {
@@ -906,8 +920,8 @@ int launch_reduce_scratch_typed(const void* in_, void* out_, int32_t* arg, const
         const int64_t inner = p.out_size[p.out_rank - 1];
         const int64_t groups = p.n_out / inner * ((inner + 31) / 32);
         const int g = (int)std::min<int64_t>(std::max<int64_t>(groups, 1), (int64_t)dev->sm_count * 16);
-        if (p.R >= 64) k_reduce_tile<SR, T, 32><<<g, 32 * 32, 0, s>>>(in, out, arg, p);
-        else k_reduce_tile<SR, T, 8><<<g, 32 * 8, 0, s>>>(in, out, arg, p);
+        if (p.R >= 64) (void)launch_pdl(k_reduce_tile<SR, T, 32>, g, 32 * 32, 0, s, in, out, arg, p);
+        else (void)launch_pdl(k_reduce_tile<SR, T, 8>, g, 32 * 8, 0, s, in, out, arg, p);
         return check_launch("k_reduce_tile");
     }
     const int64_t blocks_wanted = (int64_t)dev->sm_count * 8;
@@ -931,11 +945,11 @@ int launch_reduce_scratch_typed(const void* in_, void* out_, int32_t* arg, const
         part_v = reinterpret_cast<T*>(part_i + nb);
     }
     int g = grid_for(p.n_out * nsplit, 1, dev->sm_count, 16);
-    k_reduce_block<SR, T><<<g, NT, 0, s>>>(in, out, arg, part_v, part_i, p);
+    (void)launch_pdl(k_reduce_block<SR, T>, g, NT, 0, s, in, out, arg, part_v, part_i, p);
     int rc = check_launch("k_reduce_block");
     if (rc == TROP_OK && nsplit > 1) {
         int g2 = grid_for(p.n_out, NT, dev->sm_count);
-        k_reduce_combine<SR, T><<<g2, NT, 0, s>>>(out, arg, part_v, part_i, p);
+        (void)launch_pdl(k_reduce_combine<SR, T>, g2, NT, 0, s, out, arg, part_v, part_i, p);
         rc = check_launch("k_reduce_combine");
     }
     return rc;
