@@ -15,14 +15,18 @@
 // (line, bin range), adding into bins of its own in shared memory -- every bin
 // has one writer adding in the stated order, so every sum is the sequential
 // one, bit for bit.  A CTA takes 32 lines; its 8 warps split a span of 256
-// bins (32 per lane) and all walk the same staged block (32 lines x 32 steps of
-// argmax and dC), which the CTA loads coalesced along whichever index is
-// contiguous and double buffers.  Longer contractions repeat the walk per
-// 256-bin span.  dA and dB are two jobs of one launch (blockIdx.y).
+// bins and all walk the same staged block (32 lines x 32 steps of argmax and
+// dC), which the CTA loads coalesced along whichever index is contiguous and
+// double buffers.  Longer contractions repeat the walk per 256-bin span.  dA
+// and dB are two jobs of one launch (blockIdx.y) of k_winner_route, except
+// that for max-plus and min-plus the rows of dA, when their steps are
+// contiguous, go to k_route_lane (one lane owns a whole line) in a launch of
+// their own that the dB launch may overlap.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -59,13 +63,23 @@ struct RouteParams {
     int64_t nbatch, K;
     RouteJob job[2];
     int njobs;
+    // 0: wait for the grid before this one at the start (it may have signalled before its own
+    // results were complete); 1: the grid before is k_route_lane of the same call, which
+    // signals only after its own wait, so the inputs are complete -- wait at the end instead, so
+    // that this grid completes only after that one
+    int late_wait;
 };
 
 template <bool MUL>
 __global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
 {
     extern __shared__ __align__(16) float smem_all[];
-    if ((int)blockIdx.y >= p.njobs) return;
+    if (!p.late_wait) pdl_wait();
+    pdl_signal();
+    if ((int)blockIdx.y >= p.njobs) {
+        if (p.late_wait) pdl_wait();
+        return;
+    }
     const RouteJob& j = p.job[blockIdx.y];
     const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
     float* bins = smem_all + w * BW_KL * BW_LD;                      // this warp's [bin][line]
@@ -178,6 +192,156 @@ __global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
             }
         }
     }
+    if (p.late_wait) pdl_wait();
+}
+
+// One lane per output line with all of the line's bins in shared memory, [bin][lane] (no bank
+// conflicts whatever the bins), for lines whose steps are contiguous and 16-byte aligned (the
+// rows of dA in the common layout).  A lane reads its own line 8 steps at a time -- one full
+// 32-byte sector per array -- through a ring of RT_RING register sets (the loads of the next
+// three chunks in flight while a chunk is applied) and applies the steps four at a time: the four bins are read
+// together, and a step whose bin an earlier step of the group also hit continues from that
+// step's new value, so every bin still adds its terms in increasing step order.  Max-plus and
+// min-plus only: the term is dC itself.
+constexpr int RT_SPAN = 256;  // bins a lane holds per walk (longer contractions: one walk per span)
+constexpr int RT_STEP = 8;    // steps per chunk
+constexpr int RT_RING = 4;    // chunks in registers: one applied, three in flight
+// [span][32] bins, rounded up to whole 32-row blocks, plus one row: the transposed copy of the
+// last block (33-float rows) reaches one row past it
+size_t lane_smem(int64_t K)
+{
+    const size_t rows = ((size_t)std::min<int64_t>(K, RT_SPAN) + 31) / 32 * 32 + 1;
+    return sizeof(float) * rows * 32;
+}
+// the layouts k_route_lane serves: unit step stride and 16-byte aligned lines
+bool lane_ok(const RouteJob& j)
+{
+    return j.sIs == 1 && j.sGs == 1 && j.sIx % 4 == 0 && j.sGx % 4 == 0 && j.sIb % 4 == 0 && j.sGb % 4 == 0 &&
+           ((uintptr_t)j.I % 16) == 0 && ((uintptr_t)j.G % 16) == 0;
+}
+
+__global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
+{
+    extern __shared__ __align__(16) float bins[];  // [span][32]: bin k of lane l at k * 32 + l
+    pdl_wait();
+    pdl_signal();
+    const RouteJob& j = p.job[0];
+    const int l = threadIdx.x;
+    const int64_t lines = p.nbatch * j.X;
+    for (int64_t base = (int64_t)blockIdx.x * 32; base < lines; base += (int64_t)gridDim.x * 32) {
+        const int64_t o = base + l;
+        const bool valid = o < lines;
+        const int64_t b = valid ? o / j.X : 0, x = valid ? o - b * j.X : 0;
+        const int32_t* Il = j.I + b * j.sIb + x * j.sIx;
+        const float* Gl = j.G + b * j.sGb + x * j.sGx;
+        float* Ol = j.O + b * j.sOb + x * j.sOx;
+        for (int64_t kc = 0; kc < p.K; kc += RT_SPAN) {
+            const int kn = (int)min((int64_t)RT_SPAN, p.K - kc);
+            for (int k = 0; k < kn; ++k) bins[k * 32 + l] = 0.0f;
+            const int64_t nch = (j.S + RT_STEP - 1) / RT_STEP;
+            int kr[RT_RING][RT_STEP];
+            float gr[RT_RING][RT_STEP];
+            auto load = [&](auto slot, int64_t c) {
+                constexpr int R = decltype(slot)::value;
+                const int64_t s0 = c * RT_STEP;
+                if (valid && s0 + RT_STEP <= j.S) {
+                    const int4 k0 = __ldg(reinterpret_cast<const int4*>(Il + s0));
+                    const int4 k1 = __ldg(reinterpret_cast<const int4*>(Il + s0 + 4));
+                    const float4 g0 = __ldg(reinterpret_cast<const float4*>(Gl + s0));
+                    const float4 g1 = __ldg(reinterpret_cast<const float4*>(Gl + s0 + 4));
+                    kr[R][0] = k0.x; kr[R][1] = k0.y; kr[R][2] = k0.z; kr[R][3] = k0.w;
+                    kr[R][4] = k1.x; kr[R][5] = k1.y; kr[R][6] = k1.z; kr[R][7] = k1.w;
+                    gr[R][0] = g0.x; gr[R][1] = g0.y; gr[R][2] = g0.z; gr[R][3] = g0.w;
+                    gr[R][4] = g1.x; gr[R][5] = g1.y; gr[R][6] = g1.z; gr[R][7] = g1.w;
+                } else {
+#pragma unroll
+                    for (int t = 0; t < RT_STEP; ++t) {
+                        const bool in = valid && c < nch && s0 + t < j.S;
+                        kr[R][t] = in ? __ldg(Il + s0 + t) : -1;
+                        gr[R][t] = in ? __ldg(Gl + s0 + t) : 0.0f;
+                    }
+                }
+            };
+            // bin of a step relative to the span, -1 when it routes nowhere in this span
+            auto rel = [&](int k) {
+                const int64_t d = (int64_t)k - kc;
+                return (k >= 0 && d >= 0 && d < kn) ? (int)d : -1;
+            };
+            auto apply = [&](auto slot) {
+                constexpr int R = decltype(slot)::value;
+#pragma unroll
+                for (int q = 0; q < RT_STEP; q += 4) {
+                    int d[4];
+                    float g[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        d[t] = rel(kr[R][q + t]);
+                        g[t] = gr[R][q + t];
+                    }
+                    const float x0 = d[0] >= 0 ? bins[d[0] * 32 + l] : 0.0f;
+                    const float x1 = d[1] >= 0 ? bins[d[1] * 32 + l] : 0.0f;
+                    const float x2 = d[2] >= 0 ? bins[d[2] * 32 + l] : 0.0f;
+                    const float x3 = d[3] >= 0 ? bins[d[3] * 32 + l] : 0.0f;
+                    // each step continues from the latest earlier step of the group on its bin
+                    const float y0 = __fadd_rn(x0, g[0]);
+                    const float y1 = __fadd_rn(d[1] == d[0] ? y0 : x1, g[1]);
+                    const float y2 = __fadd_rn(d[2] == d[1] ? y1 : d[2] == d[0] ? y0 : x2, g[2]);
+                    const float y3 = __fadd_rn(d[3] == d[2] ? y2 : d[3] == d[1] ? y1 : d[3] == d[0] ? y0 : x3, g[3]);
+                    if (d[0] >= 0) bins[d[0] * 32 + l] = y0;
+                    if (d[1] >= 0) bins[d[1] * 32 + l] = y1;
+                    if (d[2] >= 0) bins[d[2] * 32 + l] = y2;
+                    if (d[3] >= 0) bins[d[3] * 32 + l] = y3;
+                }
+            };
+            using I0 = std::integral_constant<int, 0>;
+            using I1 = std::integral_constant<int, 1>;
+            using I2 = std::integral_constant<int, 2>;
+            using I3 = std::integral_constant<int, 3>;
+            static_assert(RT_RING == 4, "the ring is unrolled for four slots");
+            load(I0{}, 0);
+            load(I1{}, 1);
+            load(I2{}, 2);
+            // one ring turn: chunk c in slot R
+            auto turn = [&](auto slot, int64_t c) {
+                constexpr int R = decltype(slot)::value;
+                load(std::integral_constant<int, (R + 3) % 4>{}, c + 3);
+                apply(slot);
+            };
+            for (int64_t c = 0; c < nch; c += 4) {
+                turn(I0{}, c);
+                if (c + 1 >= nch) break;
+                turn(I1{}, c + 1);
+                if (c + 2 >= nch) break;
+                turn(I2{}, c + 2);
+                if (c + 3 >= nch) break;
+                turn(I3{}, c + 3);
+            }
+            __syncwarp();
+            if (j.sOk == 1) {
+                // bins contiguous in the gradient: 32 x 32 blocks transposed through a padded
+                // copy so that each store writes 32 consecutive bins of one line; blocks go last
+                // to first, so the copy's extra row lies in a block already written
+                for (int kb = ((kn - 1) / 32) * 32; kb >= 0; kb -= 32) {
+                    float r[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) r[t] = kb + t < kn ? bins[(kb + t) * 32 + l] : 0.0f;
+                    __syncwarp();
+                    float* tb = bins + kb * 32;  // [line][33]
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) tb[l * 33 + t] = r[t];
+                    __syncwarp();
+                    for (int rr = 0; rr < 32; ++rr) {
+                        float* Or = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(Ol), rr));
+                        if (base + rr < lines && kb + l < kn) Or[kc + kb + l] = tb[rr * 33 + l];
+                    }
+                    __syncwarp();
+                }
+            } else if (valid) {
+                for (int k = 0; k < kn; ++k) Ol[(kc + k) * j.sOk] = bins[k * 32 + l];
+            }
+            __syncwarp();
+        }
+    }
 }
 
 }  // namespace
@@ -221,12 +385,31 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
         j.sOb = sdB[0], j.sOx = sdB[2], j.sOk = sdB[1];
     }
     if (p.njobs == 0 || batch == 0 || K == 0) return TROP_OK;
+    const bool mul = semiring == TROP_MAXTIMES;
+    // for max-plus and min-plus the rows job (steps contiguous, the common layout of dA) takes
+    // the lane-per-line kernel (measured on the batch-64 256^3 gradient: 42 against 52 us for
+    // both jobs; with max-times' operand gathers it was slower); the other job follows it and
+    // may start at once (see RouteParams::late_wait)
+    if (!mul && dA && lane_ok(p.job[0])) {
+        RouteParams pa = p;
+        pa.njobs = 1;
+        const int64_t groups = (batch * pa.job[0].X + 31) / 32;
+        const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(groups, (int64_t)dev->sm_count * 16));
+        (void)launch_pdl(k_route_lane, dim3(gx), dim3(32), lane_smem(K), s, pa);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_error(e, "k_route_lane");
+        count_launches(1);
+        if (p.njobs == 1) return TROP_OK;
+        p.job[0] = p.job[1];
+        p.njobs = 1;
+        p.late_wait = 1;
+    }
     int64_t ctas = 1;
     for (int q = 0; q < p.njobs; ++q) ctas = std::max(ctas, (batch * p.job[q].X + 31) / 32);
     const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)dev->sm_count * 16));
     const dim3 grid(gx, (unsigned)p.njobs);
-    if (semiring == TROP_MAXTIMES) k_winner_route<true><<<grid, BW_THREADS, BW_SMEM, s>>>(p);
-    else k_winner_route<false><<<grid, BW_THREADS, BW_SMEM, s>>>(p);
+    if (mul) (void)launch_pdl(k_winner_route<true>, grid, dim3(BW_THREADS), BW_SMEM, s, p);
+    else (void)launch_pdl(k_winner_route<false>, grid, dim3(BW_THREADS), BW_SMEM, s, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "k_winner_route");
     count_launches(1);
@@ -240,6 +423,9 @@ int register_backward_kernels()
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BW_SMEM);
         if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (winner route smem)");
     }
+    cudaError_t e = cudaFuncSetAttribute((const void*)k_route_lane, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)lane_smem(RT_SPAN));
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (lane route smem)");
     return TROP_OK;
 }
 
