@@ -215,8 +215,9 @@ int tropical_gemm_strided_batched_argmax(int semiring, int dtype,
  * index outside [0,K) routes nowhere.  Each product and each addition rounds
  * once in binary32, in the order stated, so results are bit-reproducible.
  * dA and dB are written entirely (zero where nothing routes); either may be
- * NULL (not wanted).  A and B are read only for max-times (may be NULL
- * otherwise).  All pointers are device memory, f32 except the int32 argmax;
+ * NULL (not wanted).  The two are computed concurrently, so they must not
+ * overlap each other or any input.  A and B are read only for max-times (may
+ * be NULL otherwise).  All pointers are device memory, f32 except the int32 argmax;
  * the caller owns every buffer.  Strides in elements, any sign-free layout.
  * Errors: INVALID_ARG (negative extent, missing pointer), OVERFLOW
  *         (K > INT32_MAX), HOST_POINTER, DEVICE_MISMATCH, CUDA. */
