@@ -130,3 +130,15 @@ def test_describe_tma_needs_aligned_rows_and_one_batch_axis(trop):
     st_a = [5 * 64 * 32 + 64, 64 * 32, 32, 1]
     text = trop.plan_describe("yzmk,yzkn->yzmn", sa, st_a, sb, _contig(sb))
     assert "kernel=tiled" in text and "batch_axes=2" in text, text
+
+
+def test_describe_wide_row_strides_leave_the_32_bit_paths(trop):
+    """A row stride past 2^31 elements keeps the GEMM on 64-bit offsets: the short-K row resolve
+    (32-bit row offsets) gives way to the 64-bit panel resolve, at any M."""
+    wide = (1 << 31) + 64
+    sb = [1, 64, 128]
+    narrow = trop.plan_describe("zmk,zkn->zmn", [1, 16, 64], [16 * 64, 64, 1], sb, _contig(sb))
+    assert "route=tiled" in narrow and "resolve=rows" in narrow, narrow
+    text = trop.plan_describe("zmk,zkn->zmn", [1, 16, 64], [16 * wide, wide, 1], sb, _contig(sb))
+    assert "route=tiled" in text and "resolve=panel64" in text, text
+    assert f"sAm={wide}" in text, text
