@@ -187,6 +187,20 @@ def _spec_shape(spec: str, shapes):
     return [sizes[ch] for ch in out]
 
 
+def _check_argmax(am: torch.Tensor, out: torch.Tensor, like: torch.Tensor, contiguous: bool = True):
+    """The C ABI writes an int32 argmax in out's shape (contiguous row-major, or
+    with out's strides for the GEMM): anything else would be written past its end
+    or read back wrongly, so it is refused here."""
+    if am.dtype != torch.int32:
+        raise TropicalError(-4, f"argmax must be int32, got {am.dtype}")
+    if tuple(am.shape) != tuple(out.shape):
+        raise TropicalError(-5, f"argmax shape {tuple(am.shape)} differs from out shape {tuple(out.shape)}")
+    if am.device != like.device:
+        raise TropicalError(-3, f"argmax is on {am.device}, operands on {like.device}")
+    if contiguous and not am.is_contiguous():
+        raise TropicalError(-1, "argmax must be contiguous (row-major in out's shape)")
+
+
 def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Tensor | None = None,
                   argmax: bool | torch.Tensor = False, stream=None):
     """Unary permute / diagonal gather / tropical trace.  Returns ``out`` or
@@ -197,6 +211,7 @@ def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Ten
     am = None
     if isinstance(argmax, torch.Tensor):
         am = argmax
+        _check_argmax(am, out, x)
     elif argmax:
         am = torch.empty(out.shape, dtype=torch.int32, device=x.device)
     dx, do = tensor_desc(x), tensor_desc(out)
@@ -212,6 +227,8 @@ def permute_trace_noalloc(x: torch.Tensor, spec: str, semiring="maxplus", *, out
     must be given; split reductions use the library's fixed scratch, so calls
     must not overlap on the GPU."""
     lib = load()
+    if argmax is not None:
+        _check_argmax(argmax, out, x)
     dx, do = tensor_desc(x), tensor_desc(out)
     _check(lib.tropical_permute_trace_noalloc(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
                                               argmax.data_ptr() if argmax is not None and argmax.numel() else None,
@@ -260,6 +277,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
     am = None
     if argmax:
         am = out_argmax if out_argmax is not None else torch.empty((batch, M, N), dtype=torch.int32, device=A.device)
+        _check_argmax(am, out, A, contiguous=False)
         if am.stride() != out.stride():
             raise ValueError("argmax must have the strides of out")
     _check(lib.tropical_gemm_strided_batched_argmax(
@@ -336,6 +354,7 @@ def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argm
     am = None
     if argmax:
         am = out_argmax if out_argmax is not None else torch.empty(out.shape, dtype=torch.int32, device=A.device)
+        _check_argmax(am, out, A)
     a, b, o = tensor_desc(A), tensor_desc(B), tensor_desc(out)
     _check(lib.tropical_einsum_pairwise(spec.encode(), ctypes.byref(a), ctypes.byref(b), _sr(semiring),
                                         ctypes.byref(o), am.data_ptr() if am is not None and am.numel() else None,

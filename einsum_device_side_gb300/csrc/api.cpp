@@ -190,9 +190,10 @@ int plan_unary(const View& in, const int32_t* lo, int ro, UnaryPlan& p)
     return TROP_OK;
 }
 
-// run a planned unary op: out (strided) and argmax (contiguous in out shape, nullable)
+// run a planned unary op: out (strided) and argmax (contiguous in out shape, nullable); a
+// split reduction keeps its partials in `fixed` when given, else in pool workspace
 int exec_unary(int sr, const UnaryPlan& p, int ro, void* out, const int64_t* ostride, int32_t* argmax,
-               cudaStream_t s)
+               cudaStream_t s, const ReduceScratch* fixed = nullptr)
 {
     int64_t osize[MAXR], astride[MAXR];
     int64_t n_out = 1;
@@ -231,7 +232,7 @@ int exec_unary(int sr, const UnaryPlan& p, int ro, void* out, const int64_t* ost
         d.red_size[i] = p.u.size[p.red_ax[i]];
         d.red_s_in[i] = p.u.stride[p.red_ax[i]];
     }
-    return launch_reduce(sr, p.u.dtype, p.u.data, out, argmax, d, s);
+    return launch_reduce(sr, p.u.dtype, p.u.data, out, argmax, d, fixed, s);
 }
 
 // ------------------------------------------------------------------ pairwise planning
@@ -631,10 +632,13 @@ using namespace trop;
 
 // ====================================================================== entry points
 
-extern "C" int tropical_permute_trace(const trop_tensor* in, const char* spec, int semiring, const trop_tensor* out,
-                                      int32_t* argmax, void* stream)
+namespace {
+
+// tropical_permute_trace and its allocation-free twin: validation and lowering are shared;
+// only where a split reduction keeps its partial results differs (no_alloc: the fixed scratch)
+int permute_trace_impl(const trop_tensor* in, const char* spec, int semiring, const trop_tensor* out,
+                       int32_t* argmax, cudaStream_t stream, bool no_alloc)
 {
-    clear_error();
     if (semiring < 0 || semiring > 2) return set_error(TROP_ERR_INVALID_ARG, "unknown semiring %d", semiring);
     int nops, ra, rb, ro;
     int32_t la[MAXR], lb[MAXR], lo[MAXR];
@@ -646,6 +650,8 @@ extern "C" int tropical_permute_trace(const trop_tensor* in, const char* spec, i
     TROP_TRY(tensor_labels_check(out, ro, "out"));
     if (in->dtype != out->dtype) return set_error(TROP_ERR_DTYPE, "in and out dtypes differ");
     TROP_TRY(ensure_device(nullptr));
+    ReduceScratch fixed{};
+    if (no_alloc) TROP_TRY(noalloc_scratch(&fixed.ptr, &fixed.bytes));
     UnaryPlan p{};
     TROP_TRY(plan_unary(view_of(in, la), lo, ro, p));
     int64_t n_out = 1;
@@ -656,7 +662,16 @@ extern "C" int tropical_permute_trace(const trop_tensor* in, const char* spec, i
         n_out *= out->shape[i];
     }
     if (argmax && n_out > 0) TROP_TRY(check_device_pointer(argmax, "argmax"));
-    return exec_unary(semiring, p, ro, out->data, out->stride, argmax, (cudaStream_t)stream);
+    return exec_unary(semiring, p, ro, out->data, out->stride, argmax, stream, no_alloc ? &fixed : nullptr);
+}
+
+}  // namespace
+
+extern "C" int tropical_permute_trace(const trop_tensor* in, const char* spec, int semiring, const trop_tensor* out,
+                                      int32_t* argmax, void* stream)
+{
+    clear_error();
+    return permute_trace_impl(in, spec, semiring, out, argmax, (cudaStream_t)stream, false);
 }
 
 // Allocation-free twin of tropical_permute_trace for callers that must not
@@ -666,53 +681,7 @@ extern "C" int tropical_permute_trace_noalloc(const trop_tensor* in, const char*
                                               const trop_tensor* out, int32_t* argmax, void* stream)
 {
     clear_error();
-    if (semiring < 0 || semiring > 2) return set_error(TROP_ERR_INVALID_ARG, "unknown semiring %d", semiring);
-    int nops, ra, rb, ro;
-    int32_t la[MAXR], lb[MAXR], lo[MAXR];
-    TROP_TRY(parse_spec(spec, nops, la, ra, lb, rb, lo, ro));
-    if (nops != 1) return set_error(TROP_ERR_SPEC, "permute/trace takes one operand");
-    TROP_TRY(check_tensor(in, "in", true));
-    TROP_TRY(check_tensor(out, "out", true));
-    TROP_TRY(tensor_labels_check(in, ra, "in"));
-    TROP_TRY(tensor_labels_check(out, ro, "out"));
-    if (in->dtype != out->dtype) return set_error(TROP_ERR_DTYPE, "in and out dtypes differ");
-    TROP_TRY(ensure_device(nullptr));
-    void* scratch = nullptr;
-    size_t scratch_bytes = 0;
-    TROP_TRY(noalloc_scratch(&scratch, &scratch_bytes));
-    UnaryPlan p{};
-    TROP_TRY(plan_unary(view_of(in, la), lo, ro, p));
-    int64_t osize[MAXR], astride[MAXR], n_out = 1;
-    for (int i = 0; i < ro; ++i) {
-        if (out->shape[i] != p.u.size[p.out_ax[i]])
-            return set_error(TROP_ERR_SHAPE, "out extent %d is %lld, spec implies %lld", i, (long long)out->shape[i],
-                             (long long)p.u.size[p.out_ax[i]]);
-        osize[i] = out->shape[i];
-        n_out *= out->shape[i];
-    }
-    if (argmax && n_out > 0) TROP_TRY(check_device_pointer(argmax, "argmax"));
-    if (p.n_red == 0 || n_out == 0)  // permutes and empty outputs use no workspace on the shared path
-        return exec_unary(semiring, p, ro, out->data, out->stride, argmax, (cudaStream_t)stream);
-    int64_t R = 1;
-    for (int i = 0; i < p.n_red; ++i) R *= p.u.size[p.red_ax[i]];
-    if (argmax && R - 1 > INT32_MAX)
-        return set_error(TROP_ERR_OVERFLOW, "reduced extent %lld does not fit an int32 argmax", (long long)R);
-    contiguous_strides(ro, osize, astride);
-    ReduceDesc d{};
-    d.out_rank = ro;
-    for (int i = 0; i < ro; ++i) {
-        d.out_size[i] = osize[i];
-        d.out_s_in[i] = p.u.stride[p.out_ax[i]];
-        d.out_s_out[i] = out->stride[i];
-        d.out_s_arg[i] = astride[i];
-    }
-    d.red_rank = p.n_red;
-    for (int i = 0; i < p.n_red; ++i) {
-        d.red_size[i] = p.u.size[p.red_ax[i]];
-        d.red_s_in[i] = p.u.stride[p.red_ax[i]];
-    }
-    return launch_reduce_scratch(semiring, p.u.dtype, p.u.data, out->data, argmax, d, scratch, scratch_bytes,
-                                 (cudaStream_t)stream);
+    return permute_trace_impl(in, spec, semiring, out, argmax, (cudaStream_t)stream, true);
 }
 
 extern "C" int tropical_permute_pair(const trop_tensor* val_in, const trop_tensor* arg_in, const char* spec,

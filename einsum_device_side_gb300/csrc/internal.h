@@ -146,11 +146,15 @@ struct ReduceDesc {
     int64_t red_size[MAXR];
     int64_t red_s_in[MAXR];
 };
+// Where a split reduction keeps its partial results when `fixed` is given: a caller-provided
+// block of `bytes` (the request fails with TROP_ERR_UNSUPPORTED when they do not fit); nothing
+// is allocated.  Without it they go to pool workspace.
+struct ReduceScratch {
+    void* ptr;
+    size_t bytes;
+};
 int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* argmax,
-                  const ReduceDesc& d, cudaStream_t s);
-// The same reduction with its split partials in caller-provided scratch (no allocation).
-int launch_reduce_scratch(int semiring, int dtype, const void* in, void* out, int32_t* argmax,
-                          const ReduceDesc& d, void* scratch, size_t scratch_bytes, cudaStream_t s);
+                  const ReduceDesc& d, const ReduceScratch* fixed, cudaStream_t s);
 // Fixed scratch of noalloc.cu: its device address on the current device (looked up once per device).
 int noalloc_scratch(void** ptr, size_t* bytes);
 

@@ -11,7 +11,9 @@
 // The array lives in the module for as long as the library is loaded, on
 // every GPU that loads it.  Its name is only a host-side stand-in in host
 // code: kernels must be given the device address that cudaGetSymbolAddress
-// returns, looked up here once per device with that device current.
+// returns, looked up here once per device with that device current and kept
+// for the life of the process (like the rest of the library's per-device
+// state, it does not survive a cudaDeviceReset).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -20,7 +22,9 @@
 
 namespace trop {
 
-constexpr size_t NOALLOC_SCRATCH_BYTES = 256 * 1024;  // 16384 partial results of 16 bytes
+// 256 KiB: 21845 partial results of f32/i32 (12 bytes each) or 16384 of f64/i64 (16 bytes);
+// a split reduction makes fewer than 16 x (SM count) of them
+constexpr size_t NOALLOC_SCRATCH_BYTES = 256 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 

@@ -11,10 +11,14 @@
 // stay adjacent:
 //   * k_copy_rows   the output's fastest axis is also the input's: rows are
 //                   copied with 16-byte vectors;
-//   * k_transpose   the fastest axes differ: 64x64 (32x32 for 8-byte types)
-//                   tiles are staged through padded shared memory so both the
-//                   reads and the writes are coalesced (the tiled, padded
-//                   transpose the issue names as the later ~2.6x step);
+//   * k_transpose   the fastest axes differ: a tile of 4096 elements (2048
+//                   for 8-byte types) spanning the input-fastest axis chain x
+//                   the output-fastest chain, its shape fitted to short
+//                   chains (16x256 for a 16^6 tensor), is staged transposed
+//                   through shared memory whose rows are XOR-swizzled, so the
+//                   reads and the 16-byte vector writes are both coalesced and
+//                   free of bank conflicts (the tiled transpose the issue
+//                   names as the later ~2.6x step);
 //   * k_gather      anything else: one thread per output element, decoding
 //                   its index against the shape (the GPUArrays.jl scheme the
 //                   issue describes as the first cut).
@@ -784,8 +788,8 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
 }
 
 template <int SR, typename T>
-int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceDesc& d, cudaStream_t s,
-                        const DeviceInfo* dev)
+int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceDesc& d, const ReduceScratch* fixed,
+                        cudaStream_t s, const DeviceInfo* dev)
 {
     const T* in = static_cast<const T*>(in_);
     T* out = static_cast<T*>(out_);
@@ -850,9 +854,20 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
     int64_t* part_i = nullptr;
     void* ws = nullptr;
     if (nsplit > 1) {
+        // the partial results: pool workspace, or the caller's fixed block (never allocated)
         const size_t nb = (size_t)(p.n_out * nsplit);
-        TROP_TRY(pool_alloc(nb * (sizeof(T) + sizeof(int64_t)), s, &ws));
-        part_i = static_cast<int64_t*>(ws);
+        const size_t need = nb * (sizeof(T) + sizeof(int64_t));
+        if (fixed) {
+            if (!fixed->ptr || need > fixed->bytes)
+                return set_error(TROP_ERR_UNSUPPORTED,
+                                 "reduction needs %zu bytes of scratch for %lld partial results; the fixed scratch "
+                                 "holds %zu bytes",
+                                 need, (long long)nb, fixed->bytes);
+            part_i = static_cast<int64_t*>(fixed->ptr);
+        } else {
+            TROP_TRY(pool_alloc(need, s, &ws));
+            part_i = static_cast<int64_t*>(ws);
+        }
         part_v = reinterpret_cast<T*>(part_i + nb);
     }
     int g = grid_for(p.n_out * nsplit, 1, dev->sm_count, 16);
@@ -864,94 +879,6 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
         rc = check_launch("k_reduce_combine");
     }
     if (ws) pool_retire(ws, s);
-    return rc;
-}
-
-// Same reduction as launch_reduce_typed, but the partial results of a split
-// reduction go to caller-provided scratch instead of pool workspace; fails
-// when they would not fit.  Nothing is allocated.
-template <int SR, typename T>
-int launch_reduce_scratch_typed(const void* in_, void* out_, int32_t* arg, const ReduceDesc& d, void* scratch,
-                                size_t scratch_bytes, cudaStream_t s, const DeviceInfo* dev)
-{
-    const T* in = static_cast<const T*>(in_);
-    T* out = static_cast<T*>(out_);
-    RedParams p{};
-    p.n_out = 1;
-    p.out_rank = 0;
-    for (int i = 0; i < d.out_rank; ++i) {
-        if (d.out_size[i] == 0) return TROP_OK;
-        if (d.out_size[i] == 1) continue;
-        int k = p.out_rank++;
-        p.out_size[k] = d.out_size[i];
-        p.out_s_in[k] = d.out_s_in[i];
-        p.out_s_out[k] = d.out_s_out[i];
-        p.out_s_arg[k] = d.out_s_arg[i];
-        p.n_out *= d.out_size[i];
-    }
-    p.R = 1;
-    p.red_rank = 0;
-    for (int i = 0; i < d.red_rank; ++i) {
-        p.R *= d.red_size[i];
-        if (d.red_size[i] == 1) continue;
-        int q = p.red_rank - 1;
-        if (q >= 0 && p.red_s_in[q] == d.red_s_in[i] * d.red_size[i]) {
-            p.red_size[q] *= d.red_size[i];
-            p.red_s_in[q] = d.red_s_in[i];
-            continue;
-        }
-        p.red_size[p.red_rank] = d.red_size[i];
-        p.red_s_in[p.red_rank] = d.red_s_in[i];
-        ++p.red_rank;
-    }
-    if (p.red_rank == 0) {
-        p.red_rank = 1;
-        p.red_size[0] = 1;
-        p.red_s_in[0] = 0;
-    }
-    const int64_t threads_wanted = (int64_t)dev->sm_count * 1024;
-    if (p.R <= 64 || p.n_out >= threads_wanted) {
-        int g = grid_for(p.n_out, NT, dev->sm_count);
-        (void)launch_pdl(k_reduce_thread<SR, T>, g, NT, 0, s, in, out, arg, p);
-        return check_launch("k_reduce_thread");
-    }
-    if (p.out_rank >= 1 && p.out_s_in[p.out_rank - 1] == 1 && p.R <= (int64_t(1) << 24)) {
-        // outputs contiguous in the input: coalesced slices, no workspace
-        const int64_t inner = p.out_size[p.out_rank - 1];
-        const int64_t groups = p.n_out / inner * ((inner + 31) / 32);
-        const int g = (int)std::min<int64_t>(std::max<int64_t>(groups, 1), (int64_t)dev->sm_count * 16);
-        if (p.R >= 64) (void)launch_pdl(k_reduce_tile<SR, T, 32>, g, 32 * 32, 0, s, in, out, arg, p);
-        else (void)launch_pdl(k_reduce_tile<SR, T, 8>, g, 32 * 8, 0, s, in, out, arg, p);
-        return check_launch("k_reduce_tile");
-    }
-    const int64_t blocks_wanted = (int64_t)dev->sm_count * 8;
-    int64_t nsplit = (blocks_wanted + p.n_out - 1) / p.n_out;
-    int64_t max_split = (p.R + 2047) / 2048;
-    if (nsplit > max_split) nsplit = max_split;
-    if (nsplit < 1) nsplit = 1;
-    p.nsplit = nsplit;
-    p.chunk = (p.R + nsplit - 1) / nsplit;
-    T* part_v = nullptr;
-    int64_t* part_i = nullptr;
-    if (nsplit > 1) {
-        const size_t nb = (size_t)(p.n_out * nsplit);
-        const size_t need = nb * (sizeof(T) + sizeof(int64_t));
-        if (!scratch || need > scratch_bytes)
-            return set_error(TROP_ERR_UNSUPPORTED,
-                             "reduction needs %zu bytes of scratch for %lld partial results; the fixed scratch "
-                             "holds %zu bytes",
-                             need, (long long)nb, scratch_bytes);
-        part_i = static_cast<int64_t*>(scratch);
-        part_v = reinterpret_cast<T*>(part_i + nb);
-    }
-    int g = grid_for(p.n_out * nsplit, 1, dev->sm_count, 16);
-    (void)launch_pdl(k_reduce_block<SR, T>, g, NT, 0, s, in, out, arg, part_v, part_i, p);
-    int rc = check_launch("k_reduce_block");
-    if (rc == TROP_OK && nsplit > 1) {
-        int g2 = grid_for(p.n_out, NT, dev->sm_count);
-        (void)launch_pdl(k_reduce_combine<SR, T>, g2, NT, 0, s, out, arg, part_v, part_i, p);
-        rc = check_launch("k_reduce_combine");
-    }
     return rc;
 }
 
@@ -968,16 +895,16 @@ int launch_gather(const void* in, void* out, int elem_bytes, const int32_t* in2,
 }
 
 int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* argmax, const ReduceDesc& d,
-                  cudaStream_t s)
+                  const ReduceScratch* fixed, cudaStream_t s)
 {
     const DeviceInfo* dev = nullptr;
     TROP_TRY(ensure_device(&dev));
-#define TROP_RED(SR)                                                                         \
-    case SR:                                                                                 \
-        if (dtype == TROP_F32) return launch_reduce_typed<SR, float>(in, out, argmax, d, s, dev);   \
-        if (dtype == TROP_I32) return launch_reduce_typed<SR, int32_t>(in, out, argmax, d, s, dev); \
-        if (dtype == TROP_I64) return launch_reduce_typed<SR, int64_t>(in, out, argmax, d, s, dev); \
-        if (dtype == TROP_F64) return launch_reduce_typed<SR, double>(in, out, argmax, d, s, dev);  \
+#define TROP_RED(SR)                                                                                 \
+    case SR:                                                                                         \
+        if (dtype == TROP_F32) return launch_reduce_typed<SR, float>(in, out, argmax, d, fixed, s, dev);   \
+        if (dtype == TROP_I32) return launch_reduce_typed<SR, int32_t>(in, out, argmax, d, fixed, s, dev); \
+        if (dtype == TROP_I64) return launch_reduce_typed<SR, int64_t>(in, out, argmax, d, fixed, s, dev); \
+        if (dtype == TROP_F64) return launch_reduce_typed<SR, double>(in, out, argmax, d, fixed, s, dev);  \
         break;
     switch (semiring) {
         TROP_RED(TROP_MAXPLUS)
@@ -986,32 +913,6 @@ int launch_reduce(int semiring, int dtype, const void* in, void* out, int32_t* a
     default: break;
     }
 #undef TROP_RED
-    return set_error(TROP_ERR_DTYPE, "reduce: unsupported semiring %d / dtype %d", semiring, dtype);
-}
-
-int launch_reduce_scratch(int semiring, int dtype, const void* in, void* out, int32_t* argmax, const ReduceDesc& d,
-                          void* scratch, size_t scratch_bytes, cudaStream_t s)
-{
-    const DeviceInfo* dev = nullptr;
-    TROP_TRY(ensure_device(&dev));
-#define TROP_RED_S(SR)                                                                                          \
-    case SR:                                                                                                    \
-        if (dtype == TROP_F32)                                                                                  \
-            return launch_reduce_scratch_typed<SR, float>(in, out, argmax, d, scratch, scratch_bytes, s, dev);   \
-        if (dtype == TROP_I32)                                                                                  \
-            return launch_reduce_scratch_typed<SR, int32_t>(in, out, argmax, d, scratch, scratch_bytes, s, dev); \
-        if (dtype == TROP_I64)                                                                                  \
-            return launch_reduce_scratch_typed<SR, int64_t>(in, out, argmax, d, scratch, scratch_bytes, s, dev); \
-        if (dtype == TROP_F64)                                                                                  \
-            return launch_reduce_scratch_typed<SR, double>(in, out, argmax, d, scratch, scratch_bytes, s, dev);  \
-        break;
-    switch (semiring) {
-        TROP_RED_S(TROP_MAXPLUS)
-        TROP_RED_S(TROP_MINPLUS)
-        TROP_RED_S(TROP_MAXTIMES)
-    default: break;
-    }
-#undef TROP_RED_S
     return set_error(TROP_ERR_DTYPE, "reduce: unsupported semiring %d / dtype %d", semiring, dtype);
 }
 

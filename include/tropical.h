@@ -164,14 +164,21 @@ int tropical_permute_trace(const trop_tensor* in, const char* spec, int semiring
  * Same arguments, results and errors as tropical_permute_trace.  A split
  * reduction keeps its partial results in one fixed 256 KiB device array
  * compiled into the library (resident on every GPU that loads it) instead of
- * pool workspace; no call allocates or frees memory.  Requests whose
- * partials need more than 256 KiB fail with TROP_ERR_UNSUPPORTED.
+ * pool workspace; no call allocates or frees memory.  A partial result takes
+ * 8 bytes of index plus one element (12 bytes for f32/i32, 16 for f64/i64),
+ * and a reduction splits into fewer than 16 x (SM count) partials, so on a
+ * 152-SM GB300 a call needs at most about 39 KB of the array.  Requests
+ * whose partials would need more than 256 KiB (only possible on GPUs with
+ * more than about 1000 SMs) fail with TROP_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array: calls whose kernels overlap on
- * the GPU (other streams, other host threads) race on it, so serialise them.
- * Nothing in it needs to start at zero: each call writes every partial it
- * reads. */
+ * capture.  The address is kept for the life of the process: after
+ * cudaDeviceReset the library's per-device state (this address and the
+ * workspace pool) is stale, so do not call the library on a device that was
+ * reset in the same process.  Every call shares the one array: calls whose
+ * kernels overlap on the GPU (other streams, other host threads) race on it,
+ * so serialise them.  Nothing in it needs to start at zero: each call writes
+ * every partial it reads. */
 int tropical_permute_trace_noalloc(const trop_tensor* in, const char* spec, int semiring,
                                    const trop_tensor* out, int32_t* argmax, void* stream);
 
@@ -312,8 +319,9 @@ int tropical_tree_plan_destroy(trop_tree_plan plan);
  * configuration, for l in [0, n_labels); labels whose value no argmax
  * determines (one-operand labels reduced inside a binary node, or nodes
  * whose argmax buffer is NULL) are -1.  assignment: int32 device buffer of
- * n_labels entries.  One device thread walks the nodes backwards; nothing
- * is copied to the host. */
+ * n_labels entries.  One warp walks the nodes backwards, with the node,
+ * label and extent tables in shared memory when they fit (one thread over
+ * global memory otherwise); nothing is copied to the host. */
 int tropical_tree_backtrack(int n_inputs, const trop_tensor* inputs, int n_nodes,
                             const trop_node* nodes, int32_t* const* node_argmax,
                             int64_t root_index, int n_labels, int32_t* assignment, void* stream);

@@ -119,46 +119,36 @@ def test_identity_and_infinities(trop):
 
 
 @pytest.mark.parametrize("sr", SR)
-def test_full_size_batched_workload_sampled(trop, sr):
-    """batch 64 x 256^3 exactly as benchmarked: sampled outputs vs the oracle,
-    and an every-output certificate (A[m,I] (x) B[I,n] == C)."""
+def test_full_size_batched_workload(trop, sr):
+    """batch 64 x 256^3 exactly as benchmarked: every output's value and argmax
+    bitwise against the oracle (4,194,304 outputs per semiring), plus the argmax
+    certificate A[m,I] (x) B[I,n] == C on the device."""
     a, b = synth.gemm_batched_inputs(sr)
     ad, bd = _dev(a), _dev(b)
     c, i = trop.gemm(ad, bd, sr)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(100 + sr)
-    samples = rng.choice(c.numel(), size=20000, replace=False).astype(np.int64)
-    samples[:3] = [0, c.numel() - 1, 12345]
-    rc, ri = oracle.gemm(a, b, sr, samples=samples, nthreads=0)
-    cf, if_ = c.reshape(-1).cpu().numpy(), i.reshape(-1).cpu().numpy()
-    np.testing.assert_array_equal(cf[samples], rc)
-    np.testing.assert_array_equal(if_[samples], ri)
-    # certificate on every output (torch float32 add/mul round once as well)
+    rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == rc.tobytes(), "values differ from the oracle"
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
     idx = i.long()
     a_sel = torch.gather(ad, 2, idx)                                 # A[b, m, I[b,m,n]]
     b_sel = torch.gather(bd, 1, idx)                                 # B[b, I[b,m,n], n]
     t = a_sel * b_sel if sr == 2 else a_sel + b_sel
     assert torch.equal(t, c)
-    assert (i >= 0).all() and (i < 256).all()
 
 
 # ---------------------------------------------------------------- split tiles (stream-K) and the resolve pass
 
 @pytest.mark.parametrize("sr", SR)
 @pytest.mark.parametrize("batch", [64, 128])
-def test_split_tail_plain_full_size_sampled(trop, sr, batch):
+def test_split_tail_plain_full_size(trop, sr, batch):
     """Batched 256^3 without argmax: the last partial wave is cut along k and the
-    segments merged by the last CTA to finish; sampled outputs vs the oracle."""
+    segments merged by the last CTA to finish; every output vs the oracle."""
     a, b = synth.gemm_batched_inputs(sr, batch=batch)
     c = trop.gemm(_dev(a), _dev(b), sr, argmax=False)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(200 + sr + batch)
-    samples = rng.choice(c.numel(), size=20000, replace=False).astype(np.int64)
-    # the last tiles are the split ones: sample all of the final 64x64 tile too
-    tail = (c.numel() - 1 - np.arange(64)[:, None] * 256 - np.arange(64)[None, :]).reshape(-1)
-    samples = np.unique(np.concatenate([samples, tail]))
-    rc, _ = oracle.gemm(a, b, sr, samples=samples, nthreads=0)
-    assert c.reshape(-1).cpu().numpy()[samples].tobytes() == rc.tobytes()
+    rc, _ = oracle.gemm(a, b, sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == rc.tobytes()
 
 
 @pytest.mark.parametrize("sr", SR)
@@ -216,23 +206,17 @@ def test_split_gemms_on_two_streams(trop):
 
 
 @pytest.mark.parametrize("sr", SR)
-def test_whole_tiles_long_contraction_sampled(trop, sr):
+def test_whole_tiles_long_contraction(trop, sr):
     """Enough whole tiles that none is split, with K > 4096 (too many k-tiles to
     resolve the argmax inside the tile): chunk codes go through the separate
-    resolve pass.  Sampled outputs vs the oracle, plus a certificate on all."""
+    resolve pass.  Every output's value and argmax vs the oracle."""
     a, b = synth.gemm_batched_inputs(sr, batch=60, m=128, n=128, k=4200)
     ad, bd = _dev(a), _dev(b)
     c, i = trop.gemm(ad, bd, sr)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(300 + sr)
-    samples = rng.choice(c.numel(), size=4000, replace=False).astype(np.int64)
-    rc, ri = oracle.gemm(a, b, sr, samples=samples, nthreads=0)
-    np.testing.assert_array_equal(c.reshape(-1).cpu().numpy()[samples], rc)
-    np.testing.assert_array_equal(i.reshape(-1).cpu().numpy()[samples], ri)
-    idx = i.long()
-    t = torch.gather(ad, 2, idx) * torch.gather(bd, 1, idx) if sr == 2 else \
-        torch.gather(ad, 2, idx) + torch.gather(bd, 1, idx)
-    assert torch.equal(t, c)
+    rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == rc.tobytes()
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
 
 
 def test_argmax_gemm_streams_and_graph_replay(trop):
