@@ -107,6 +107,7 @@ def load(path: str | None = None):
         "tropical_debug_fail_next_event_records": (None, [I]),
         "tropical_set_pool_capacity": (None, [I]),
         "tropical_device_wait_timeouts": (I, [ctypes.POINTER(ctypes.c_uint), I]),
+        "tropical_debug_set_wait_mode": (None, [I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -514,6 +515,12 @@ def device_wait_timeouts(reset: bool = False) -> int:
     n = ctypes.c_uint(0)
     _check(load().tropical_device_wait_timeouts(ctypes.byref(n), int(bool(reset))))
     return n.value
+
+
+def debug_set_wait_mode(mode: int):
+    """Test hook: 1 = the TMA-fed GEMM's first operand wait gives up (then recovers), 2 = it
+    then fails after its copies landed (the next call reports the error), 0 = normal."""
+    load().tropical_debug_set_wait_mode(int(mode))
 
 
 def set_pool_capacity(n: int):

@@ -681,6 +681,7 @@ extern "C" int tropical_permute_trace_noalloc(const trop_tensor* in, const char*
                                               const trop_tensor* out, int32_t* argmax, void* stream)
 {
     clear_error();
+    NoAllocScope no_alloc;  // every launcher below allocates nothing on this thread
     return permute_trace_impl(in, spec, semiring, out, argmax, (cudaStream_t)stream, true);
 }
 

@@ -164,6 +164,10 @@ struct TiledParams {
     uint32_t r_rem;
     int r32;
     FastDiv div_M, div_npan;
+    // TMA-fed kernel only: where a wait that could not be completed is reported (a word in
+    // host-mapped memory, read by the library's next call) and the test mode of its waits
+    uint32_t* err;
+    int wait_mode;
 };
 
 __device__ __forceinline__ void tile_coord(const TiledParams& p, uint32_t t, uint32_t& b, int& m0, int& n0)
@@ -604,7 +608,7 @@ struct TmaMaps {
     CUtensorMap b;  // B as [batch][K][N] (N fastest), box [1][BK][BN]
 };
 
-// bounded waits on this device that gave up (a copy that never landed); stays 0
+// bounded waits on this device that gave up once (each then waited again with the full bound)
 __device__ unsigned int g_wait_timeouts;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) { return (uint32_t)__cvta_generic_to_shared(ptr); }
@@ -641,6 +645,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
         if (global_ns() - t0 > 200000000ull) return false;
     return true;
 }
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar)
 {
     asm volatile(
@@ -658,9 +663,9 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
     static_assert(BK % 4 == 0 && CH % 4 == 0 && (BK / CH) % 2 == 0, "k quads, an even number of chunks per k-tile");
     __shared__ __align__(128) float As[TMA_STAGES][BM][BK];
     __shared__ __align__(128) float Bs[TMA_STAGES][BK][BN];
-    __shared__ __align__(8) uint64_t full[TMA_STAGES];
+    __shared__ __align__(8) uint64_t full[TMA_STAGES];  // operand boxes of a stage landed
     __shared__ uint16_t sid[TM * TN][THREADS];
-    __shared__ int s_fail;
+    __shared__ int s_fail, s_gaveup;
 
     const int tid = threadIdx.x;
     const int tm = tid / (BN / TN), tn = tid % (BN / TN);
@@ -673,6 +678,7 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
         for (int s = 0; s < TMA_STAGES; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_fail = 0;
+        s_gaveup = 0;
     }
     __syncthreads();
     // Launched as a programmatic dependent of whatever precedes it on the stream: nothing in
@@ -686,8 +692,9 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
         tma_load_3d(&As[s][0][0], &maps.a, kt * BK, m0, (int)b, &full[s]);
         tma_load_3d(&Bs[s][0][0], &maps.b, n0, kt * BK, (int)b, &full[s]);
     };
+    int issued = 0;  // k-tiles whose copies thread 0 has issued
     if (tid == 0)
-        for (int kt = 0; kt < min(nkt, TMA_STAGES); ++kt) issue(kt);
+        for (; issued < min(nkt, TMA_STAGES); ++issued) issue(issued);
 
     float best[TM][TN], snap[TM][TN];  // two accumulator sets, roles swapped every chunk
 #pragma unroll
@@ -697,7 +704,16 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
 
     for (int kt = 0; kt < nkt; ++kt) {
         const int s = kt % TMA_STAGES;
-        if (!mbar_wait(&full[s], (uint32_t)(kt / TMA_STAGES) & 1u)) s_fail = 1;
+        const uint32_t ph = (uint32_t)(kt / TMA_STAGES) & 1u;
+        // A wait that gives up is counted and waited once more with the full bound, so a copy
+        // that lands late still gives exact results; if it has not landed then either, the
+        // tile's results are abandoned and the failure reported (below).  Test modes 1 and 2
+        // make the first wait give up at once; mode 2 then treats the second one as failed
+        // after it completed, so nothing is in flight when the failure path runs.
+        if (!((p.wait_mode == 0 || kt != 0) && mbar_wait(&full[s], ph))) {
+            s_gaveup = 1;
+            if (!mbar_wait(&full[s], ph) || p.wait_mode == 2) s_fail = 1;
+        }
 #pragma unroll
         for (int kq = 0; kq < BK; kq += 4) {
             // chunk parity and the first quad of a chunk are known at compile time (BK / CH even)
@@ -738,22 +754,37 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
                         if (O::better(dst_[i][jj], src_[i][jj])) sid[i * TN + jj][tid] = chunk;
             }
         }
-        __syncthreads();  // every thread is done with stage s
-        if (s_fail) {
-            // a copy did not land in time: wait (bounded) for the copies still in flight, store nothing
-            if (tid == 0) {
-                atomicAdd(&g_wait_timeouts, 1u);
-                for (int k2 = kt; k2 < min(nkt, kt + TMA_STAGES); ++k2)
-                    mbar_wait(&full[k2 % TMA_STAGES], (uint32_t)(k2 / TMA_STAGES) & 1u);
-            }
-            return;
+        __syncthreads();  // every thread is done with stage s (and sees the same s_fail)
+        if (s_fail) break;
+        if (tid == 0 && issued < nkt) issue(issued++);
+    }
+    int64_t oa, ob, oc, oi;
+    batch_offsets(p.bt, b, oa, ob, oc, oi);
+    if (tid == 0 && s_gaveup) atomicAdd(&g_wait_timeouts, 1u);
+    if (s_fail) {
+        // Abandon the tile: wait (bounded) for every copy still in flight into this CTA's
+        // shared memory, mark its outputs "nothing to resolve" so the resolve pass reads no
+        // stale chunk codes, and report the failure in the host-mapped error word.
+        if (tid == 0)
+            for (int k2 = max(0, issued - TMA_STAGES); k2 < issued; ++k2)
+                (void)mbar_wait(&full[k2 % TMA_STAGES], (uint32_t)(k2 / TMA_STAGES) & 1u);
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int m = m0 + row_of(tm, i);
+            if (m >= p.M) continue;
+            int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (n0 + tn * 4 + q < p.N) irow[(int64_t)(n0 + tn * 4 + q) * p.sIn] = 0;
         }
-        if (tid == 0 && kt + TMA_STAGES < nkt) issue(kt + TMA_STAGES);
+        if (tid == 0 && p.err) {
+            *(volatile uint32_t*)p.err = 1u;
+            __threadfence_system();
+        }
+        return;
     }
 
     // ---------------- store values and -(chunk + 1) (0: nothing beat the zero) through the strides
-    int64_t oa, ob, oc, oi;
-    batch_offsets(p.bt, b, oa, ob, oc, oi);
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int m = m0 + row_of(tm, i);
@@ -826,6 +857,7 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
     using O = Ops<SR>;
     using S = PanelShape<PW>;
     constexpr int NCOL = S::NCOL, RSUB = S::RSUB, RRP = S::RRP, ROWS = S::ROWS;
+    const int nchunks = p.K / CH;  // whole chunks on this path
     const int cl = PW >= 32 ? lane : lane % PW;  // column (of the first column group)
     const int rs = PW >= 32 ? 0 : lane / PW;     // row within a row slot
     bool colok[NCOL];
@@ -860,8 +892,11 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
 #pragma unroll
             for (int h = 0; h < NCOL; ++h) {
                 val[r][h] = nval[r][h];
-                const int kc = (-ncode[r][h] - 1) * CH;
-                live[r][h] = ncode[r][h] < 0 && kc >= k0 && kc < k0 + kn;
+                // a code is live when it names a chunk of this staged group (a code outside
+                // the contraction is never followed, whatever the buffer held)
+                const int ch = ncode[r][h] < 0 ? -(ncode[r][h] + 1) : INT_MAX;
+                const int kc = ch < nchunks ? ch * CH : -1;
+                live[r][h] = kc >= k0 && kc < k0 + kn;
                 ka[r][h] = live[r][h] ? kc : k0;
             }
         if (ms + RWARPS * ROWS < me) load_step(ms + RWARPS * ROWS);
@@ -917,6 +952,7 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
     uint64_t ubeg, uend;
     resolve_range(p, ubeg, uend);
     const int ngr = (p.K + GK - 1) / GK;
+    const int nchunks = (p.K + CH - 1) / CH;
     const uint32_t npan = (uint32_t)((p.N + PW - 1) / PW);  // panels per batch
     // common layout: unit column strides, whole chunks, 16-byte aligned A segments
     const bool fast = p.vecA && p.K % CH == 0 && p.sCn == 1 && p.sIn == 1;
@@ -996,8 +1032,10 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         val[r][h] = nval[r][h];
-                        const int kc = (-ncode[r][h] - 1) * CH;  // ncode < 0: chunk -ncode-1
-                        ka[r][h] = (ncode[r][h] < 0 && kc >= k0 && kc < k0 + kn) ? kc : -1;
+                        // ncode < 0: chunk -ncode-1 (never followed outside the contraction)
+                        const int ch = ncode[r][h] < 0 ? -(ncode[r][h] + 1) : INT_MAX;
+                        const int kc = ch < nchunks ? ch * CH : -1;
+                        ka[r][h] = (kc >= k0 && kc < k0 + kn) ? kc : -1;
                     }
                 if (ms + RWARPS * RR < me) load_step(ms + RWARPS * RR);
                 float av[RR][2][CH];
@@ -1061,6 +1099,7 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
     const uint32_t npan = (uint32_t)((p.N + BN - 1) / BN);
     // lane l holds chunk l of every row; lanes past the last chunk read the last one (unused)
     const int achunk = min(lane, p.K / CH - 1);
+    const int nchunks = p.K / CH;
     const int sA = p.sAm32, sC = p.sCm32, sI = p.sIm32;
     bool waited = false;
     for (uint64_t u = ubeg; u < uend;) {
@@ -1139,7 +1178,7 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 // code -(c + 1): chunk c pending; 0: final (nothing beat the zero)
-                const bool live = s.ok[h] && s.c[h] < 0;
+                const bool live = s.ok[h] && s.c[h] < 0 && ~s.c[h] < nchunks;
                 const int c = live ? ~s.c[h] : 0;
                 const float v = s.v[h];
                 float a[CH];
@@ -1521,6 +1560,22 @@ bool make_map(CUtensorMap* map, const float* base, uint64_t cols, uint64_t rows,
 #endif
 constexpr uint64_t SK_MAX_FILL_PCT = TROP_SK_MAX_FILL_PCT, SK_MIN_UNITS = 4, SK_MAX_SEGS = 32;
 
+// The stream-K decision for T tiles of nkt k-tiles on G resident CTAs: whether the last R
+// tiles are cut along k, and then L (k-tiles per stream-K CTA) and the number of those CTAs.
+bool sk_split(uint64_t T, uint64_t G, uint64_t nkt, bool arg, uint64_t& R, uint64_t& L, uint64_t& n_sk)
+{
+    R = T % G;
+    // With argmax the merge of a split tile sits on the tail's critical path; measured on
+    // batched 256^3 problems it paid off only when the whole problem is under half a wave.
+    const bool sk_ok = !arg || T * 2 <= G;
+    if (!(sk_ok && R > 0 && R * 100 <= G * SK_MAX_FILL_PCT && R * nkt < (uint64_t(1) << 31))) return false;
+    const uint64_t U = R * nkt;
+    // at least SK_MIN_UNITS k-tiles and at most SK_MAX_SEGS segments per tile; L <= nkt as R < G
+    L = std::max({(U + G - 1) / G, std::min<uint64_t>(SK_MIN_UNITS, nkt), (nkt + SK_MAX_SEGS - 1) / SK_MAX_SEGS});
+    n_sk = (U + L - 1) / L;
+    return n_sk > R;
+}
+
 template <int SR, bool ARG>
 int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 {
@@ -1571,19 +1626,12 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     constexpr int TN = tile_tn<ARG>(), THREADS = tile_threads<TN>();
     const uint64_t G = (uint64_t)dev->sm_count *
                        resident_ctas((const void*)k_gemm_tiled<SR, ARG, TN>, THREADS, 0, occ_gemm);
-    const uint64_t R = T % G;
+    uint64_t R = 0, L = 0, n_sk = 0;
     uint64_t G_sk = 0;
     void* ws = nullptr;
-    // With argmax the merge of a split tile sits on the tail's critical path; measured on
-    // batched 256^3 problems it paid off only when the whole problem is under half a wave.
-    const bool sk_ok = !ARG || T * 2 <= G;
-    if (sk_ok && R > 0 && R * 100 <= G * SK_MAX_FILL_PCT && R * p.nkt < (uint64_t(1) << 31)) {
+    if (sk_split(T, G, p.nkt, ARG, R, L, n_sk)) {
         const uint64_t U = R * p.nkt;
-        // at least SK_MIN_UNITS k-tiles and at most SK_MAX_SEGS segments per tile; L <= nkt as R < G
-        const uint64_t L = std::max({(U + G - 1) / G, std::min<uint64_t>(SK_MIN_UNITS, p.nkt),
-                                     (p.nkt + SK_MAX_SEGS - 1) / SK_MAX_SEGS});
-        const uint64_t n_sk = (U + L - 1) / L;
-        if (n_sk > R) {
+        {
             const size_t seg_elems = (size_t)n_sk * 2 * TILE_ELEMS;
             uint32_t* cnt = nullptr;
             if (stream_tickets(s, (size_t)R, &cnt) == TROP_OK &&
@@ -1608,6 +1656,8 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     if constexpr (ARG) {
         // whole tiles, one batch axis, whole k-tiles: operands by TMA
         if (!G_sk && tma_layout_ok(g, p.bt, nbatch)) {
+            TROP_TRY(device_error_word(&p.err));
+            p.wait_mode = wait_test_mode();
             TmaMaps maps;
             const int64_t sAb = p.bt.nb ? p.bt.sA[0] : 0, sBb = p.bt.nb ? p.bt.sB[0] : 0;
             if (make_map(&maps.a, p.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)nbatch, g.sAm, sAb, BK, BM) &&
@@ -1895,7 +1945,21 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
     const bool arg = g.I != nullptr;
     if (r == R_TILED) {
         const bool staged = g.sCn != 1 || (arg && g.sIn != 1);
-        char extra[96] = "";
+        char extra[128] = "";
+        // the last wave's stream-K split depends on the SM count: the current device's when one
+        // is visible (a host query), else a GB300's 152
+        int sms = 152, dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sms = 152;
+        }
+        uint64_t T = 1;
+        for (int d = 0; d < g.nb; ++d) T *= (uint64_t)g.bsize[d];
+        T *= (uint64_t)((g.M + BM - 1) / BM) * (uint64_t)((g.N + BN - 1) / BN);
+        const uint64_t nkt = (uint64_t)((g.K + BK - 1) / BK);
+        uint64_t R = 0, L = 0, n_sk = 0;
+        const bool split = sk_split(T, (uint64_t)sms * (arg ? TROP_ARG_MINB : TROP_PLAIN_MINB), nkt, arg, R, L, n_sk);
         if (arg) {
             // the staged product is contiguous: describe the kernels on that layout
             GemmDesc gs = g;
@@ -1907,10 +1971,11 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
             const Batch bt = make_batch(gs, nbatch);
             bool va = ((uintptr_t)gs.A % 16) == 0 && gs.sAm % 4 == 0;
             for (int d = 0; d < bt.nb; ++d) va = va && bt.sA[d] % 4 == 0;
-            snprintf(extra, sizeof(extra), " kernel=%s resolve=%s", tma_layout_ok(gs, bt, nbatch) ? "tma" : "tiled",
-                     resolve_kind(gs, va));
+            snprintf(extra, sizeof(extra), " kernel=%s resolve=%s",
+                     !split && tma_layout_ok(gs, bt, nbatch) ? "tma" : "tiled", resolve_kind(gs, va));
         }
-        snprintf(buf, n, " route=tiled%s%s%s", swap ? " swap" : "", staged ? " staged" : "", extra);
+        snprintf(buf, n, " route=tiled%s%s%s%s", swap ? " swap" : "", staged ? " staged" : "",
+                 split ? " split_tail" : "", extra);
     }
     else if (r == R_STREAM)
         snprintf(buf, n, " route=stream%s vec=%d", swap ? " swap" : "", stream_vec(g, arg) ? 4 : 1);

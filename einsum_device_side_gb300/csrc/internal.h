@@ -34,10 +34,21 @@ struct DeviceInfo {
     size_t smem_per_sm;
     size_t l2_bytes;
 };
-// Set up the current device once; fills *info.
+// Set up the current device once; fills *info.  Also reports (once) an error word set by a
+// kernel that abandoned its work, allocating that word on the device's first call unless a
+// NoAllocScope is active on the calling thread (the allocation-free entry point).
 int ensure_device(const DeviceInfo** info);
+struct NoAllocScope {
+    NoAllocScope();
+    ~NoAllocScope();
+};
 // Validate a device pointer for the current device (nbytes > 0 only).
 int check_device_pointer(const void* p, const char* name);
+// Device address of the current device's error word (host-mapped; allocated on first use).
+// A kernel that abandons its work sets it; ensure_device reports and clears it.
+int device_error_word(uint32_t** dev_ptr);
+// Test mode of the TMA-fed GEMM's bounded waits (tropical_debug_set_wait_mode): 0 normal.
+int wait_test_mode();
 
 // ---------------------------------------------------------------- counters
 void count_launches(int64_t n);

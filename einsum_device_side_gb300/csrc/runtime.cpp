@@ -106,6 +106,56 @@ FastDiv make_fastdiv(uint32_t d)
     return f;
 }
 
+// ------------------------------------------------------------------ device error word
+// One word per device in pinned host memory that kernels can write (device-mapped): set by a
+// kernel that had to abandon its work -- the TMA-fed GEMM when an operand copy did not land
+// within twice its bounded wait.  Allocated by the first call on the device that may
+// allocate (the allocation-free entry point never does), read without any synchronisation at
+// the start of every later call and reported once, then cleared.
+static std::mutex g_err_mu;
+static volatile uint32_t* g_err_host[64];
+static uint32_t* g_err_dev[64];
+static std::atomic<int> g_wait_mode{0};
+
+int device_error_word(uint32_t** dev_ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return set_error(TROP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_dev[dev]) {
+        void* h = nullptr;
+        e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
+        if (e != cudaSuccess) return cuda_error(e, "cudaHostAlloc (device error word)");
+        std::memset(h, 0, 64);
+        void* d = nullptr;
+        e = cudaHostGetDevicePointer(&d, h, 0);
+        if (e != cudaSuccess) {
+            cudaFreeHost(h);
+            return cuda_error(e, "cudaHostGetDevicePointer (device error word)");
+        }
+        g_err_host[dev] = static_cast<volatile uint32_t*>(h);
+        g_err_dev[dev] = static_cast<uint32_t*>(d);
+    }
+    *dev_ptr = g_err_dev[dev];
+    return TROP_OK;
+}
+
+// nonzero error word of `dev`: clear it and return the error to report
+static int take_device_error(int dev)
+{
+    volatile uint32_t* w = g_err_host[dev];
+    if (!w || *w == 0) return TROP_OK;
+    *w = 0;
+    return set_error(TROP_ERR_CUDA,
+                     "a kernel on device %d abandoned its work: an operand copy of the TMA-fed GEMM did not land "
+                     "within its bounded waits, so the values and argmax of that earlier call are undefined",
+                     dev);
+}
+
+int wait_test_mode() { return g_wait_mode.load(std::memory_order_relaxed); }
+
 // ------------------------------------------------------------------ device set-up
 static std::mutex g_dev_mu;
 static DeviceInfo g_dev[64];
@@ -113,8 +163,13 @@ static bool g_dev_ready[64];
 
 extern int register_kernels_for_device();  // kernels.cu: loads kernels once
 
+static thread_local int t_no_alloc = 0;
+NoAllocScope::NoAllocScope() { ++t_no_alloc; }
+NoAllocScope::~NoAllocScope() { --t_no_alloc; }
+
 int ensure_device(const DeviceInfo** info)
 {
+    const bool may_allocate = t_no_alloc == 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
@@ -139,7 +194,11 @@ int ensure_device(const DeviceInfo** info)
         count_module_init();
     }
     if (info) *info = &g_dev[dev];
-    return TROP_OK;
+    if (may_allocate && !g_err_dev[dev]) {
+        uint32_t* w = nullptr;
+        TROP_TRY(device_error_word(&w));
+    }
+    return take_device_error(dev);
 }
 
 int check_device_pointer(const void* p, const char* name)
@@ -502,10 +561,22 @@ int trop::stream_tickets(cudaStream_t s, size_t count, uint32_t** out)
 extern "C" int tropical_sync_pool(void)
 {
     clear_error();
-    Pool& P = pool();
-    std::lock_guard<std::mutex> lk(P.mu);
-    while (!P.retiring_.empty()) P.wait_oldest_locked();
-    return TROP_OK;
+    {
+        Pool& P = pool();
+        std::lock_guard<std::mutex> lk(P.mu);
+        while (!P.retiring_.empty()) P.wait_oldest_locked();
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TROP_OK;
+    }
+    return dev >= 0 && dev < 64 ? take_device_error(dev) : TROP_OK;
+}
+
+extern "C" void tropical_debug_set_wait_mode(int mode)
+{
+    g_wait_mode.store(mode < 0 || mode > 2 ? 0 : mode, std::memory_order_relaxed);
 }
 
 extern "C" int tropical_release_pool(void)

@@ -340,12 +340,27 @@ void tropical_reset_stats(void);
 
 /* Bounded waits inside kernels on the current device that gave up, since load
  * or since the last reset.  The TMA-fed GEMM waits for each operand copy on an
- * mbarrier for at most about 0.2 s; a CTA whose copy did not land by then
- * counts one here and stores nothing (so a wrong result is never silent when
- * this count is read).  Reads a device counter: blocks until the device is
- * idle.  reset != 0 zeroes the counter after reading it.  Returns TROP_OK, or
- * TROP_ERR_INVALID_ARG for a NULL count, or TROP_ERR_CUDA. */
+ * mbarrier for at most about 0.2 s.  A CTA whose wait gives up counts one here
+ * and waits once more with the full bound: a copy that lands late still gives
+ * exact results.  If it has not landed then either, the CTA waits (bounded) for
+ * its copies in flight, abandons its tile (its argmax entries are set to 0, its
+ * values left as they were) and sets a device error word in host-mapped memory;
+ * the first library call made on the device after that kernel finished (or
+ * tropical_sync_pool) returns TROP_ERR_CUDA naming the failure, once.  The
+ * values and argmax of the call whose kernel abandoned a tile are undefined.
+ * Reads a device counter: blocks until the device is idle.  reset != 0 zeroes
+ * the counter after reading it.  Returns TROP_OK, or TROP_ERR_INVALID_ARG for a
+ * NULL count, or TROP_ERR_CUDA. */
 int tropical_device_wait_timeouts(unsigned int* count, int reset);
+
+/* Test hook for the bounded waits above (host-side; it changes no device
+ * setting): mode 1 makes the first operand wait of every CTA of the TMA-fed
+ * GEMMs launched afterwards give up at once (then wait again with the full
+ * bound, so results stay exact and the counter above grows); mode 2 does the
+ * same and then treats that second wait as failed after it completed, so each
+ * CTA takes the failure path with no copy in flight (the next call reports
+ * TROP_ERR_CUDA).  0 restores normal waits; other values are taken as 0. */
+void tropical_debug_set_wait_mode(int mode);
 
 /* Message of the last failure on this host thread ("" if none). */
 const char* tropical_last_error(void);

@@ -115,10 +115,19 @@ def _contig(shape):
 def test_describe_names_gemm_kernel_and_resolve(trop, k, kernel, resolve):
     """The planner reports which argmax GEMM kernel and resolve pass a layout takes: the TMA-fed
     kernel needs one batch axis, K a multiple of 16 and 16-byte row strides; the row resolve
-    needs K <= 256 in whole chunks of 8."""
-    sa, sb = [8, 128, k], [8, k, 128]
+    needs K <= 256 in whole chunks of 8.  Batch 64 of 128 x 128 tiles fills more than half a
+    wave, so no tile is split along k (a split tail takes the cp.async kernel)."""
+    sa, sb = [64, 128, k], [64, k, 128]
     text = trop.plan_describe("zmk,zkn->zmn", sa, _contig(sa), sb, _contig(sb))
     assert f"kernel={kernel}" in text and f"resolve={resolve}" in text, text
+
+
+def test_describe_small_problems_split_the_tail_on_the_cpasync_kernel(trop):
+    """Under half a wave of tiles the argmax GEMM cuts its tiles along k (stream-K), which
+    only the cp.async kernel does: the planner says so instead of naming the TMA kernel."""
+    sa, sb = [8, 128, 256], [8, 256, 128]
+    text = trop.plan_describe("zmk,zkn->zmn", sa, _contig(sa), sb, _contig(sb))
+    assert "split_tail" in text and "kernel=tiled" in text, text
 
 
 def test_describe_tma_needs_aligned_rows_and_one_batch_axis(trop):

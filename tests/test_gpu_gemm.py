@@ -308,24 +308,79 @@ def test_short_contraction_padded_rows_and_ties(trop, sr):
     np.testing.assert_array_equal(i.cpu().numpy(), ri)
 
 
+@pytest.mark.parametrize("sr", SR)
+def test_tma_gemm_given_up_wait_recovers_exactly(trop, sr):
+    """A first operand wait that gives up is counted and waited again with the full bound:
+    the results stay bit-exact against the oracle (test mode 1 makes every CTA's first wait
+    give up at once)."""
+    a, b = synth.gemm_batched_inputs(sr, batch=32)
+    ad, bd = _dev(a), _dev(b)
+    desc = trop.plan_describe("zmk,zkn->zmn", list(ad.shape), list(ad.stride()), list(bd.shape), list(bd.stride()))
+    assert "kernel=tma" in desc, desc
+    trop.device_wait_timeouts(reset=True)
+    trop.debug_set_wait_mode(1)
+    try:
+        c, i = trop.gemm(ad, bd, sr)
+        torch.cuda.synchronize()
+    finally:
+        trop.debug_set_wait_mode(0)
+    assert trop.device_wait_timeouts(reset=True) == 32 * 4 * 4    # one per CTA (32 x 4 x 4 tiles)
+    rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+    assert c.cpu().numpy().tobytes() == rc.tobytes()
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
+
+
+def test_tma_gemm_failed_wait_is_reported(trop):
+    """When a wait cannot be completed the tile is abandoned and the failure reported by
+    the next call (test mode 2 fails every CTA after its copies have landed, so nothing is
+    in flight); the report comes once, and the next call is bit-exact again."""
+    from einsum_device_side_gb300 import TropicalError
+    a, b = synth.gemm_batched_inputs(0, batch=32)
+    ad, bd = _dev(a), _dev(b)
+    desc = trop.plan_describe("zmk,zkn->zmn", list(ad.shape), list(ad.stride()), list(bd.shape), list(bd.stride()))
+    assert "kernel=tma" in desc, desc
+    c = torch.full((32, 256, 256), 7.0, device="cuda")
+    i = torch.full((32, 256, 256), -5, dtype=torch.int32, device="cuda")
+    trop.debug_set_wait_mode(2)
+    try:
+        trop.gemm(ad, bd, 0, out=c, out_argmax=i)
+        torch.cuda.synchronize()
+    finally:
+        trop.debug_set_wait_mode(0)
+    assert bool((c == 7.0).all()), "an abandoned tile stores no values"
+    assert bool((i == 0).all()), "an abandoned tile leaves no chunk code for the resolve pass"
+    with pytest.raises(TropicalError) as ex:
+        trop.gemm(ad, bd, 0, out=c, out_argmax=i)
+    assert ex.value.name == "CUDA" and "abandoned" in str(ex.value)
+    trop.device_wait_timeouts(reset=True)
+    c2, i2 = trop.gemm(ad, bd, 0)                    # reported once: this call runs normally
+    rc, ri = oracle.gemm(a, b, 0, nthreads=0)
+    assert c2.cpu().numpy().tobytes() == rc.tobytes()
+    np.testing.assert_array_equal(i2.cpu().numpy(), ri)
+
+
 def test_tma_gemm_waits_never_gave_up(trop):
     """Every operand copy of the TMA-fed GEMM landed within its bounded wait (the device
     counter of given-up waits stays 0 after the full-size calls)."""
     for sr in SR:
-        a, b = synth.gemm_batched_inputs(sr, batch=8)
-        trop.gemm(_dev(a), _dev(b), sr)
+        a, b = synth.gemm_batched_inputs(sr, batch=32)
+        ad, bd = _dev(a), _dev(b)
+        desc = trop.plan_describe("zmk,zkn->zmn", list(ad.shape), list(ad.stride()), list(bd.shape), list(bd.stride()))
+        assert "kernel=tma" in desc, desc
+        trop.gemm(ad, bd, sr)
     assert trop.device_wait_timeouts() == 0
 
 
 # ---------------------------------------------------------------- the TMA-fed kernel (one batch axis, K % 16 == 0)
 
 @pytest.mark.parametrize("sr", SR)
-@pytest.mark.parametrize("shape", [(3, 70, 44, 48), (2, 130, 132, 256), (1, 200, 68, 128), (2, 64, 64, 16),
-                                   (1, 33, 260, 512), (2, 65, 64, 1024)])
+@pytest.mark.parametrize("shape", [(120, 70, 44, 48), (30, 130, 132, 256), (40, 200, 68, 128), (240, 64, 64, 16),
+                                   (48, 33, 260, 512), (120, 65, 64, 1024)])
 def test_tma_path_integer_ties_padded_rows(trop, sr, shape):
     """Small integers (ties between k in every chunk and across k-tiles), A's and the output's
     rows padded past their extents, ragged M and N: values and argmax equal the oracle's.  The
-    planner confirms the layout takes the TMA-fed kernel (K = 512 and 1024 then take the panel
+    batches give more than half a wave of tiles, so no tile is split along k and the planner
+    confirms the layout takes the TMA-fed kernel (K = 512 and 1024 then take the panel
     resolve, the others the row resolve)."""
     bt, m, n, k = shape
     a = synth.uniform_int(41, (bt, m, k), -4, 4).astype(np.float32)
