@@ -56,7 +56,7 @@ class TropNode(ctypes.Structure):
 
 _STAT_FIELDS = ["module_inits", "kernel_launches", "pool_allocs", "pool_hits", "pool_device_mallocs",
                 "pool_retired", "pool_released", "pool_event_waits", "pool_leaked", "pool_bytes_cached",
-                "stream_syncs"]
+                "stream_syncs", "plan_cache_hits", "plan_cache_misses"]
 
 
 class TropStats(ctypes.Structure):
@@ -64,11 +64,28 @@ class TropStats(ctypes.Structure):
 
 
 _lib = None
+_fc = None  # the CPython binding of the hot entry points (csrc/fastcall.c), when built
+
+
+def _load_fastcall(lib_path: str):
+    """The fast-call extension built beside the library (None if this Python had no headers
+    to build it with; the ctypes binding then serves every call)."""
+    import glob
+    import importlib.machinery
+    import importlib.util
+    found = glob.glob(os.path.join(os.path.dirname(lib_path), "_fastcall*.so"))
+    if not found:
+        return None
+    loader = importlib.machinery.ExtensionFileLoader("_fastcall", found[0])
+    spec = importlib.util.spec_from_file_location("_fastcall", found[0], loader=loader)
+    mod = importlib.util.module_from_spec(spec)
+    loader.exec_module(mod)
+    return mod
 
 
 def load(path: str | None = None):
     """Load the shared library (once).  Raises if it has not been built."""
-    global _lib
+    global _lib, _fc
     if _lib is not None:
         return _lib
     path = path or LIB_PATH
@@ -106,6 +123,7 @@ def load(path: str | None = None):
         "tropical_plan_describe": (I, [ctypes.c_char_p, I, i64p, i64p, I, i64p, i64p, ctypes.c_char_p, I]),
         "tropical_debug_fail_next_event_records": (None, [I]),
         "tropical_set_pool_capacity": (None, [I]),
+        "tropical_set_plan_cache_capacity": (None, [I]),
         "tropical_device_wait_timeouts": (I, [ctypes.POINTER(ctypes.c_uint), I]),
         "tropical_debug_set_wait_mode": (None, [I]),
     }
@@ -115,6 +133,7 @@ def load(path: str | None = None):
         f.argtypes = args
     del i32p
     _lib = lib
+    _fc = _load_fastcall(path)
     return lib
 
 
@@ -124,8 +143,31 @@ def _check(rc: int):
         raise TropicalError(rc, msg)
 
 
+_SPECS: dict = {}
+
+
+def _spec(spec: str) -> bytes:
+    b = _SPECS.get(spec)
+    if b is None:
+        if len(_SPECS) >= 4096:
+            _SPECS.clear()
+        b = _SPECS[spec] = spec.encode()
+    return b
+
+
+def _dt(t: torch.Tensor) -> int:
+    code = _DTYPES.get(t.dtype)
+    if code is None:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return code
+
+
+def _ptr(t) -> int | None:
+    return t.data_ptr() if t is not None and t.numel() else None
+
+
 def _sr(semiring) -> int:
-    if isinstance(semiring, str):
+    if semiring.__class__ is str:
         return SEMIRINGS[semiring]
     return int(semiring)
 
@@ -138,8 +180,8 @@ def _stream(stream=None, like: torch.Tensor | None = None) -> int:
     if stream is not None:
         return stream.cuda_stream
     if _raw_stream is not None:
-        dev = like.get_device() if like is not None and like.is_cuda else torch.cuda.current_device()
-        return _raw_stream(dev)
+        dev = like.get_device() if like is not None else -1
+        return _raw_stream(dev if dev >= 0 else torch.cuda.current_device())
     return torch.cuda.current_stream().cuda_stream
 
 
@@ -206,18 +248,28 @@ def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Ten
                   argmax: bool | torch.Tensor = False, stream=None):
     """Unary permute / diagonal gather / tropical trace.  Returns ``out`` or
     ``(out, argmax)`` when ``argmax`` is True or a tensor."""
-    lib = load()
+    lib = _lib or load()
     if out is None:
         out = torch.empty(_spec_shape(spec, [x.shape]), dtype=x.dtype, device=x.device)
     am = None
-    if isinstance(argmax, torch.Tensor):
-        am = argmax
-        _check_argmax(am, out, x)
-    elif argmax:
-        am = torch.empty(out.shape, dtype=torch.int32, device=x.device)
-    dx, do = tensor_desc(x), tensor_desc(out)
-    _check(lib.tropical_permute_trace(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
-                                      am.data_ptr() if am is not None and am.numel() else None, _stream(stream, x)))
+    if argmax is not False:
+        if isinstance(argmax, torch.Tensor):
+            am = argmax
+            _check_argmax(am, out, x)
+        elif argmax:
+            am = torch.empty(out.shape, dtype=torch.int32, device=x.device)
+    st = _stream(stream, x)
+    if _fc is not None:
+        # data_ptr() of an empty tensor may be 0: the C ABI accepts NULL data when an extent is 0
+        # (an unknown dtype goes as -1, which the C ABI refuses with TROP_ERR_DTYPE)
+        rc = _fc.permute_trace(x.data_ptr(), _DTYPES.get(x.dtype, -1), x.shape, x.stride(),
+                               _SPECS.get(spec) or _spec(spec), _sr(semiring), out.data_ptr(),
+                               _DTYPES.get(out.dtype, -1), out.shape, out.stride(),
+                               None if am is None else am.data_ptr(), st, False)
+    else:
+        dx, do = tensor_desc(x), tensor_desc(out)
+        rc = lib.tropical_permute_trace(ctypes.byref(dx), _spec(spec), _sr(semiring), ctypes.byref(do), _ptr(am), st)
+    _check(rc)
     return (out, am) if am is not None else out
 
 
@@ -227,27 +279,40 @@ def permute_trace_noalloc(x: torch.Tensor, spec: str, semiring="maxplus", *, out
     cannot let it allocate device memory.  ``out`` (and ``argmax``, if wanted)
     must be given; split reductions use the library's fixed scratch, so calls
     must not overlap on the GPU."""
-    lib = load()
+    lib = _lib or load()
     if argmax is not None:
         _check_argmax(argmax, out, x)
-    dx, do = tensor_desc(x), tensor_desc(out)
-    _check(lib.tropical_permute_trace_noalloc(ctypes.byref(dx), spec.encode(), _sr(semiring), ctypes.byref(do),
-                                              argmax.data_ptr() if argmax is not None and argmax.numel() else None,
-                                              _stream(stream, x)))
+    st = _stream(stream, x)
+    if _fc is not None:
+        rc = _fc.permute_trace(_ptr(x), _dt(x), x.shape, x.stride(), _spec(spec), _sr(semiring), _ptr(out),
+                               _dt(out), out.shape, out.stride(), _ptr(argmax), st, True)
+    else:
+        dx, do = tensor_desc(x), tensor_desc(out)
+        rc = lib.tropical_permute_trace_noalloc(ctypes.byref(dx), _spec(spec), _sr(semiring), ctypes.byref(do),
+                                                _ptr(argmax), st)
+    _check(rc)
     return (out, argmax) if argmax is not None else out
 
 
 def permute_pair(val: torch.Tensor, arg: torch.Tensor, spec: str, out_val=None, out_arg=None, stream=None):
     """Permute a result and its int32 argmax through one index mapping."""
-    lib = load()
-    shape = _spec_shape(spec, [val.shape])
-    if out_val is None:
-        out_val = torch.empty(shape, dtype=val.dtype, device=val.device)
-    if out_arg is None:
-        out_arg = torch.empty(shape, dtype=torch.int32, device=val.device)
-    a, b, c, d = tensor_desc(val), tensor_desc(arg), tensor_desc(out_val), tensor_desc(out_arg)
-    _check(lib.tropical_permute_pair(ctypes.byref(a), ctypes.byref(b), spec.encode(), ctypes.byref(c),
-                                     ctypes.byref(d), _stream(stream, val)))
+    lib = _lib or load()
+    if out_val is None or out_arg is None:
+        shape = _spec_shape(spec, [val.shape])
+        if out_val is None:
+            out_val = torch.empty(shape, dtype=val.dtype, device=val.device)
+        if out_arg is None:
+            out_arg = torch.empty(shape, dtype=torch.int32, device=val.device)
+    st = _stream(stream, val)
+    if _fc is not None:
+        rc = _fc.permute_pair(_ptr(val), _dt(val), val.shape, val.stride(), _ptr(arg), _dt(arg), arg.shape,
+                              arg.stride(), _spec(spec), _ptr(out_val), _dt(out_val), out_val.shape, out_val.stride(),
+                              _ptr(out_arg), _dt(out_arg), out_arg.shape, out_arg.stride(), st)
+    else:
+        a, b, c, d = tensor_desc(val), tensor_desc(arg), tensor_desc(out_val), tensor_desc(out_arg)
+        rc = lib.tropical_permute_pair(ctypes.byref(a), ctypes.byref(b), _spec(spec), ctypes.byref(c),
+                                       ctypes.byref(d), st)
+    _check(rc)
     return out_val, out_arg
 
 
@@ -255,7 +320,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
          stream=None):
     """Strided-batched tropical GEMM: A [batch, M, K], B [batch, K, N] (any
     strides, batch stride 0 allowed).  Returns (C, argmax) or C."""
-    lib = load()
+    lib = _lib or load()
     if A.dim() == 2:
         A = A.unsqueeze(0)
     if B.dim() == 2:
@@ -281,12 +346,10 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
         _check_argmax(am, out, A, contiguous=False)
         if am.stride() != out.stride():
             raise ValueError("argmax must have the strides of out")
-    _check(lib.tropical_gemm_strided_batched_argmax(
-        _sr(semiring), _DTYPES[A.dtype], batch, M, N, K,
-        A.data_ptr() if A.numel() else None, A.stride(0), A.stride(1), A.stride(2),
-        B.data_ptr() if B.numel() else None, B.stride(0), B.stride(1), B.stride(2),
-        out.data_ptr() if out.numel() else None, out.stride(0), out.stride(1), out.stride(2),
-        am.data_ptr() if am is not None and am.numel() else None, _stream(stream, out)))
+    sa, sb, so = A.stride(), B.stride(), out.stride()
+    call = _fc.gemm if _fc is not None else lib.tropical_gemm_strided_batched_argmax
+    _check(call(_sr(semiring), _DTYPES[A.dtype], batch, M, N, K, _ptr(A), sa[0], sa[1], sa[2],
+                _ptr(B), sb[0], sb[1], sb[2], _ptr(out), so[0], so[1], so[2], _ptr(am), _stream(stream, out)))
     return (out, am) if argmax else out
 
 
@@ -349,17 +412,22 @@ def einsum(spec: str, A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argm
            out_argmax=None, stream=None):
     """Pairwise tropical einsum, e.g. ``einsum('zacd,zdce->zea', A, B)``.
     Returns (out, argmax) or out."""
-    lib = load()
+    lib = _lib or load()
     if out is None:
         out = torch.empty(_spec_shape(spec, [A.shape, B.shape]), dtype=A.dtype, device=A.device)
     am = None
     if argmax:
         am = out_argmax if out_argmax is not None else torch.empty(out.shape, dtype=torch.int32, device=A.device)
         _check_argmax(am, out, A)
-    a, b, o = tensor_desc(A), tensor_desc(B), tensor_desc(out)
-    _check(lib.tropical_einsum_pairwise(spec.encode(), ctypes.byref(a), ctypes.byref(b), _sr(semiring),
-                                        ctypes.byref(o), am.data_ptr() if am is not None and am.numel() else None,
-                                        _stream(stream, out)))
+    st = _stream(stream, out)
+    if _fc is not None:
+        rc = _fc.einsum(_spec(spec), _ptr(A), _dt(A), A.shape, A.stride(), _ptr(B), _dt(B), B.shape, B.stride(),
+                        _sr(semiring), _ptr(out), _dt(out), out.shape, out.stride(), _ptr(am), st)
+    else:
+        a, b, o = tensor_desc(A), tensor_desc(B), tensor_desc(out)
+        rc = lib.tropical_einsum_pairwise(_spec(spec), ctypes.byref(a), ctypes.byref(b), _sr(semiring),
+                                          ctypes.byref(o), _ptr(am), st)
+    _check(rc)
     return (out, am) if argmax else out
 
 
@@ -515,6 +583,11 @@ def device_wait_timeouts(reset: bool = False) -> int:
     n = ctypes.c_uint(0)
     _check(load().tropical_device_wait_timeouts(ctypes.byref(n), int(bool(reset))))
     return n.value
+
+
+def set_plan_cache_capacity(n: int):
+    """Bound of the pairwise einsum's plan cache (0 disables it)."""
+    load().tropical_set_plan_cache_capacity(int(n))
 
 
 def debug_set_wait_mode(mode: int):

@@ -61,6 +61,37 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
+def _ext_path() -> str:
+    import sysconfig
+    return os.path.join(BUILD, "_fastcall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
+def build_fastcall(force: bool = False) -> str | None:
+    """The CPython binding of the hot entry points (csrc/fastcall.c), linked against the
+    library in the same folder.  Returns its path, or None when this Python has no
+    development headers (the ctypes binding then serves every call)."""
+    import sysconfig
+    src = os.path.join(CSRC, "fastcall.c")
+    out = _ext_path()
+    inc = sysconfig.get_paths().get("include", "")
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    deps = [src, LIB, os.path.join(ROOT, "include", "tropical.h")]
+    if not force and os.path.exists(out) and all(os.path.getmtime(d) <= os.path.getmtime(out) for d in deps):
+        return out
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        return None
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [cc, "-O2", "-shared", "-fPIC", "-std=c11", "-I", inc, "-I", os.path.join(ROOT, "include"), src,
+           "-o", tmp, "-L", BUILD, "-l:" + os.path.basename(LIB), "-Wl,-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"fastcall build failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, out)
+    return out
+
+
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     if force:
@@ -69,6 +100,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     if os.path.exists(LIB) and all(os.path.getmtime(o) <= os.path.getmtime(LIB) for o in objs):
+        build_fastcall(force=force)
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"]
@@ -76,6 +108,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    build_fastcall(force=True)
     return LIB
 
 

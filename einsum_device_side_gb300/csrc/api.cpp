@@ -12,9 +12,15 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <list>
+#include <memory>
+#include <mutex>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "internal.h"
@@ -269,41 +275,70 @@ struct Workspace {
     }
 };
 
-// reduce the one-operand labels of `v` (not in `keep`) into a contiguous
-// workspace tensor holding the kept labels in v's order
-int prereduce(int sr, const View& v, const std::vector<bool>& keep_mask, Workspace* ws, bool dry, View& out)
+// One pre-pass of an operand recorded by the lowering: a (+)-reduction of its one-operand
+// labels (reduce) or a permute, into a contiguous workspace tensor of `bytes`.  At run time its
+// input is the operand's current buffer (the caller's, or the previous pre-pass's workspace).
+struct PrePass {
+    int operand;  // 0: A, 1: B
+    bool reduce;
+    UnaryPlan up;  // reduce: up.u is the input view (its data pointer is filled at run time)
+    int ro;
+    int64_t ostride[MAXR];
+    GatherDesc gd;  // permute
+    int elem_bytes;
+    size_t bytes;
+};
+
+// A pairwise einsum lowered for one layout (labels, extents, strides, dtype, semiring): the
+// pre-passes, then the GEMM.  Nothing in it depends on the data pointers, which run_lowered
+// fills in: the GEMM reads each operand from the caller's buffer or from the workspace of that
+// operand's last pre-pass.
+struct LoweredPair {
+    bool empty = false;  // no output element: nothing runs
+    int npre = 0;
+    PrePass pre[4];
+    int last_pre[2] = {-1, -1};
+    GemmDesc g{};  // A, B, C and I are filled at run time
+    std::string text;
+};
+
+// reduce the one-operand labels of `v` (not in `keep`) into a contiguous workspace tensor
+// holding the kept labels in v's order
+void prereduce(const View& v, const std::vector<bool>& keep_mask, int operand, LoweredPair& L, View& out)
 {
     out = View{};
     out.dtype = v.dtype;
-    UnaryPlan up{};
-    up.u = v;
+    PrePass& P = L.pre[L.npre];
+    P = PrePass{};
+    P.operand = operand;
+    P.reduce = true;
+    P.up.u = v;
     int ro = 0;
     int32_t lo[MAXR];
-    up.n_red = 0;
+    P.up.n_red = 0;
     for (int i = 0; i < v.rank; ++i) {
         if (keep_mask[i]) {
-            up.out_ax[ro] = i;
+            P.up.out_ax[ro] = i;
             lo[ro++] = v.lab[i];
         } else {
-            up.red_ax[up.n_red++] = i;
+            P.up.red_ax[P.up.n_red++] = i;
         }
     }
+    P.ro = ro;
     out.rank = ro;
     for (int i = 0; i < ro; ++i) {
         out.lab[i] = lo[i];
-        out.size[i] = v.size[up.out_ax[i]];
+        out.size[i] = v.size[P.up.out_ax[i]];
     }
     contiguous_strides(ro, out.size, out.stride);
-    if (dry) return TROP_OK;
-    int64_t n = numel(out);
-    void* p = nullptr;
-    TROP_TRY(ws->alloc((size_t)std::max<int64_t>(n, 1) * dtype_bytes(v.dtype), &p));
-    out.data = p;
-    return exec_unary(sr, up, ro, p, out.stride, nullptr, ws->s);
+    std::copy(out.stride, out.stride + ro, P.ostride);
+    P.elem_bytes = (int)dtype_bytes(v.dtype);
+    P.bytes = (size_t)std::max<int64_t>(numel(out), 1) * dtype_bytes(v.dtype);
+    L.last_pre[operand] = L.npre++;
 }
 
 // permute v into a contiguous workspace tensor with labels in `order`
-int permute_to(const View& v, const std::vector<int32_t>& order, Workspace* ws, bool dry, View& out)
+void permute_to(const View& v, const std::vector<int32_t>& order, int operand, LoweredPair& L, View& out)
 {
     out = View{};
     out.dtype = v.dtype;
@@ -314,19 +349,20 @@ int permute_to(const View& v, const std::vector<int32_t>& order, Workspace* ws, 
         out.size[i] = v.size[j];
     }
     contiguous_strides(out.rank, out.size, out.stride);
-    if (dry) return TROP_OK;
-    void* p = nullptr;
-    TROP_TRY(ws->alloc((size_t)std::max<int64_t>(numel(out), 1) * dtype_bytes(v.dtype), &p));
-    out.data = p;
-    GatherDesc d{};
-    d.rank = out.rank;
+    PrePass& P = L.pre[L.npre];
+    P = PrePass{};
+    P.operand = operand;
+    P.reduce = false;
+    P.gd.rank = out.rank;
     for (int i = 0; i < out.rank; ++i) {
         int j = find_label(v, order[i]);
-        d.size[i] = v.size[j];
-        d.s_in[i] = v.stride[j];
-        d.s_out[i] = out.stride[i];
+        P.gd.size[i] = v.size[j];
+        P.gd.s_in[i] = v.stride[j];
+        P.gd.s_out[i] = out.stride[i];
     }
-    return launch_gather(v.data, p, (int)dtype_bytes(v.dtype), nullptr, nullptr, d, ws->s);
+    P.elem_bytes = (int)dtype_bytes(v.dtype);
+    P.bytes = (size_t)std::max<int64_t>(numel(out), 1) * dtype_bytes(v.dtype);
+    L.last_pre[operand] = L.npre++;
 }
 
 bool chain_merges(const std::vector<int32_t>& labs, const View& v)
@@ -381,8 +417,11 @@ std::vector<int32_t> pick_group(const std::vector<int32_t>& cands, const View& v
     return g;
 }
 
-int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t* lo, int ro, void* out,
-                          const int64_t* ostride, int32_t* argmax, cudaStream_t s, bool dry, std::string* text)
+// The lowering of a pairwise einsum: label classes, unit labels dropped, groups of labels that
+// merge into one GEMM axis, permutes only where strides cannot feed the GEMM.
+// has_argmax: whether an argmax is written (decides the int32 range check and its layout).
+int lower_pairwise(int sr, const View& A0, const View& B0, const int32_t* lo, int ro, const int64_t* ostride,
+                   bool has_argmax, LoweredPair& L)
 {
     if ((A0.dtype != TROP_F32 && A0.dtype != TROP_F64) || B0.dtype != A0.dtype)
         return set_error(TROP_ERR_DTYPE, "pairwise tropical einsum needs two f32 or two f64 operands");
@@ -414,8 +453,6 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         return -1;
     };
 
-    Workspace ws;
-    ws.s = s;
     std::string desc;
 
     // one-operand labels absent from the output: (+)-reduce first
@@ -432,19 +469,20 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         }
         if (n_out > 0 && ra) {
             View t;
-            TROP_TRY(prereduce(sr, A, keepA, &ws, dry, t));
+            prereduce(A, keepA, 0, L, t);
             A = t;
             desc += "reduceA ";
         }
         if (n_out > 0 && rb) {
             View t;
-            TROP_TRY(prereduce(sr, B, keepB, &ws, dry, t));
+            prereduce(B, keepB, 1, L, t);
             B = t;
             desc += "reduceB ";
         }
     }
     if (n_out == 0) {
-        if (text) *text = "empty output";
+        L.empty = true;
+        L.text = "empty output";
         return TROP_OK;
     }
 
@@ -461,7 +499,7 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         if (find_label(A, B.lab[i]) < 0) Ln.push_back(B.lab[i]);
     int64_t K = 1;
     for (int32_t l : Lk) K *= A.size[find_label(A, l)];
-    if (argmax && K - 1 > INT32_MAX)
+    if (has_argmax && K - 1 > INT32_MAX)
         return set_error(TROP_ERR_OVERFLOW, "contracted extent %lld does not fit an int32 argmax", (long long)K);
     // size-1 contracted labels do not change the linear index
     {
@@ -521,7 +559,7 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         for (int i = 0; i < A.rank; ++i)
             if (std::find(order.begin(), order.end(), A.lab[i]) == order.end()) order.insert(order.begin(), A.lab[i]);
         View t;
-        TROP_TRY(permute_to(A, order, &ws, dry, t));
+        permute_to(A, order, 0, L, t);
         A = t;
         desc += "permA ";
     }
@@ -534,7 +572,7 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         for (int i = 0; i < B.rank; ++i)
             if (std::find(order.begin(), order.end(), B.lab[i]) == order.end()) order.insert(order.begin(), B.lab[i]);
         View t;
-        TROP_TRY(permute_to(B, order, &ws, dry, t));
+        permute_to(B, order, 1, L, t);
         B = t;
         desc += "permB ";
     }
@@ -547,16 +585,16 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         sBk = Lk.empty() ? 0 : chain_stride(Lk, B);
     }
 
-    GemmDesc g{};
+    GemmDesc& g = L.g;
+    g = GemmDesc{};
     g.semiring = sr;
     g.dtype = A0.dtype;
     g.M = group_sizes(Gm, A);
     g.N = group_sizes(Gn, B);
     g.K = group_sizes(Lk, A);
-    g.A = A.data;
-    g.B = B.data;
-    g.C = out;
-    g.I = argmax;
+    // the data pointers are the run's; a description takes every pointer as 256-byte aligned
+    g.A = g.B = g.C = nullptr;
+    g.I = has_argmax ? reinterpret_cast<int32_t*>(uintptr_t(256)) : nullptr;
     g.sAk = sAk;
     g.sBk = sBk;
     if (!Gm.empty()) {
@@ -605,17 +643,130 @@ int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t*
         }
         TROP_TRY(add_batch(l));
     }
-    if (text) {
-        char buf[512];
-        char route[96];
-        describe_gemm(g, route, sizeof route);
-        snprintf(buf, sizeof buf, "%sgemm M=%lld N=%lld K=%lld batch_axes=%d sAm=%lld sAk=%lld sBk=%lld sBn=%lld sCm=%lld sCn=%lld%s",
-                 desc.c_str(), (long long)g.M, (long long)g.N, (long long)g.K, g.nb, (long long)g.sAm,
-                 (long long)g.sAk, (long long)g.sBk, (long long)g.sBn, (long long)g.sCm, (long long)g.sCn, route);
-        *text = buf;
+    char buf[512];
+    char route[128];
+    describe_gemm(g, route, sizeof route);
+    snprintf(buf, sizeof buf, "%sgemm M=%lld N=%lld K=%lld batch_axes=%d sAm=%lld sAk=%lld sBk=%lld sBn=%lld sCm=%lld sCn=%lld%s",
+             desc.c_str(), (long long)g.M, (long long)g.N, (long long)g.K, g.nb, (long long)g.sAm,
+             (long long)g.sAk, (long long)g.sBk, (long long)g.sBn, (long long)g.sCm, (long long)g.sCn, route);
+    L.text = buf;
+    return TROP_OK;
+}
+
+// Run a lowered pairwise einsum on actual buffers: each pre-pass into pool workspace (retired
+// through the stream's event when the call ends), then the GEMM.
+int run_lowered(int sr, const LoweredPair& L, const void* a_data, const void* b_data, void* out, int32_t* argmax,
+                cudaStream_t s)
+{
+    if (L.empty) return TROP_OK;
+    Workspace ws;
+    ws.s = s;
+    const void* cur[2] = {a_data, b_data};
+    for (int i = 0; i < L.npre; ++i) {
+        const PrePass& P = L.pre[i];
+        void* p = nullptr;
+        TROP_TRY(ws.alloc(P.bytes, &p));
+        if (P.reduce) {
+            UnaryPlan up = P.up;
+            up.u.data = const_cast<void*>(cur[P.operand]);
+            TROP_TRY(exec_unary(sr, up, P.ro, p, P.ostride, nullptr, s));
+        } else {
+            TROP_TRY(launch_gather(cur[P.operand], p, P.elem_bytes, nullptr, nullptr, P.gd, s));
+        }
+        cur[P.operand] = p;
     }
-    if (dry) return TROP_OK;
+    GemmDesc g = L.g;
+    g.A = cur[0];
+    g.B = cur[1];
+    g.C = out;
+    g.I = argmax;
     return launch_gemm(g, s, nullptr);
+}
+
+// ------------------------------------------------------------------ plan cache
+// Lowered pairwise einsums kept per layout, so that a repeated call (the same spec on tensors
+// of the same shapes, strides, dtype and 16-byte alignment, the same semiring, with or without
+// argmax) skips the lowering -- the analogue of the plan cache the tenferro-rs note keeps per
+// contraction ("Problem").  Least recently used entries go first beyond the bound (64 by
+// default, TROP_PLAN_CACHE from the environment at load; 0 disables it).
+struct PlanCache {
+    std::mutex mu;
+    size_t capacity;
+    std::list<std::pair<std::string, std::shared_ptr<const LoweredPair>>> lru;  // front: most recent
+    std::unordered_map<std::string, decltype(lru)::iterator> map;
+    PlanCache()
+    {
+        const char* e = std::getenv("TROP_PLAN_CACHE");
+        capacity = e ? (size_t)std::max(0L, std::strtol(e, nullptr, 10)) : 64;
+    }
+};
+PlanCache& plan_cache()
+{
+    static PlanCache c;
+    return c;
+}
+void key_put(std::string& k, const void* p, size_t n) { k.append(static_cast<const char*>(p), n); }
+void key_view(std::string& k, const View& v)
+{
+    key_put(k, &v.rank, sizeof v.rank);
+    key_put(k, &v.dtype, sizeof v.dtype);
+    key_put(k, v.lab, sizeof(int32_t) * v.rank);
+    key_put(k, v.size, sizeof(int64_t) * v.rank);
+    key_put(k, v.stride, sizeof(int64_t) * v.rank);
+}
+
+int plan_and_run_pairwise(int sr, const View& A0, const View& B0, const int32_t* lo, int ro, void* out,
+                          const int64_t* ostride, int32_t* argmax, cudaStream_t s)
+{
+    PlanCache& C = plan_cache();
+    size_t capacity;
+    {
+        std::lock_guard<std::mutex> lk(C.mu);
+        capacity = C.capacity;
+    }
+    if (capacity == 0) {
+        LoweredPair L;
+        TROP_TRY(lower_pairwise(sr, A0, B0, lo, ro, ostride, argmax != nullptr, L));
+        return run_lowered(sr, L, A0.data, B0.data, out, argmax, s);
+    }
+    std::string key;
+    key.reserve(1024);
+    const uint8_t head[2] = {(uint8_t)sr, (uint8_t)(argmax != nullptr)};
+    key_put(key, head, sizeof head);
+    // 16-byte alignment of every buffer (kernel choices below the lowering depend on it)
+    const uint8_t align[4] = {(uint8_t)((uintptr_t)A0.data & 15), (uint8_t)((uintptr_t)B0.data & 15),
+                              (uint8_t)((uintptr_t)out & 15), (uint8_t)((uintptr_t)argmax & 15)};
+    key_put(key, align, sizeof align);
+    key_view(key, A0);
+    key_view(key, B0);
+    key_put(key, &ro, sizeof ro);
+    key_put(key, lo, sizeof(int32_t) * ro);
+    key_put(key, ostride, sizeof(int64_t) * ro);
+    std::shared_ptr<const LoweredPair> L;
+    {
+        std::lock_guard<std::mutex> lk(C.mu);
+        auto it = C.map.find(key);
+        if (it != C.map.end()) {
+            C.lru.splice(C.lru.begin(), C.lru, it->second);
+            L = it->second->second;
+        }
+    }
+    count_plan(L != nullptr);
+    if (!L) {
+        auto fresh = std::make_shared<LoweredPair>();
+        TROP_TRY(lower_pairwise(sr, A0, B0, lo, ro, ostride, argmax != nullptr, *fresh));
+        L = fresh;
+        std::lock_guard<std::mutex> lk(C.mu);
+        if (C.map.find(key) == C.map.end()) {
+            C.lru.emplace_front(key, L);
+            C.map[key] = C.lru.begin();
+            while (C.map.size() > C.capacity) {
+                C.map.erase(C.lru.back().first);
+                C.lru.pop_back();
+            }
+        }
+    }
+    return run_lowered(sr, *L, A0.data, B0.data, out, argmax, s);
 }
 
 int tensor_labels_check(const trop_tensor* t, int rank, const char* name)
@@ -846,8 +997,18 @@ extern "C" int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, 
         n_out *= out->shape[i];
     }
     if (argmax && n_out > 0) TROP_TRY(check_device_pointer(argmax, "argmax"));
-    return plan_and_run_pairwise(semiring, vA, vB, lo, ro, out->data, out->stride, argmax,
-                                 (cudaStream_t)stream, false, nullptr);
+    return plan_and_run_pairwise(semiring, vA, vB, lo, ro, out->data, out->stride, argmax, (cudaStream_t)stream);
+}
+
+extern "C" void tropical_set_plan_cache_capacity(int capacity)
+{
+    PlanCache& C = plan_cache();
+    std::lock_guard<std::mutex> lk(C.mu);
+    C.capacity = capacity < 0 ? 0 : (size_t)capacity;
+    while (C.map.size() > C.capacity) {
+        C.map.erase(C.lru.back().first);
+        C.lru.pop_back();
+    }
 }
 
 extern "C" int tropical_plan_describe(const char* spec, int rank_a, const int64_t* shape_a, const int64_t* stride_a,
@@ -886,8 +1047,9 @@ extern "C" int tropical_plan_describe(const char* spec, int rank_a, const int64_
     }
     contiguous_strides(ro, osize, ostride);
     std::string text;
-    TROP_TRY(plan_and_run_pairwise(TROP_MAXPLUS, A, B, lo, ro, nullptr, ostride, (int32_t*)1, nullptr, true, &text));
-    snprintf(buf, (size_t)buflen, "%s", text.c_str());
+    LoweredPair L;
+    TROP_TRY(lower_pairwise(TROP_MAXPLUS, A, B, lo, ro, ostride, true, L));
+    snprintf(buf, (size_t)buflen, "%s", L.text.c_str());
     return TROP_OK;
 }
 
@@ -1057,8 +1219,7 @@ int run_tree(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop_no
             rc = plan_unary(a, nd.out_labels, nd.n_out, up);
             if (rc == TROP_OK) rc = exec_unary(semiring, up, nd.n_out, dst, ostride, am, s);
         } else {
-            rc = plan_and_run_pairwise(semiring, a, b, nd.out_labels, nd.n_out, dst, ostride, am,
-                                       s, false, nullptr);
+            rc = plan_and_run_pairwise(semiring, a, b, nd.out_labels, nd.n_out, dst, ostride, am, s);
         }
         // retire intermediates whose last consumer is this node
         const int ids[2] = {nd.lhs, nd.rhs};

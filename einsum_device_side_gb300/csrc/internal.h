@@ -53,6 +53,7 @@ int wait_test_mode();
 // ---------------------------------------------------------------- counters
 void count_launches(int64_t n);
 void count_module_init();
+void count_plan(bool hit);  // plan cache of the pairwise einsum (api.cpp)
 void count_pool(int field, int64_t n);  // field: see pool.cu
 enum { ST_ALLOC, ST_HIT, ST_MALLOC, ST_RETIRED, ST_RELEASED, ST_EVWAIT, ST_LEAKED, ST_BYTES };
 

@@ -81,6 +81,8 @@ void count_launches(int64_t n)
     else c_launches += n;
 }
 void count_module_init() { c_module_inits += 1; }
+static std::atomic<int64_t> c_plan_hits{0}, c_plan_misses{0};
+void count_plan(bool hit) { (hit ? c_plan_hits : c_plan_misses) += 1; }
 void count_pool(int field, int64_t n) { c_pool[field] += n; }
 
 // ------------------------------------------------------------------ fast divmod
@@ -626,6 +628,8 @@ extern "C" int tropical_stats(trop_stats* out)
     out->pool_released = c_pool[ST_RELEASED].load();
     out->pool_event_waits = c_pool[ST_EVWAIT].load();
     out->pool_leaked = c_pool[ST_LEAKED].load();
+    out->plan_cache_hits = c_plan_hits.load();
+    out->plan_cache_misses = c_plan_misses.load();
     {
         Pool& P = pool();
         std::lock_guard<std::mutex> lk(P.mu);
@@ -639,12 +643,14 @@ extern "C" void tropical_reset_stats(void)
 {
     c_launches = 0;
     c_stream_syncs = 0;
+    c_plan_hits = 0;
+    c_plan_misses = 0;
     for (int i = 0; i < 7; ++i) c_pool[i] = 0;  // ST_BYTES is derived, module_inits kept
 }
 
 extern "C" const char* tropical_last_error(void) { return g_last_error.c_str(); }
 
-extern "C" int tropical_version(void) { return 1; }
+extern "C" int tropical_version(void) { return 2; }
 
 extern "C" void tropical_debug_fail_next_event_records(int count)
 {

@@ -132,6 +132,9 @@ typedef struct {
     int64_t pool_leaked;         /* event record failed: block leaked, never reused */
     int64_t pool_bytes_cached;   /* bytes held by the pool (free + retiring) */
     int64_t stream_syncs;        /* stream synchronizations issued (stays 0) */
+    int64_t plan_cache_hits;     /* pairwise einsums (eager calls and tree nodes) whose
+                                    lowering came from the plan cache */
+    int64_t plan_cache_misses;   /* ... that were lowered (and then cached) */
 } trop_stats;
 
 /* Set up the kernels for `device` once (kernel attributes, device
@@ -238,6 +241,13 @@ int tropical_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, in
 
 /* Pairwise tropical einsum [I52 Summary and "Resolved design for step 3";
  * PR35 Summary]:  spec "zacd,zdce->zea" over letters a-z A-Z.
+ * Plan cache [WR "Problem": the einsum path caches one plan per contraction]:
+ * the lowering (pre-passes and GEMM layout) is kept per layout -- labels,
+ * extents, strides, dtype, semiring, whether argmax is written and the 16-byte
+ * alignment of every buffer -- in a bounded LRU of 64 entries (the environment
+ * variable TROP_PLAN_CACHE at load sets the bound; 0 disables it), so a
+ * repeated call skips it; trop_stats counts hits and misses.  The contraction
+ * tree executor's nodes use the same cache.
  *   out[o] = (+) over all assignments of the labels absent from the output
  *            of A[..] (x) B[..]   (A, B and out all f32 or all f64)
  *   argmax[o] = row-major linear index over the CONTRACTED labels (present
@@ -365,7 +375,8 @@ void tropical_debug_set_wait_mode(int mode);
 /* Message of the last failure on this host thread ("" if none). */
 const char* tropical_last_error(void);
 
-/* Library / ABI version (increments on incompatible changes). */
+/* Library / ABI version (increments on incompatible changes; 2: trop_stats gained the plan
+ * cache counters). */
 int tropical_version(void);
 
 /* Host-only planner inspection (no device work, no GPU needed): describes how
@@ -384,6 +395,11 @@ void tropical_debug_fail_next_event_records(int count);
 /* Set the retirement-queue bound (default 16, or TROP_POOL_CAPACITY from the
  * environment at load).  Values < 1 are clamped to 1. */
 void tropical_set_pool_capacity(int capacity);
+
+/* Set the bound of the pairwise einsum's plan cache (see tropical_einsum_pairwise;
+ * default 64, or TROP_PLAN_CACHE from the environment at load).  0 disables the
+ * cache and drops its entries; a smaller bound drops the least recently used. */
+void tropical_set_plan_cache_capacity(int capacity);
 
 #ifdef __cplusplus
 }

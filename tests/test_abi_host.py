@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(trop):
 
 
 def test_version_and_stats_without_gpu(trop):
-    assert trop.version() == 1
+    assert trop.version() == 2
     s = trop.stats()
     assert s["stream_syncs"] == 0
 
@@ -151,3 +151,22 @@ def test_describe_wide_row_strides_leave_the_32_bit_paths(trop):
     text = trop.plan_describe("zmk,zkn->zmn", [1, 16, 64], [16 * wide, wide, 1], sb, _contig(sb))
     assert "route=tiled" in text and "resolve=panel64" in text, text
     assert f"sAm={wide}" in text, text
+
+
+def test_fastcall_binding_loads_and_marshals(trop):
+    """The CPython binding of the hot entry points is built beside the library and reaches
+    the same C ABI: wrong argument counts raise, and an unknown semiring comes back as the
+    library's INVALID_ARG code before any device work."""
+    import sysconfig
+    if not os.path.exists(os.path.join(sysconfig.get_paths()["include"], "Python.h")):
+        pytest.skip("no Python headers: the ctypes binding serves every call")
+    fc = trop._fc
+    assert fc is not None
+    with pytest.raises(TypeError):
+        fc.gemm(1, 2)
+    rc = fc.permute_trace(None, 0, (2, 3), (3, 1), b"ij->ji", 7, None, 0, (3, 2), (2, 1), None, None, False)
+    assert rc == -1 and "semiring" in fc.last_error()
+    rc = fc.gemm(7, 0, 1, 2, 2, 2, None, 0, 0, 0, None, 0, 0, 0, None, 0, 0, 0, None, None)
+    assert rc == -1
+    with pytest.raises(ValueError):
+        fc.permute_trace(None, 0, (1,) * 33, (1,) * 33, b"a->a", 0, None, 0, (1,), (1,), None, None, False)

@@ -224,3 +224,80 @@ def test_ising_workload_24x24_full_size(trop):
     assert w == wo
     np.testing.assert_array_equal(spins, so)
     assert oracle.ising_energy(jh, jv, spins) == -w
+
+
+# ---------------------------------------------------------------- plan cache
+
+def test_plan_cache_lowers_a_repeated_einsum_once(trop):
+    """A repeated pairwise einsum on tensors of the same layout is lowered once (the plan cache
+    counts one miss, then hits) and its results stay bitwise equal to the oracle's; a change of
+    layout (strides) is a new entry; disabling the cache lowers every call."""
+    trop.set_plan_cache_capacity(64)
+    A = synth.uniform_f32(61, (3, 40, 5, 6), -1, 1)
+    B = synth.uniform_f32(62, (3, 6, 5, 33), -1, 1)
+    ro, roa = oracle.einsum("zacd,zdce->zea", A, B, nthreads=0)
+    Ad, Bd = _dev(A), _dev(B)
+    s0 = trop.stats()
+    for _ in range(5):
+        o, oa = trop.einsum("zacd,zdce->zea", Ad, Bd)
+        assert o.cpu().numpy().tobytes() == ro.tobytes()
+        np.testing.assert_array_equal(oa.cpu().numpy(), roa)
+    s1 = trop.stats()
+    assert s1["plan_cache_misses"] - s0["plan_cache_misses"] == 1
+    assert s1["plan_cache_hits"] - s0["plan_cache_hits"] == 4
+    # a transposed view of B: another layout, another lowering, same values
+    Bt = _dev(np.ascontiguousarray(np.transpose(B, (0, 3, 2, 1)))).permute(0, 3, 2, 1)
+    o, oa = trop.einsum("zacd,zdce->zea", Ad, Bt)
+    assert o.cpu().numpy().tobytes() == ro.tobytes()
+    np.testing.assert_array_equal(oa.cpu().numpy(), roa)
+    s2 = trop.stats()
+    assert s2["plan_cache_misses"] - s1["plan_cache_misses"] == 1
+    trop.set_plan_cache_capacity(0)
+    try:
+        for _ in range(2):
+            o, oa = trop.einsum("zacd,zdce->zea", Ad, Bd)
+        assert o.cpu().numpy().tobytes() == ro.tobytes()
+        s3 = trop.stats()
+        assert s3["plan_cache_hits"] == s2["plan_cache_hits"]
+    finally:
+        trop.set_plan_cache_capacity(64)
+
+
+def test_plan_cache_evicts_least_recently_used(trop):
+    """Beyond its bound the cache drops the least recently used layout: with a bound of 4,
+    five distinct layouts in turn evict the first."""
+    trop.set_plan_cache_capacity(4)
+    try:
+        ops = []
+        for k in range(5):
+            a = _dev(synth.uniform_f32(70 + k, (8, 9 + k), -1, 1))
+            b = _dev(synth.uniform_f32(80 + k, (9 + k, 7), -1, 1))
+            ops.append((a, b))
+        for a, b in ops:
+            trop.einsum("ij,jk->ik", a, b)
+        s0 = trop.stats()
+        trop.einsum("ij,jk->ik", *ops[4])          # most recent: a hit
+        trop.einsum("ij,jk->ik", *ops[0])          # evicted: a miss
+        s1 = trop.stats()
+        assert s1["plan_cache_hits"] - s0["plan_cache_hits"] == 1
+        assert s1["plan_cache_misses"] - s0["plan_cache_misses"] == 1
+    finally:
+        trop.set_plan_cache_capacity(64)
+
+
+def test_tree_nodes_share_the_plan_cache(trop):
+    """The contraction-tree executor lowers each node through the same cache: a second run
+    of the 4x4 spin-glass tree lowers nothing and gives the same value."""
+    from einsum_device_side_gb300 import ising
+    trop.set_plan_cache_capacity(1024)
+    try:
+        jh, jv = synth.ising_couplings(4, 4)
+        w0, _, _ = ising.ground_state(jh, jv, device="cuda")
+        s0 = trop.stats()
+        w1, _, _ = ising.ground_state(jh, jv, device="cuda")
+        s1 = trop.stats()
+        assert w1 == w0 == oracle.ising_ground(jh, jv, 4, 4)[0]
+        assert s1["plan_cache_misses"] == s0["plan_cache_misses"]
+        assert s1["plan_cache_hits"] > s0["plan_cache_hits"]
+    finally:
+        trop.set_plan_cache_capacity(64)
