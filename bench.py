@@ -271,7 +271,9 @@ def secondary(trop, torch, pk, reps=20):
                                     "GB/s_device": None if tg is None else 2 * x.nbytes / tg / 1e9}
     tr = torch.from_numpy(synth.trace_inputs()).cuda()
     yo = torch.empty((128, 64, 64), device="cuda")
-    t = timed(lambda: trop.permute_trace(tr, "iijk->ijk", out=yo), reps)
+    # host-bound calls: many per timed region so the event bracket's own latency is amortised
+    hb = max(reps, 400)
+    t = timed(lambda: trop.permute_trace(tr, "iijk->ijk", out=yo), hb)
     tg = graph_timed(lambda: trop.permute_trace(tr, "iijk->ijk", out=yo))
     moved = 2 * 128 * 64 * 64 * 4
     gbs = moved / t / 1e9
@@ -282,7 +284,7 @@ def secondary(trop, torch, pk, reps=20):
                                       "replayed CUDA graph of 20 calls; permutes rotate 3 buffer pairs (384 MiB)"}
     # the '->jk' variant of the trace: (+)-reduction over the diagonal label as well
     yj = torch.empty((64, 64), device="cuda")
-    t = timed(lambda: trop.permute_trace(tr, "iijk->jk", out=yj), reps)
+    t = timed(lambda: trop.permute_trace(tr, "iijk->jk", out=yj), hb)
     tg = graph_timed(lambda: trop.permute_trace(tr, "iijk->jk", out=yj))
     moved = 128 * 64 * 64 * 4 + 64 * 64 * 4
     out["trace_iijk->jk"] = {"us": t * 1e6, "us_device": None if tg is None else tg * 1e6,
@@ -299,10 +301,16 @@ def secondary(trop, torch, pk, reps=20):
     def c1():
         trop.gemm(a64d, b64d, 0, out=c64, out_argmax=i64)
         trop.permute_pair(c64, i64, "bmn->bnm", out_val=ct, out_arg=it)
-    t = timed(c1, reps)
+    t = timed(c1, hb)
     tg = graph_timed(c1)
-    out["gemm64_argmax_transpose"] = {"us": t * 1e6, "us_device": None if tg is None else tg * 1e6,
-                                      "G semiring-ops/s_device": None if tg is None else 64 ** 3 / tg / 1e9}
+    tgemm = timed(lambda: trop.gemm(a64d, b64d, 0, out=c64, out_argmax=i64), hb)
+    tpair = timed(lambda: trop.permute_pair(c64, i64, "bmn->bnm", out_val=ct, out_arg=it), hb)
+    out["gemm64_argmax_transpose"] = {"us": t * 1e6, "us_per_api_call": t * 1e6 / 2,
+                                      "us_gemm_call": tgemm * 1e6, "us_permute_pair_call": tpair * 1e6,
+                                      "us_device": None if tg is None else tg * 1e6,
+                                      "G semiring-ops/s_device": None if tg is None else 64 ** 3 / tg / 1e9,
+                                      "note": "us: the two API calls (GEMM + value/argmax transpose) back to back; "
+                                              "us_device: both inside a replayed CUDA graph"}
     # backward of the batched GEMM (winner routing): dA and dB of the batch-64 256^3 max-plus call
     ga, gb = synth.gemm_batched_inputs(0)
     gad, gbd = torch.from_numpy(ga).cuda(), torch.from_numpy(gb).cuda()
@@ -332,12 +340,30 @@ def secondary(trop, torch, pk, reps=20):
     o = torch.empty((16, 512, 512), device="cuda")
     oa = torch.empty((16, 512, 512), dtype=torch.int32, device="cuda")
     t = timed(lambda: trop.einsum("zacd,zdce->zea", Ad, Bd, out=o, out_argmax=oa), 5)
+    # the same eager call with the plan cache off (every call lowered again), then on again
+    trop.set_plan_cache_capacity(0)
+    t_nocache = timed(lambda: trop.einsum("zacd,zdce->zea", Ad, Bd, out=o, out_argmax=oa), 5)
+    trop.set_plan_cache_capacity(64)
+    # a small, host-bound instance of the same spec: where the lowering shows
+    As, Bs = synth.einsum_inputs(z=2, a=40, e=36, c=4, d=5)
+    Asd, Bsd = torch.from_numpy(As).cuda(), torch.from_numpy(Bs).cuda()
+    os_ = torch.empty((2, 36, 40), device="cuda")
+    oas = torch.empty((2, 36, 40), dtype=torch.int32, device="cuda")
+    small = lambda: trop.einsum("zacd,zdce->zea", Asd, Bsd, out=os_, out_argmax=oas)  # noqa: E731
+    t_small = timed(small, hb)
+    trop.set_plan_cache_capacity(0)
+    t_small_nocache = timed(small, hb)
+    trop.set_plan_cache_capacity(64)
     ops = 16 * 512 * 512 * 1024
     plan = trop.tree_plan([Ad, Bd], [(0, 1, [0, 1, 2, 3], [0, 3, 2, 4], [0, 4, 1])], "maxplus", o, [oa])
     tp = timed(plan.run, 5)
     plan.close()
     out["einsum_zacd,zdce->zea"] = {"ms": t * 1e3, "G semiring-ops/s": ops / t / 1e9, "ms_plan": tp * 1e3,
-                                    "G semiring-ops/s_plan": ops / tp / 1e9}
+                                    "G semiring-ops/s_plan": ops / tp / 1e9,
+                                    "ms_eager_plan_cache_off": t_nocache * 1e3,
+                                    "us_small_eager": t_small * 1e6, "us_small_eager_plan_cache_off": t_small_nocache * 1e6,
+                                    "note": "ms: eager calls with the plan cache (lowered once); small: the same spec "
+                                            "at z=2, a=40, e=36, c=4, d=5 (host bound)"}
     return out
 
 

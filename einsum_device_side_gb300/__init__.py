@@ -134,6 +134,9 @@ def load(path: str | None = None):
     del i32p
     _lib = lib
     _fc = _load_fastcall(path)
+    if _fc is not None:
+        _fc.set_torch_handles(torch.float32, torch.int32, torch.int64, torch.float64,
+                              _raw_stream or (lambda dev: torch.cuda.current_stream(dev).cuda_stream))
     return lib
 
 
@@ -236,9 +239,9 @@ def _check_argmax(am: torch.Tensor, out: torch.Tensor, like: torch.Tensor, conti
     or read back wrongly, so it is refused here."""
     if am.dtype != torch.int32:
         raise TropicalError(-4, f"argmax must be int32, got {am.dtype}")
-    if tuple(am.shape) != tuple(out.shape):
+    if am.shape != out.shape:
         raise TropicalError(-5, f"argmax shape {tuple(am.shape)} differs from out shape {tuple(out.shape)}")
-    if am.device != like.device:
+    if am.get_device() != like.get_device():
         raise TropicalError(-3, f"argmax is on {am.device}, operands on {like.device}")
     if contiguous and not am.is_contiguous():
         raise TropicalError(-1, "argmax must be contiguous (row-major in out's shape)")
@@ -258,18 +261,16 @@ def permute_trace(x: torch.Tensor, spec: str, semiring="maxplus", out: torch.Ten
             _check_argmax(am, out, x)
         elif argmax:
             am = torch.empty(out.shape, dtype=torch.int32, device=x.device)
-    st = _stream(stream, x)
     if _fc is not None:
-        # data_ptr() of an empty tensor may be 0: the C ABI accepts NULL data when an extent is 0
-        # (an unknown dtype goes as -1, which the C ABI refuses with TROP_ERR_DTYPE)
-        rc = _fc.permute_trace(x.data_ptr(), _DTYPES.get(x.dtype, -1), x.shape, x.stride(),
-                               _SPECS.get(spec) or _spec(spec), _sr(semiring), out.data_ptr(),
-                               _DTYPES.get(out.dtype, -1), out.shape, out.stride(),
-                               None if am is None else am.data_ptr(), st, False)
+        # the binding reads the tensors' data_ptr(), dtype, shape and stride() itself (data_ptr()
+        # of an empty tensor may be 0: the C ABI accepts NULL data when an extent is 0)
+        rc = _fc.permute_trace_t(x, spec, semiring, out, am, stream, False)
     else:
         dx, do = tensor_desc(x), tensor_desc(out)
-        rc = lib.tropical_permute_trace(ctypes.byref(dx), _spec(spec), _sr(semiring), ctypes.byref(do), _ptr(am), st)
-    _check(rc)
+        rc = lib.tropical_permute_trace(ctypes.byref(dx), _spec(spec), _sr(semiring), ctypes.byref(do), _ptr(am),
+                                        _stream(stream, x))
+    if rc:
+        _check(rc)
     return (out, am) if am is not None else out
 
 
@@ -282,14 +283,12 @@ def permute_trace_noalloc(x: torch.Tensor, spec: str, semiring="maxplus", *, out
     lib = _lib or load()
     if argmax is not None:
         _check_argmax(argmax, out, x)
-    st = _stream(stream, x)
     if _fc is not None:
-        rc = _fc.permute_trace(_ptr(x), _dt(x), x.shape, x.stride(), _spec(spec), _sr(semiring), _ptr(out),
-                               _dt(out), out.shape, out.stride(), _ptr(argmax), st, True)
+        rc = _fc.permute_trace_t(x, spec, semiring, out, argmax, stream, True)
     else:
         dx, do = tensor_desc(x), tensor_desc(out)
         rc = lib.tropical_permute_trace_noalloc(ctypes.byref(dx), _spec(spec), _sr(semiring), ctypes.byref(do),
-                                                _ptr(argmax), st)
+                                                _ptr(argmax), _stream(stream, x))
     _check(rc)
     return (out, argmax) if argmax is not None else out
 
@@ -303,15 +302,12 @@ def permute_pair(val: torch.Tensor, arg: torch.Tensor, spec: str, out_val=None, 
             out_val = torch.empty(shape, dtype=val.dtype, device=val.device)
         if out_arg is None:
             out_arg = torch.empty(shape, dtype=torch.int32, device=val.device)
-    st = _stream(stream, val)
     if _fc is not None:
-        rc = _fc.permute_pair(_ptr(val), _dt(val), val.shape, val.stride(), _ptr(arg), _dt(arg), arg.shape,
-                              arg.stride(), _spec(spec), _ptr(out_val), _dt(out_val), out_val.shape, out_val.stride(),
-                              _ptr(out_arg), _dt(out_arg), out_arg.shape, out_arg.stride(), st)
+        rc = _fc.permute_pair_t(val, arg, spec, out_val, out_arg, stream)
     else:
         a, b, c, d = tensor_desc(val), tensor_desc(arg), tensor_desc(out_val), tensor_desc(out_arg)
         rc = lib.tropical_permute_pair(ctypes.byref(a), ctypes.byref(b), _spec(spec), ctypes.byref(c),
-                                       ctypes.byref(d), st)
+                                       ctypes.byref(d), _stream(stream, val))
     _check(rc)
     return out_val, out_arg
 
@@ -348,8 +344,14 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
             raise ValueError("argmax must have the strides of out")
     sa, sb, so = A.stride(), B.stride(), out.stride()
     call = _fc.gemm if _fc is not None else lib.tropical_gemm_strided_batched_argmax
-    _check(call(_sr(semiring), _DTYPES[A.dtype], batch, M, N, K, _ptr(A), sa[0], sa[1], sa[2],
-                _ptr(B), sb[0], sb[1], sb[2], _ptr(out), so[0], so[1], so[2], _ptr(am), _stream(stream, out)))
+    dev = out.get_device()
+    st = stream.cuda_stream if stream is not None else (_raw_stream(dev) if dev >= 0 and _raw_stream
+                                                        else _stream(None, out))
+    rc = call(SEMIRINGS.get(semiring, semiring), _DTYPES[A.dtype], batch, M, N, K, A.data_ptr(), sa[0], sa[1],
+              sa[2], B.data_ptr(), sb[0], sb[1], sb[2], out.data_ptr(), so[0], so[1], so[2],
+              None if am is None else am.data_ptr(), st)
+    if rc:
+        _check(rc)
     return (out, am) if argmax else out
 
 

@@ -150,6 +150,153 @@ static PyObject* fc_einsum(PyObject* self, PyObject* const* a, Py_ssize_t nargs)
     return PyLong_FromLong(rc);
 }
 
+/* ---- tensor-taking variants: the same calls, reading each tensor's data_ptr(), dtype, shape and
+ * stride() through the C API (the tensors are treated as plain Python objects with those
+ * attributes), so the Python wrapper does no per-argument work.  set_torch_handles() gives the
+ * dtype objects (matched by identity: float32, int32, int64, float64 -> the trop_dtype codes)
+ * and the function returning a device's current raw stream. */
+static PyObject* g_dtype_obj[4];
+static PyObject* g_raw_stream;
+static PyObject *s_data_ptr, *s_shape, *s_stride, *s_dtype, *s_get_device, *s_cuda_stream;
+
+static PyObject* fc_set_torch_handles(PyObject* self, PyObject* const* a, Py_ssize_t nargs)
+{
+    (void)self;
+    if (check_nargs(nargs, 5, "set_torch_handles") < 0) return NULL;
+    for (int i = 0; i < 4; ++i) {
+        Py_XDECREF(g_dtype_obj[i]);
+        Py_INCREF(a[i]);
+        g_dtype_obj[i] = a[i];
+    }
+    Py_XDECREF(g_raw_stream);
+    Py_INCREF(a[4]);
+    g_raw_stream = a[4];
+    Py_RETURN_NONE;
+}
+
+static int obj_tensor(trop_tensor* t, PyObject* obj)
+{
+    PyObject* p = PyObject_CallMethodNoArgs(obj, s_data_ptr);
+    if (!p) return -1;
+    const int bad = as_ptr(p, &t->data) < 0;
+    Py_DECREF(p);
+    if (bad) return -1;
+    PyObject* dt = PyObject_GetAttr(obj, s_dtype);
+    if (!dt) return -1;
+    t->dtype = -1;  /* unknown dtypes reach the C ABI as -1, which it refuses */
+    for (int i = 0; i < 4; ++i)
+        if (dt == g_dtype_obj[i]) t->dtype = i;
+    Py_DECREF(dt);
+    PyObject* shape = PyObject_GetAttr(obj, s_shape);
+    if (!shape) return -1;
+    PyObject* stride = PyObject_CallMethodNoArgs(obj, s_stride);
+    if (!stride) {
+        Py_DECREF(shape);
+        return -1;
+    }
+    int rc = 0;
+    const Py_ssize_t n = PyTuple_Check(shape) && PyTuple_Check(stride) ? PyTuple_GET_SIZE(shape) : -1;
+    if (n < 0 || n > TROP_MAX_RANK || PyTuple_GET_SIZE(stride) != n) {
+        PyErr_SetString(PyExc_ValueError, "tensor rank above 32 or unreadable shape/stride");
+        rc = -1;
+    } else {
+        t->rank = (int32_t)n;
+        for (Py_ssize_t i = 0; i < n && rc == 0; ++i)
+            if (as_i64(PyTuple_GET_ITEM(shape, i), &t->shape[i]) < 0 || as_i64(PyTuple_GET_ITEM(stride, i), &t->stride[i]) < 0)
+                rc = -1;
+    }
+    Py_DECREF(shape);
+    Py_DECREF(stride);
+    return rc;
+}
+
+/* the stream handle: stream.cuda_stream, or the current raw stream of obj's device */
+static int obj_stream(PyObject* stream, PyObject* obj, void** out)
+{
+    PyObject* h;
+    if (stream != Py_None) {
+        h = PyObject_GetAttr(stream, s_cuda_stream);
+    } else {
+        if (!g_raw_stream) {
+            PyErr_SetString(PyExc_RuntimeError, "set_torch_handles was not called");
+            return -1;
+        }
+        PyObject* dev = PyObject_CallMethodNoArgs(obj, s_get_device);
+        if (!dev) return -1;
+        h = PyObject_CallOneArg(g_raw_stream, dev);
+        Py_DECREF(dev);
+    }
+    if (!h) return -1;
+    const int rc = as_ptr(h, out);
+    Py_DECREF(h);
+    return rc;
+}
+
+static int obj_semiring(PyObject* o, long* sr)
+{
+    if (PyUnicode_Check(o)) {
+        *sr = PyUnicode_CompareWithASCIIString(o, "maxplus") == 0    ? 0
+              : PyUnicode_CompareWithASCIIString(o, "minplus") == 0  ? 1
+              : PyUnicode_CompareWithASCIIString(o, "maxtimes") == 0 ? 2
+                                                                      : -1;
+        if (*sr < 0) {
+            PyErr_SetString(PyExc_KeyError, "semiring must be 'maxplus', 'minplus' or 'maxtimes'");
+            return -1;
+        }
+        return 0;
+    }
+    *sr = PyLong_AsLong(o);
+    return (*sr == -1 && PyErr_Occurred()) ? -1 : 0;
+}
+
+/* permute_trace_t(x, spec: str, semiring, out, argmax tensor or None, stream or None, no_alloc) */
+static PyObject* fc_permute_trace_t(PyObject* self, PyObject* const* a, Py_ssize_t nargs)
+{
+    (void)self;
+    if (check_nargs(nargs, 7, "permute_trace_t") < 0) return NULL;
+    trop_tensor in, out;
+    void *argmax = NULL, *stream;
+    long sr;
+    if (obj_tensor(&in, a[0]) < 0 || obj_tensor(&out, a[3]) < 0 || obj_semiring(a[2], &sr) < 0 ||
+        obj_stream(a[5], a[0], &stream) < 0)
+        return NULL;
+    if (a[4] != Py_None) {
+        PyObject* p = PyObject_CallMethodNoArgs(a[4], s_data_ptr);
+        if (!p) return NULL;
+        const int bad = as_ptr(p, &argmax) < 0;
+        Py_DECREF(p);
+        if (bad) return NULL;
+    }
+    const char* spec = PyUnicode_AsUTF8(a[1]);
+    const int no_alloc = PyObject_IsTrue(a[6]);
+    if (!spec || no_alloc < 0) return NULL;
+    int rc;
+    Py_BEGIN_ALLOW_THREADS
+    rc = no_alloc ? tropical_permute_trace_noalloc(&in, spec, (int)sr, &out, (int32_t*)argmax, stream)
+                  : tropical_permute_trace(&in, spec, (int)sr, &out, (int32_t*)argmax, stream);
+    Py_END_ALLOW_THREADS
+    return PyLong_FromLong(rc);
+}
+
+/* permute_pair_t(val, arg, spec: str, out_val, out_arg, stream or None) */
+static PyObject* fc_permute_pair_t(PyObject* self, PyObject* const* a, Py_ssize_t nargs)
+{
+    (void)self;
+    if (check_nargs(nargs, 6, "permute_pair_t") < 0) return NULL;
+    trop_tensor vi, ai, vo, ao;
+    void* stream;
+    if (obj_tensor(&vi, a[0]) < 0 || obj_tensor(&ai, a[1]) < 0 || obj_tensor(&vo, a[3]) < 0 ||
+        obj_tensor(&ao, a[4]) < 0 || obj_stream(a[5], a[0], &stream) < 0)
+        return NULL;
+    const char* spec = PyUnicode_AsUTF8(a[2]);
+    if (!spec) return NULL;
+    int rc;
+    Py_BEGIN_ALLOW_THREADS
+    rc = tropical_permute_pair(&vi, &ai, spec, &vo, &ao, stream);
+    Py_END_ALLOW_THREADS
+    return PyLong_FromLong(rc);
+}
+
 static PyObject* fc_last_error(PyObject* self, PyObject* const* a, Py_ssize_t nargs)
 {
     (void)self;
@@ -164,10 +311,26 @@ static PyMethodDef methods[] = {
     {"gemm", (PyCFunction)(void (*)(void))fc_gemm, METH_FASTCALL, "tropical_gemm_strided_batched_argmax"},
     {"einsum", (PyCFunction)(void (*)(void))fc_einsum, METH_FASTCALL, "tropical_einsum_pairwise"},
     {"last_error", (PyCFunction)(void (*)(void))fc_last_error, METH_FASTCALL, "tropical_last_error"},
+    {"set_torch_handles", (PyCFunction)(void (*)(void))fc_set_torch_handles, METH_FASTCALL,
+     "dtype objects (float32, int32, int64, float64) and the current-raw-stream function"},
+    {"permute_trace_t", (PyCFunction)(void (*)(void))fc_permute_trace_t, METH_FASTCALL,
+     "tropical_permute_trace on tensor objects"},
+    {"permute_pair_t", (PyCFunction)(void (*)(void))fc_permute_pair_t, METH_FASTCALL,
+     "tropical_permute_pair on tensor objects"},
     {NULL, NULL, 0, NULL},
 };
 
 static struct PyModuleDef module = {PyModuleDef_HEAD_INIT, "_fastcall", "hot entry points of the C ABI", -1,
                                     methods, NULL, NULL, NULL, NULL};
 
-PyMODINIT_FUNC PyInit__fastcall(void) { return PyModule_Create(&module); }
+PyMODINIT_FUNC PyInit__fastcall(void)
+{
+    s_data_ptr = PyUnicode_InternFromString("data_ptr");
+    s_shape = PyUnicode_InternFromString("shape");
+    s_stride = PyUnicode_InternFromString("stride");
+    s_dtype = PyUnicode_InternFromString("dtype");
+    s_get_device = PyUnicode_InternFromString("get_device");
+    s_cuda_stream = PyUnicode_InternFromString("cuda_stream");
+    if (!s_data_ptr || !s_shape || !s_stride || !s_dtype || !s_get_device || !s_cuda_stream) return NULL;
+    return PyModule_Create(&module);
+}

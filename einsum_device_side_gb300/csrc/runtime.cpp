@@ -115,8 +115,8 @@ FastDiv make_fastdiv(uint32_t d)
 // allocate (the allocation-free entry point never does), read without any synchronisation at
 // the start of every later call and reported once, then cleared.
 static std::mutex g_err_mu;
-static volatile uint32_t* g_err_host[64];
-static uint32_t* g_err_dev[64];
+static std::atomic<volatile uint32_t*> g_err_host[64];
+static std::atomic<uint32_t*> g_err_dev[64];
 static std::atomic<int> g_wait_mode{0};
 
 int device_error_word(uint32_t** dev_ptr)
@@ -125,8 +125,12 @@ int device_error_word(uint32_t** dev_ptr)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return set_error(TROP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    if (uint32_t* w = g_err_dev[dev].load(std::memory_order_acquire)) {
+        *dev_ptr = w;
+        return TROP_OK;
+    }
     std::lock_guard<std::mutex> lk(g_err_mu);
-    if (!g_err_dev[dev]) {
+    if (!g_err_dev[dev].load(std::memory_order_relaxed)) {
         void* h = nullptr;
         e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
         if (e != cudaSuccess) return cuda_error(e, "cudaHostAlloc (device error word)");
@@ -137,17 +141,17 @@ int device_error_word(uint32_t** dev_ptr)
             cudaFreeHost(h);
             return cuda_error(e, "cudaHostGetDevicePointer (device error word)");
         }
-        g_err_host[dev] = static_cast<volatile uint32_t*>(h);
-        g_err_dev[dev] = static_cast<uint32_t*>(d);
+        g_err_host[dev].store(static_cast<volatile uint32_t*>(h), std::memory_order_release);
+        g_err_dev[dev].store(static_cast<uint32_t*>(d), std::memory_order_release);
     }
-    *dev_ptr = g_err_dev[dev];
+    *dev_ptr = g_err_dev[dev].load(std::memory_order_relaxed);
     return TROP_OK;
 }
 
 // nonzero error word of `dev`: clear it and return the error to report
 static int take_device_error(int dev)
 {
-    volatile uint32_t* w = g_err_host[dev];
+    volatile uint32_t* w = g_err_host[dev].load(std::memory_order_acquire);
     if (!w || *w == 0) return TROP_OK;
     *w = 0;
     return set_error(TROP_ERR_CUDA,
@@ -169,6 +173,8 @@ static thread_local int t_no_alloc = 0;
 NoAllocScope::NoAllocScope() { ++t_no_alloc; }
 NoAllocScope::~NoAllocScope() { --t_no_alloc; }
 
+static std::atomic<bool> g_dev_done[64];  // set up, with its error word (lock-free fast path)
+
 int ensure_device(const DeviceInfo** info)
 {
     const bool may_allocate = t_no_alloc == 0;
@@ -176,6 +182,10 @@ int ensure_device(const DeviceInfo** info)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return set_error(TROP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    if (g_dev_done[dev].load(std::memory_order_acquire)) {
+        if (info) *info = &g_dev[dev];
+        return take_device_error(dev);
+    }
     std::lock_guard<std::mutex> lk(g_dev_mu);
     if (!g_dev_ready[dev]) {
         cudaDeviceProp p;
@@ -196,10 +206,11 @@ int ensure_device(const DeviceInfo** info)
         count_module_init();
     }
     if (info) *info = &g_dev[dev];
-    if (may_allocate && !g_err_dev[dev]) {
+    if (may_allocate && !g_err_dev[dev].load(std::memory_order_acquire)) {
         uint32_t* w = nullptr;
         TROP_TRY(device_error_word(&w));
     }
+    if (g_err_dev[dev].load(std::memory_order_acquire)) g_dev_done[dev].store(true, std::memory_order_release);
     return take_device_error(dev);
 }
 

@@ -38,17 +38,24 @@ namespace {
 
 constexpr int NT = 256;  // threads per block for the unary kernels
 
+// The axes a row-copy or transpose block iterates over, at most R of them.  Kernels come in
+// two capacities: REST_SMALL axes (nearly every merged layout) and MAXR; the small one keeps the
+// launch's parameter block near 400 bytes instead of 1.4 KB, which is measurable host time per
+// launch (about 0.25 us on GB300).
+constexpr int REST_SMALL = 8;
+template <int R>
 struct RestDims {
     int rank;
-    FastDiv div[MAXR];
-    int64_t s_in[MAXR];
-    int64_t s_out[MAXR];
-    int64_t s_in2[MAXR];
-    int64_t s_out2[MAXR];
+    FastDiv div[R];
+    int64_t s_in[R];
+    int64_t s_out[R];
+    int64_t s_in2[R];
+    int64_t s_out2[R];
 };
 
 // decode idx (< 2^31) over rest dims, last fastest
-__device__ __forceinline__ void decode_rest(const RestDims& r, uint32_t idx, int64_t& oi, int64_t& oo,
+template <int R>
+__device__ __forceinline__ void decode_rest(const RestDims<R>& r, uint32_t idx, int64_t& oi, int64_t& oo,
                                             int64_t& oi2, int64_t& oo2)
 {
     oi = oo = oi2 = oo2 = 0;
@@ -96,17 +103,18 @@ __global__ void k_gather(const T* __restrict__ in, T* __restrict__ out, const in
 }
 
 // ------------------------------------------------------------------ row copy
+template <int R>
 struct RowParams {
     uint32_t L;      // row length in elements
     uint32_t Lv;     // row length in vectors
     uint32_t total;  // rows * Lv
     FastDiv divLv;
-    RestDims rest;
+    RestDims<R> rest;
 };
 
-template <typename T, typename V, bool PAIR>
+template <typename T, typename V, bool PAIR, int R>
 __global__ void k_copy_rows(const T* __restrict__ in, T* __restrict__ out, const int32_t* __restrict__ in2,
-                            int32_t* __restrict__ out2, RowParams p)
+                            int32_t* __restrict__ out2, RowParams<R> p)
 {
     pdl_wait();
     pdl_signal();
@@ -132,6 +140,7 @@ __global__ void k_copy_rows(const T* __restrict__ in, T* __restrict__ out, const
 // elements (powers of two); its shape adapts when a chain is short (16 x 256
 // when the input's fastest axis has 16 elements; TB > 1 stacks several
 // outer-axis slices when both chains are short), so every tile stays full.
+template <int R>
 struct TransParams {
     uint32_t nI, nJ, nR;         // flattened chain extents, remaining-axes count
     uint32_t TI, TJ, TB;         // tile shape (powers of two)
@@ -146,7 +155,7 @@ struct TransParams {
     int vec_in;                          // input rows 16-byte aligned for vector loads
     int vec_out;                         // output rows 16-byte aligned for vector stores
     int sw;                              // shared-memory swizzle step (see tile_pos)
-    RestDims rest;
+    RestDims<R> rest;
 };
 
 // Shared-memory slot of tile element (x, c): x = slice * TJ + GJ index, in [0, L) with
@@ -179,10 +188,10 @@ struct TileCfg {
 #ifndef TROP_TRANSPOSE_CARVEOUT
 #define TROP_TRANSPOSE_CARVEOUT 60
 #endif
-template <typename T, bool PAIR>
+template <typename T, bool PAIR, int R>
 __global__ void __launch_bounds__(NT, PAIR ? 3 : TROP_TRANSPOSE_MINB) k_transpose(const T* __restrict__ in, T* __restrict__ out,
                                                   const int32_t* __restrict__ in2, int32_t* __restrict__ out2,
-                                                  TransParams p)
+                                                  TransParams<R> p)
 {
     pdl_wait();
     pdl_signal();
@@ -613,7 +622,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
     const bool small_idx = total < (int64_t(1) << 31);
     const int last = d.rank - 1;
 
-    auto fill_rest = [&](RestDims& r, int skip_mask) {
+    auto fill_rest = [&](auto& r, int skip_mask) {
         r.rank = 0;
         for (int i = 0; i < d.rank; ++i) {
             if (skip_mask & (1 << i)) continue;
@@ -628,39 +637,48 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
 
     if (d.rank >= 1 && small_idx && same_map && d.s_in[last] == 1 && d.s_out[last] == 1 && d.rank <= 31) {
         // ---- row copy
-        RowParams p{};
-        p.L = (uint32_t)d.size[last];
-        constexpr int W = 16 / sizeof(T);
-        bool vec = (p.L % W) == 0 && ((uintptr_t)in % 16) == 0 && ((uintptr_t)out % 16) == 0;
-        for (int i = 0; i < last; ++i) vec = vec && (d.s_in[i] % W) == 0 && (d.s_out[i] % W) == 0;
-        fill_rest(p.rest, 1 << last);
-        const int64_t rows = total / p.L;
-        if (vec) {
-            p.Lv = p.L / W;
-            p.total = (uint32_t)(rows * p.Lv);
-            p.divLv = make_fastdiv(p.Lv);
-            using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
-            int g = grid_for(p.total, NT, dev->sm_count);
-            if (pair) (void)launch_pdl(k_copy_rows<T, V, true>, g, NT, 0, s, in, out, in2, out2, p);
-            else (void)launch_pdl(k_copy_rows<T, V, false>, g, NT, 0, s, in, out, in2, out2, p);
-        } else {
-            p.Lv = p.L;
-            p.total = (uint32_t)total;
-            p.divLv = make_fastdiv(p.Lv);
-            int g = grid_for(p.total, NT, dev->sm_count);
-            if (pair) (void)launch_pdl(k_copy_rows<T, T, true>, g, NT, 0, s, in, out, in2, out2, p);
-            else (void)launch_pdl(k_copy_rows<T, T, false>, g, NT, 0, s, in, out, in2, out2, p);
+        auto launch_rows = [&](auto& p) {
+            p.L = (uint32_t)d.size[last];
+            constexpr int W = 16 / sizeof(T);
+            bool vec = (p.L % W) == 0 && ((uintptr_t)in % 16) == 0 && ((uintptr_t)out % 16) == 0;
+            for (int i = 0; i < last; ++i) vec = vec && (d.s_in[i] % W) == 0 && (d.s_out[i] % W) == 0;
+            fill_rest(p.rest, 1 << last);
+            constexpr int R = sizeof(p.rest.div) / sizeof(p.rest.div[0]);
+            const int64_t rows = total / p.L;
+            if (vec) {
+                p.Lv = p.L / W;
+                p.total = (uint32_t)(rows * p.Lv);
+                p.divLv = make_fastdiv(p.Lv);
+                using V = typename std::conditional<sizeof(T) == 8, longlong2, int4>::type;
+                int g = grid_for(p.total, NT, dev->sm_count);
+                if (pair) (void)launch_pdl(k_copy_rows<T, V, true, R>, g, NT, 0, s, in, out, in2, out2, p);
+                else (void)launch_pdl(k_copy_rows<T, V, false, R>, g, NT, 0, s, in, out, in2, out2, p);
+            } else {
+                p.Lv = p.L;
+                p.total = (uint32_t)total;
+                p.divLv = make_fastdiv(p.Lv);
+                int g = grid_for(p.total, NT, dev->sm_count);
+                if (pair) (void)launch_pdl(k_copy_rows<T, T, true, R>, g, NT, 0, s, in, out, in2, out2, p);
+                else (void)launch_pdl(k_copy_rows<T, T, false, R>, g, NT, 0, s, in, out, in2, out2, p);
+            }
+            return check_launch("k_copy_rows");
+        };
+        if (d.rank - 1 <= REST_SMALL) {
+            RowParams<REST_SMALL> p{};
+            return launch_rows(p);
         }
-        return check_launch("k_copy_rows");
+        RowParams<MAXR> p{};
+        return launch_rows(p);
     }
 
     int din = -1;
     for (int i = 0; i < d.rank; ++i)
         if (d.s_in[i] == 1) din = i;
-    if (d.rank >= 2 && small_idx && same_map && d.s_out[last] == 1 && din >= 0 && din != last) {
-        // ---- tiled transpose over two axis chains
+    // ---- tiled transpose over two axis chains (the rest axes fit the small parameter block
+    // whenever the whole layout has at most REST_SMALL axes); returns 1 when it does not apply
+    auto try_transpose = [&](auto& p) -> int {
+        constexpr int R = sizeof(p.rest.div) / sizeof(p.rest.div[0]);
         constexpr int CHAIN_I = TileCfg<sizeof(T)>::TIMAX, CHAIN_J = TileCfg<sizeof(T)>::TJMAX;
-        TransParams p{};
         int used = 0;
         // output-fastest chain
         int gj[4], ngj = 0;
@@ -764,10 +782,22 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             // at least W so the storer's W-wide runs stay whole
             p.sw = (int)std::max<int64_t>(W, (int64_t)32 * W / ti_);
             const int g = (int)std::min<int64_t>(tiles, (int64_t)dev->sm_count * 64);
-            if (pair) (void)launch_pdl(k_transpose<T, true>, g, NT, 0, s, in, out, in2, out2, p);
-            else (void)launch_pdl(k_transpose<T, false>, g, NT, 0, s, in, out, in2, out2, p);
+            if (pair) (void)launch_pdl(k_transpose<T, true, R>, g, NT, 0, s, in, out, in2, out2, p);
+            else (void)launch_pdl(k_transpose<T, false, R>, g, NT, 0, s, in, out, in2, out2, p);
             return check_launch("k_transpose");
         }
+        return 1;
+    };
+    if (d.rank >= 2 && small_idx && same_map && d.s_out[last] == 1 && din >= 0 && din != last) {
+        int rc;
+        if (d.rank <= REST_SMALL) {
+            TransParams<REST_SMALL> p{};
+            rc = try_transpose(p);
+        } else {
+            TransParams<MAXR> p{};
+            rc = try_transpose(p);
+        }
+        if (rc != 1) return rc;
     }
 
     // ---- generic gather
@@ -924,10 +954,10 @@ int register_unary_kernels()
     const void* ks[] = {
         (const void*)k_gather<int32_t, false>, (const void*)k_gather<int64_t, false>,
         (const void*)k_gather<int32_t, true>, (const void*)k_gather<int64_t, true>,
-        (const void*)k_copy_rows<int32_t, int4, false>, (const void*)k_copy_rows<int64_t, longlong2, false>,
-        (const void*)k_copy_rows<int32_t, int4, true>, (const void*)k_copy_rows<int32_t, int32_t, false>,
-        (const void*)k_transpose<int32_t, false>, (const void*)k_transpose<int64_t, false>,
-        (const void*)k_transpose<int32_t, true>, (const void*)k_transpose<int64_t, true>,
+        (const void*)k_copy_rows<int32_t, int4, false, REST_SMALL>, (const void*)k_copy_rows<int64_t, longlong2, false, REST_SMALL>,
+        (const void*)k_copy_rows<int32_t, int4, true, REST_SMALL>, (const void*)k_copy_rows<int32_t, int32_t, false, REST_SMALL>,
+        (const void*)k_transpose<int32_t, false, REST_SMALL>, (const void*)k_transpose<int64_t, false, REST_SMALL>,
+        (const void*)k_transpose<int32_t, true, REST_SMALL>, (const void*)k_transpose<int64_t, true, REST_SMALL>,
         (const void*)k_reduce_thread<TROP_MAXPLUS, float>, (const void*)k_reduce_block<TROP_MAXPLUS, float>,
         (const void*)k_reduce_tile<TROP_MAXPLUS, float, 8>, (const void*)k_reduce_tile<TROP_MAXPLUS, float, 32>,
         (const void*)k_reduce_combine<TROP_MAXPLUS, float>,
@@ -937,8 +967,10 @@ int register_unary_kernels()
         if (e != cudaSuccess) return cuda_error(e, "cudaFuncGetAttributes (unary kernels)");
     }
     // shared-memory carveout of the transpose (see TROP_TRANSPOSE_CARVEOUT)
-    const void* kt[] = {(const void*)k_transpose<int32_t, false>, (const void*)k_transpose<int64_t, false>,
-                        (const void*)k_transpose<int32_t, true>, (const void*)k_transpose<int64_t, true>};
+    const void* kt[] = {(const void*)k_transpose<int32_t, false, REST_SMALL>, (const void*)k_transpose<int64_t, false, REST_SMALL>,
+                        (const void*)k_transpose<int32_t, true, REST_SMALL>, (const void*)k_transpose<int64_t, true, REST_SMALL>,
+                        (const void*)k_transpose<int32_t, false, MAXR>, (const void*)k_transpose<int64_t, false, MAXR>,
+                        (const void*)k_transpose<int32_t, true, MAXR>, (const void*)k_transpose<int64_t, true, MAXR>};
     for (const void* k : kt) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, TROP_TRANSPOSE_CARVEOUT);
         if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (transpose carveout)");
