@@ -147,6 +147,9 @@ def einsum(spec, a: np.ndarray, b: np.ndarray | None = None, semiring: int = MAX
                            len(lo), _arr(ctypes.c_int32, lo), out.ctypes.data,
                            arg.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                            samp_ptr, ns, int(nthreads))
+    if rc == -5:
+        raise OverflowError("an integer tropical product falls outside the operand type "
+                            "(the inputs violate the no-overflow precondition)")
     if rc != 0:
         raise ValueError(f"oracle_einsum failed with code {rc}")
     return out, arg

@@ -28,7 +28,14 @@
  *        max-plus : (+) = max, (x) = +, zero = -inf
  *        min-plus : (+) = min, (x) = +, zero = +inf
  *        max-times: (+) = max, (x) = *, zero = 0   (nonnegative domain)
- *    For i32/i64 (unary only) the zero is the type's min / max / 0.
+ *    Integer operands (i32 / i64) take the same definition in exact integer
+ *    arithmetic: each tropical product a + b (or a * b) is the exact integer,
+ *    computed here in a wider type, and the inputs must make every product
+ *    that is formed fit the operand type -- the pages fix no overflow policy
+ *    for integer contractions, and this precondition is the reading taken (a
+ *    product outside the type makes the oracle refuse the input with
+ *    E_OVERFLOW instead of guessing).  The zero is the type's min / max / 0;
+ *    it is only ever the start of the running (+), never an operand value.
  *    f64 (unary and pairwise) is the same definition in binary64: the
  *    tropical-gemm PR #35 "CPU Dtype Handling" commit supports f32 and f64
  *    ("no more silent precision loss"); each product rounds once in binary64.
@@ -74,7 +81,7 @@
 
 enum { SR_MAXPLUS = 0, SR_MINPLUS = 1, SR_MAXTIMES = 2 };
 enum { DT_F32 = 0, DT_I32 = 1, DT_I64 = 2, DT_F64 = 3 };
-enum { OK = 0, E_ARG = -1, E_SHAPE = -2, E_DTYPE = -3, E_NOMEM = -4 };
+enum { OK = 0, E_ARG = -1, E_SHAPE = -2, E_DTYPE = -3, E_NOMEM = -4, E_OVERFLOW = -5 };
 
 #define MAXLAB 64
 
@@ -129,6 +136,21 @@ static int i64_better(int sr, int64_t t, int64_t best)
     return sr == SR_MINPLUS ? (t < best) : (t > best);
 }
 
+/* exact integer tropical product; *fits = 0 when it lies outside the operand type */
+static int64_t int_otimes(int sr, int dtype, int64_t a, int64_t b, int* fits)
+{
+    const __int128 p = sr == SR_MAXTIMES ? (__int128)a * (__int128)b : (__int128)a + (__int128)b;
+    const __int128 lo = dtype == DT_I32 ? (__int128)INT32_MIN : (__int128)INT64_MIN;
+    const __int128 hi = dtype == DT_I32 ? (__int128)INT32_MAX : (__int128)INT64_MAX;
+    *fits = p >= lo && p <= hi;
+    return (int64_t)p;
+}
+
+static int64_t int_load(int dtype, const void* base, int64_t off)
+{
+    return dtype == DT_I32 ? (int64_t)((const int32_t*)base)[off] : ((const int64_t*)base)[off];
+}
+
 /* ------------------------------------------------------------------------ */
 /* label bookkeeping                                                         */
 
@@ -178,7 +200,7 @@ static int64_t offset_of(int n, const int* ids, const int64_t* stride, const int
 /*
  * oracle_einsum
  *   sr         semiring
- *   dtype      element type of A, B and out (pairwise: f32 only)
+ *   dtype      element type of A, B and out (f32, i32, i64 or f64)
  *   nA, labA, shA, stA, A   first operand: rank, label per axis, extents,
  *                           strides in elements, base pointer
  *   nB < 0  -> unary (B ignored); otherwise the second operand likewise
@@ -205,7 +227,6 @@ int oracle_einsum(int sr, int dtype,
     if (sr < 0 || sr > 2 || nA < 0 || nA > MAXLAB || nO < 0 || nO > MAXLAB || nB > MAXLAB) return E_ARG;
     if (dtype < 0 || dtype > 3) return E_DTYPE;
     const int pairwise = nB >= 0;
-    if (pairwise && dtype != DT_F32 && dtype != DT_F64) return E_DTYPE;
 
     labels_t t;
     t.n = 0;
@@ -251,6 +272,7 @@ int oracle_einsum(int sr, int dtype,
     const int64_t nR_assign = count_of(R, nR, t.size);
     for (int64_t s = 0; samples && s < nsamples; ++s)
         if (samples[s] < 0 || samples[s] >= total) return E_ARG;
+    int overflow = 0; /* an integer product outside the operand type was formed */
 
 #ifdef _OPENMP
     if (nthreads <= 0) nthreads = omp_get_max_threads();
@@ -323,9 +345,28 @@ int oracle_einsum(int sr, int dtype,
             if (nK_assign > 0) {
                 for (int i = 0; i < nK; ++i) val[K[i]] = 0;
                 do {
-                    int64_t off = offset_of(nA, idA, stA, val);
-                    int64_t v = dtype == DT_I32 ? (int64_t)((const int32_t*)A)[off]
-                                                : ((const int64_t*)A)[off];
+                    int64_t v;
+                    if (!pairwise) {
+                        v = int_load(dtype, A, offset_of(nA, idA, stA, val));
+                    } else {
+                        v = i64_zero(sr, dtype);
+                        if (nR_assign > 0) {
+                            for (int i = 0; i < nR; ++i) val[R[i]] = 0;
+                            do {
+                                const int64_t a = int_load(dtype, A, offset_of(nA, idA, stA, val));
+                                const int64_t b = int_load(dtype, B, offset_of(nB, idB, stB, val));
+                                int fits;
+                                const int64_t p = int_otimes(sr, dtype, a, b, &fits);
+                                if (!fits) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                                    overflow = 1;
+                                }
+                                if (i64_better(sr, p, v)) v = p;
+                            } while (odometer_next(R, nR, t.size, val));
+                        }
+                    }
                     if (i64_better(sr, v, best)) { best = v; idx = (int32_t)k; }
                     ++k;
                 } while (odometer_next(K, nK, t.size, val));
@@ -335,7 +376,7 @@ int oracle_einsum(int sr, int dtype,
         }
         if (argmax) argmax[w] = idx;
     }
-    return OK;
+    return overflow ? E_OVERFLOW : OK;
 }
 
 /* ------------------------------------------------------------------------ */
