@@ -335,6 +335,16 @@ def secondary(trop, torch, pk, reps=20):
                                "frac_f64_nominal": ops / t / f64_peak,
                                "note": "peak = nominal binary64 rate (%.2f TFLOP/s, an FMA counted as 2) / 2 = "
                                        "one double add per semiring op" % F64_TFLOPS_NOMINAL}
+    # the same batched GEMM on int32 operands (exact integer products), max-plus with argmax
+    ia = synth.uniform_int(synth.seed_for(synth.W_GEMM_BATCHED, 8), (64, 256, 256), -1000, 1000, np.int32)
+    ib = synth.uniform_int(synth.seed_for(synth.W_GEMM_BATCHED, 9), (64, 256, 256), -1000, 1000, np.int32)
+    iad, ibd = torch.from_numpy(ia).cuda(), torch.from_numpy(ib).cuda()
+    ic = torch.empty((64, 256, 256), dtype=torch.int32, device="cuda")
+    ii = torch.empty((64, 256, 256), dtype=torch.int32, device="cuda")
+    t = timed(lambda: trop.gemm(iad, ibd, 0, out=ic, out_argmax=ii), max(3, reps // 4))
+    ops = 64 * 256 ** 3
+    out["gemm_i32_b64x256"] = {"us": t * 1e6, "G semiring-ops/s": ops / t / 1e9,
+                               "note": "k_gemm_int, 4 x 4 outputs per thread, strict compare per term"}
     A, B = synth.einsum_inputs()
     Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     o = torch.empty((16, 512, 512), device="cuda")

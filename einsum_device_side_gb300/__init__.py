@@ -330,8 +330,9 @@ def gemm(A: torch.Tensor, B: torch.Tensor, semiring="maxplus", argmax: bool = Tr
     N = B.shape[2]
     if B.shape[1] != K:
         raise ValueError("inner extents differ")
-    if A.dtype not in (torch.float32, torch.float64) or B.dtype != A.dtype:
-        raise TypeError(f"gemm needs two float32 or two float64 operands, got {A.dtype} and {B.dtype}")
+    if A.dtype not in _DTYPES or B.dtype != A.dtype:
+        raise TypeError(f"gemm needs two operands of one dtype (float32, float64, int32, int64), "
+                        f"got {A.dtype} and {B.dtype}")
     if out is None:
         out = torch.empty((batch, M, N), dtype=A.dtype, device=A.device)
     elif out.dtype != A.dtype:

@@ -21,7 +21,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtropical_gb300.so")
-SOURCES = ["runtime.cpp", "api.cpp", "unary.cu", "gemm.cu", "gemm64.cu", "backtrack.cu", "backward.cu", "noalloc.cu"]
+SOURCES = ["runtime.cpp", "api.cpp", "unary.cu", "gemm.cu", "gemm64.cu", "gemm_int.cu", "backtrack.cu", "backward.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
           "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=false",

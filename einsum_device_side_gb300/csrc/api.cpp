@@ -31,6 +31,7 @@ int register_unary_kernels();
 int register_gemm_kernels();
 int register_backward_kernels();
 int register_gemm64_kernels();
+int register_gemm_int_kernels();
 int register_backtrack_kernels();
 int launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s);
 
@@ -40,6 +41,7 @@ int register_kernels_for_device()
     TROP_TRY(register_gemm_kernels());
     TROP_TRY(register_backward_kernels());
     TROP_TRY(register_gemm64_kernels());
+    TROP_TRY(register_gemm_int_kernels());
     TROP_TRY(register_backtrack_kernels());
     return TROP_OK;
 }
@@ -423,8 +425,8 @@ std::vector<int32_t> pick_group(const std::vector<int32_t>& cands, const View& v
 int lower_pairwise(int sr, const View& A0, const View& B0, const int32_t* lo, int ro, const int64_t* ostride,
                    bool has_argmax, LoweredPair& L)
 {
-    if ((A0.dtype != TROP_F32 && A0.dtype != TROP_F64) || B0.dtype != A0.dtype)
-        return set_error(TROP_ERR_DTYPE, "pairwise tropical einsum needs two f32 or two f64 operands");
+    if (dtype_bytes(A0.dtype) == 0 || B0.dtype != A0.dtype)
+        return set_error(TROP_ERR_DTYPE, "pairwise tropical einsum needs two operands of one dtype (f32, f64, i32, i64)");
     View A, B;
     TROP_TRY(unique_view(A0, A));
     TROP_TRY(unique_view(B0, B));
@@ -891,7 +893,7 @@ extern "C" int tropical_gemm_strided_batched_argmax(int semiring, int dtype, int
 {
     clear_error();
     if (semiring < 0 || semiring > 2) return set_error(TROP_ERR_INVALID_ARG, "unknown semiring %d", semiring);
-    if (dtype != TROP_F32 && dtype != TROP_F64) return set_error(TROP_ERR_DTYPE, "tropical GEMM supports f32 and f64");
+    if (dtype_bytes(dtype) == 0) return set_error(TROP_ERR_DTYPE, "tropical GEMM: unknown dtype %d", dtype);
     if (batch < 0 || M < 0 || N < 0 || K < 0) return set_error(TROP_ERR_INVALID_ARG, "negative extent");
     if (argmax && K - 1 > INT32_MAX)
         return set_error(TROP_ERR_OVERFLOW, "K = %lld does not fit an int32 argmax", (long long)K);
@@ -978,7 +980,7 @@ extern "C" int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, 
     TROP_TRY(tensor_labels_check(A, ra, "A"));
     TROP_TRY(tensor_labels_check(B, rb, "B"));
     TROP_TRY(tensor_labels_check(out, ro, "out"));
-    if (out->dtype != TROP_F32 && out->dtype != TROP_F64) return set_error(TROP_ERR_DTYPE, "out must be f32 or f64");
+    if (dtype_bytes(out->dtype) == 0) return set_error(TROP_ERR_DTYPE, "out has an unknown dtype %d", out->dtype);
     if (A->dtype != out->dtype || B->dtype != out->dtype)
         return set_error(TROP_ERR_DTYPE, "A, B and out must share one dtype");
     TROP_TRY(ensure_device(nullptr));
@@ -1103,8 +1105,8 @@ int tree_shapes(int n_inputs, const trop_tensor* inputs, int n_nodes, const trop
         const int nops = nd.rhs < 0 ? 1 : 2;
         if (nd.n_out < 0 || nd.n_out > MAXR || (nd.n_out > 0 && !nd.out_labels))
             return set_error(TROP_ERR_INVALID_ARG, "node %d: bad output labels", j);
-        if (nops == 2 && dtype != TROP_F32 && dtype != TROP_F64)
-            return set_error(TROP_ERR_DTYPE, "node %d: binary nodes need f32 or f64", j);
+        if (nops == 2 && dtype_bytes(dtype) == 0)
+            return set_error(TROP_ERR_DTYPE, "node %d: unknown dtype %d", j, dtype);
         int32_t all_lab[2 * MAXR];
         int64_t all_size[2 * MAXR];
         int nall = 0;

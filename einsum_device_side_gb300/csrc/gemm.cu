@@ -1939,6 +1939,10 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
         snprintf(buf, n, " route=tiled_f64");
         return;
     }
+    if (g1.dtype == TROP_I32 || g1.dtype == TROP_I64) {
+        snprintf(buf, n, " route=tiled_int");
+        return;
+    }
     bool swap = false;
     const Route r = choose(g0, swap);
     const GemmDesc g = swap ? swapped(g0) : g0;
@@ -1993,6 +1997,10 @@ int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name)
     if (g.dtype == TROP_F64) {
         if (kernel_name) *kernel_name = "k_gemm_tiled_f64";
         return launch_gemm_f64(g, s);
+    }
+    if (g.dtype == TROP_I32 || g.dtype == TROP_I64) {
+        if (kernel_name) *kernel_name = "k_gemm_int";
+        return launch_gemm_int(g, s);
     }
     if (g.dtype != TROP_F32) return set_error(TROP_ERR_DTYPE, "tropical GEMM: unsupported dtype %d", g.dtype);
     const bool arg = g.I != nullptr;

@@ -173,7 +173,7 @@ int noalloc_scratch(void** ptr, size_t* bytes);
 // Strided-batched tropical GEMM with a multi-dimensional batch.
 struct GemmDesc {
     int semiring;
-    int dtype;  // TROP_F32 (gemm.cu) or TROP_F64 (gemm64.cu); A, B and C share it
+    int dtype;  // TROP_F32 (gemm.cu), TROP_F64 (gemm64.cu), TROP_I32 / TROP_I64 (gemm_int.cu); A, B, C share it
     int64_t M, N, K;
     const void* A;
     const void* B;
@@ -187,6 +187,8 @@ struct GemmDesc {
 int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name);
 // The binary64 GEMM (gemm64.cu); launch_gemm forwards TROP_F64 descriptors here.
 int launch_gemm_f64(const GemmDesc& g, cudaStream_t s);
+// The integer GEMM (gemm_int.cu); launch_gemm forwards TROP_I32 / TROP_I64 descriptors here.
+int launch_gemm_int(const GemmDesc& g, cudaStream_t s);
 // The route launch_gemm takes for g (kernel, operand swap, vector width, staging) as text.
 void describe_gemm(const GemmDesc& g, char* buf, size_t n);
 

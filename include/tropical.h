@@ -39,6 +39,13 @@
  * exact, so results do not depend on evaluation order.  f64 operands: I52
  * "Resolved design for step 3" kernel (a) lists f32/f64 operands; PR35
  * "Summary of latest fixes" handles f32 and f64 on its CPU path.
+ * Integer operands (TROP_I32, TROP_I64; I52 "Resolved design for step 3"
+ * kernel (a) lists integer types, PR35 "Summary of latest fixes" handles
+ * dtypes beyond f32): each (x) is the exact integer a + b (a * b for
+ * max-times) and every product formed must fit the operand type -- the pages
+ * fix no overflow policy, so this precondition is the library's reading (a
+ * product outside the type wraps; not checked).  The zeros are the type's
+ * min / max / 0 and only start the running (+).
  * Argmax: the smallest contracted linear index that reaches the result; 0
  * when no term beats the semiring zero (e.g. an empty contraction).
  * Preconditions (not checked): no NaN; no -0.0; max-plus operands below
@@ -199,8 +206,9 @@ int tropical_permute_pair(const trop_tensor* val_in, const trop_tensor* arg_in, 
  *   C[b,m,n] = (+)_{k<K} A[b,m,k] (x) B[b,k,n]
  *   argmax[b,m,n] = smallest k reaching C[b,m,n] (0 if none beats zero).
  * Element (b,m,k) of A is A[b*sAb + m*sAm + k*sAk]; likewise B and C.
- * argmax (nullable, int32) uses C's strides.  dtype: TROP_F32 or TROP_F64,
- * shared by A, B and C (the pointers carry no type: the caller guarantees it).
+ * argmax (nullable, int32) uses C's strides.  dtype: TROP_F32, TROP_F64,
+ * TROP_I32 or TROP_I64, shared by A, B and C (the pointers carry no type: the
+ * caller guarantees it).
  * Errors: INVALID_ARG (negative extent, null pointer with nonzero extent),
  *         DTYPE, OVERFLOW (K > INT32_MAX with argmax), HOST_POINTER,
  *         DEVICE_MISMATCH, CUDA. */
@@ -249,7 +257,8 @@ int tropical_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, in
  * repeated call skips it; trop_stats counts hits and misses.  The contraction
  * tree executor's nodes use the same cache.
  *   out[o] = (+) over all assignments of the labels absent from the output
- *            of A[..] (x) B[..]   (A, B and out all f32 or all f64)
+ *            of A[..] (x) B[..]   (A, B and out of one dtype: f32, f64, i32
+ *            or i64)
  *   argmax[o] = row-major linear index over the CONTRACTED labels (present
  *            in both operands, absent from the output), ordered by first
  *            appearance in A's spec, of the smallest index reaching out[o].
@@ -276,7 +285,7 @@ int tropical_einsum_pairwise(const char* spec, const trop_tensor* A, const trop_
  *   j receives node j's argmax (contiguous, node output shape), with the
  *   meaning of tropical_einsum_pairwise (binary) or tropical_permute_trace
  *   (unary).
- * All inputs must share out's dtype; binary nodes need f32 or f64.
+ * All inputs must share out's dtype (f32, f64, i32 or i64).
  * Errors: as the pairwise/unary calls, plus INVALID_ARG for bad operand ids.
  * Validation of the whole tree happens before the first launch. */
 int tropical_contract_tree(int n_inputs, const trop_tensor* inputs, int n_nodes,
