@@ -14,7 +14,9 @@
 // walked in increasing order by the lanes that own its bins, one lane per
 // (line, bin range), adding into bins of its own in shared memory -- every bin
 // has one writer adding in the stated order, so every sum is the sequential
-// one, bit for bit.  A CTA takes 32 lines; its 8 warps split a span of 256
+// one, bit for bit.  For max-times both gradients take k_route_match instead
+// (a warp per line, the lanes of one bin applied in step order), which keeps
+// its gathers of the other operand in flight across a whole warp.  A CTA takes 32 lines; its 8 warps split a span of 256
 // bins and all walk the same staged block (32 lines x 32 steps of argmax and
 // dC), which the CTA loads coalesced along whichever index is contiguous and
 // double buffers.  Longer contractions repeat the walk per 256-bin span.  dA
@@ -35,6 +37,9 @@ namespace {
 
 #ifndef TROP_ROUTE_WARPS
 #define TROP_ROUTE_WARPS 4
+#endif
+#ifndef TROP_ROUTE_MATCH
+#define TROP_ROUTE_MATCH 1
 #endif
 constexpr int BW_WARPS = TROP_ROUTE_WARPS, BW_THREADS = BW_WARPS * 32;
 constexpr int BW_SPAN = 256;                // bins a CTA covers per walk
@@ -344,6 +349,165 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
     }
 }
 
+// One warp per output line, RM_WARPS lines per CTA, each line's RM_SPAN bins in shared memory
+// ([line][bin], rows padded to RM_LD).  A line's steps are taken RM_CHUNK at a time, every load
+// of a chunk issued before any of it is used (a warp keeps 2 KB in flight, which the HBM latency
+// needs): read directly into registers when a line's steps are contiguous (the rows of dA: lane
+// i holds steps i, i + 32, ...), otherwise staged by the CTA through shared memory, loaded
+// coalesced along the lines (the columns of dB).  Lane i of warp w then takes step s0 + i of
+// line w, 32 steps at a time.  Lanes whose steps hit the same bin find each other with
+// __match_any_sync; a lane's rank in its group (the lanes below it) is its place in step order,
+// and the group's adds are applied rank by rank, so every bin still adds its terms in increasing
+// step order with one rounding each -- the sequential sum, bit for bit, with 1 KB of bins per
+// line.  Max-times multiplies each term by the other operand's entry at the winner first (a
+// gather, issued for the whole chunk before the first term is applied).
+#ifndef TROP_RM_WARPS
+#define TROP_RM_WARPS 16
+#endif
+constexpr int RM_WARPS = TROP_RM_WARPS, RM_THREADS = RM_WARPS * 32;
+constexpr int RM_SPAN = 256;                 // bins per line and walk
+constexpr int RM_LD = RM_SPAN + 1;           // [line][bin] rows: the column-wise output read is conflict-free
+constexpr int RM_CHUNK = 256;                // steps of a line loaded together
+constexpr int RM_NB = RM_CHUNK / 32;         // batches per chunk
+constexpr int RM_CLD = RM_CHUNK + 1;         // staged [line][step] rows
+constexpr int RM_PER = RM_CHUNK / 32;        // staged elements per thread and array (RM_CHUNK x RM_WARPS / RM_THREADS)
+constexpr size_t RM_SMEM =
+    sizeof(float) * ((size_t)RM_WARPS * RM_LD + 2 * (size_t)RM_WARPS * RM_CLD) + 2 * RM_WARPS * sizeof(int64_t);
+static_assert(RM_WARPS == 8 || RM_WARPS == 16 || RM_WARPS == 32, "lines per CTA");
+
+template <bool MUL>
+__global__ void __launch_bounds__(RM_THREADS) k_route_match(RouteParams p)
+{
+    extern __shared__ __align__(16) float sm_match[];
+    if (!p.late_wait) pdl_wait();
+    pdl_signal();
+    if ((int)blockIdx.y >= p.njobs) {
+        if (p.late_wait) pdl_wait();
+        return;
+    }
+    // the job's fields in registers once (indexing the parameter block by blockIdx.y would
+    // reload them from the constant bank at every use)
+    const RouteJob j = blockIdx.y == 0 ? p.job[0] : p.job[1];
+    const int64_t K = p.K, S = j.S, X = j.X;
+    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+    float* bins = sm_match;                                                        // [RM_WARPS][RM_LD]
+    int* ck = reinterpret_cast<int*>(sm_match + RM_WARPS * RM_LD);                 // [RM_WARPS][RM_CLD]
+    float* cg = sm_match + RM_WARPS * RM_LD + RM_WARPS * RM_CLD;                   // [RM_WARPS][RM_CLD]
+    int64_t* line_i = reinterpret_cast<int64_t*>(sm_match + RM_WARPS * RM_LD + 2 * RM_WARPS * RM_CLD);
+    int64_t* line_p = line_i + RM_WARPS;
+    const int64_t lines = p.nbatch * X;
+    const bool direct = j.sIs == 1 && j.sGs == 1;  // a line's steps are contiguous
+    const unsigned lanes_below = (1u << l) - 1u;
+    float* mybins = bins + w * RM_LD;
+    for (int64_t base = (int64_t)blockIdx.x * RM_WARPS; base < lines; base += (int64_t)gridDim.x * RM_WARPS) {
+        __syncthreads();  // the previous group's readers of the tables, stages and bins are done
+        if (tid < RM_WARPS) {
+            const int64_t o = base + tid;
+            const int64_t b = o < lines ? o / X : 0, x = o < lines ? o - b * X : 0;
+            line_i[tid] = o < lines ? b * j.sIb + x * j.sIx : -1;
+            line_p[tid] = b * j.sPb;
+        }
+        __syncthreads();
+        const int64_t my_off = line_i[w];
+        const bool my_valid = my_off >= 0;
+        const float* Pl = MUL ? j.P + line_p[w] : nullptr;
+        for (int64_t kc = 0; kc < K; kc += RM_SPAN) {
+            const int kn = (int)min((int64_t)RM_SPAN, K - kc);
+            const int kc32 = (int)kc;
+            __syncthreads();  // the previous span's output reads of the bins are done
+            for (int k = l; k < RM_SPAN; k += 32) mybins[k] = 0.0f;
+            __syncwarp();
+            for (int64_t c0 = 0; c0 < S; c0 += RM_CHUNK) {
+                // ---- the chunk's steps: this lane's RM_NB steps c0 + 32 t + l
+                int rk[RM_NB];
+                float rg[RM_NB];
+                if (direct) {
+                    const int32_t* ip = j.I + (my_valid ? my_off : 0) + c0 + l;
+                    const float* gp = j.G + (my_valid ? my_off : 0) + c0 + l;
+#pragma unroll
+                    for (int t = 0; t < RM_NB; ++t) {
+                        const bool in = my_valid && c0 + 32 * t + l < S;
+                        rk[t] = in ? __ldg(ip + 32 * t) : -1;
+                        rg[t] = in ? __ldg(gp + 32 * t) : 0.0f;
+                    }
+                } else {
+                    // staged: element e of the [RM_WARPS][RM_CHUNK] block, lines fastest
+                    int sk[RM_PER];
+                    float sg[RM_PER];
+#pragma unroll
+                    for (int u = 0; u < RM_PER; ++u) {
+                        const int e = tid + u * RM_THREADS, r = e % RM_WARPS, t = e / RM_WARPS;
+                        const int64_t off = line_i[r], st = c0 + t;
+                        const bool in = off >= 0 && st < S;
+                        sk[u] = in ? __ldg(j.I + off + st * j.sIs) : -1;
+                        sg[u] = in ? __ldg(j.G + off + st * j.sGs) : 0.0f;
+                    }
+                    __syncthreads();  // the previous chunk's readers of the stage are done
+#pragma unroll
+                    for (int u = 0; u < RM_PER; ++u) {
+                        const int e = tid + u * RM_THREADS, r = e % RM_WARPS, t = e / RM_WARPS;
+                        ck[r * RM_CLD + t] = sk[u];
+                        cg[r * RM_CLD + t] = sg[u];
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int t = 0; t < RM_NB; ++t) {
+                        rk[t] = ck[w * RM_CLD + 32 * t + l];
+                        rg[t] = cg[w * RM_CLD + 32 * t + l];
+                    }
+                }
+                // ---- max-times: the other operand at each step's winner, all gathers in flight together
+                if (MUL) {
+#pragma unroll
+                    for (int t = 0; t < RM_NB; ++t) {
+                        const int d = rk[t] - kc32;
+                        if (rk[t] >= 0 && (unsigned)d < (unsigned)kn)
+                            rg[t] = __fmul_rn(rg[t], __ldg(Pl + (int64_t)rk[t] * j.sPk + (c0 + 32 * t + l) * j.sPs));
+                    }
+                }
+                // ---- the batches in step order
+#pragma unroll
+                for (int t = 0; t < RM_NB; ++t) {
+                    const int d = rk[t] - kc32;
+                    const bool in = rk[t] >= 0 && (unsigned)d < (unsigned)kn;
+                    // lanes of one bin group together; distinct negative keys keep the others apart
+                    const unsigned grp = __match_any_sync(0xffffffffu, in ? d : -1 - l);
+                    const int rank = __popc(grp & lanes_below);
+                    if (in && rank == 0) mybins[d] = __fadd_rn(mybins[d], rg[t]);
+                    unsigned more = __ballot_sync(0xffffffffu, in && rank > 0);
+                    for (int rr = 1; more; ++rr) {
+                        __syncwarp();
+                        if (in && rank == rr) mybins[d] = __fadd_rn(mybins[d], rg[t]);
+                        more = __ballot_sync(0xffffffffu, in && rank > rr);
+                    }
+                    __syncwarp();
+                }
+            }
+            __syncthreads();  // every line's bins are final
+            if (j.sOk == 1) {
+                // bins contiguous in the gradient: warp w writes line w, lanes along k
+                const int64_t o = base + w;
+                if (o < lines) {
+                    const int64_t b = o / X, x = o - b * X;
+                    float* Or = j.O + b * j.sOb + x * j.sOx + kc;
+                    for (int kk = l; kk < kn; kk += 32) Or[kk] = mybins[kk];
+                }
+            } else {
+                // lines fastest (consecutive x when sOx == 1): thread (bin, line) of RM_WARPS lines
+                const int r = tid % RM_WARPS;
+                const int64_t o = base + r;
+                if (o < lines) {
+                    const int64_t b = o / X, x = o - b * X;
+                    float* Or = j.O + b * j.sOb + x * j.sOx + kc * j.sOk;
+                    for (int kk = tid / RM_WARPS; kk < kn; kk += RM_THREADS / RM_WARPS)
+                        Or[(int64_t)kk * j.sOk] = bins[r * RM_LD + kk];
+                }
+            }
+        }
+    }
+    if (p.late_wait) pdl_wait();
+}
+
 }  // namespace
 
 int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int64_t K, const float* A,
@@ -386,6 +550,30 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
     }
     if (p.njobs == 0 || batch == 0 || K == 0) return TROP_OK;
     const bool mul = semiring == TROP_MAXTIMES;
+    auto launch_match = [&](RouteParams& q) -> int {
+        int64_t ctas = 1;
+        for (int i = 0; i < q.njobs; ++i) ctas = std::max(ctas, (batch * q.job[i].X + RM_WARPS - 1) / RM_WARPS);
+        const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)dev->sm_count * 16));
+        const dim3 grid(gx, (unsigned)q.njobs);
+        if (mul) (void)launch_pdl(k_route_match<true>, grid, dim3(RM_THREADS), RM_SMEM, s, q);
+        else (void)launch_pdl(k_route_match<false>, grid, dim3(RM_THREADS), RM_SMEM, s, q);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_error(e, "k_route_match");
+        count_launches(1);
+        return TROP_OK;
+    };
+    if (TROP_ROUTE_MATCH && mul) {
+        // max-times: each gradient in a launch of the match-rank kernel of its own; the second
+        // (dB) starts at once and waits at its end (RouteParams::late_wait), so the two overlap
+        if (!dA || p.njobs == 1) return launch_match(p);
+        RouteParams pa = p;
+        pa.njobs = 1;
+        TROP_TRY(launch_match(pa));
+        p.job[0] = p.job[1];
+        p.njobs = 1;
+        p.late_wait = 1;
+        return launch_match(p);
+    }
     // for max-plus and min-plus the rows job (steps contiguous, the common layout of dA) takes
     // the lane-per-line kernel (measured on the batch-64 256^3 gradient: 42 against 52 us for
     // both jobs; with max-times' operand gathers it was slower); the other job follows it and
@@ -418,6 +606,11 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
 
 int register_backward_kernels()
 {
+    const void* km[] = {(const void*)k_route_match<true>, (const void*)k_route_match<false>};
+    for (const void* k : km) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RM_SMEM);
+        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (match route smem)");
+    }
     const void* ks[] = {(const void*)k_winner_route<true>, (const void*)k_winner_route<false>};
     for (const void* k : ks) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BW_SMEM);
