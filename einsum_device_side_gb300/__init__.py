@@ -25,6 +25,8 @@ __all__ = [
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtropical_gb300.so")
+# the bounds-checked build (build.py --debug), loaded instead when TROP_LIBRARY=debug
+LIB_DEBUG_PATH = os.path.join(_HERE, "_build_debug", "libtropical_gb300.so")
 SEMIRINGS = {"maxplus": 0, "minplus": 1, "maxtimes": 2}
 _DTYPES = {torch.float32: 0, torch.int32: 1, torch.int64: 2, torch.float64: 3}
 MAX_RANK = 32
@@ -84,11 +86,13 @@ def _load_fastcall(lib_path: str):
 
 
 def load(path: str | None = None):
-    """Load the shared library (once).  Raises if it has not been built."""
+    """Load the shared library (once).  Raises if it has not been built.  With TROP_LIBRARY=debug
+    in the environment the bounds-checked build is loaded instead (through ctypes only)."""
     global _lib, _fc
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    debug = os.environ.get("TROP_LIBRARY", "") == "debug"
+    path = path or (LIB_DEBUG_PATH if debug else LIB_PATH)
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with `python -m einsum_device_side_gb300.build` "
                            "(there is no CPU fallback)")
@@ -126,6 +130,9 @@ def load(path: str | None = None):
         "tropical_set_plan_cache_capacity": (None, [I]),
         "tropical_device_wait_timeouts": (I, [ctypes.POINTER(ctypes.c_uint), I]),
         "tropical_debug_set_wait_mode": (None, [I]),
+        "tropical_debug_bounds_report": (I, [ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_uint64), I]),
+        "tropical_debug_bounds_trim": (I, [I64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -133,7 +140,7 @@ def load(path: str | None = None):
         f.argtypes = args
     del i32p
     _lib = lib
-    _fc = _load_fastcall(path)
+    _fc = None if debug else _load_fastcall(path)
     if _fc is not None:
         _fc.set_torch_handles(torch.float32, torch.int32, torch.int64, torch.float64,
                               _raw_stream or (lambda dev: torch.cuda.current_stream(dev).cuda_stream))
@@ -597,6 +604,34 @@ def debug_set_wait_mode(mode: int):
     """Test hook: 1 = the TMA-fed GEMM's first operand wait gives up (then recovers), 2 = it
     then fails after its copies landed (the next call reports the error), 0 = normal."""
     load().tropical_debug_set_wait_mode(int(mode))
+
+
+# translation units of the library, by the id the bounds-checked build records with a line
+_BOUNDS_FILES = {1: "unary.cu", 2: "gemm.cu", 3: "gemm64.cu", 4: "gemm_int.cu", 5: "backward.cu", 6: "backtrack.cu"}
+
+
+def debug_bounds_report(reset: bool = False) -> dict | None:
+    """The bounds-checked build's violation record for the current device: {"count", "file",
+    "line", "addr"} (the first violation's source location and address), or None from the
+    normal build, which checks nothing.  Read once the work to inspect has completed."""
+    lib = load()
+    cnt, line, addr = ctypes.c_uint(0), ctypes.c_int(0), ctypes.c_uint64(0)
+    rc = lib.tropical_debug_bounds_report(ctypes.byref(cnt), ctypes.byref(line), ctypes.byref(addr), int(reset))
+    if rc == -10:  # TROP_ERR_UNSUPPORTED: the normal build
+        return None
+    _check(rc)
+    return {"count": cnt.value, "file": _BOUNDS_FILES.get(line.value >> 16, "?"), "line": line.value & 0xFFFF,
+            "addr": addr.value}
+
+
+def debug_bounds_trim(nbytes: int) -> bool:
+    """Test hook of the bounds-checked build: cut every byte range made from now on short by
+    ``nbytes`` (0 restores exact ranges).  Returns False from the normal build."""
+    rc = load().tropical_debug_bounds_trim(int(nbytes))
+    if rc == -10:  # TROP_ERR_UNSUPPORTED: the normal build
+        return False
+    _check(rc)
+    return True
 
 
 def set_pool_capacity(n: int):

@@ -6,6 +6,12 @@ extension machinery: the library has a plain C ABI (include/tropical.h).
 
 Numerics flags: no fast-math, ``-fmad=false`` (no multiply-add contraction),
 ``-ftz=false`` (subnormals kept), so every tropical product rounds once.
+
+``build(variant="debug")`` makes the bounds-checked library instead, in
+``_build_debug/`` (``-DTROP_DEBUG_BOUNDS=1``): every global access of every kernel is
+tested against the byte range of its tensor and a violation is recorded, not made
+(``tropical_debug_bounds_report``).  It has no CPython binding; the package loads it,
+through ctypes, when ``TROP_LIBRARY=debug`` is set.
 """
 
 from __future__ import annotations
@@ -21,6 +27,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtropical_gb300.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libtropical_gb300.so")
+VARIANTS = {"release": (BUILD, LIB, []), "debug": (BUILD_DEBUG, LIB_DEBUG, ["-DTROP_DEBUG_BOUNDS=1"])}
 SOURCES = ["runtime.cpp", "api.cpp", "unary.cu", "gemm.cu", "gemm64.cu", "gemm_int.cu", "backtrack.cu", "backward.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,16 +48,18 @@ def nvcc() -> str:
 def _stale(obj: str, src: str) -> bool:
     if not os.path.exists(obj):
         return True
-    deps = [src, os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "tropical.h")]
+    deps = [src, os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "bounds.h"),
+            os.path.join(ROOT, "include", "tropical.h")]
     return any(os.path.getmtime(d) > os.path.getmtime(obj) for d in deps)
 
 
-def _compile(src: str, verbose: bool) -> str:
+def _compile(src: str, verbose: bool, variant: str = "release") -> str:
+    out_dir, _, defs = VARIANTS[variant]
     path = os.path.join(CSRC, src)
-    obj = os.path.join(BUILD, src + ".o")
+    obj = os.path.join(out_dir, src + ".o")
     if not _stale(obj, path):
         return obj
-    cmd = [nvcc(), *ARCH, *COMMON, "-c", path, "-o", obj + ".tmp"]
+    cmd = [nvcc(), *ARCH, *COMMON, *defs, "-c", path, "-o", obj + ".tmp"]
     if verbose and src.endswith(".cu"):
         cmd.insert(1, "-Xptxas=-v")
     if src.endswith(".cpp"):
@@ -93,25 +104,29 @@ def build_fastcall(force: bool = False) -> str | None:
     return out
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, variant: str = "release") -> str:
+    out_dir, lib, _ = VARIANTS[variant]
+    os.makedirs(out_dir, exist_ok=True)
     if force:
-        for f in os.listdir(BUILD):
-            os.remove(os.path.join(BUILD, f))
+        for f in os.listdir(out_dir):
+            os.remove(os.path.join(out_dir, f))
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    if os.path.exists(LIB) and all(os.path.getmtime(o) <= os.path.getmtime(LIB) for o in objs):
-        build_fastcall(force=force)
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, variant), SOURCES))
+    if os.path.exists(lib) and all(os.path.getmtime(o) <= os.path.getmtime(lib) for o in objs):
+        if variant == "release":
+            build_fastcall(force=force)
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    build_fastcall(force=True)
-    return LIB
+    os.replace(tmp, lib)
+    if variant == "release":
+        build_fastcall(force=True)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv,
+                variant="debug" if "--debug" in sys.argv else "release"))

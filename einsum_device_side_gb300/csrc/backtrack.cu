@@ -12,15 +12,28 @@
 
 #include <cstdint>
 
+#define TROP_TU 6  // this file's id in a bounds-violation record
 #include "internal.h"
 
 namespace trop {
 
 namespace {
 
+// In the bounds-checked build the walks take the violation record as one more argument and check
+// each argmax read against its node's table (the product of its output extents) and each label
+// against the assignment; in the normal build neither exists.
+#if TROP_DEBUG_BOUNDS
+#define BT_REC_PARAM , unsigned* rec
+#define BT_REC_ARG , bounds_record()
+#define BT_SPAN(base, n) (Span{reinterpret_cast<const char*>(base), reinterpret_cast<const char*>((base) + (n)), rec})
+#else
+#define BT_REC_PARAM
+#define BT_REC_ARG
+#endif
+
 __global__ void k_backtrack(const BtNode* __restrict__ nodes, int n_nodes, const int32_t* __restrict__ labs,
                             const int64_t* __restrict__ sizes, int64_t root_index, int n_labels,
-                            int32_t* __restrict__ assign)
+                            int32_t* __restrict__ assign BT_REC_PARAM)
 {
     if (blockIdx.x != 0) return;
     for (int l = threadIdx.x; l < n_labels; l += blockDim.x) assign[l] = -1;
@@ -42,18 +55,24 @@ __global__ void k_backtrack(const BtNode* __restrict__ nodes, int n_nodes, const
         if (!nd.argmax || nd.n_k == 0) continue;
         int64_t o = 0;
         bool known = true;
+#if TROP_DEBUG_BOUNDS
+        int64_t total = 1;
+#endif
         for (int i = 0; i < nd.n_out; ++i) {
             const int32_t l = labs[nd.lab_off + i];
             const int32_t v = assign[l];
             if (v < 0) known = false;
             o = o * sizes[l] + (v < 0 ? 0 : v);
+#if TROP_DEBUG_BOUNDS
+            total *= sizes[l];
+#endif
         }
         if (!known) continue;
-        int64_t a = nd.argmax[o];
+        int64_t a = TROP_IN(nd.argmax + o, 4, BT_SPAN(nd.argmax, total)) ? nd.argmax[o] : 0;
         for (int i = nd.n_k - 1; i >= 0; --i) {
             const int32_t l = labs[nd.lab_off + nd.n_out + i];
             const int64_t sz = sizes[l];
-            assign[l] = (int32_t)(a % sz);
+            if (TROP_IN(assign + l, 4, BT_SPAN(assign, n_labels))) assign[l] = (int32_t)(a % sz);
             a /= sz;
         }
     }
@@ -74,7 +93,7 @@ __host__ __device__ inline size_t bt_smem_bytes(int n_nodes, int n_labs, int n_l
 __global__ void __launch_bounds__(256) k_backtrack_smem(const BtNode* __restrict__ nodes_g, int n_nodes,
                                                         const int32_t* __restrict__ labs_g, int n_labs,
                                                         const int64_t* __restrict__ sizes_g, int64_t root_index,
-                                                        int n_labels, int32_t* __restrict__ assign_g)
+                                                        int n_labels, int32_t* __restrict__ assign_g BT_REC_PARAM)
 {
     extern __shared__ __align__(16) unsigned char bsm[];
     BtNode* nodes = reinterpret_cast<BtNode*>(bsm);
@@ -130,11 +149,12 @@ __global__ void __launch_bounds__(256) k_backtrack_smem(const BtNode* __restrict
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) o += __shfl_xor_sync(full, o, d);
         if (lane == 0) {
-            int64_t a = nd.argmax[o];
+            // (st of lane 0: the product of the node's output extents, its table's size)
+            int64_t a = TROP_IN(nd.argmax + o, 4, BT_SPAN(nd.argmax, st)) ? nd.argmax[o] : 0;
             for (int i = nd.n_k - 1; i >= 0; --i) {
                 const int32_t l = labs[nd.lab_off + nd.n_out + i];
                 const int64_t s = sizes[l];
-                assign[l] = (int32_t)(a % s);
+                if (TROP_IN(assign + l, 4, BT_SPAN(assign, n_labels))) assign[l] = (int32_t)(a % s);
                 a /= s;
             }
         }
@@ -157,9 +177,10 @@ int launch_backtrack(const BtNode* nodes_dev, int n_nodes, const int32_t* labels
     const size_t smem = bt_smem_bytes(n_nodes, n_labs, n_labels);
     if (smem <= BT_SMEM_MAX)
         k_backtrack_smem<<<1, 256, smem, s>>>(nodes_dev, n_nodes, labels_dev, n_labs, sizes_dev, root_index, n_labels,
-                                              assignment);
+                                              assignment BT_REC_ARG);
     else
-        k_backtrack<<<1, 256, 0, s>>>(nodes_dev, n_nodes, labels_dev, sizes_dev, root_index, n_labels, assignment);
+        k_backtrack<<<1, 256, 0, s>>>(nodes_dev, n_nodes, labels_dev, sizes_dev, root_index, n_labels,
+                                      assignment BT_REC_ARG);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "k_backtrack");
     count_launches(1);

@@ -30,6 +30,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#define TROP_TU 5  // this file's id in a bounds-violation record
 #include "internal.h"
 
 namespace trop {
@@ -62,7 +63,14 @@ struct RouteJob {
     int64_t sPb, sPk, sPs;
     float* O;
     int64_t sOb, sOx, sOk;
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // I, G, P, O
+#endif
 };
+
+// checked global accesses of job j (plain accesses in the normal build): tensor k of
+// RouteJob::sp must hold `bytes` at ptr
+#define R_IN(ptr, bytes, k) TROP_IN(ptr, bytes, j.sp[k])
 
 struct RouteParams {
     int64_t nbatch, K;
@@ -117,8 +125,8 @@ __global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
                 const int r = along_walk ? e >> 5 : e & 31, t = along_walk ? e & 31 : e >> 5;
                 const int64_t off = line_i[r], s = s0 + t;
                 const bool in = off >= 0 && s < j.S;
-                rk[i] = in ? __ldg(j.I + off + s * j.sIs) : -1;
-                rg[i] = in ? __ldg(j.G + off + s * j.sGs) : 0.0f;
+                rk[i] = in && R_IN(j.I + off + s * j.sIs, 4, 0) ? __ldg(j.I + off + s * j.sIs) : -1;
+                rg[i] = in && R_IN(j.G + off + s * j.sGs, 4, 1) ? __ldg(j.G + off + s * j.sGs) : 0.0f;
             }
         };
         auto put = [&](int q) {
@@ -155,7 +163,9 @@ __global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const unsigned d = (unsigned)(mk[t] - klo32);
-                        pv[t] = d < kl ? __ldg(Pl + (int64_t)mk[t] * j.sPk + (s0 + t) * j.sPs) : 0.0f;
+                        pv[t] = d < kl && R_IN(Pl + (int64_t)mk[t] * j.sPk + (s0 + t) * j.sPs, 4, 2)
+                                    ? __ldg(Pl + (int64_t)mk[t] * j.sPk + (s0 + t) * j.sPs)
+                                    : 0.0f;
                     }
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
@@ -187,13 +197,15 @@ __global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
                     if (orr >= lines) break;
                     const int64_t br = orr / j.X, xr = orr - br * j.X;
                     float* Or = j.O + br * j.sOb + xr * j.sOx + klo;
-                    for (int kk = l; kk < kt; kk += 32) Or[kk] = bins[kk * BW_LD + r];
+                    for (int kk = l; kk < kt; kk += 32)
+                        if (R_IN(Or + kk, 4, 3)) Or[kk] = bins[kk * BW_LD + r];
                 }
             } else if (valid) {
                 // lanes along the lines (consecutive x when sOx == 1)
                 const int64_t o = base + l, b = o / j.X, x = o - b * j.X;
                 float* Or = j.O + b * j.sOb + x * j.sOx + klo * j.sOk;
-                for (int kk = 0; kk < kt; ++kk) Or[kk * j.sOk] = bins[kk * BW_LD + l];
+                for (int kk = 0; kk < kt; ++kk)
+                    if (R_IN(Or + kk * j.sOk, 4, 3)) Or[kk * j.sOk] = bins[kk * BW_LD + l];
             }
         }
     }
@@ -250,10 +262,12 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
                 constexpr int R = decltype(slot)::value;
                 const int64_t s0 = c * RT_STEP;
                 if (valid && s0 + RT_STEP <= j.S) {
-                    const int4 k0 = __ldg(reinterpret_cast<const int4*>(Il + s0));
-                    const int4 k1 = __ldg(reinterpret_cast<const int4*>(Il + s0 + 4));
-                    const float4 g0 = __ldg(reinterpret_cast<const float4*>(Gl + s0));
-                    const float4 g1 = __ldg(reinterpret_cast<const float4*>(Gl + s0 + 4));
+                    const int4 kz = make_int4(-1, -1, -1, -1);
+                    const float4 gz = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int4 k0 = R_IN(Il + s0, 16, 0) ? __ldg(reinterpret_cast<const int4*>(Il + s0)) : kz;
+                    const int4 k1 = R_IN(Il + s0 + 4, 16, 0) ? __ldg(reinterpret_cast<const int4*>(Il + s0 + 4)) : kz;
+                    const float4 g0 = R_IN(Gl + s0, 16, 1) ? __ldg(reinterpret_cast<const float4*>(Gl + s0)) : gz;
+                    const float4 g1 = R_IN(Gl + s0 + 4, 16, 1) ? __ldg(reinterpret_cast<const float4*>(Gl + s0 + 4)) : gz;
                     kr[R][0] = k0.x; kr[R][1] = k0.y; kr[R][2] = k0.z; kr[R][3] = k0.w;
                     kr[R][4] = k1.x; kr[R][5] = k1.y; kr[R][6] = k1.z; kr[R][7] = k1.w;
                     gr[R][0] = g0.x; gr[R][1] = g0.y; gr[R][2] = g0.z; gr[R][3] = g0.w;
@@ -262,8 +276,8 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
 #pragma unroll
                     for (int t = 0; t < RT_STEP; ++t) {
                         const bool in = valid && c < nch && s0 + t < j.S;
-                        kr[R][t] = in ? __ldg(Il + s0 + t) : -1;
-                        gr[R][t] = in ? __ldg(Gl + s0 + t) : 0.0f;
+                        kr[R][t] = in && R_IN(Il + s0 + t, 4, 0) ? __ldg(Il + s0 + t) : -1;
+                        gr[R][t] = in && R_IN(Gl + s0 + t, 4, 1) ? __ldg(Gl + s0 + t) : 0.0f;
                     }
                 }
             };
@@ -337,12 +351,13 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
                     __syncwarp();
                     for (int rr = 0; rr < 32; ++rr) {
                         float* Or = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(Ol), rr));
-                        if (base + rr < lines && kb + l < kn) Or[kc + kb + l] = tb[rr * 33 + l];
+                        if (base + rr < lines && kb + l < kn && R_IN(Or + kc + kb + l, 4, 3)) Or[kc + kb + l] = tb[rr * 33 + l];
                     }
                     __syncwarp();
                 }
             } else if (valid) {
-                for (int k = 0; k < kn; ++k) Ol[(kc + k) * j.sOk] = bins[k * 32 + l];
+                for (int k = 0; k < kn; ++k)
+                    if (R_IN(Ol + (kc + k) * j.sOk, 4, 3)) Ol[(kc + k) * j.sOk] = bins[k * 32 + l];
             }
             __syncwarp();
         }
@@ -427,8 +442,8 @@ __global__ void __launch_bounds__(RM_THREADS) k_route_match(RouteParams p)
 #pragma unroll
                     for (int t = 0; t < RM_NB; ++t) {
                         const bool in = my_valid && c0 + 32 * t + l < S;
-                        rk[t] = in ? __ldg(ip + 32 * t) : -1;
-                        rg[t] = in ? __ldg(gp + 32 * t) : 0.0f;
+                        rk[t] = in && R_IN(ip + 32 * t, 4, 0) ? __ldg(ip + 32 * t) : -1;
+                        rg[t] = in && R_IN(gp + 32 * t, 4, 1) ? __ldg(gp + 32 * t) : 0.0f;
                     }
                 } else {
                     // staged: element e of the [RM_WARPS][RM_CHUNK] block, lines fastest
@@ -439,8 +454,8 @@ __global__ void __launch_bounds__(RM_THREADS) k_route_match(RouteParams p)
                         const int e = tid + u * RM_THREADS, r = e % RM_WARPS, t = e / RM_WARPS;
                         const int64_t off = line_i[r], st = c0 + t;
                         const bool in = off >= 0 && st < S;
-                        sk[u] = in ? __ldg(j.I + off + st * j.sIs) : -1;
-                        sg[u] = in ? __ldg(j.G + off + st * j.sGs) : 0.0f;
+                        sk[u] = in && R_IN(j.I + off + st * j.sIs, 4, 0) ? __ldg(j.I + off + st * j.sIs) : -1;
+                        sg[u] = in && R_IN(j.G + off + st * j.sGs, 4, 1) ? __ldg(j.G + off + st * j.sGs) : 0.0f;
                     }
                     __syncthreads();  // the previous chunk's readers of the stage are done
 #pragma unroll
@@ -461,8 +476,10 @@ __global__ void __launch_bounds__(RM_THREADS) k_route_match(RouteParams p)
 #pragma unroll
                     for (int t = 0; t < RM_NB; ++t) {
                         const int d = rk[t] - kc32;
-                        if (rk[t] >= 0 && (unsigned)d < (unsigned)kn)
-                            rg[t] = __fmul_rn(rg[t], __ldg(Pl + (int64_t)rk[t] * j.sPk + (c0 + 32 * t + l) * j.sPs));
+                        if (rk[t] >= 0 && (unsigned)d < (unsigned)kn) {
+                            const float* pp = Pl + (int64_t)rk[t] * j.sPk + (c0 + 32 * t + l) * j.sPs;
+                            rg[t] = __fmul_rn(rg[t], R_IN(pp, 4, 2) ? __ldg(pp) : 0.0f);
+                        }
                     }
                 }
                 // ---- the batches in step order
@@ -490,7 +507,8 @@ __global__ void __launch_bounds__(RM_THREADS) k_route_match(RouteParams p)
                 if (o < lines) {
                     const int64_t b = o / X, x = o - b * X;
                     float* Or = j.O + b * j.sOb + x * j.sOx + kc;
-                    for (int kk = l; kk < kn; kk += 32) Or[kk] = mybins[kk];
+                    for (int kk = l; kk < kn; kk += 32)
+                        if (R_IN(Or + kk, 4, 3)) Or[kk] = mybins[kk];
                 }
             } else {
                 // lines fastest (consecutive x when sOx == 1): thread (bin, line) of RM_WARPS lines
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(RM_THREADS) k_route_match(RouteParams p)
                     const int64_t b = o / X, x = o - b * X;
                     float* Or = j.O + b * j.sOb + x * j.sOx + kc * j.sOk;
                     for (int kk = tid / RM_WARPS; kk < kn; kk += RM_THREADS / RM_WARPS)
-                        Or[(int64_t)kk * j.sOk] = bins[r * RM_LD + kk];
+                        if (R_IN(Or + (int64_t)kk * j.sOk, 4, 3)) Or[(int64_t)kk * j.sOk] = bins[r * RM_LD + kk];
                 }
             }
         }
@@ -550,6 +568,18 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
     }
     if (p.njobs == 0 || batch == 0 || K == 0) return TROP_OK;
     const bool mul = semiring == TROP_MAXTIMES;
+#if TROP_DEBUG_BOUNDS
+    for (int i = 0; i < p.njobs; ++i) {
+        RouteJob& j = p.job[i];
+        const int64_t xs[3] = {batch, j.X, j.S}, ks[3] = {batch, K, j.S}, os[3] = {batch, j.X, K};
+        const int64_t si[3] = {j.sIb, j.sIx, j.sIs}, sg[3] = {j.sGb, j.sGx, j.sGs};
+        const int64_t sp_[3] = {j.sPb, j.sPk, j.sPs}, so[3] = {j.sOb, j.sOx, j.sOk};
+        j.sp[0] = span_of(j.I, 4, 3, xs, si);
+        j.sp[1] = span_of(j.G, 4, 3, xs, sg);
+        j.sp[2] = span_of(mul ? j.P : nullptr, 4, 3, ks, sp_);
+        j.sp[3] = span_of(j.O, 4, 3, os, so);
+    }
+#endif
     auto launch_match = [&](RouteParams& q) -> int {
         int64_t ctas = 1;
         for (int i = 0; i < q.njobs; ++i) ctas = std::max(ctas, (batch * q.job[i].X + RM_WARPS - 1) / RM_WARPS);

@@ -52,6 +52,7 @@
 #include <cstdint>
 #include <cstdio>
 
+#define TROP_TU 2  // this file's id in a bounds-violation record
 #include "internal.h"
 
 namespace trop {
@@ -168,7 +169,14 @@ struct TiledParams {
     // host-mapped memory, read by the library's next call) and the test mode of its waits
     uint32_t* err;
     int wait_mode;
+#if TROP_DEBUG_BOUNDS
+    Span sp[7];  // A, B, C, I, seg_v, seg_c, sk_cnt
+#endif
 };
+
+// checked global accesses of the tiled kernels (plain accesses in the normal build): operand k
+// of TiledParams::sp must hold `bytes` at ptr
+#define T_IN(ptr, bytes, k) TROP_IN(ptr, bytes, p.sp[k])
 
 __device__ __forceinline__ void tile_coord(const TiledParams& p, uint32_t t, uint32_t& b, int& m0, int& n0)
 {
@@ -260,8 +268,10 @@ __device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int 
 #pragma unroll
             for (int q = 0; q < MERGE_BATCH; ++q) {
                 const int e = ((q0 + q) * THREADS + tid) * 4;
-                sv[q] = __ldcg(reinterpret_cast<const float4*>(p.seg_v + base + e));
-                if (ARG) sc[q] = __ldcg(reinterpret_cast<const uint2*>(p.seg_c + base + e));
+                sv[q] = T_IN(p.seg_v + base + e, 16, 4) ? __ldcg(reinterpret_cast<const float4*>(p.seg_v + base + e))
+                                                        : make_float4(O::zero(), O::zero(), O::zero(), O::zero());
+                if (ARG) sc[q] = T_IN(p.seg_c + base + e, 8, 5) ? __ldcg(reinterpret_cast<const uint2*>(p.seg_c + base + e))
+                                                                : make_uint2(0u, 0u);
             }
 #pragma unroll
             for (int q = 0; q < MERGE_BATCH; ++q) {
@@ -283,20 +293,24 @@ __device__ __forceinline__ void sk_merge(const TiledParams& p, uint32_t tl, int 
             if (m >= p.M) continue;
             float* crow = p.C + oc + (int64_t)m * p.sCm;
             if (p.vecC && n + 3 < p.N) {
-                *reinterpret_cast<float4*>(crow + n) = make_float4(v[q][0], v[q][1], v[q][2], v[q][3]);
+                if (T_IN(crow + n, 16, 2))
+                    *reinterpret_cast<float4*>(crow + n) = make_float4(v[q][0], v[q][1], v[q][2], v[q][3]);
             } else {
 #pragma unroll
                 for (int x = 0; x < 4; ++x)
-                    if (n + x < p.N) crow[(int64_t)(n + x) * p.sCn] = v[q][x];
+                    if (n + x < p.N && T_IN(crow + (int64_t)(n + x) * p.sCn, 4, 2))
+                        crow[(int64_t)(n + x) * p.sCn] = v[q][x];
             }
             if (ARG) {
                 int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
                 if (p.vecI && n + 3 < p.N) {
-                    *reinterpret_cast<int4*>(irow + n) = make_int4(-cd[q][0], -cd[q][1], -cd[q][2], -cd[q][3]);
+                    if (T_IN(irow + n, 16, 3))
+                        *reinterpret_cast<int4*>(irow + n) = make_int4(-cd[q][0], -cd[q][1], -cd[q][2], -cd[q][3]);
                 } else {
 #pragma unroll
                     for (int x = 0; x < 4; ++x)
-                        if (n + x < p.N) irow[(int64_t)(n + x) * p.sIn] = -cd[q][x];
+                        if (n + x < p.N && T_IN(irow + (int64_t)(n + x) * p.sIn, 4, 3))
+                            irow[(int64_t)(n + x) * p.sIn] = -cd[q][x];
                 }
             }
         }
@@ -374,11 +388,12 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                 const int m = m0 + la_m + (THREADS / 4) * r, k = k0 + la_k;
                 const float* src = A + (int64_t)m * p.sAm + k;
                 if (m < p.M && k + 3 < p.K && p.vecA) {
-                    ra[r] = __ldg(reinterpret_cast<const float4*>(src));
+                    ra[r] = T_IN(src, 16, 0) ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(zero, zero, zero, zero);
                 } else {
                     float v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = (m < p.M && k + q < p.K) ? __ldg(src + q) : zero;
+                    for (int q = 0; q < 4; ++q)
+                        v[q] = (m < p.M && k + q < p.K && T_IN(src + q, 4, 0)) ? __ldg(src + q) : zero;
                     ra[r] = make_float4(v[0], v[1], v[2], v[3]);
                 }
             }
@@ -402,13 +417,15 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                 const int kk = lb_k + (THREADS / 16) * r, k = k0 + kk, n = n0 + lb_n;
                 float* dst = &Bs[buf][kk][lb_n];
                 if (p.vecB) {
-                    const int valid = (k < p.K) ? max(0, min(4, p.N - n)) : 0;
+                    int valid = (k < p.K) ? max(0, min(4, p.N - n)) : 0;
+                    if (valid && !T_IN(B + (int64_t)k * p.sBk + n, valid * 4, 1)) valid = 0;
                     const float* src = valid ? B + (int64_t)k * p.sBk + n : B;
                     cp_async16(dst, src, valid * 4);
                 } else {
                     const float* src = B + (int64_t)k * p.sBk + n;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = (k < p.K && n + q < p.N) ? __ldg(src + q) : 0.0f;
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = (k < p.K && n + q < p.N && T_IN(src + q, 4, 1)) ? __ldg(src + q) : 0.0f;
                 }
             }
             cp_async_commit();
@@ -524,21 +541,25 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                 for (int h = 0; h < NG; ++h) {
                     const int n = n0 + h * (BN / 2) + tn * 4;
                     if (p.vecC && n + 3 < p.N) {
-                        *reinterpret_cast<float4*>(crow + n) =
-                            make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
+                        if (T_IN(crow + n, 16, 2))
+                            *reinterpret_cast<float4*>(crow + n) =
+                                make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
                     } else {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            if (n + q < p.N) crow[(int64_t)(n + q) * p.sCn] = best[i][4 * h + q];
+                            if (n + q < p.N && T_IN(crow + (int64_t)(n + q) * p.sCn, 4, 2))
+                                crow[(int64_t)(n + q) * p.sCn] = best[i][4 * h + q];
                     }
                     if (ARG) {
                         if (p.vecI && n + 3 < p.N) {
-                            *reinterpret_cast<int4*>(irow + n) =
-                                make_int4(code[4 * h], code[4 * h + 1], code[4 * h + 2], code[4 * h + 3]);
+                            if (T_IN(irow + n, 16, 3))
+                                *reinterpret_cast<int4*>(irow + n) =
+                                    make_int4(code[4 * h], code[4 * h + 1], code[4 * h + 2], code[4 * h + 3]);
                         } else {
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                if (n + q < p.N) irow[(int64_t)(n + q) * p.sIn] = code[4 * h + q];
+                                if (n + q < p.N && T_IN(irow + (int64_t)(n + q) * p.sIn, 4, 3))
+                                    irow[(int64_t)(n + q) * p.sIn] = code[4 * h + q];
                         }
                     }
                 }
@@ -553,14 +574,16 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
 #pragma unroll
                 for (int h = 0; h < NG; ++h) {
                     const int c = h * (BN / 2) + tn * 4;
-                    *reinterpret_cast<float4*>(sv + r * BN + c) =
-                        make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
+                    if (T_IN(sv + r * BN + c, 16, 4))
+                        *reinterpret_cast<float4*>(sv + r * BN + c) =
+                            make_float4(best[i][4 * h], best[i][4 * h + 1], best[i][4 * h + 2], best[i][4 * h + 3]);
                     if (ARG) {
                         uint32_t cd[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             cd[q] = best[i][4 * h + q] != zero ? (uint32_t)sid[i * TN + 4 * h + q][tid] + 1u : 0u;
-                        *reinterpret_cast<uint2*>(sc + r * BN + c) = make_uint2(cd[0] | (cd[1] << 16), cd[2] | (cd[3] << 16));
+                        if (T_IN(sc + r * BN + c, 8, 5))
+                            *reinterpret_cast<uint2*>(sc + r * BN + c) = make_uint2(cd[0] | (cd[1] << 16), cd[2] | (cd[3] << 16));
                     }
                 }
             }
@@ -572,7 +595,7 @@ __global__ void __launch_bounds__(tile_threads<TN>(), ARG ? TROP_ARG_MINB : TROP
                 uint32_t j0, j1;
                 int slot0;
                 sk_segments(p, tl, j0, j1, slot0);
-                const bool last = atomicAdd(&p.sk_cnt[tl], 1u) == j1 - j0;
+                const bool last = T_IN(p.sk_cnt + tl, 4, 6) && atomicAdd(&p.sk_cnt[tl], 1u) == j1 - j0;
                 if (last) p.sk_cnt[tl] = 0;  // zero again for the next launch on this stream
                 s_last = last;
             }
@@ -775,7 +798,8 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
             int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (n0 + tn * 4 + q < p.N) irow[(int64_t)(n0 + tn * 4 + q) * p.sIn] = 0;
+                if (n0 + tn * 4 + q < p.N && T_IN(irow + (int64_t)(n0 + tn * 4 + q) * p.sIn, 4, 3))
+                    irow[(int64_t)(n0 + tn * 4 + q) * p.sIn] = 0;
         }
         if (tid == 0 && p.err) {
             *(volatile uint32_t*)p.err = 1u;
@@ -796,18 +820,19 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
         for (int jj = 0; jj < TN; ++jj) code[jj] = best[i][jj] != zero ? -((int32_t)sid[i * TN + jj][tid] + 1) : 0;
         const int n = n0 + tn * 4;
         if (p.vecC && n + 3 < p.N) {
-            *reinterpret_cast<float4*>(crow + n) = make_float4(best[i][0], best[i][1], best[i][2], best[i][3]);
+            if (T_IN(crow + n, 16, 2))
+                *reinterpret_cast<float4*>(crow + n) = make_float4(best[i][0], best[i][1], best[i][2], best[i][3]);
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (n + q < p.N) crow[(int64_t)(n + q) * p.sCn] = best[i][q];
+                if (n + q < p.N && T_IN(crow + (int64_t)(n + q) * p.sCn, 4, 2)) crow[(int64_t)(n + q) * p.sCn] = best[i][q];
         }
         if (p.vecI && n + 3 < p.N) {
-            *reinterpret_cast<int4*>(irow + n) = make_int4(code[0], code[1], code[2], code[3]);
+            if (T_IN(irow + n, 16, 3)) *reinterpret_cast<int4*>(irow + n) = make_int4(code[0], code[1], code[2], code[3]);
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (n + q < p.N) irow[(int64_t)(n + q) * p.sIn] = code[q];
+                if (n + q < p.N && T_IN(irow + (int64_t)(n + q) * p.sIn, 4, 3)) irow[(int64_t)(n + q) * p.sIn] = code[q];
         }
     }
 }
@@ -876,8 +901,8 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
 #pragma unroll
             for (int h = 0; h < NCOL; ++h) {
                 const bool ok = m < me && colok[h];
-                nval[r][h] = ok ? cr[h * 32] : 0.0f;
-                ncode[r][h] = ok ? ir[h * 32] : 0;
+                nval[r][h] = ok && T_IN(cr + h * 32, 4, 2) ? cr[h * 32] : 0.0f;
+                ncode[r][h] = ok && T_IN(ir + h * 32, 4, 3) ? ir[h * 32] : 0;
             }
         }
     };
@@ -910,7 +935,9 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
             for (int h = 0; h < NCOL; ++h)
 #pragma unroll
                 for (int kk = 0; kk < CH; kk += 4) {
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(arow + ka[r][h] + kk));
+                    const float4 x = T_IN(arow + ka[r][h] + kk, 16, 0)
+                                         ? __ldg(reinterpret_cast<const float4*>(arow + ka[r][h] + kk))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                     av[r][h][kk] = x.x;
                     av[r][h][kk + 1] = x.y;
                     av[r][h][kk + 2] = x.z;
@@ -930,7 +957,8 @@ __device__ __forceinline__ void resolve_rows_fast(const TiledParams& p, const fl
                     idx = t.y == val[r][h] ? kk + 1 : idx;
                     idx = t.x == val[r][h] ? kk : idx;
                 }
-                if (live[r][h]) ib[(int64_t)(ms + r * RSUB + rs) * p.sIm + h * 32] = ka[r][h] + idx;
+                if (live[r][h] && T_IN(ib + (int64_t)(ms + r * RSUB + rs) * p.sIm + h * 32, 4, 3))
+                    ib[(int64_t)(ms + r * RSUB + rs) * p.sIm + h * 32] = ka[r][h] + idx;
             }
     }
 }
@@ -987,12 +1015,15 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
                 const int kk = e / (PW / 4), nq = (e % (PW / 4)) * 4, gk = k0 + kk, gn = n0 + nq;
                 float* dst = EBf + kk * PW + nq;
                 if (p.vecB) {
-                    const int valid = max(0, min(4, p.N - gn));
+                    int valid = max(0, min(4, p.N - gn));
+                    if (valid && !T_IN(B + (int64_t)gk * p.sBk + gn, valid * 4, 1)) valid = 0;
                     cp_async16(dst, valid ? B + (int64_t)gk * p.sBk + gn : B, valid * 4);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        dst[q] = (gn + q < p.N) ? __ldg(B + (int64_t)gk * p.sBk + gn + q) : 0.0f;
+                        dst[q] = (gn + q < p.N && T_IN(B + (int64_t)gk * p.sBk + gn + q, 4, 1))
+                                     ? __ldg(B + (int64_t)gk * p.sBk + gn + q)
+                                     : 0.0f;
                 }
             }
             cp_async_commit();
@@ -1017,8 +1048,8 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const bool in = m < me && colok[h];
-                        nval[r][h] = in ? Cb[(int64_t)m * p.sCm + offC[h]] : 0.0f;
-                        ncode[r][h] = in ? Ib[(int64_t)m * p.sIm + offI[h]] : 0;
+                        nval[r][h] = in && T_IN(Cb + (int64_t)m * p.sCm + offC[h], 4, 2) ? Cb[(int64_t)m * p.sCm + offC[h]] : 0.0f;
+                        ncode[r][h] = in && T_IN(Ib + (int64_t)m * p.sIm + offI[h], 4, 3) ? Ib[(int64_t)m * p.sIm + offI[h]] : 0;
                     }
                 }
             };
@@ -1047,7 +1078,8 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
                         const int kmax = ka[r][h] >= 0 ? min(CH, p.K - ka[r][h]) : 0;
                         const float* src = arow + (ka[r][h] >= 0 ? ka[r][h] : 0);
 #pragma unroll
-                        for (int kk = 0; kk < CH; ++kk) av[r][h][kk] = kk < kmax ? __ldg(src + kk) : 0.0f;
+                        for (int kk = 0; kk < CH; ++kk)
+                            av[r][h][kk] = kk < kmax && T_IN(src + kk, 4, 0) ? __ldg(src + kk) : 0.0f;
                     }
                 }
 #pragma unroll
@@ -1061,7 +1093,8 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
 #pragma unroll
                         for (int kk = CH - 1; kk >= 0; --kk)
                             if (kk < kmax && O::mul(av[r][h][kk], EB[kl + kk][c]) == val[r][h]) idx = kk;
-                        Ib[(int64_t)(ms + r) * p.sIm + offI[h]] = ka[r][h] + idx;
+                        if (T_IN(Ib + (int64_t)(ms + r) * p.sIm + offI[h], 4, 3))
+                            Ib[(int64_t)(ms + r) * p.sIm + offI[h]] = ka[r][h] + idx;
                     }
             }
         }
@@ -1131,14 +1164,14 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
             src += valid ? (int64_t)(tid / (BN / 4)) * p.sBk : 0;
             if (p.vecB) {  // 16-byte aligned rows of B
                 for (int k = tid / (BN / 4); k < p.K; k += RTHREADS / (BN / 4), src += step)
-                    cp_async16(EB + k * BN + q, src, valid * 4);
+                    cp_async16(EB + k * BN + q, src, valid && T_IN(src, valid * 4, 1) ? valid * 4 : 0);
                 cp_async_commit();
                 cp_async_wait_all();
             } else {
                 for (int k = tid / (BN / 4); k < p.K; k += RTHREADS / (BN / 4), src += step) {
                     float v[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) v[e] = e < valid ? __ldg(src + e) : 0.0f;
+                    for (int e = 0; e < 4; ++e) v[e] = e < valid && T_IN(src + e, 4, 1) ? __ldg(src + e) : 0.0f;
                     *reinterpret_cast<float4*>(EB + k * BN + q) = make_float4(v[0], v[1], v[2], v[3]);
                 }
             }
@@ -1163,12 +1196,12 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
             const float* cr = Cb + (int64_t)mm * sC;
             const int32_t* ir = Ib + (int64_t)mm * sI;
             const float* ar = Al + (int64_t)mm * sA;
-            s.v[0] = cr[c0];
-            s.v[1] = cr[c1];
-            s.c[0] = ir[c0];
-            s.c[1] = ir[c1];
-            s.a[0] = __ldg(reinterpret_cast<const float4*>(ar));
-            s.a[1] = __ldg(reinterpret_cast<const float4*>(ar + 4));
+            s.v[0] = T_IN(cr + c0, 4, 2) ? cr[c0] : 0.0f;
+            s.v[1] = T_IN(cr + c1, 4, 2) ? cr[c1] : 0.0f;
+            s.c[0] = T_IN(ir + c0, 4, 3) ? ir[c0] : 0;
+            s.c[1] = T_IN(ir + c1, 4, 3) ? ir[c1] : 0;
+            s.a[0] = T_IN(ar, 16, 0) ? __ldg(reinterpret_cast<const float4*>(ar)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            s.a[1] = T_IN(ar + 4, 16, 0) ? __ldg(reinterpret_cast<const float4*>(ar + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
             s.ok[0] = rok && col0;
             s.ok[1] = rok && col1;
         };
@@ -1198,7 +1231,7 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
                 const bool s1 = (s2 ? p5 : p1) != v;
                 const float x = s2 ? (s1 ? t[6] : t[4]) : (s1 ? t[2] : t[0]);
                 const int idx = (s2 ? 4 : 0) + (s1 ? 2 : 0) + (x != v ? 1 : 0);
-                if (live) irow[h * 32] = c * CH + idx;
+                if (live && T_IN(irow + h * 32, 4, 3)) irow[h * 32] = c * CH + idx;
             }
         };
         constexpr int WSTEP = RWARPS;
@@ -1238,6 +1271,9 @@ struct StreamParams {
     // consecutive memory); 0: the columns vary fastest
     uint32_t binner;
     FastDiv div_binner;
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // A, B, C, I
+#endif
 };
 
 template <int SR, bool ARG, int VEC, int MAXM>
@@ -1274,19 +1310,24 @@ __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
         for (int k = 0; k < p.K; ++k) {
             float bv[VEC];
             if (VEC == 4) {
-                float4 x = __ldg(reinterpret_cast<const float4*>(Bb + (int64_t)k * p.sBk));
+                float4 x = T_IN(Bb + (int64_t)k * p.sBk, 16, 1) ? __ldg(reinterpret_cast<const float4*>(Bb + (int64_t)k * p.sBk))
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
                 bv[0] = x.x;
                 bv[VEC > 1 ? 1 : 0] = x.y;
                 bv[VEC > 2 ? 2 : 0] = x.z;
                 bv[VEC > 3 ? 3 : 0] = x.w;
             } else {
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) bv[v] = __ldg(Bb + (int64_t)k * p.sBk + (int64_t)v * p.sBn);
+                for (int v = 0; v < VEC; ++v)
+                    bv[v] = T_IN(Bb + (int64_t)k * p.sBk + (int64_t)v * p.sBn, 4, 1)
+                                ? __ldg(Bb + (int64_t)k * p.sBk + (int64_t)v * p.sBn)
+                                : 0.0f;
             }
 #pragma unroll
             for (int m = 0; m < MAXM; ++m) {
                 if (m < p.M) {
-                    const float a = __ldg(Ab + (int64_t)m * p.sAm + (int64_t)k * p.sAk);
+                    const float* ap = Ab + (int64_t)m * p.sAm + (int64_t)k * p.sAk;
+                    const float a = T_IN(ap, 4, 0) ? __ldg(ap) : 0.0f;
 #pragma unroll
                     for (int v = 0; v < VEC; ++v) {
                         const float t = O::mul(a, bv[v]);
@@ -1304,17 +1345,18 @@ __global__ void __launch_bounds__(256) k_gemm_stream(StreamParams p)
                 float* cp = p.C + oc + (int64_t)m * p.sCm + (int64_t)n * p.sCn;
                 int32_t* ip = ARG ? p.I + oi + (int64_t)m * p.sIm + (int64_t)n * p.sIn : nullptr;
                 if (VEC == 4) {
-                    *reinterpret_cast<float4*>(cp) =
-                        make_float4(best[m][0], best[m][VEC > 1 ? 1 : 0], best[m][VEC > 2 ? 2 : 0],
-                                    best[m][VEC > 3 ? 3 : 0]);
-                    if (ARG)
+                    if (T_IN(cp, 16, 2))
+                        *reinterpret_cast<float4*>(cp) =
+                            make_float4(best[m][0], best[m][VEC > 1 ? 1 : 0], best[m][VEC > 2 ? 2 : 0],
+                                        best[m][VEC > 3 ? 3 : 0]);
+                    if (ARG && T_IN(ip, 16, 3))
                         *reinterpret_cast<int4*>(ip) = make_int4(idx[m][0], idx[m][VEC > 1 ? 1 : 0],
                                                                  idx[m][VEC > 2 ? 2 : 0], idx[m][VEC > 3 ? 3 : 0]);
                 } else {
 #pragma unroll
                     for (int v = 0; v < VEC; ++v) {
-                        cp[(int64_t)v * p.sCn] = best[m][v];
-                        if (ARG) ip[(int64_t)v * p.sIn] = idx[m][v];
+                        if (T_IN(cp + (int64_t)v * p.sCn, 4, 2)) cp[(int64_t)v * p.sCn] = best[m][v];
+                        if (ARG && T_IN(ip + (int64_t)v * p.sIn, 4, 3)) ip[(int64_t)v * p.sIn] = idx[m][v];
                     }
                 }
             }
@@ -1332,6 +1374,9 @@ struct GenericParams {
     int64_t sAm, sAk, sBk, sBn, sCm, sCn, sIm, sIn;
     int nb;
     int64_t bsize[MAXB], sA[MAXB], sB[MAXB], sC[MAXB], sI[MAXB];
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // A, B, C, I
+#endif
 };
 
 template <int SR, bool ARG>
@@ -1361,14 +1406,15 @@ __global__ void k_gemm_generic(GenericParams p)
         float best = O::zero();
         int64_t idx = 0;
         for (int64_t k = 0; k < p.K; ++k) {
-            const float t = O::mul(__ldg(a + k * p.sAk), __ldg(b + k * p.sBk));
+            const float t = O::mul(T_IN(a + k * p.sAk, 4, 0) ? __ldg(a + k * p.sAk) : 0.0f,
+                                   T_IN(b + k * p.sBk, 4, 1) ? __ldg(b + k * p.sBk) : 0.0f);
             if (O::better(t, best)) {
                 best = t;
                 idx = k;
             }
         }
-        p.C[oc + m * p.sCm + n * p.sCn] = best;
-        if (ARG) p.I[oi + m * p.sIm + n * p.sIn] = (int32_t)idx;
+        if (T_IN(p.C + oc + m * p.sCm + n * p.sCn, 4, 2)) p.C[oc + m * p.sCm + n * p.sCn] = best;
+        if (ARG && T_IN(p.I + oi + m * p.sIm + n * p.sIn, 4, 3)) p.I[oi + m * p.sIm + n * p.sIn] = (int32_t)idx;
     }
 }
 
@@ -1581,6 +1627,9 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 {
     static std::atomic<int> occ_gemm{0};
     TiledParams p{};
+#if TROP_DEBUG_BOUNDS
+    gemm_spans(g, sizeof(float), p.sp);
+#endif
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
@@ -1643,6 +1692,11 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                 p.seg_v = static_cast<float*>(ws);
                 p.seg_c = ARG ? reinterpret_cast<uint16_t*>(p.seg_v + seg_elems) : nullptr;
                 p.sk_cnt = cnt;
+#if TROP_DEBUG_BOUNDS
+                p.sp[4] = span_bytes(p.seg_v, seg_elems * sizeof(float));
+                p.sp[5] = span_bytes(p.seg_c, ARG ? seg_elems * sizeof(uint16_t) : 0);
+                p.sp[6] = span_bytes(cnt, (size_t)R * sizeof(uint32_t));
+#endif
             } else {
                 clear_error();  // no workspace: whole tiles only
                 ws = nullptr;
@@ -1701,6 +1755,9 @@ template <int SR, bool ARG>
 int run_stream(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 {
     StreamParams p{};
+#if TROP_DEBUG_BOUNDS
+    gemm_spans(g, sizeof(float), p.sp);
+#endif
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
@@ -1756,6 +1813,9 @@ template <int SR, bool ARG>
 int run_generic(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 {
     GenericParams p{};
+#if TROP_DEBUG_BOUNDS
+    gemm_spans(g, sizeof(float), p.sp);
+#endif
     p.M = g.M;
     p.N = g.N;
     p.K = g.K;

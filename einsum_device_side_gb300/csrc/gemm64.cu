@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#define TROP_TU 3  // this file's id in a bounds-violation record
 #include "internal.h"
 
 namespace trop {
@@ -69,6 +70,9 @@ struct Gemm64Params {
     int a_kfast, b_kfast;  // staging walks k fastest (that operand's k stride is 1)
     int nb;
     int64_t bsize[MAXB], sA[MAXB], sB[MAXB], sC[MAXB], sI[MAXB];
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // A, B, C, I
+#endif
 };
 
 template <int SR, bool ARG>
@@ -119,7 +123,8 @@ __global__ void __launch_bounds__(D_THREADS, TROP_F64_MINB) k_gemm_tiled_f64(Gem
                 const int mm = p.a_kfast ? (e / D_BK) : (e & (D_BM - 1));
                 const int64_t m = m0 + mm;
                 double v = 0.0;
-                if (kk < kc && m < p.M) v = __ldg(A + m * p.sAm + (k0 + kk) * p.sAk);
+                if (kk < kc && m < p.M && TROP_IN(A + m * p.sAm + (k0 + kk) * p.sAk, sizeof(*A), p.sp[0]))
+                    v = __ldg(A + m * p.sAm + (k0 + kk) * p.sAk);
                 As[kk][mm] = v;
             }
 #pragma unroll
@@ -129,7 +134,8 @@ __global__ void __launch_bounds__(D_THREADS, TROP_F64_MINB) k_gemm_tiled_f64(Gem
                 const int nn = p.b_kfast ? (e / D_BK) : (e & (D_BN - 1));
                 const int64_t n = n0 + nn;
                 double v = 0.0;
-                if (kk < kc && n < p.N) v = __ldg(B + (k0 + kk) * p.sBk + n * p.sBn);
+                if (kk < kc && n < p.N && TROP_IN(B + (k0 + kk) * p.sBk + n * p.sBn, sizeof(*B), p.sp[1]))
+                    v = __ldg(B + (k0 + kk) * p.sBk + n * p.sBn);
                 Bs[kk][nn] = v;
             }
             __syncthreads();
@@ -167,8 +173,9 @@ __global__ void __launch_bounds__(D_THREADS, TROP_F64_MINB) k_gemm_tiled_f64(Gem
             for (int j = 0; j < 4; ++j) {
                 const int64_t n = n0 + tx + 16 * j;
                 if (n >= p.N) continue;
-                p.C[oc + m * p.sCm + n * p.sCn] = from_okey(best[i][j]);
-                if (ARG) p.I[oi + m * p.sIm + n * p.sIn] = idx[i][j];
+                if (TROP_IN(p.C + oc + m * p.sCm + n * p.sCn, sizeof(*p.C), p.sp[2]))
+                    p.C[oc + m * p.sCm + n * p.sCn] = from_okey(best[i][j]);
+                if (ARG && TROP_IN(p.I + oi + m * p.sIm + n * p.sIn, 4, p.sp[3])) p.I[oi + m * p.sIm + n * p.sIn] = idx[i][j];
             }
         }
     }
@@ -201,6 +208,9 @@ int run_f64(const GemmDesc& g0, cudaStream_t s, const DeviceInfo* dev)
         }
     }
     Gemm64Params p{};
+#if TROP_DEBUG_BOUNDS
+    gemm_spans(g, sizeof(*p.A), p.sp);
+#endif
     p.M = g.M;
     p.N = g.N;
     p.K = g.K;

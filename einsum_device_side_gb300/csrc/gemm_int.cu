@@ -21,6 +21,7 @@
 #include <climits>
 #include <type_traits>
 
+#define TROP_TU 4  // this file's id in a bounds-violation record
 #include "internal.h"
 
 namespace trop {
@@ -55,6 +56,9 @@ struct GemmIntParams {
     int a_kfast, b_kfast;  // staging walks k fastest (that operand's k stride is 1)
     int nb;
     int64_t bsize[MAXB], sA[MAXB], sB[MAXB], sC[MAXB], sI[MAXB];
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // A, B, C, I
+#endif
 };
 
 template <int SR, typename T, bool ARG>
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(I_THREADS) k_gemm_int(GemmIntParams<T> p)
                 const int mm = p.a_kfast ? (e / I_BK) : (e & (I_BM - 1));
                 const int64_t m = m0 + mm;
                 T v = T(0);
-                if (kk < kc && m < p.M) v = __ldg(A + m * p.sAm + (k0 + kk) * p.sAk);
+                if (kk < kc && m < p.M && TROP_IN(A + m * p.sAm + (k0 + kk) * p.sAk, sizeof(*A), p.sp[0]))
+                    v = __ldg(A + m * p.sAm + (k0 + kk) * p.sAk);
                 As[kk][mm] = v;
             }
 #pragma unroll
@@ -116,7 +121,8 @@ __global__ void __launch_bounds__(I_THREADS) k_gemm_int(GemmIntParams<T> p)
                 const int nn = p.b_kfast ? (e / I_BK) : (e & (I_BN - 1));
                 const int64_t n = n0 + nn;
                 T v = T(0);
-                if (kk < kc && n < p.N) v = __ldg(B + (k0 + kk) * p.sBk + n * p.sBn);
+                if (kk < kc && n < p.N && TROP_IN(B + (k0 + kk) * p.sBk + n * p.sBn, sizeof(*B), p.sp[1]))
+                    v = __ldg(B + (k0 + kk) * p.sBk + n * p.sBn);
                 Bs[kk][nn] = v;
             }
             __syncthreads();
@@ -154,8 +160,9 @@ __global__ void __launch_bounds__(I_THREADS) k_gemm_int(GemmIntParams<T> p)
             for (int j = 0; j < 4; ++j) {
                 const int64_t n = n0 + tx + 16 * j;
                 if (n >= p.N) continue;
-                p.C[oc + m * p.sCm + n * p.sCn] = best[i][j];
-                if (ARG) p.I[oi + m * p.sIm + n * p.sIn] = idx[i][j];
+                if (TROP_IN(p.C + oc + m * p.sCm + n * p.sCn, sizeof(*p.C), p.sp[2]))
+                    p.C[oc + m * p.sCm + n * p.sCn] = best[i][j];
+                if (ARG && TROP_IN(p.I + oi + m * p.sIm + n * p.sIn, 4, p.sp[3])) p.I[oi + m * p.sIm + n * p.sIn] = idx[i][j];
             }
         }
     }
@@ -187,6 +194,9 @@ int run_int(const GemmDesc& g0, cudaStream_t s, const DeviceInfo* dev)
         }
     }
     GemmIntParams<T> p{};
+#if TROP_DEBUG_BOUNDS
+    gemm_spans(g, sizeof(*p.A), p.sp);
+#endif
     p.M = g.M;
     p.N = g.N;
     p.K = g.K;

@@ -9,6 +9,7 @@
 #include <map>
 
 #include "tropical.h"
+#include "bounds.h"
 
 namespace trop {
 
@@ -184,6 +185,25 @@ struct GemmDesc {
     int64_t bsize[MAXB];
     int64_t sAb[MAXB], sBb[MAXB], sCb[MAXB], sIb[MAXB];
 };
+// The byte ranges of A, B, C (elements of elem_bytes) and I that g addresses, into sp[0..3]
+// (bounds-checked build only; nothing in the normal build).
+inline void gemm_spans(const GemmDesc& g, size_t elem_bytes, Span* sp)
+{
+#if TROP_DEBUG_BOUNDS
+    int64_t sz[MAXB + 2], st[MAXB + 2];
+    auto one = [&](const void* base, size_t eb, int64_t r, int64_t c, int64_t sr, int64_t sc, const int64_t* sb) {
+        for (int i = 0; i < g.nb; ++i) sz[i] = g.bsize[i], st[i] = sb[i];
+        sz[g.nb] = r, st[g.nb] = sr, sz[g.nb + 1] = c, st[g.nb + 1] = sc;
+        return span_of(base, eb, g.nb + 2, sz, st);
+    };
+    sp[0] = one(g.A, elem_bytes, g.M, g.K, g.sAm, g.sAk, g.sAb);
+    sp[1] = one(g.B, elem_bytes, g.K, g.N, g.sBk, g.sBn, g.sBb);
+    sp[2] = one(g.C, elem_bytes, g.M, g.N, g.sCm, g.sCn, g.sCb);
+    sp[3] = one(g.I, 4, g.M, g.N, g.sIm, g.sIn, g.sIb);
+#else
+    (void)g, (void)elem_bytes, (void)sp;
+#endif
+}
 int launch_gemm(const GemmDesc& g, cudaStream_t s, const char** kernel_name);
 // The binary64 GEMM (gemm64.cu); launch_gemm forwards TROP_F64 descriptors here.
 int launch_gemm_f64(const GemmDesc& g, cudaStream_t s);

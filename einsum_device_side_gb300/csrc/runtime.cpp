@@ -162,6 +162,23 @@ static int take_device_error(int dev)
 
 int wait_test_mode() { return g_wait_mode.load(std::memory_order_relaxed); }
 
+#if TROP_DEBUG_BOUNDS
+// words 4..7 of the device's host-mapped block: the bounds-violation record (bounds.h)
+unsigned* bounds_record()
+{
+    uint32_t* w = nullptr;
+    if (device_error_word(&w) != TROP_OK) {
+        clear_error();
+        return nullptr;
+    }
+    return w + 4;
+}
+
+// test hook: bytes cut from the top of every span made from now on (0: exact ranges)
+static std::atomic<int64_t> g_span_trim{0};
+int64_t bounds_span_trim() { return g_span_trim.load(std::memory_order_relaxed); }
+#endif
+
 // ------------------------------------------------------------------ device set-up
 static std::mutex g_dev_mu;
 static DeviceInfo g_dev[64];
@@ -585,6 +602,43 @@ extern "C" int tropical_sync_pool(void)
         return TROP_OK;
     }
     return dev >= 0 && dev < 64 ? take_device_error(dev) : TROP_OK;
+}
+
+extern "C" int tropical_debug_bounds_report(unsigned int* count, int* line, uint64_t* addr, int reset)
+{
+    clear_error();
+    if (!count) return set_error(TROP_ERR_INVALID_ARG, "count pointer is NULL");
+    *count = 0;
+    if (line) *line = 0;
+    if (addr) *addr = 0;
+#if TROP_DEBUG_BOUNDS
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return set_error(TROP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    volatile uint32_t* h = g_err_host[dev].load(std::memory_order_acquire);
+    if (!h) return TROP_OK;  // nothing launched with a record yet
+    *count = h[4];
+    if (line) *line = (int)h[5];
+    if (addr) *addr = (uint64_t)h[6] | ((uint64_t)h[7] << 32);
+    if (reset) h[4] = h[5] = h[6] = h[7] = 0;
+    return TROP_OK;
+#else
+    (void)reset;
+    return set_error(TROP_ERR_UNSUPPORTED, "this library was built without bounds checks (TROP_DEBUG_BOUNDS=0)");
+#endif
+}
+
+extern "C" int tropical_debug_bounds_trim(int64_t bytes)
+{
+    clear_error();
+    if (bytes < 0) return set_error(TROP_ERR_INVALID_ARG, "trim of %lld bytes", (long long)bytes);
+#if TROP_DEBUG_BOUNDS
+    g_span_trim.store(bytes, std::memory_order_relaxed);
+    return TROP_OK;
+#else
+    return set_error(TROP_ERR_UNSUPPORTED, "this library was built without bounds checks (TROP_DEBUG_BOUNDS=0)");
+#endif
 }
 
 extern "C" void tropical_debug_set_wait_mode(int mode)

@@ -30,6 +30,7 @@
 #include <algorithm>
 #include <cstring>
 
+#define TROP_TU 1  // this file's id in a bounds-violation record
 #include "internal.h"
 
 namespace trop {
@@ -76,6 +77,9 @@ struct GatherParams {
     int64_t total;
     int64_t size[MAXR];
     int64_t s_in[MAXR], s_out[MAXR], s_in2[MAXR], s_out2[MAXR];
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // in, out, in2, out2
+#endif
 };
 
 template <typename T, bool PAIR>
@@ -97,8 +101,8 @@ __global__ void k_gather(const T* __restrict__ in, T* __restrict__ out, const in
                 oo2 += c * p.s_out2[d];
             }
         }
-        out[oo] = in[oi];
-        if (PAIR) out2[oo2] = in2[oi2];
+        if (TROP_IN(in + oi, sizeof(T), p.sp[0]) && TROP_IN(out + oo, sizeof(T), p.sp[1])) out[oo] = in[oi];
+        if (PAIR && TROP_IN(in2 + oi2, 4, p.sp[2]) && TROP_IN(out2 + oo2, 4, p.sp[3])) out2[oo2] = in2[oi2];
     }
 }
 
@@ -110,6 +114,9 @@ struct RowParams {
     uint32_t total;  // rows * Lv
     FastDiv divLv;
     RestDims<R> rest;
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // in, out, in2, out2
+#endif
 };
 
 template <typename T, typename V, bool PAIR, int R>
@@ -124,11 +131,14 @@ __global__ void k_copy_rows(const T* __restrict__ in, T* __restrict__ out, const
         uint32_t col = (e - row * p.Lv) * W;
         int64_t oi, oo, oi2, oo2;
         decode_rest(p.rest, row, oi, oo, oi2, oo2);
-        *reinterpret_cast<V*>(out + oo + col) = __ldg(reinterpret_cast<const V*>(in + oi + col));
+        if (TROP_IN(in + oi + col, sizeof(V), p.sp[0]) && TROP_IN(out + oo + col, sizeof(V), p.sp[1]))
+            *reinterpret_cast<V*>(out + oo + col) = __ldg(reinterpret_cast<const V*>(in + oi + col));
         if (PAIR) {
             // the companion is int32: copy W of them element-wise
 #pragma unroll
-            for (int q = 0; q < W; ++q) out2[oo2 + col + q] = __ldg(in2 + oi2 + col + q);
+            for (int q = 0; q < W; ++q)
+                if (TROP_IN(in2 + oi2 + col + q, 4, p.sp[2]) && TROP_IN(out2 + oo2 + col + q, 4, p.sp[3]))
+                    out2[oo2 + col + q] = __ldg(in2 + oi2 + col + q);
         }
     }
 }
@@ -156,6 +166,9 @@ struct TransParams {
     int vec_out;                         // output rows 16-byte aligned for vector stores
     int sw;                              // shared-memory swizzle step (see tile_pos)
     RestDims<R> rest;
+#if TROP_DEBUG_BOUNDS
+    Span sp[4];  // in, out, in2, out2
+#endif
 };
 
 // Shared-memory slot of tile element (x, c): x = slice * TJ + GJ index, in [0, L) with
@@ -268,10 +281,12 @@ __global__ void __launch_bounds__(NT, PAIR ? 3 : TROP_TRANSPOSE_MINB) k_transpos
                 const int e = threadIdx.x + u * NT;
                 const int c = (e & ((1 << lvi) - 1)) * W, rj = e >> lvi;
                 const int r = rj & (TJ - 1), b = rj >> lTJ;
-                v[u] = __ldg(reinterpret_cast<const V*>(in + bin_s[b] + row_in[r] + i0 + c));
-                if (PAIR)
-                    v2[PAIR ? u : 0] = __ldg(reinterpret_cast<const int4*>(
-                        in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c));
+                const T* src = in + bin_s[b] + row_in[r] + i0 + c;
+                v[u] = TROP_IN(src, sizeof(V), p.sp[0]) ? __ldg(reinterpret_cast<const V*>(src)) : V{};
+                if (PAIR) {
+                    const int32_t* src2 = in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c;
+                    v2[PAIR ? u : 0] = TROP_IN(src2, 16, p.sp[2]) ? __ldg(reinterpret_cast<const int4*>(src2)) : int4{};
+                }
             }
 #pragma unroll
             for (int u = 0; u < VPT; ++u) {
@@ -291,10 +306,12 @@ __global__ void __launch_bounds__(NT, PAIR ? 3 : TROP_TRANSPOSE_MINB) k_transpos
                 const int c = e & (TI - 1), rj = e >> lTI;
                 const int r = rj & (TJ - 1), b = rj >> lTJ;
                 if (r0 + b < p.nR && j0 + r < p.nJ && i0 + c < p.nI) {
-                    tile[tile_pos<W>(rj, c, L, sw)] = __ldg(in + bin_s[b] + row_in[r] + i0 + c);
-                    if (PAIR)
-                        tile2[PAIR ? tile_pos<W>(rj, c, L, sw) : 0] =
-                            __ldg(in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c);
+                    const T* src = in + bin_s[b] + row_in[r] + i0 + c;
+                    tile[tile_pos<W>(rj, c, L, sw)] = TROP_IN(src, sizeof(T), p.sp[0]) ? __ldg(src) : T{};
+                    if (PAIR) {
+                        const int32_t* src2 = in2 + bin2_s[PAIR ? b : 0] + row_in2[PAIR ? r : 0] + i0 + c;
+                        tile2[PAIR ? tile_pos<W>(rj, c, L, sw) : 0] = TROP_IN(src2, 4, p.sp[2]) ? __ldg(src2) : 0;
+                    }
                 }
             }
         }
@@ -307,20 +324,25 @@ __global__ void __launch_bounds__(NT, PAIR ? 3 : TROP_TRANSPOSE_MINB) k_transpos
                 const int r = ri & (TI - 1), b = ri >> lTI;
                 const int at = tile_pos<W>((b << lTJ) + c, r, L, sw);
                 const V v = *reinterpret_cast<const V*>(&tile[at]);
-                *reinterpret_cast<V*>(out + bout_s[b] + row_out[r] + j0 + c) = v;
-                if (PAIR)
-                    *reinterpret_cast<int4*>(out2 + bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c) =
-                        *reinterpret_cast<const int4*>(&tile2[PAIR ? at : 0]);
+                T* dst = out + bout_s[b] + row_out[r] + j0 + c;
+                if (TROP_IN(dst, sizeof(V), p.sp[1])) *reinterpret_cast<V*>(dst) = v;
+                if (PAIR) {
+                    int32_t* dst2 = out2 + bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c;
+                    if (TROP_IN(dst2, 16, p.sp[3]))
+                        *reinterpret_cast<int4*>(dst2) = *reinterpret_cast<const int4*>(&tile2[PAIR ? at : 0]);
+                }
             }
         } else {
             for (int e = threadIdx.x; e < TB * TJ * TI; e += NT) {
                 const int c = e & (TJ - 1), ri = e >> lTJ;
                 const int r = ri & (TI - 1), b = ri >> lTI;
                 if (r0 + b < p.nR && i0 + r < p.nI && j0 + c < p.nJ) {
-                    out[bout_s[b] + row_out[r] + j0 + c] = tile[tile_pos<W>((b << lTJ) + c, r, L, sw)];
-                    if (PAIR)
-                        out2[bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c] =
-                            tile2[PAIR ? tile_pos<W>((b << lTJ) + c, r, L, sw) : 0];
+                    T* dst = out + bout_s[b] + row_out[r] + j0 + c;
+                    if (TROP_IN(dst, sizeof(T), p.sp[1])) *dst = tile[tile_pos<W>((b << lTJ) + c, r, L, sw)];
+                    if (PAIR) {
+                        int32_t* dst2 = out2 + bout2_s[PAIR ? b : 0] + row_out2[PAIR ? r : 0] + j0 + c;
+                        if (TROP_IN(dst2, 4, p.sp[3])) *dst2 = tile2[PAIR ? tile_pos<W>((b << lTJ) + c, r, L, sw) : 0];
+                    }
                 }
             }
         }
@@ -360,6 +382,8 @@ struct Semi<SR, int64_t> {
     __device__ static bool better(int64_t a, int64_t b) { return SR == TROP_MINPLUS ? a < b : a > b; }
 };
 
+constexpr int64_t NO_INDEX = INT64_MAX;
+
 struct RedParams {
     int64_t n_out;
     int64_t R;  // reduced extent
@@ -369,7 +393,26 @@ struct RedParams {
     int64_t red_size[MAXR], red_s_in[MAXR];
     int64_t nsplit;  // chunks per output (block kernel)
     int64_t chunk;   // reduced elements per chunk
+#if TROP_DEBUG_BOUNDS
+    Span sp[5];  // in, out, arg, part_v, part_i
+#endif
 };
+
+// checked forms of the reduce kernels' global accesses (plain accesses in the normal build)
+template <typename T>
+__device__ __forceinline__ T red_load(const T* at, const RedParams& p)
+{
+    return TROP_IN(at, sizeof(T), p.sp[0]) ? __ldg(at) : T{};
+}
+template <typename T>
+__device__ __forceinline__ void red_store(T* out, int64_t oo, T v, int32_t* arg, int64_t oa, int32_t idx,
+                                          const RedParams& p)
+{
+    if (TROP_IN(out + oo, sizeof(T), p.sp[1])) out[oo] = v;
+    if (arg && TROP_IN(arg + oa, 4, p.sp[2])) arg[oa] = idx;
+}
+// a merged first index: NO_INDEX when nothing beat the zero, stored as 0
+__device__ __forceinline__ int32_t final_index(int64_t idx) { return idx == NO_INDEX ? 0 : (int32_t)idx; }
 
 __device__ __forceinline__ void out_offsets(const RedParams& p, int64_t o, int64_t& oi, int64_t& oo, int64_t& oa)
 {
@@ -395,8 +438,6 @@ __device__ __forceinline__ int64_t red_offset(const RedParams& p, int64_t r)
     return off;
 }
 
-constexpr int64_t NO_INDEX = INT64_MAX;
-
 // one thread per output element, ascending reduced index, strict update
 template <int SR, typename T>
 __global__ void k_reduce_thread(const T* __restrict__ in, T* __restrict__ out, int32_t* __restrict__ arg,
@@ -412,14 +453,13 @@ __global__ void k_reduce_thread(const T* __restrict__ in, T* __restrict__ out, i
         T best = S::zero();
         int64_t idx = 0;
         for (int64_t r = 0; r < p.R; ++r) {
-            T v = __ldg(in + oi + red_offset(p, r));
+            T v = red_load(in + oi + red_offset(p, r), p);
             if (S::better(v, best)) {
                 best = v;
                 idx = r;
             }
         }
-        out[oo] = best;
-        if (arg) arg[oa] = (int32_t)idx;
+        red_store(out, oo, best, arg, oa, (int32_t)idx, p);
     }
 }
 
@@ -445,7 +485,7 @@ __global__ void __launch_bounds__(NT) k_reduce_block(const T* __restrict__ in, T
         T best = S::zero();
         int64_t idx = NO_INDEX;
         for (int64_t r = r0 + threadIdx.x; r < r1; r += NT) {
-            T v = __ldg(in + oi + red_offset(p, r));
+            T v = red_load(in + oi + red_offset(p, r), p);
             if (S::better(v, best)) {
                 best = v;
                 idx = r;
@@ -469,11 +509,10 @@ __global__ void __launch_bounds__(NT) k_reduce_block(const T* __restrict__ in, T
         }
         if (threadIdx.x == 0) {
             if (p.nsplit == 1) {
-                out[oo] = sv[0];
-                if (arg) arg[oa] = si[0] == NO_INDEX ? 0 : (int32_t)si[0];
+                red_store(out, oo, sv[0], arg, oa, final_index(si[0]), p);
             } else {
-                part_v[w] = sv[0];
-                part_i[w] = si[0];
+                if (TROP_IN(part_v + w, sizeof(T), p.sp[3])) part_v[w] = sv[0];
+                if (TROP_IN(part_i + w, 8, p.sp[4])) part_i[w] = si[0];
             }
         }
         __syncthreads();
@@ -508,7 +547,7 @@ __global__ void __launch_bounds__(32 * RS) k_reduce_tile(const T* __restrict__ i
         if (valid) {
 #pragma unroll 4
             for (int64_t r = y; r < p.R; r += RS) {
-                const T v = __ldg(in + oi + red_offset(p, r));
+                const T v = red_load(in + oi + red_offset(p, r), p);
                 if (S::better(v, best)) {
                     best = v;
                     idx = r;
@@ -528,8 +567,7 @@ __global__ void __launch_bounds__(32 * RS) k_reduce_tile(const T* __restrict__ i
                     idx = i;
                 }
             }
-            out[oo] = best;
-            if (arg) arg[oa] = idx == NO_INDEX ? 0 : (int32_t)idx;
+            red_store(out, oo, best, arg, oa, final_index(idx), p);
         }
         __syncthreads();
     }
@@ -550,14 +588,14 @@ __global__ void k_reduce_combine(T* __restrict__ out, int32_t* __restrict__ arg,
         T best = S::zero();
         int64_t idx = NO_INDEX;
         for (int64_t c = 0; c < p.nsplit; ++c) {
-            T v = part_v[o * p.nsplit + c];
+            const int64_t w = o * p.nsplit + c;
+            T v = TROP_IN(part_v + w, sizeof(T), p.sp[3]) ? part_v[w] : S::zero();
             if (S::better(v, best)) {
                 best = v;
-                idx = part_i[o * p.nsplit + c];
+                idx = TROP_IN(part_i + w, 8, p.sp[4]) ? part_i[w] : NO_INDEX;
             }
         }
-        out[oo] = best;
-        if (arg) arg[oa] = idx == NO_INDEX ? 0 : (int32_t)idx;
+        red_store(out, oo, best, arg, oa, final_index(idx), p);
     }
 }
 
@@ -621,6 +659,17 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
     }();
     const bool small_idx = total < (int64_t(1) << 31);
     const int last = d.rank - 1;
+    // the byte ranges the four views can address (bounds-checked build only)
+    auto set_spans = [&](auto& p) {
+#if TROP_DEBUG_BOUNDS
+        p.sp[0] = span_of(in, sizeof(T), d.rank, d.size, d.s_in);
+        p.sp[1] = span_of(out, sizeof(T), d.rank, d.size, d.s_out);
+        p.sp[2] = span_of(in2, 4, d.rank, d.size, d.s_in2);
+        p.sp[3] = span_of(out2, 4, d.rank, d.size, d.s_out2);
+#else
+        (void)p;
+#endif
+    };
 
     auto fill_rest = [&](auto& r, int skip_mask) {
         r.rank = 0;
@@ -643,6 +692,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             bool vec = (p.L % W) == 0 && ((uintptr_t)in % 16) == 0 && ((uintptr_t)out % 16) == 0;
             for (int i = 0; i < last; ++i) vec = vec && (d.s_in[i] % W) == 0 && (d.s_out[i] % W) == 0;
             fill_rest(p.rest, 1 << last);
+            set_spans(p);
             constexpr int R = sizeof(p.rest.div) / sizeof(p.rest.div[0]);
             const int64_t rows = total / p.L;
             if (vec) {
@@ -728,6 +778,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
             p.gi_s_out2[k] = d.s_out2[ax];
         }
         fill_rest(p.rest, used);
+        set_spans(p);
         int64_t nrest = 1;
         for (int i = 0; i < d.rank; ++i)
             if (!(used & (1 << i))) nrest *= d.size[i];
@@ -811,6 +862,7 @@ int launch_gather_typed(const void* in_, void* out_, const int32_t* in2, int32_t
         p.s_in2[i] = d.s_in2[i];
         p.s_out2[i] = d.s_out2[i];
     }
+    set_spans(p);
     int g = grid_for(total, NT, dev->sm_count);
     if (pair) (void)launch_pdl(k_gather<T, true>, g, NT, 0, s, in, out, in2, out2, p);
     else (void)launch_pdl(k_gather<T, false>, g, NT, 0, s, in, out, in2, out2, p);
@@ -857,6 +909,16 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
         p.red_size[0] = 1;
         p.red_s_in[0] = 0;
     }
+#if TROP_DEBUG_BOUNDS
+    {
+        int64_t sz[2 * MAXR], st[2 * MAXR];
+        for (int i = 0; i < p.out_rank; ++i) sz[i] = p.out_size[i], st[i] = p.out_s_in[i];
+        for (int i = 0; i < p.red_rank; ++i) sz[p.out_rank + i] = p.red_size[i], st[p.out_rank + i] = p.red_s_in[i];
+        p.sp[0] = span_of(in, sizeof(T), p.out_rank + p.red_rank, sz, st);
+        p.sp[1] = span_of(out, sizeof(T), p.out_rank, p.out_size, p.out_s_out);
+        p.sp[2] = span_of(arg, 4, p.out_rank, p.out_size, p.out_s_arg);
+    }
+#endif
     const int64_t threads_wanted = (int64_t)dev->sm_count * 1024;
     if (p.R <= 64 || p.n_out >= threads_wanted) {
         int g = grid_for(p.n_out, NT, dev->sm_count);
@@ -899,6 +961,10 @@ int launch_reduce_typed(const void* in_, void* out_, int32_t* arg, const ReduceD
             part_i = static_cast<int64_t*>(ws);
         }
         part_v = reinterpret_cast<T*>(part_i + nb);
+#if TROP_DEBUG_BOUNDS
+        p.sp[3] = span_bytes(part_v, nb * sizeof(T));
+        p.sp[4] = span_bytes(part_i, nb * sizeof(int64_t));
+#endif
     }
     int g = grid_for(p.n_out * nsplit, 1, dev->sm_count, 16);
     (void)launch_pdl(k_reduce_block<SR, T>, g, NT, 0, s, in, out, arg, part_v, part_i, p);

@@ -372,6 +372,28 @@ void tropical_reset_stats(void);
  * NULL count, or TROP_ERR_CUDA. */
 int tropical_device_wait_timeouts(unsigned int* count, int reset);
 
+/* Bounds violations recorded by the library's debug build (compiled with
+ * TROP_DEBUG_BOUNDS=1): every global load, store and copy of its kernels is
+ * first tested against the byte range of the tensor view it belongs to
+ * (computed on the host from extents and strides); an access outside it is
+ * skipped and counted, and the first one's location and address kept.
+ * *line = (file id << 16) | source line, the file ids being 1 unary.cu, 2
+ * gemm.cu, 3 gemm64.cu, 4 gemm_int.cu, 5 backward.cu, 6 backtrack.cu.
+ * Reads the record of the current device without synchronising: call it once
+ * the work to inspect has completed.  reset != 0 clears the record.  The
+ * normal build returns TROP_ERR_UNSUPPORTED with *count = 0.  It stands in
+ * for an external memory checker; TMA box copies are bounded by their tensor
+ * maps instead and are not tested. */
+int tropical_debug_bounds_report(unsigned int* count, int* line, uint64_t* addr, int reset);
+
+/* Test hook of the debug build: every byte range made after this call is cut
+ * short by `bytes` at its top, so that the last `bytes` of each tensor read
+ * or written count as outside it (the access itself is skipped, and it was
+ * inside the tensor's memory anyway).  It shows that the checks fire; 0
+ * restores exact ranges.  Returns TROP_OK, TROP_ERR_INVALID_ARG for a negative
+ * count, or TROP_ERR_UNSUPPORTED from the normal build. */
+int tropical_debug_bounds_trim(int64_t bytes);
+
 /* Test hook for the bounded waits above (host-side; it changes no device
  * setting): mode 1 makes the first operand wait of every CTA of the TMA-fed
  * GEMMs launched afterwards give up at once (then wait again with the full
