@@ -1106,12 +1106,14 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
 // ------------------------------------------------------------------ argmax resolve, short K
 // The same replacement for contractions of at most 32 chunks (K <= 256) in the common layout
 // (unit column strides, whole chunks, 16-byte aligned A rows, row strides below 2^31).  A warp
-// takes one row of a 64-column panel per step.  Lane l loads chunk l of the row -- the warp
-// reads the row once, coalesced -- and an output whose pending chunk is c takes that chunk's
-// CH values of A from lane c by shuffles; B's rows sit in shared memory as in the general
-// pass (lane l owns columns l and l + 32, so the staged reads are free of bank conflicts).
-// No global load waits on another, so the next row's C, I and A are in flight while a row is
-// searched; the two rows in flight live in two register sets used in turn.
+// takes one row of a 64-column panel per step.  Lane l loads chunk l of the row (one 32-byte
+// load when the rows are 32-byte aligned) -- the warp reads the row once, coalesced -- and an
+// output whose pending chunk is c takes that chunk's CH values of A from lane c by shuffles;
+// B's rows sit in shared memory as in the general pass (lane l owns columns l and l + 32, so
+// the staged reads are free of bank conflicts).  The value C is not read: it is the best
+// product of the pending chunk.  No global load waits on another, so the next row's codes and
+// A are in flight while a row is searched; the two rows in flight live in two register sets
+// used in turn.
 #ifndef TROP_RESOLVE2_MINB
 #define TROP_RESOLVE2_MINB 3
 #endif
@@ -1119,7 +1121,22 @@ constexpr int SHORT_K = 32 * CH;  // one chunk per lane
 static_assert(SHORT_K <= RGK, "the staged B rows cover a short contraction");
 static_assert(CH == 8, "the short resolve searches a chunk of 8 by halving");
 
-template <int SR>
+// A lane's chunk of A: one 32-byte load when the rows are 32-byte aligned (V8), else two 16-byte ones
+template <bool V8>
+__device__ __forceinline__ void load_chunk(const float* p, float (&a)[CH])
+{
+    if constexpr (V8) {
+        asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]), "=f"(a[4]), "=f"(a[5]), "=f"(a[6]), "=f"(a[7])
+                     : "l"(p));
+    } else {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 y = __ldg(reinterpret_cast<const float4*>(p + 4));
+        a[0] = x.x, a[1] = x.y, a[2] = x.z, a[3] = x.w, a[4] = y.x, a[5] = y.y, a[6] = y.z, a[7] = y.w;
+    }
+}
+
+template <int SR, bool V8>
 __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve_rows(TiledParams p)
 {
     pdl_signal();  // a programmatic dependent (the next GEMM) may take SMs as this grid drains
@@ -1133,7 +1150,7 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
     // lane l holds chunk l of every row; lanes past the last chunk read the last one (unused)
     const int achunk = min(lane, p.K / CH - 1);
     const int nchunks = p.K / CH;
-    const int sA = p.sAm32, sC = p.sCm32, sI = p.sIm32;
+    const int sA = p.sAm32, sI = p.sIm32;
     bool waited = false;
     for (uint64_t u = ubeg; u < uend;) {
         // rows mb .. me-1 of panel pn
@@ -1150,7 +1167,6 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
         const int c0 = min(lane, ncl), c1 = min(lane + 32, ncl);
         const float* __restrict__ Al = p.A + oa + achunk * CH;
         const float* __restrict__ B = p.B + ob;
-        const float* __restrict__ Cb = p.C + oc + n0;
         const int32_t* __restrict__ Ib = p.I + oi + n0;
         int32_t* __restrict__ Il = p.I + oi + n0 + lane;
 
@@ -1185,48 +1201,49 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve
         const bool col0 = lane <= ncl, col1 = lane + 32 <= ncl;
         // one row per warp step, two register sets used in turn (no copy between steps)
         struct RowSet {
-            float v[2];
             int32_t c[2];
-            float4 a[2];
+            float a[CH];
             bool ok[2];
         };
         auto load_row = [&](RowSet& s, int m) {
             const bool rok = m < me;
             const int mm = rok ? m : me - 1;
-            const float* cr = Cb + (int64_t)mm * sC;
             const int32_t* ir = Ib + (int64_t)mm * sI;
             const float* ar = Al + (int64_t)mm * sA;
-            s.v[0] = T_IN(cr + c0, 4, 2) ? cr[c0] : 0.0f;
-            s.v[1] = T_IN(cr + c1, 4, 2) ? cr[c1] : 0.0f;
             s.c[0] = T_IN(ir + c0, 4, 3) ? ir[c0] : 0;
             s.c[1] = T_IN(ir + c1, 4, 3) ? ir[c1] : 0;
-            s.a[0] = T_IN(ar, 16, 0) ? __ldg(reinterpret_cast<const float4*>(ar)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            s.a[1] = T_IN(ar + 4, 16, 0) ? __ldg(reinterpret_cast<const float4*>(ar + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (T_IN(ar, 4 * CH, 0)) {
+                load_chunk<V8>(ar, s.a);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk) s.a[kk] = 0.0f;
+            }
             s.ok[0] = rok && col0;
             s.ok[1] = rok && col1;
         };
         auto search_row = [&](const RowSet& s, int m) {
-            const float ar[CH] = {s.a[0].x, s.a[0].y, s.a[0].z, s.a[0].w, s.a[1].x, s.a[1].y, s.a[1].z, s.a[1].w};
             int32_t* irow = Il + (int64_t)m * sI;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 // code -(c + 1): chunk c pending; 0: final (nothing beat the zero)
                 const bool live = s.ok[h] && s.c[h] < 0 && ~s.c[h] < nchunks;
                 const int c = live ? ~s.c[h] : 0;
-                const float v = s.v[h];
                 float a[CH];
 #pragma unroll
-                for (int kk = 0; kk < CH; ++kk) a[kk] = __shfl_sync(0xffffffffu, ar[kk], c);
+                for (int kk = 0; kk < CH; ++kk) a[kk] = __shfl_sync(0xffffffffu, s.a[kk], c);
                 const float* eb = EB + c * (CH * BN) + h * 32 + lane;
-                // every product of the chunk is at most v (at least v for min-plus) and one equals
-                // it, so the prefix (+) of the products first reaches v at the first such k:
-                // halve the range on the prefixes of 4 and then 2 products, then test one product
+                // Chunk c is the last one whose products strictly raised the running result, so
+                // the largest of its products (smallest for min-plus) is the output's value v and
+                // no product of the chunk passes it: the prefix (+) of the products first reaches
+                // v at the first k that attains it.  Halve the range on the prefixes of 4 and then
+                // 2 products, then test one product.
                 float t[CH];
 #pragma unroll
                 for (int kk = 0; kk < CH; ++kk) t[kk] = O::mul(a[kk], eb[kk * BN]);
                 const float p1 = O::fold3(t[0], t[1], t[1]);
                 const float p3 = O::fold3(p1, t[2], t[3]);
                 const float p5 = O::fold3(p3, t[4], t[5]);
+                const float v = O::fold3(p5, t[6], t[7]);
                 const bool s2 = p3 != v;
                 const bool s1 = (s2 ? p5 : p1) != v;
                 const float x = s2 ? (s1 ? t[6] : t[4]) : (s1 ? t[2] : t[0]);
@@ -1525,7 +1542,7 @@ int launch_resolve_short(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t
     const uint64_t npan = (uint64_t)((p.N + BN - 1) / BN);
     p.r_units = (uint64_t)nbatch * npan * (uint64_t)M;
     const uint64_t slots =
-        (uint64_t)dev->sm_count * resident_ctas((const void*)k_argmax_resolve_rows<SR>, RTHREADS, SMEM_RESOLVE, occ);
+        (uint64_t)dev->sm_count * resident_ctas((const void*)k_argmax_resolve_rows<SR, false>, RTHREADS, SMEM_RESOLVE, occ);
     const uint64_t per_cta = (uint64_t)RWARPS;
     const uint64_t want = (p.r_units + per_cta - 1) / per_cta;
     const uint64_t grid = std::max<uint64_t>(1, std::min(slots, want));
@@ -1540,7 +1557,11 @@ int launch_resolve_short(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR>, p);
+    // A's chunks by one 32-byte load each when every row start is 32-byte aligned
+    bool v8 = ((uintptr_t)p.A % 32) == 0 && p.sAm % 8 == 0;
+    for (int d = 0; d < p.bt.nb; ++d) v8 = v8 && p.bt.sA[d] % 8 == 0;
+    cudaError_t e = v8 ? cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR, true>, p)
+                       : cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR, false>, p);
     if (e != cudaSuccess) return cuda_error(e, "k_argmax_resolve_rows");
     return check_launch("k_argmax_resolve_rows");
 }
@@ -2081,8 +2102,10 @@ int register_gemm_kernels()
             (const void*)k_argmax_resolve<TROP_MAXTIMES, 64>, (const void*)k_argmax_resolve<TROP_MAXPLUS, 32>,
             (const void*)k_argmax_resolve<TROP_MINPLUS, 32>,  (const void*)k_argmax_resolve<TROP_MAXTIMES, 32>,
             (const void*)k_argmax_resolve<TROP_MAXPLUS, 16>,  (const void*)k_argmax_resolve<TROP_MINPLUS, 16>,
-            (const void*)k_argmax_resolve<TROP_MAXTIMES, 16>,  (const void*)k_argmax_resolve_rows<TROP_MAXPLUS>,
-            (const void*)k_argmax_resolve_rows<TROP_MINPLUS>,   (const void*)k_argmax_resolve_rows<TROP_MAXTIMES>};
+            (const void*)k_argmax_resolve<TROP_MAXTIMES, 16>,  (const void*)k_argmax_resolve_rows<TROP_MAXPLUS, false>,
+            (const void*)k_argmax_resolve_rows<TROP_MINPLUS, false>,   (const void*)k_argmax_resolve_rows<TROP_MAXTIMES, false>,
+            (const void*)k_argmax_resolve_rows<TROP_MAXPLUS, true>,
+            (const void*)k_argmax_resolve_rows<TROP_MINPLUS, true>,    (const void*)k_argmax_resolve_rows<TROP_MAXTIMES, true>};
         for (const void* k : kr) {
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_RESOLVE);
             if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (argmax resolve smem)");
