@@ -33,6 +33,10 @@
 //                    B by cp.async; needs sAk == 1 and sBn == 1 (the planner
 //                    permutes other layouts).  A thin last wave is cut along k
 //                    (stream-K, see the schedule below).
+//   k_gemm_tma_fused the TMA-fed tiles and their short-K resolve (K <= 256) in
+//                    one launch: CTAs take GEMM tiles, then resolve items, from
+//                    a counter; a resolve item waits for its batch's tiles, so
+//                    the resolve starts in the GEMM's last, part-filled wave.
 //   k_argmax_resolve_rows  chunk -> exact index for K <= 256: a warp reads a
 //                    row of A once, one chunk per lane, and outputs take their
 //                    chunk's values by shuffles.
@@ -169,8 +173,15 @@ struct TiledParams {
     // host-mapped memory, read by the library's next call) and the test mode of its waits
     uint32_t* err;
     int wait_mode;
+    // fused kernel only (k_gemm_tma_fused): its work items are the n_tiles GEMM tiles followed
+    // by the resolve items, items_per_batch per batch (rblocks row blocks of each column panel).
+    // sched[0] hands out items in order; sched[1 + b] counts the stored tiles of batch b and
+    // sched[1 + nbatch + b] its finished resolve items (all zero between launches).
+    uint32_t* sched;
+    uint32_t n_tiles, n_items, tiles_per_batch, items_per_batch, rblocks;
+    FastDiv div_ipb, div_rblocks;
 #if TROP_DEBUG_BOUNDS
-    Span sp[7];  // A, B, C, I, seg_v, seg_c, sk_cnt
+    Span sp[8];  // A, B, C, I, seg_v, seg_c, sk_cnt, sched
 #endif
 };
 
@@ -627,8 +638,9 @@ constexpr int TMA_STAGES = TROP_TMA_STAGES;
 constexpr uint32_t TMA_STAGE_BYTES = (BM * BK + BK * BN) * sizeof(float);
 
 struct TmaMaps {
-    CUtensorMap a;  // A as [batch][M][K] (K fastest), box [1][BM][BK]
-    CUtensorMap b;  // B as [batch][K][N] (N fastest), box [1][BK][BN]
+    CUtensorMap a;   // A as [batch][M][K] (K fastest), box [1][BM][BK]
+    CUtensorMap b;   // B as [batch][K][N] (N fastest), box [1][BK][BN]
+    CUtensorMap bp;  // B again, box [1][K][FPW]: a resolve panel (fused kernel only)
 };
 
 // bounded waits on this device that gave up once (each then waited again with the full bound)
@@ -677,25 +689,39 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-template <int SR>
-__global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
-    k_gemm_tma(const __grid_constant__ TmaMaps maps, TiledParams p)
+// shared memory of one TMA-fed tile
+struct __align__(128) TmaTileSmem {
+    float As[TMA_STAGES][BM][BK];
+    float Bs[TMA_STAGES][BK][BN];
+    uint64_t full[TMA_STAGES];  // operand boxes of a stage landed
+    uint16_t sid[TM * 4][tile_threads<4>()];
+    int s_fail, s_gaveup;
+};
+
+// Tile t of the TMA-fed argmax GEMM: values and -(chunk + 1) codes through the strides.  With
+// PDL the programmatic-dependent wait (and the signal to the next grid) comes between the
+// barrier set-up and the first copy.  *bat receives the tile's batch.
+template <int SR, bool PDL>
+__device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams& p, uint32_t t, TmaTileSmem& sm,
+                                         uint32_t* bat)
 {
     using O = Ops<SR>;
-    constexpr int TN = 4, THREADS = tile_threads<TN>();
+    constexpr int TN = 4;
     static_assert(BK % 4 == 0 && CH % 4 == 0 && (BK / CH) % 2 == 0, "k quads, an even number of chunks per k-tile");
-    __shared__ __align__(128) float As[TMA_STAGES][BM][BK];
-    __shared__ __align__(128) float Bs[TMA_STAGES][BK][BN];
-    __shared__ __align__(8) uint64_t full[TMA_STAGES];  // operand boxes of a stage landed
-    __shared__ uint16_t sid[TM * TN][THREADS];
-    __shared__ int s_fail, s_gaveup;
+    auto& As = sm.As;
+    auto& Bs = sm.Bs;
+    auto& full = sm.full;
+    auto& sid = sm.sid;
+    int& s_fail = sm.s_fail;
+    int& s_gaveup = sm.s_gaveup;
 
     const int tid = threadIdx.x;
     const int tm = tid / (BN / TN), tn = tid % (BN / TN);
     const float zero = O::zero();
     uint32_t b;
     int m0, n0;
-    tile_coord(p, blockIdx.x, b, m0, n0);
+    tile_coord(p, t, b, m0, n0);
+    *bat = b;
     const int nkt = (int)p.nkt;
     if (tid == 0) {
         for (int s = 0; s < TMA_STAGES; ++s) mbar_init(&full[s], 1);
@@ -704,11 +730,13 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
         s_gaveup = 0;
     }
     __syncthreads();
-    // Launched as a programmatic dependent of whatever precedes it on the stream: nothing in
-    // global memory is touched before that grid has completed (the wait), so the launch only
-    // hides its latency.  Then the resolve pass may start filling SMs as this grid drains.
-    pdl_wait();
-    pdl_signal();
+    if constexpr (PDL) {
+        // Launched as a programmatic dependent of whatever precedes it on the stream: nothing in
+        // global memory is touched before that grid has completed (the wait), so the launch only
+        // hides its latency.  Then the resolve pass may start filling SMs as this grid drains.
+        pdl_wait();
+        pdl_signal();
+    }
     auto issue = [&](int kt) {
         const int s = kt % TMA_STAGES;
         mbar_expect_tx(&full[s], TMA_STAGE_BYTES);
@@ -834,6 +862,224 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
             for (int q = 0; q < 4; ++q)
                 if (n + q < p.N && T_IN(irow + (int64_t)(n + q) * p.sIn, 4, 3)) irow[(int64_t)(n + q) * p.sIn] = code[q];
         }
+    }
+}
+
+template <int SR>
+__global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
+    k_gemm_tma(const __grid_constant__ TmaMaps maps, TiledParams p)
+{
+    __shared__ TmaTileSmem sm;
+    uint32_t b;
+    tma_tile<SR, true>(maps, p, blockIdx.x, sm, &b);
+}
+
+// ------------------------------------------------------------------ fused GEMM + short-K resolve
+// One launch does both passes for K <= 256.  Its CTAs take work items in order from a counter:
+// first the GEMM tiles (batch-major), then the resolve items, each a block of FRB rows of one
+// FPW-column panel of one batch.  A resolve item waits (bounded) until every tile of its batch
+// has been stored, so in the last, part-filled wave of tiles the CTAs left over already resolve
+// the batches finished in the waves before -- the resolve fills the GEMM's tail instead of
+// following it.  Items are handed out in order, so a resolve item is taken only after every
+// tile has been taken by a running CTA: the tiles it waits for are resident and finish without
+// waiting on anything, hence no deadlock whatever the block scheduler does.
+//
+// A resolve item stages B's panel [K][FPW] (32 KiB at K = 256) by one TMA copy, issued before
+// the wait.  A warp takes rows r0 + w, r0 + w + 4, ...; lane l owns column n0 + l.  Lane l also
+// loads chunk l of the row's A; an output pending in chunk c takes that chunk's values from
+// lane c by shuffles and B's from the staged panel (lane l reads column l: no bank conflict),
+// and the first k whose product attains the chunk's best product is the argmax.  FG rows are
+// loaded per group, and the next group is in flight while one is searched.
+// A lane's chunk of A: one 32-byte load when the rows are 32-byte aligned (V8), else two 16-byte ones
+template <bool V8>
+__device__ __forceinline__ void load_chunk(const float* p, float (&a)[CH])
+{
+    if constexpr (V8) {
+        asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]), "=f"(a[4]), "=f"(a[5]), "=f"(a[6]), "=f"(a[7])
+                     : "l"(p));
+    } else {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 y = __ldg(reinterpret_cast<const float4*>(p + 4));
+        a[0] = x.x, a[1] = x.y, a[2] = x.z, a[3] = x.w, a[4] = y.x, a[5] = y.y, a[6] = y.z, a[7] = y.w;
+    }
+}
+
+constexpr int FPW = 32;  // resolve panel columns, one per lane
+#ifndef TROP_FUSED_ROWS
+#define TROP_FUSED_ROWS 128
+#endif
+constexpr int FRB = TROP_FUSED_ROWS;  // rows of a resolve item
+constexpr int FG = 4;                 // rows of a warp in one load group
+constexpr int FWARPS = tile_threads<4>() / 32;
+
+struct __align__(128) FusedResolveSmem {
+    float EB[32 * CH][FPW];  // the panel's rows of B (K <= 32 chunks)
+    uint64_t bar;
+};
+union FusedSmem {
+    TmaTileSmem g;
+    FusedResolveSmem r;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* ptr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+// Wait until *ctr >= need (acquire); false after about one second without it.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t need)
+{
+    if (ld_acquire_u32(ctr) >= need) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_u32(ctr) < need) {
+        if (global_ns() - t0 > 1000000000ull) return false;
+        __nanosleep(256);
+    }
+    return true;
+}
+
+template <int SR, bool V8>
+__device__ __forceinline__ void fused_resolve(const TmaMaps& maps, const TiledParams& p, uint32_t r,
+                                              FusedResolveSmem& sm, int& s_ok)
+{
+    using O = Ops<SR>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t b = fdiv(r, p.div_ipb);
+    const uint32_t rem = r - b * p.items_per_batch;
+    const uint32_t pn = fdiv(rem, p.div_rblocks);
+    const int n0 = (int)pn * FPW;
+    const int r0 = (int)(rem - pn * p.rblocks) * FRB;
+    const int r1 = min(p.M, r0 + FRB);
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // B's panel is an input of the GEMM, not a result: its copy overlaps the wait
+        mbar_expect_tx(&sm.bar, (uint32_t)(p.K * FPW * sizeof(float)));
+        tma_load_3d(&sm.EB[0][0], &maps.bp, n0, 0, (int)b, &sm.bar);
+        s_ok = T_IN(p.sched + 1 + b, 4, 7) && wait_count(p.sched + 1 + b, p.tiles_per_batch) ? 1 : 0;
+    }
+    const bool landed = mbar_wait(&sm.bar, 0);
+    // thread 0's acquire of the batch's count, then this barrier: the batch's codes are visible
+    const bool all_landed = __syncthreads_and(landed ? 1 : 0) != 0;
+    if (!s_ok || !all_landed) {
+        // a wait gave up: leave the codes (the results are undefined), let the panel copy land
+        // before the CTA exits, and report the failure in the host-mapped error word
+        if (!landed) (void)mbar_wait(&sm.bar, 0);
+        if (tid == 0 && p.err) {
+            *(volatile uint32_t*)p.err = 1u;
+            __threadfence_system();
+        }
+        return;
+    }
+    const int nchunks = p.K / CH;
+    int64_t oa, ob, oc, oi;
+    batch_offsets(p.bt, b, oa, ob, oc, oi);
+    const int achunk = min(lane, nchunks - 1);  // lanes past the last chunk read it again (unused)
+    const float* __restrict__ Al = p.A + oa + achunk * CH;
+    const int ncl = p.N - 1 - n0;  // the panel's last column
+    const bool colok = lane <= ncl;
+    const int32_t* __restrict__ Ir = p.I + oi + n0 + min(lane, ncl);
+    int32_t* __restrict__ Iw = p.I + oi + n0 + lane;
+    const int sA = p.sAm32, sI = p.sIm32;
+    const float* eb0 = &sm.EB[0][lane];
+    struct Row {
+        int32_t c;
+        float a[CH];
+    };
+    constexpr int STEP = FWARPS * FG;  // rows between a warp's groups
+    auto load = [&](Row (&g)[FG], int mb) {
+#pragma unroll
+        for (int j = 0; j < FG; ++j) {
+            const int m = mb + j * FWARPS;
+            const int mm = m < r1 ? m : r1 - 1;
+            // codes were stored by other CTAs of this launch: read them through L2
+            g[j].c = T_IN(Ir + (int64_t)mm * sI, 4, 3) ? __ldcg(Ir + (int64_t)mm * sI) : 0;
+            if (T_IN(Al + (int64_t)mm * sA, 4 * CH, 0)) {
+                load_chunk<V8>(Al + (int64_t)mm * sA, g[j].a);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < CH; ++kk) g[j].a[kk] = 0.0f;
+            }
+        }
+    };
+    auto search = [&](const Row (&g)[FG], int mb) {
+#pragma unroll
+        for (int j = 0; j < FG; ++j) {
+            const int m = mb + j * FWARPS;
+            // code -(c + 1): chunk c pending; 0: final (nothing beat the zero)
+            const bool live = m < r1 && colok && g[j].c < 0 && ~g[j].c < nchunks;
+            const int c = live ? ~g[j].c : 0;
+            float a[CH], t[CH];
+#pragma unroll
+            for (int kk = 0; kk < CH; ++kk) a[kk] = __shfl_sync(0xffffffffu, g[j].a[kk], c);
+            const float* eb = eb0 + c * (CH * FPW);
+#pragma unroll
+            for (int kk = 0; kk < CH; ++kk) t[kk] = O::mul(a[kk], eb[kk * FPW]);
+            // the chunk's best product is the output's value; its first k is the argmax
+            const float p1 = O::fold3(t[0], t[1], t[1]);
+            const float p3 = O::fold3(p1, t[2], t[3]);
+            const float p5 = O::fold3(p3, t[4], t[5]);
+            const float v = O::fold3(p5, t[6], t[7]);
+            const bool s2 = p3 != v;
+            const bool s1 = (s2 ? p5 : p1) != v;
+            const float x = s2 ? (s1 ? t[6] : t[4]) : (s1 ? t[2] : t[0]);
+            const int idx = (s2 ? 4 : 0) + (s1 ? 2 : 0) + (x != v ? 1 : 0);
+            if (live && T_IN(Iw + (int64_t)m * sI, 4, 3)) Iw[(int64_t)m * sI] = c * CH + idx;
+        }
+    };
+    Row g0[FG], g1[FG];
+    int ms = r0 + warp;
+    if (ms < r1) load(g0, ms);
+    while (ms < r1) {
+        if (ms + STEP < r1) load(g1, ms + STEP);
+        search(g0, ms);
+        ms += STEP;
+        if (ms >= r1) break;
+        if (ms + STEP < r1) load(g0, ms + STEP);
+        search(g1, ms);
+        ms += STEP;
+    }
+    __syncthreads();
+    if (tid == 0 && T_IN(p.sched + 1 + p.nbatch + b, 4, 7) &&
+        atomicAdd(p.sched + 1 + p.nbatch + b, 1u) == p.items_per_batch - 1) {
+        // the batch's last resolve item: every item of it has passed its wait, so the batch's
+        // counters can be zeroed for the next launch
+        p.sched[1 + b] = 0;
+        p.sched[1 + p.nbatch + b] = 0;
+    }
+}
+
+template <int SR, bool V8>
+__global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
+    k_gemm_tma_fused(const __grid_constant__ TmaMaps maps, TiledParams p)
+{
+    __shared__ FusedSmem sm;
+    __shared__ uint32_t s_item;
+    __shared__ int s_ok;
+    // a programmatic dependent of the grid before: take an item only once it has completed
+    pdl_wait();
+    pdl_signal();
+    if (threadIdx.x == 0) {
+        const uint32_t it = T_IN(p.sched, 4, 7) ? atomicAdd(p.sched, 1u) : 0u;
+        if (it == p.n_items - 1) p.sched[0] = 0;  // the last item taken: zero for the next launch
+        s_item = it;
+    }
+    __syncthreads();
+    const uint32_t it = s_item;
+    if (it < p.n_tiles) {
+        uint32_t b;
+        tma_tile<SR, false>(maps, p, it, sm.g, &b);
+        // publish the tile: its values and codes are stored
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0 && T_IN(p.sched + 1 + b, 4, 7)) atomicAdd(p.sched + 1 + b, 1u);
+    } else if (it < p.n_items) {
+        fused_resolve<SR, V8>(maps, p, it - p.n_tiles, sm.r, s_ok);
     }
 }
 
@@ -1120,21 +1366,6 @@ __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE_MINB) k_argmax_resolve(
 constexpr int SHORT_K = 32 * CH;  // one chunk per lane
 static_assert(SHORT_K <= RGK, "the staged B rows cover a short contraction");
 static_assert(CH == 8, "the short resolve searches a chunk of 8 by halving");
-
-// A lane's chunk of A: one 32-byte load when the rows are 32-byte aligned (V8), else two 16-byte ones
-template <bool V8>
-__device__ __forceinline__ void load_chunk(const float* p, float (&a)[CH])
-{
-    if constexpr (V8) {
-        asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]), "=f"(a[4]), "=f"(a[5]), "=f"(a[6]), "=f"(a[7])
-                     : "l"(p));
-    } else {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(p));
-        const float4 y = __ldg(reinterpret_cast<const float4*>(p + 4));
-        a[0] = x.x, a[1] = x.y, a[2] = x.z, a[3] = x.w, a[4] = y.x, a[5] = y.y, a[6] = y.z, a[7] = y.w;
-    }
-}
 
 template <int SR, bool V8>
 __global__ void __launch_bounds__(RTHREADS, TROP_RESOLVE2_MINB) k_argmax_resolve_rows(TiledParams p)
@@ -1496,6 +1727,25 @@ const char* resolve_kind(const GemmDesc& g, bool vecA)
     return g.K <= PanelShape<32>::GK ? "panel32" : "panel16";
 }
 
+// The fused GEMM + resolve launch (k_gemm_tma_fused) serves the layouts of the short-K row
+// resolve once the TMA-fed kernel is chosen, when its item count fits 31 bits.
+#ifndef TROP_TMA_FUSED
+#define TROP_TMA_FUSED 1
+#endif
+bool fused_ok(const GemmDesc& g, bool vecA, uint64_t T, int64_t nbatch)
+{
+    if (!TROP_TMA_FUSED || resolve_kind(g, vecA)[0] != 'r') return false;
+    const uint64_t items = T + (uint64_t)nbatch * (uint64_t)((g.N + FPW - 1) / FPW) * (uint64_t)((g.M + FRB - 1) / FRB);
+    return items < (uint64_t(1) << 31);
+}
+// every row of A starts 32-byte aligned: a resolve lane loads its chunk of A in one piece
+bool a_rows_32b(const TiledParams& p)
+{
+    bool v8 = ((uintptr_t)p.A % 32) == 0 && p.sAm % 8 == 0;
+    for (int d = 0; d < p.bt.nb; ++d) v8 = v8 && p.bt.sA[d] % 8 == 0;
+    return v8;
+}
+
 void resolve_split(TiledParams& p, uint64_t grid, uint32_t npan)
 {
     p.r_per = p.r_units / grid;
@@ -1558,9 +1808,7 @@ int launch_resolve_short(TiledParams& p, int64_t M, int64_t nbatch, cudaStream_t
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // A's chunks by one 32-byte load each when every row start is 32-byte aligned
-    bool v8 = ((uintptr_t)p.A % 32) == 0 && p.sAm % 8 == 0;
-    for (int d = 0; d < p.bt.nb; ++d) v8 = v8 && p.bt.sA[d] % 8 == 0;
-    cudaError_t e = v8 ? cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR, true>, p)
+    cudaError_t e = a_rows_32b(p) ? cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR, true>, p)
                        : cudaLaunchKernelEx(&cfg, k_argmax_resolve_rows<SR, false>, p);
     if (e != cudaSuccess) return cuda_error(e, "k_argmax_resolve_rows");
     return check_launch("k_argmax_resolve_rows");
@@ -1727,7 +1975,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     p.T_dp = (uint32_t)(G_sk ? T - R : T);
 
     int rc = TROP_OK;
-    bool launched = false;
+    bool launched = false, fused = false;
     if constexpr (ARG) {
         // whole tiles, one batch axis, whole k-tiles: operands by TMA
         if (!G_sk && tma_layout_ok(g, p.bt, nbatch)) {
@@ -1746,8 +1994,32 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                 attr[0].val.programmaticStreamSerializationAllowed = 1;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
-                const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tma<SR>, maps, p);
-                rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma") : check_launch("k_gemm_tma");
+                if (fused_ok(g, p.vecA != 0, T, nbatch) &&
+                    make_map(&maps.bp, p.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)nbatch, g.sBk, sBb, FPW,
+                             (uint32_t)g.K) &&
+                    stream_tickets(s, 1 + 2 * (size_t)nbatch, &p.sched) == TROP_OK) {
+                    // GEMM and resolve in one launch (k_gemm_tma_fused)
+                    const uint32_t npan = (uint32_t)((g.N + FPW - 1) / FPW);
+                    p.rblocks = (uint32_t)((g.M + FRB - 1) / FRB);
+                    p.items_per_batch = npan * p.rblocks;
+                    p.tiles_per_batch = p.tiles_m * p.tiles_n;
+                    p.n_tiles = (uint32_t)T;
+                    p.n_items = (uint32_t)(T + (uint64_t)nbatch * p.items_per_batch);
+                    p.div_ipb = make_fastdiv(p.items_per_batch);
+                    p.div_rblocks = make_fastdiv(p.rblocks);
+#if TROP_DEBUG_BOUNDS
+                    p.sp[7] = span_bytes(p.sched, (1 + 2 * (size_t)nbatch) * sizeof(uint32_t));
+#endif
+                    cfg.gridDim = dim3(p.n_items);
+                    const cudaError_t e = a_rows_32b(p) ? cudaLaunchKernelEx(&cfg, k_gemm_tma_fused<SR, true>, maps, p)
+                                                        : cudaLaunchKernelEx(&cfg, k_gemm_tma_fused<SR, false>, maps, p);
+                    rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma_fused") : check_launch("k_gemm_tma_fused");
+                    fused = true;
+                } else {
+                    clear_error();  // (no tickets: the two-pass form below)
+                    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tma<SR>, maps, p);
+                    rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma") : check_launch("k_gemm_tma");
+                }
                 launched = true;
             }
         }
@@ -1756,7 +2028,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
         (void)launch_pdl(k_gemm_tiled<SR, ARG, TN>, dim3((unsigned)(p.T_dp + G_sk)), dim3(THREADS), 0, s, p);
         rc = check_launch("k_gemm_tiled");
     }
-    if (rc == TROP_OK && ARG) rc = launch_resolve<SR>(p, g, nbatch, s, dev);
+    if (rc == TROP_OK && ARG && !fused) rc = launch_resolve<SR>(p, g, nbatch, s, dev);
     if (ws) pool_retire(ws, s);
     return rc;
 }
@@ -2056,8 +2328,9 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
             const Batch bt = make_batch(gs, nbatch);
             bool va = ((uintptr_t)gs.A % 16) == 0 && gs.sAm % 4 == 0;
             for (int d = 0; d < bt.nb; ++d) va = va && bt.sA[d] % 4 == 0;
-            snprintf(extra, sizeof(extra), " kernel=%s resolve=%s",
-                     !split && tma_layout_ok(gs, bt, nbatch) ? "tma" : "tiled", resolve_kind(gs, va));
+            const bool tma = !split && tma_layout_ok(gs, bt, nbatch);
+            snprintf(extra, sizeof(extra), " kernel=%s resolve=%s", tma ? "tma" : "tiled",
+                     tma && fused_ok(gs, va, T, nbatch) ? "fused" : resolve_kind(gs, va));
         }
         snprintf(buf, n, " route=tiled%s%s%s%s", swap ? " swap" : "", staged ? " staged" : "",
                  split ? " split_tail" : "", extra);

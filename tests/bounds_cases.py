@@ -3,8 +3,8 @@
 Run as a script in a process of its own with TROP_LIBRARY=debug (the package then loads
 ``_build_debug/libtropical_gb300.so``): every stage of the path -- permutes (row copy,
 tiled transpose, generic gather, value + argmax pairs), traces and reductions (per-thread,
-tiled and split), the f32 GEMM on each of its routes (TMA-fed with both resolve passes,
-register-tiled with stream-K, streaming, generic), the f64 and integer GEMMs, the backward
+tiled and split), the f32 GEMM on each of its routes (TMA-fed with the fused short-K resolve
+or followed by the panel resolve, register-tiled with stream-K, streaming, generic), the f64 and integer GEMMs, the backward
 in all three semirings, pairwise einsums and a contraction tree with back-tracking -- is
 compared with the oracle, and the library's violation record is read at the end.  Prints
 one JSON line: {"library", "cases", "failures": [...], "report": {...}}.
@@ -116,7 +116,7 @@ def main() -> int:
             same(f"gemm {dtype} sr{sr} {shape} argmax", i.cpu().numpy(), wa)
 
     for sr in (0, 1, 2):
-        case(f"gemm TMA + short resolve sr{sr}", lambda sr=sr: gemm(sr, (64, 256, 256, 256)))
+        case(f"gemm TMA fused with the resolve sr{sr}", lambda sr=sr: gemm(sr, (64, 256, 256, 256)))
         case(f"gemm TMA + panel resolve sr{sr}", lambda sr=sr: gemm(sr, (32, 256, 256, 1024)))
         case(f"gemm tiled ragged sr{sr}", lambda sr=sr: gemm(sr, (3, 70, 45, 37)))
         case(f"gemm stream-K sr{sr}", lambda sr=sr: gemm(sr, (2, 129, 65, 1030)))

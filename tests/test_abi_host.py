@@ -108,14 +108,15 @@ def _contig(shape):
     return list(reversed(st))
 
 
-@pytest.mark.parametrize("k, kernel, resolve", [(256, "tma", "rows"), (64, "tma", "rows"), (16, "tma", "rows"),
+@pytest.mark.parametrize("k, kernel, resolve", [(256, "tma", "fused"), (64, "tma", "fused"), (16, "tma", "fused"),
                                                 (512, "tma", "panel32"), (1024, "tma", "panel16"),
                                                 (40, "tiled", "rows"), (72, "tiled", "rows"),
                                                 (257, "tiled", "panel64")])
 def test_describe_names_gemm_kernel_and_resolve(trop, k, kernel, resolve):
     """The planner reports which argmax GEMM kernel and resolve pass a layout takes: the TMA-fed
     kernel needs one batch axis, K a multiple of 16 and 16-byte row strides; the row resolve
-    needs K <= 256 in whole chunks of 8.  Batch 64 of 128 x 128 tiles fills more than half a
+    needs K <= 256 in whole chunks of 8, and after the TMA-fed kernel it runs in the same launch
+    ("fused").  Batch 64 of 128 x 128 tiles fills more than half a
     wave, so no tile is split along k (a split tail takes the cp.async kernel)."""
     sa, sb = [64, 128, k], [64, k, 128]
     text = trop.plan_describe("zmk,zkn->zmn", sa, _contig(sa), sb, _contig(sb))
@@ -143,11 +144,12 @@ def test_describe_tma_needs_aligned_rows_and_one_batch_axis(trop):
 
 def test_describe_wide_row_strides_leave_the_32_bit_paths(trop):
     """A row stride past 2^31 elements keeps the GEMM on 64-bit offsets: the short-K row resolve
-    (32-bit row offsets) gives way to the 64-bit panel resolve, at any M."""
+    (32-bit row offsets, in its own launch or fused with the TMA-fed GEMM) gives way to the
+    64-bit panel resolve, at any M."""
     wide = (1 << 31) + 64
     sb = [1, 64, 128]
     narrow = trop.plan_describe("zmk,zkn->zmn", [1, 16, 64], [16 * 64, 64, 1], sb, _contig(sb))
-    assert "route=tiled" in narrow and "resolve=rows" in narrow, narrow
+    assert "route=tiled" in narrow and ("resolve=rows" in narrow or "resolve=fused" in narrow), narrow
     text = trop.plan_describe("zmk,zkn->zmn", [1, 16, 64], [16 * wide, wide, 1], sb, _contig(sb))
     assert "route=tiled" in text and "resolve=panel64" in text, text
     assert f"sAm={wide}" in text, text
