@@ -58,7 +58,7 @@ class TropNode(ctypes.Structure):
 
 _STAT_FIELDS = ["module_inits", "kernel_launches", "pool_allocs", "pool_hits", "pool_device_mallocs",
                 "pool_retired", "pool_released", "pool_event_waits", "pool_leaked", "pool_bytes_cached",
-                "stream_syncs", "plan_cache_hits", "plan_cache_misses"]
+                "stream_syncs", "plan_cache_hits", "plan_cache_misses", "gemm_early_starts"]
 
 
 class TropStats(ctypes.Structure):

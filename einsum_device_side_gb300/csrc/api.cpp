@@ -1342,6 +1342,7 @@ extern "C" int tropical_tree_plan_run(trop_tree_plan plan, void* stream)
     if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
     if (dev != plan->device)
         return set_error(TROP_ERR_DEVICE_MISMATCH, "plan belongs to device %d, current device is %d", plan->device, dev);
+    note_stream_op();  // a graph launch: the next kernel waits for the whole graph
     e = cudaGraphLaunch(plan->exec, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
     count_launches(plan->launches);

@@ -180,6 +180,9 @@ struct TiledParams {
     uint32_t* sched;
     uint32_t n_tiles, n_items, tiles_per_batch, items_per_batch, rblocks;
     FastDiv div_ipb, div_rblocks;
+    // 1: the grid before on the stream is a fused GEMM whose outputs this launch does not read,
+    // so the wait for it comes only ahead of this launch's first global store; 0: at the start
+    int late;
 #if TROP_DEBUG_BOUNDS
     Span sp[8];  // A, B, C, I, seg_v, seg_c, sk_cnt, sched
 #endif
@@ -811,6 +814,9 @@ __device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams&
     }
     int64_t oa, ob, oc, oi;
     batch_offsets(p.bt, b, oa, ob, oc, oi);
+    // (fused kernel: the grid before may still run when its wait was left until the stores;
+    // nothing is stored before it has completed)
+    if constexpr (!PDL) pdl_wait();
     if (tid == 0 && s_gaveup) atomicAdd(&g_wait_timeouts, 1u);
     if (s_fail) {
         // Abandon the tile: wait (bounded) for every copy still in flight into this CTA's
@@ -958,11 +964,15 @@ __device__ __forceinline__ void fused_resolve(const TmaMaps& maps, const TiledPa
     }
     __syncthreads();
     if (tid == 0) {
-        // B's panel is an input of the GEMM, not a result: its copy overlaps the wait
+        // B's panel is an input of the GEMM, not a result: its copy overlaps the waits
         mbar_expect_tx(&sm.bar, (uint32_t)(p.K * FPW * sizeof(float)));
         tma_load_3d(&sm.EB[0][0], &maps.bp, n0, 0, (int)b, &sm.bar);
-        s_ok = T_IN(p.sched + 1 + b, 4, 7) && wait_count(p.sched + 1 + b, p.tiles_per_batch) ? 1 : 0;
     }
+    // the grid before has completed (when it was not waited for at the start): the counters of
+    // this ticket half were last used two launches back, by a grid now complete
+    pdl_wait();
+    if (tid == 0)
+        s_ok = T_IN(p.sched + 1 + b, 4, 7) && wait_count(p.sched + 1 + b, p.tiles_per_batch) ? 1 : 0;
     const bool landed = mbar_wait(&sm.bar, 0);
     // thread 0's acquire of the batch's count, then this barrier: the batch's codes are visible
     const bool all_landed = __syncthreads_and(landed ? 1 : 0) != 0;
@@ -1061,15 +1071,25 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
     __shared__ FusedSmem sm;
     __shared__ uint32_t s_item;
     __shared__ int s_ok;
-    // a programmatic dependent of the grid before: take an item only once it has completed
-    pdl_wait();
-    pdl_signal();
+    // A programmatic dependent of the grid before.  Normally nothing starts before that grid
+    // has completed.  With p.late (that grid is a fused GEMM whose outputs this launch does not
+    // read) the tiles load and compute at once and wait only ahead of their stores, and the
+    // resolve items ahead of their counters.  The item counter is the other half of the
+    // stream's tickets: its last user is the launch two back, whose CTAs had all taken their
+    // items (and the last one zeroed it) before the grid before was let start.
+    if (!p.late) pdl_wait();
     if (threadIdx.x == 0) {
         const uint32_t it = T_IN(p.sched, 4, 7) ? atomicAdd(p.sched, 1u) : 0u;
-        if (it == p.n_items - 1) p.sched[0] = 0;  // the last item taken: zero for the next launch
+        if (it == p.n_items - 1) {
+            // the last item taken: zero the counter for the launch after next, performed before
+            // this CTA lets the next launch start
+            p.sched[0] = 0;
+            __threadfence();
+        }
         s_item = it;
     }
     __syncthreads();
+    pdl_signal();  // after the claim: the next launch may reuse the counters this one left
     const uint32_t it = s_item;
     if (it < p.n_tiles) {
         uint32_t b;
@@ -1738,6 +1758,41 @@ bool fused_ok(const GemmDesc& g, bool vecA, uint64_t T, int64_t nbatch)
     const uint64_t items = T + (uint64_t)nbatch * (uint64_t)((g.N + FPW - 1) / FPW) * (uint64_t)((g.M + FRB - 1) / FRB);
     return items < (uint64_t(1) << 31);
 }
+// The byte range [lo, hi) a GEMM operand view addresses (batch axes, then rows and columns).
+void view_range(const void* base, size_t eb, const GemmDesc& g, int64_t rows, int64_t cols, int64_t srow,
+                int64_t scol, const int64_t* sb, uintptr_t& lo, uintptr_t& hi)
+{
+    int64_t a = 0, z = 0;
+    bool empty = rows <= 0 || cols <= 0;
+    auto add = [&](int64_t n, int64_t st) {
+        if (n <= 0) empty = true;
+        else (st < 0 ? a : z) += (n - 1) * st;
+    };
+    for (int d = 0; d < g.nb; ++d) add(g.bsize[d], sb[d]);
+    add(rows, srow);
+    add(cols, scol);
+    const uintptr_t b = (uintptr_t)base;
+    lo = empty ? b : b + a * (int64_t)eb;
+    hi = empty ? b : b + (z + 1) * (int64_t)eb;
+}
+// the two outputs (values, argmax) of g, into a launch record
+void output_ranges(const GemmDesc& g, LaunchRecord& r)
+{
+    view_range(g.C, sizeof(float), g, g.M, g.N, g.sCm, g.sCn, g.sCb, r.lo[0], r.hi[0]);
+    view_range(g.I, sizeof(int32_t), g, g.M, g.N, g.sIm, g.sIn, g.sIb, r.lo[1], r.hi[1]);
+}
+// whether g reads (A or B) any byte the launch of r writes
+bool reads_overlap(const GemmDesc& g, const LaunchRecord& r)
+{
+    uintptr_t lo[2], hi[2];
+    view_range(g.A, sizeof(float), g, g.M, g.K, g.sAm, g.sAk, g.sAb, lo[0], hi[0]);
+    view_range(g.B, sizeof(float), g, g.K, g.N, g.sBk, g.sBn, g.sBb, lo[1], hi[1]);
+    for (int i = 0; i < 2; ++i)
+        for (int j = 0; j < 2; ++j)
+            if (lo[i] < r.hi[j] && r.lo[j] < hi[i]) return true;
+    return false;
+}
+
 // every row of A starts 32-byte aligned: a resolve lane loads its chunk of A in one piece
 bool a_rows_32b(const TiledParams& p)
 {
@@ -1994,10 +2049,18 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                 attr[0].val.programmaticStreamSerializationAllowed = 1;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
+                const size_t half = 1 + 2 * (size_t)nbatch;  // tickets of one launch
                 if (fused_ok(g, p.vecA != 0, T, nbatch) &&
                     make_map(&maps.bp, p.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)nbatch, g.sBk, sBb, FPW,
                              (uint32_t)g.K) &&
-                    stream_tickets(s, 1 + 2 * (size_t)nbatch, &p.sched) == TROP_OK) {
+                    stream_tickets(s, 2 * half, &p.sched) == TROP_OK) {
+                    // two halves of tickets used in turn by the fused GEMMs on a stream; start early
+                    // when the GEMM just before is one of them and wrote nothing this one reads
+                    const LaunchRecord prev = capture_arena() ? LaunchRecord{} : stream_record(s);
+                    const bool follows = prev.valid && prev.seq == launch_seq();
+                    const int parity = follows ? prev.parity ^ 1 : 0;
+                    p.late = follows && !reads_overlap(g, prev) ? 1 : 0;
+                    p.sched += parity * half;
                     // GEMM and resolve in one launch (k_gemm_tma_fused)
                     const uint32_t npan = (uint32_t)((g.N + FPW - 1) / FPW);
                     p.rblocks = (uint32_t)((g.M + FRB - 1) / FRB);
@@ -2008,13 +2071,22 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                     p.div_ipb = make_fastdiv(p.items_per_batch);
                     p.div_rblocks = make_fastdiv(p.rblocks);
 #if TROP_DEBUG_BOUNDS
-                    p.sp[7] = span_bytes(p.sched, (1 + 2 * (size_t)nbatch) * sizeof(uint32_t));
+                    p.sp[7] = span_bytes(p.sched, half * sizeof(uint32_t));
 #endif
                     cfg.gridDim = dim3(p.n_items);
                     const cudaError_t e = a_rows_32b(p) ? cudaLaunchKernelEx(&cfg, k_gemm_tma_fused<SR, true>, maps, p)
                                                         : cudaLaunchKernelEx(&cfg, k_gemm_tma_fused<SR, false>, maps, p);
                     rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma_fused") : check_launch("k_gemm_tma_fused");
                     fused = true;
+                    if (rc == TROP_OK) {
+                        if (p.late) count_early_start();
+                        LaunchRecord cur{};
+                        cur.valid = !capture_arena();
+                        cur.seq = launch_seq();
+                        cur.parity = parity;
+                        output_ranges(g, cur);
+                        set_stream_record(s, cur);
+                    }
                 } else {
                     clear_error();  // (no tickets: the two-pass form below)
                     const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tma<SR>, maps, p);

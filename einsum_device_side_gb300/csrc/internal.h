@@ -53,6 +53,25 @@ int wait_test_mode();
 
 // ---------------------------------------------------------------- counters
 void count_launches(int64_t n);
+// Kernels this library has launched (on any device or stream, captured or not), plus stream
+// operations that end a chain of programmatic dependents (graph launches): a value that has
+// not moved since a launch means nothing of this library was enqueued after it.
+uint64_t launch_seq();
+void note_stream_op();
+void count_early_start();
+
+// The last fused GEMM launched on a stream (gemm.cu): the launch_seq() right after it, the half
+// of its stream tickets it used, and the byte ranges [lo, hi) of its two outputs.  A GEMM that
+// follows it directly may read its operands before that grid has completed when they lie
+// outside those ranges.
+struct LaunchRecord {
+    bool valid;
+    uint64_t seq;
+    int parity;
+    uintptr_t lo[2], hi[2];
+};
+LaunchRecord stream_record(cudaStream_t s);
+void set_stream_record(cudaStream_t s, const LaunchRecord& r);
 void count_module_init();
 void count_plan(bool hit);  // plan cache of the pairwise einsum (api.cpp)
 void count_pool(int field, int64_t n);  // field: see pool.cu

@@ -75,14 +75,19 @@ static thread_local CaptureArena* t_arena = nullptr;
 void set_capture_arena(CaptureArena* a) { t_arena = a; }
 CaptureArena* capture_arena() { return t_arena; }
 
+static std::atomic<uint64_t> g_launch_seq{0};
 void count_launches(int64_t n)
 {
     if (t_arena) t_arena->launches += n;
     else c_launches += n;
+    g_launch_seq.fetch_add(1, std::memory_order_acq_rel);
 }
+uint64_t launch_seq() { return g_launch_seq.load(std::memory_order_acquire); }
+void note_stream_op() { g_launch_seq.fetch_add(1, std::memory_order_acq_rel); }
 void count_module_init() { c_module_inits += 1; }
-static std::atomic<int64_t> c_plan_hits{0}, c_plan_misses{0};
+static std::atomic<int64_t> c_plan_hits{0}, c_plan_misses{0}, c_early{0};
 void count_plan(bool hit) { (hit ? c_plan_hits : c_plan_misses) += 1; }
+void count_early_start() { c_early += 1; }
 void count_pool(int field, int64_t n) { c_pool[field] += n; }
 
 // ------------------------------------------------------------------ fast divmod
@@ -544,6 +549,45 @@ Tickets& tickets()
 }
 }  // namespace
 
+namespace {
+struct Records {
+    std::mutex mu;
+    std::map<std::pair<int, cudaStream_t>, trop::LaunchRecord> last;
+};
+Records& records()
+{
+    static Records* r = new Records();
+    return *r;
+}
+}  // namespace
+
+trop::LaunchRecord trop::stream_record(cudaStream_t s)
+{
+    LaunchRecord r{};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return r;
+    }
+    Records& R = records();
+    std::lock_guard<std::mutex> lk(R.mu);
+    auto it = R.last.find(std::make_pair(dev, s));
+    if (it != R.last.end()) r = it->second;
+    return r;
+}
+
+void trop::set_stream_record(cudaStream_t s, const LaunchRecord& r)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    Records& R = records();
+    std::lock_guard<std::mutex> lk(R.mu);
+    R.last[std::make_pair(dev, s)] = r;
+}
+
 int trop::stream_tickets(cudaStream_t s, size_t count, uint32_t** out)
 {
     *out = nullptr;
@@ -695,6 +739,7 @@ extern "C" int tropical_stats(trop_stats* out)
     out->pool_leaked = c_pool[ST_LEAKED].load();
     out->plan_cache_hits = c_plan_hits.load();
     out->plan_cache_misses = c_plan_misses.load();
+    out->gemm_early_starts = c_early.load();
     {
         Pool& P = pool();
         std::lock_guard<std::mutex> lk(P.mu);
@@ -710,6 +755,7 @@ extern "C" void tropical_reset_stats(void)
     c_stream_syncs = 0;
     c_plan_hits = 0;
     c_plan_misses = 0;
+    c_early = 0;
     for (int i = 0; i < 7; ++i) c_pool[i] = 0;  // ST_BYTES is derived, module_inits kept
 }
 

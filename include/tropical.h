@@ -142,6 +142,9 @@ typedef struct {
     int64_t plan_cache_hits;     /* pairwise einsums (eager calls and tree nodes) whose
                                     lowering came from the plan cache */
     int64_t plan_cache_misses;   /* ... that were lowered (and then cached) */
+    int64_t gemm_early_starts;   /* argmax GEMMs (one-launch form) that began loading and
+                                    computing before the GEMM just before them on the stream
+                                    had finished: their operands were outside its outputs */
 } trop_stats;
 
 /* Set up the kernels for `device` once (kernel attributes, device

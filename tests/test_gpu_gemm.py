@@ -399,3 +399,67 @@ def test_tma_path_integer_ties_padded_rows(trop, sr, shape):
     rc, ri = oracle.gemm(a, b, sr, nthreads=0)
     assert c.cpu().numpy().tobytes() == np.ascontiguousarray(rc).tobytes()
     np.testing.assert_array_equal(i.cpu().numpy(), ri)
+
+
+# ---------------------------------------------------------------- back-to-back one-launch GEMMs
+
+def _gemm_set(sr, batch=24):
+    """batch x 256^3: enough tiles for the TMA-fed kernel with its resolve in the same launch."""
+    return synth.gemm_batched_inputs(sr, batch=batch)
+
+
+def test_back_to_back_gemms_start_early_and_stay_exact(trop):
+    """Three argmax GEMMs on one stream with disjoint buffers: the second and third read nothing
+    the one before writes, so each starts loading and computing before that one has finished
+    (gemm_early_starts), and every output still equals the oracle's, over repeated rounds."""
+    sets = [_gemm_set(sr) for sr in SR]
+    dev = [(_dev(a), _dev(b)) for a, b in sets]
+    ref = [oracle.gemm(a, b, sr, nthreads=0) for sr, (a, b) in zip(SR, sets)]
+    outs = [(torch.empty((24, 256, 256), device="cuda"), torch.empty((24, 256, 256), dtype=torch.int32, device="cuda"))
+            for _ in SR]
+    desc = trop.plan_describe("zmk,zkn->zmn", [24, 256, 256], [65536, 256, 1], [24, 256, 256], [65536, 256, 1])
+    assert "resolve=fused" in desc, desc
+    trop.reset_stats()
+    rounds = 8
+    for _ in range(rounds):
+        for sr in SR:
+            trop.gemm(dev[sr][0], dev[sr][1], sr, out=outs[sr][0], out_argmax=outs[sr][1])
+    torch.cuda.synchronize()
+    assert trop.stats()["gemm_early_starts"] >= rounds * 3 - 1
+    for sr in SR:
+        assert outs[sr][0].cpu().numpy().tobytes() == ref[sr][0].tobytes()
+        np.testing.assert_array_equal(outs[sr][1].cpu().numpy(), ref[sr][1])
+
+
+def test_gemm_reading_the_previous_output_waits_for_it(trop):
+    """A GEMM whose operand is the previous GEMM's output must not start before that one has
+    finished: no early start is counted for it, and the chain's result equals the oracle's."""
+    a, b = _gemm_set(0)
+    _, b2 = synth.gemm_batched_inputs(0, batch=24, m=256, n=256, k=256)
+    ad, bd, b2d = _dev(a), _dev(b), _dev(b2[:, :, ::-1])
+    c1, _ = trop.gemm(ad, bd, 0)
+    trop.reset_stats()
+    c2, i2 = trop.gemm(c1, b2d, 0)          # reads c1, written by the call just before
+    torch.cuda.synchronize()
+    assert trop.stats()["gemm_early_starts"] == 0
+    rc1, _ = oracle.gemm(a, b, 0, nthreads=0)
+    rc2, ri2 = oracle.gemm(rc1, np.ascontiguousarray(b2[:, :, ::-1]), 0, nthreads=0)
+    assert c2.cpu().numpy().tobytes() == rc2.tobytes()
+    np.testing.assert_array_equal(i2.cpu().numpy(), ri2)
+
+
+def test_gemm_after_another_library_kernel_waits(trop):
+    """A permute of this library between two GEMMs ends the chain: the second GEMM waits for
+    the grid before it at its start (no early start), results exact."""
+    a, b = _gemm_set(1)
+    ad, bd = _dev(a), _dev(b)
+    trop.gemm(ad, bd, 1)
+    x = _dev(synth.uniform_f32(5, (64, 64), -1, 1))
+    trop.permute_trace(x, "ij->ji")
+    trop.reset_stats()
+    c, i = trop.gemm(ad, bd, 1)
+    torch.cuda.synchronize()
+    assert trop.stats()["gemm_early_starts"] == 0
+    rc, ri = oracle.gemm(a, b, 1, nthreads=0)
+    assert c.cpu().numpy().tobytes() == rc.tobytes()
+    np.testing.assert_array_equal(i.cpu().numpy(), ri)
