@@ -58,7 +58,7 @@ def code_sha256(path):
 def gemm_traffic():
     """DRAM bytes of one tropical GEMM call from the committed ncu summary, or
     None when the GEMM source's code changed since those counters were taken."""
-    f = os.path.join(ROOT, "profiles", "k_gemm_tma_traffic.txt")
+    f = os.path.join(ROOT, "profiles", "k_gemm_tma_fused_traffic.txt")
     if not os.path.exists(f):
         return None
     kv = dict(line.split(": ", 1) for line in open(f).read().splitlines() if ": " in line)
@@ -280,8 +280,8 @@ def secondary(trop, torch, pk, reps=20):
     out["trace_iijk->ijk"] = {"GB/s": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "us": t * 1e6,
                               "us_device": None if tg is None else tg * 1e6,
                               "GB/s_device": None if tg is None else moved / tg / 1e9,
-                              "note": "us: one API call (host bound at 4 MiB); us_device: per call inside a "
-                                      "replayed CUDA graph of 20 calls; permutes rotate 3 buffer pairs (384 MiB)"}
+                              "note": "us: one API call, timed over many back to back (host bound at 4 MiB); "
+                                      "us_device: per call inside a replayed CUDA graph of 20 calls"}
     # the '->jk' variant of the trace: (+)-reduction over the diagonal label as well
     yj = torch.empty((64, 64), device="cuda")
     t = timed(lambda: trop.permute_trace(tr, "iijk->jk", out=yj), hb)
@@ -323,6 +323,16 @@ def secondary(trop, torch, pk, reps=20):
     out["gemm_backward_b64x256"] = {"us": t * 1e6, "GB/s": moved / t / 1e9, "frac_hbm": moved / t / 1e9 / pk["hbm_gbs"],
                                     "note": "dA and dB of one max-plus call; bytes = argmax and dC read once per "
                                             "gradient + both gradients written"}
+    # max-times: each routed term is dC times the other operand at the winner (gathered)
+    ma, mb = synth.gemm_batched_inputs(2)
+    mad, mbd = torch.from_numpy(ma).cuda(), torch.from_numpy(mb).cuda()
+    _, mi = trop.gemm(mad, mbd, 2)
+    t = timed(lambda: trop.gemm_backward(mad, mbd, gdc, mi, 2, out_a=gda, out_b=gdb), reps)
+    moved_mt = moved + mad.numel() * 4 + mbd.numel() * 4
+    out["gemm_backward_maxtimes_b64x256"] = {"us": t * 1e6, "GB/s": moved_mt / t / 1e9,
+                                             "frac_hbm": moved_mt / t / 1e9 / pk["hbm_gbs"],
+                                             "note": "as the max-plus entry, plus A and B read once for the "
+                                                     "operand factors"}
     # the same batched GEMM in binary64 (max-plus with argmax): one double add per semiring op
     fa, fb = synth.gemm_batched_inputs(0, dtype="f64")
     fad, fbd = torch.from_numpy(fa).cuda(), torch.from_numpy(fb).cuda()
@@ -566,10 +576,10 @@ def run_gpu(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": region_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "strided-batched tropical GEMM + int32 argmax, batch 64 x M=N=K=256, "
-                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 GEMM calls (k_gemm_tma + k_argmax_resolve_rows each)",
+                               "maxplus + minplus (uniform(-1,1)) + maxtimes (uniform(0,1)); one step = 3 GEMM calls, back to back on one stream (one k_gemm_tma_fused launch each: TMA-fed tiles + argmax resolve)",
                    "parallelism": f"replicas x{world}",
                    "l2": f"{N_SETS} rotated input sets (288 MiB of operands) so each step reads cold inputs"},
-        "roofline": {"bound": "alu", "kernel": "k_gemm_tma+k_argmax_resolve_rows (one tropical GEMM call)",
+        "roofline": {"bound": "alu", "kernel": "k_gemm_tma_fused (one tropical GEMM call)",
                      "achieved": achieved, "peak": peak_ops / 1e9,
                      "unit": "G semiring-ops/s", "frac": achieved / (peak_ops / 1e9), "traffic": traffic,
                      "peak_def": f"{sms} SMs x 128 FP32 lanes x {pk['sm_max_mhz']:.0f} MHz / 2 (add + max)",
