@@ -32,6 +32,6 @@ def test_code_hash_sees_code_and_string_literals(tmp_path):
 
 
 def test_traffic_record_parses():
-    f = os.path.join(ROOT, "profiles", "k_gemm_tma_traffic.txt")
+    f = os.path.join(ROOT, "profiles", "k_gemm_tma_fused_traffic.txt")
     kv = dict(line.split(": ", 1) for line in open(f).read().splitlines() if ": " in line)
     assert int(kv["bytes_per_launch"]) > 0 and len(kv["source_code_sha256"]) == 64
