@@ -11,19 +11,18 @@
 // selection, deterministic with duplicate indices and free of atomics.)
 //
 // The adjoint needs no sort: each output line (a row of dA, a column of dB) is
-// walked in increasing order by the lanes that own its bins, one lane per
-// (line, bin range), adding into bins of its own in shared memory -- every bin
-// has one writer adding in the stated order, so every sum is the sequential
-// one, bit for bit.  For max-times both gradients take k_route_match instead
-// (a warp per line, the lanes of one bin applied in step order), which keeps
-// its gathers of the other operand in flight across a whole warp.  A CTA takes 32 lines; its 8 warps split a span of 256
-// bins and all walk the same staged block (32 lines x 32 steps of argmax and
-// dC), which the CTA loads coalesced along whichever index is contiguous and
-// double buffers.  Longer contractions repeat the walk per 256-bin span.  dA
-// and dB are two jobs of one launch (blockIdx.y) of k_winner_route, except
-// that for max-plus and min-plus the rows of dA, when their steps are
-// contiguous, go to k_route_lane (one lane owns a whole line) in a launch of
-// their own that the dB launch may overlap.
+// walked in increasing step order, and every bin of it has one writer adding in
+// that order, so every sum is the sequential one, bit for bit.
+//   k_route_lane   max-plus and min-plus, both gradients in one launch
+//                  (blockIdx.y): one lane per line with all of the line's bins
+//                  in shared memory; rows of dA by 16-byte vector loads along
+//                  the line, columns of dB by one load per step (consecutive
+//                  lanes, consecutive columns: 128 contiguous bytes a step).
+//   k_route_match  max-times: a warp per line, the lanes of one bin applied in
+//                  step order, which keeps the gathers of the other operand in
+//                  flight across a whole warp; dA and dB in two launches that
+//                  overlap.
+// Longer contractions repeat the walk per 256-bin span.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,19 +34,6 @@
 
 namespace trop {
 namespace {
-
-#ifndef TROP_ROUTE_WARPS
-#define TROP_ROUTE_WARPS 4
-#endif
-#ifndef TROP_ROUTE_MATCH
-#define TROP_ROUTE_MATCH 1
-#endif
-constexpr int BW_WARPS = TROP_ROUTE_WARPS, BW_THREADS = BW_WARPS * 32;
-constexpr int BW_SPAN = 256;                // bins a CTA covers per walk
-constexpr int BW_KL = BW_SPAN / BW_WARPS;   // bins per lane
-constexpr int BW_LD = 33;                   // padded rows: [bin][line] and [line][step]
-constexpr int BW_BLK = 32 * BW_LD;          // one staged 32 x 32 block
-constexpr size_t BW_SMEM = sizeof(float) * (BW_WARPS * BW_KL * BW_LD + 4 * BW_BLK) + 2 * 32 * sizeof(int64_t);
 
 // One gradient: owners (b, x), x < X, each walking s < S.
 //   index and dC of (b, x, s):     I[b*sIb + x*sIx + s*sIs], G[b*sGb + x*sGx + s*sGs]
@@ -63,6 +49,7 @@ struct RouteJob {
     int64_t sPb, sPk, sPs;
     float* O;
     int64_t sOb, sOx, sOk;
+    int vec;  // k_route_lane: the line's steps are contiguous and 16-byte aligned (vector loads)
 #if TROP_DEBUG_BOUNDS
     Span sp[4];  // I, G, P, O
 #endif
@@ -77,149 +64,24 @@ struct RouteParams {
     RouteJob job[2];
     int njobs;
     // 0: wait for the grid before this one at the start (it may have signalled before its own
-    // results were complete); 1: the grid before is k_route_lane of the same call, which
-    // signals only after its own wait, so the inputs are complete -- wait at the end instead, so
-    // that this grid completes only after that one
+    // results were complete); 1: the grid before is the other gradient's k_route_match of the
+    // same call, which signals only after its own wait, so the inputs are complete -- wait at the
+    // end instead, so that this grid completes only after that one
     int late_wait;
 };
 
-template <bool MUL>
-__global__ void __launch_bounds__(BW_THREADS) k_winner_route(RouteParams p)
-{
-    extern __shared__ __align__(16) float smem_all[];
-    if (!p.late_wait) pdl_wait();
-    pdl_signal();
-    if ((int)blockIdx.y >= p.njobs) {
-        if (p.late_wait) pdl_wait();
-        return;
-    }
-    const RouteJob& j = p.job[blockIdx.y];
-    const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-    float* bins = smem_all + w * BW_KL * BW_LD;                      // this warp's [bin][line]
-    int* tk = reinterpret_cast<int*>(smem_all + BW_WARPS * BW_KL * BW_LD);  // [2][line][step]
-    float* tg = smem_all + BW_WARPS * BW_KL * BW_LD + 2 * BW_BLK;          // [2][line][step]
-    int64_t* line_i = reinterpret_cast<int64_t*>(smem_all + BW_WARPS * BW_KL * BW_LD + 4 * BW_BLK);  // [32]
-    int64_t* line_p = line_i + 32;                                   // [32] batch offset of P per line
-    const int64_t lines = p.nbatch * j.X;
-    // contiguous walk: a warp's loads cover 32 steps of one line; else 32 lines of one step
-    const bool along_walk = j.sIs == 1 && j.sIx != 1;
-    for (int64_t base = (int64_t)blockIdx.x * 32; base < lines; base += (int64_t)gridDim.x * 32) {
-        __syncthreads();  // the previous group's readers of the tables are done
-        if (tid < 32) {
-            const int64_t o = base + tid;
-            const int64_t b = o < lines ? o / j.X : 0, x = o < lines ? o - b * j.X : 0;
-            // offset of the line in argmax and dC (the entry point gives both dC's strides)
-            line_i[tid] = o < lines ? b * j.sIb + x * j.sIx : -1;
-            line_p[tid] = b * j.sPb;
-        }
-        __syncthreads();
-        // a block moves in two halves: its loads go to registers before the current block's walk,
-        // the shared stores after it, so the walk hides the load latency
-        constexpr int PER = 1024 / BW_THREADS;
-        int rk[PER];
-        float rg[PER];
-        auto fetch = [&](int64_t s0) {
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int e = tid + i * BW_THREADS;
-                const int r = along_walk ? e >> 5 : e & 31, t = along_walk ? e & 31 : e >> 5;
-                const int64_t off = line_i[r], s = s0 + t;
-                const bool in = off >= 0 && s < j.S;
-                rk[i] = in && R_IN(j.I + off + s * j.sIs, 4, 0) ? __ldg(j.I + off + s * j.sIs) : -1;
-                rg[i] = in && R_IN(j.G + off + s * j.sGs, 4, 1) ? __ldg(j.G + off + s * j.sGs) : 0.0f;
-            }
-        };
-        auto put = [&](int q) {
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int e = tid + i * BW_THREADS;
-                const int r = along_walk ? e >> 5 : e & 31, t = along_walk ? e & 31 : e >> 5;
-                tk[q * BW_BLK + r * BW_LD + t] = rk[i];
-                tg[q * BW_BLK + r * BW_LD + t] = rg[i];
-            }
-        };
-        const bool valid = line_i[l] >= 0;
-        const float* Pl = MUL ? j.P + line_p[l] : nullptr;
-        for (int64_t kc = 0; kc < p.K; kc += BW_SPAN) {
-            __syncthreads();  // the previous span's stores and walks are done with bins and stages
-            const int64_t klo = kc + (int64_t)w * BW_KL;  // this lane's bins: [klo, klo + kl)
-            const int klo32 = (int)klo;                    // K < 2^31: every index fits 32 bits
-            const unsigned kl = (unsigned)max((int64_t)0, min((int64_t)BW_KL, p.K - klo));
-#pragma unroll
-            for (int kk = 0; kk < BW_KL; ++kk) bins[kk * BW_LD + l] = 0.0f;
-            int q = 0;
-            fetch(0);
-            put(0);
-            for (int64_t s0 = 0; s0 < j.S; s0 += 32) {
-                __syncthreads();  // block s0 staged; the other buffer's readers are done
-                const bool more = s0 + 32 < j.S;
-                if (more) fetch(s0 + 32);
-                const int* mk = tk + q * BW_BLK + l * BW_LD;
-                const float* mg = tg + q * BW_BLK + l * BW_LD;
-                // a step is this lane's when its bin lies in [klo, klo + kl): one unsigned compare
-                if (MUL) {
-                    // the other operand's terms of the block: loads in flight together, then applied in order
-                    float pv[32];
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const unsigned d = (unsigned)(mk[t] - klo32);
-                        pv[t] = d < kl && R_IN(Pl + (int64_t)mk[t] * j.sPk + (s0 + t) * j.sPs, 4, 2)
-                                    ? __ldg(Pl + (int64_t)mk[t] * j.sPk + (s0 + t) * j.sPs)
-                                    : 0.0f;
-                    }
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const unsigned d = (unsigned)(mk[t] - klo32);
-                        if (d < kl) {
-                            float* dst = &bins[d * BW_LD + l];
-                            *dst = __fadd_rn(*dst, __fmul_rn(mg[t], pv[t]));
-                        }
-                    }
-                } else {
-#pragma unroll 8
-                    for (int t = 0; t < 32; ++t) {
-                        const unsigned d = (unsigned)(mk[t] - klo32);
-                        if (d < kl) {
-                            float* dst = &bins[d * BW_LD + l];
-                            *dst = __fadd_rn(*dst, mg[t]);
-                        }
-                    }
-                }
-                if (more) put(q ^ 1);
-                q ^= 1;
-            }
-            __syncwarp();
-            const int kt = (int)max((int64_t)0, min((int64_t)BW_KL, p.K - klo));
-            if (j.sOk == 1) {
-                // lanes along k: line r, 32 consecutive bins per store
-                for (int r = 0; r < 32; ++r) {
-                    const int64_t orr = base + r;
-                    if (orr >= lines) break;
-                    const int64_t br = orr / j.X, xr = orr - br * j.X;
-                    float* Or = j.O + br * j.sOb + xr * j.sOx + klo;
-                    for (int kk = l; kk < kt; kk += 32)
-                        if (R_IN(Or + kk, 4, 3)) Or[kk] = bins[kk * BW_LD + r];
-                }
-            } else if (valid) {
-                // lanes along the lines (consecutive x when sOx == 1)
-                const int64_t o = base + l, b = o / j.X, x = o - b * j.X;
-                float* Or = j.O + b * j.sOb + x * j.sOx + klo * j.sOk;
-                for (int kk = 0; kk < kt; ++kk)
-                    if (R_IN(Or + kk * j.sOk, 4, 3)) Or[kk * j.sOk] = bins[kk * BW_LD + l];
-            }
-        }
-    }
-    if (p.late_wait) pdl_wait();
-}
 
 // One lane per output line with all of the line's bins in shared memory, [bin][lane] (no bank
-// conflicts whatever the bins), for lines whose steps are contiguous and 16-byte aligned (the
-// rows of dA in the common layout).  A lane reads its own line 8 steps at a time -- one full
-// 32-byte sector per array -- through a ring of RT_RING register sets (the loads of the next
-// three chunks in flight while a chunk is applied) and applies the steps four at a time: the four bins are read
-// together, and a step whose bin an earlier step of the group also hit continues from that
-// step's new value, so every bin still adds its terms in increasing step order.  Max-plus and
-// min-plus only: the term is dC itself.
+// conflicts whatever the bins); both gradients in one launch, the job picked by blockIdx.y.  A
+// lane reads its own line 8 steps at a time through a ring of RT_RING register sets (the loads
+// of the next three chunks in flight while a chunk is applied): when the line's steps are
+// contiguous and 16-byte aligned (RouteJob::vec, the rows of dA) by 16-byte vectors, one full
+// 32-byte sector per array, otherwise one load per step through the step strides (the columns
+// of dB: consecutive lanes are consecutive columns, so a warp reads 128 contiguous bytes a
+// step).  Steps are applied four at a time: the four bins are read together, and a step whose
+// bin an earlier step of the group also hit continues from that step's new value, so every bin
+// still adds its terms in increasing step order.  Max-plus and min-plus only: the term is dC
+// itself.
 constexpr int RT_SPAN = 256;  // bins a lane holds per walk (longer contractions: one walk per span)
 constexpr int RT_STEP = 8;    // steps per chunk
 constexpr int RT_RING = 4;    // chunks in registers: one applied, three in flight
@@ -230,7 +92,7 @@ size_t lane_smem(int64_t K)
     const size_t rows = ((size_t)std::min<int64_t>(K, RT_SPAN) + 31) / 32 * 32 + 1;
     return sizeof(float) * rows * 32;
 }
-// the layouts k_route_lane serves: unit step stride and 16-byte aligned lines
+// lines k_route_lane reads by vectors: unit step stride and 16-byte aligned lines
 bool lane_ok(const RouteJob& j)
 {
     return j.sIs == 1 && j.sGs == 1 && j.sIx % 4 == 0 && j.sGx % 4 == 0 && j.sIb % 4 == 0 && j.sGb % 4 == 0 &&
@@ -240,28 +102,43 @@ bool lane_ok(const RouteJob& j)
 __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
 {
     extern __shared__ __align__(16) float bins[];  // [span][32]: bin k of lane l at k * 32 + l
-    pdl_wait();
+    if (!p.late_wait) pdl_wait();
     pdl_signal();
-    const RouteJob& j = p.job[0];
+    if ((int)blockIdx.y >= p.njobs) {
+        if (p.late_wait) pdl_wait();
+        return;
+    }
+    // the job's fields in registers (the job is picked by blockIdx.y)
+    const RouteJob& jr = p.job[blockIdx.y];
+    const int vec = jr.vec;
+    const int64_t S = jr.S, X = jr.X, K = p.K;
+    const int64_t sIs = jr.sIs, sGs = jr.sGs, sOk = jr.sOk;
+    const int32_t* const I0 = jr.I;
+    const float* const G0 = jr.G;
+    float* const O0 = jr.O;
+    const int64_t sIb = jr.sIb, sIx = jr.sIx, sGb = jr.sGb, sGx = jr.sGx, sOb = jr.sOb, sOx = jr.sOx;
+#if TROP_DEBUG_BOUNDS
+    const RouteJob& j = jr;  // the spans the checks read
+#endif
     const int l = threadIdx.x;
-    const int64_t lines = p.nbatch * j.X;
+    const int64_t lines = p.nbatch * X;
     for (int64_t base = (int64_t)blockIdx.x * 32; base < lines; base += (int64_t)gridDim.x * 32) {
         const int64_t o = base + l;
         const bool valid = o < lines;
-        const int64_t b = valid ? o / j.X : 0, x = valid ? o - b * j.X : 0;
-        const int32_t* Il = j.I + b * j.sIb + x * j.sIx;
-        const float* Gl = j.G + b * j.sGb + x * j.sGx;
-        float* Ol = j.O + b * j.sOb + x * j.sOx;
-        for (int64_t kc = 0; kc < p.K; kc += RT_SPAN) {
-            const int kn = (int)min((int64_t)RT_SPAN, p.K - kc);
+        const int64_t b = valid ? o / X : 0, x = valid ? o - b * X : 0;
+        const int32_t* Il = I0 + b * sIb + x * sIx;
+        const float* Gl = G0 + b * sGb + x * sGx;
+        float* Ol = O0 + b * sOb + x * sOx;
+        for (int64_t kc = 0; kc < K; kc += RT_SPAN) {
+            const int kn = (int)min((int64_t)RT_SPAN, K - kc);
             for (int k = 0; k < kn; ++k) bins[k * 32 + l] = 0.0f;
-            const int64_t nch = (j.S + RT_STEP - 1) / RT_STEP;
+            const int64_t nch = (S + RT_STEP - 1) / RT_STEP;
             int kr[RT_RING][RT_STEP];
             float gr[RT_RING][RT_STEP];
             auto load = [&](auto slot, int64_t c) {
                 constexpr int R = decltype(slot)::value;
                 const int64_t s0 = c * RT_STEP;
-                if (valid && s0 + RT_STEP <= j.S) {
+                if (vec && valid && s0 + RT_STEP <= S) {
                     const int4 kz = make_int4(-1, -1, -1, -1);
                     const float4 gz = make_float4(0.f, 0.f, 0.f, 0.f);
                     const int4 k0 = R_IN(Il + s0, 16, 0) ? __ldg(reinterpret_cast<const int4*>(Il + s0)) : kz;
@@ -273,18 +150,26 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
                     gr[R][0] = g0.x; gr[R][1] = g0.y; gr[R][2] = g0.z; gr[R][3] = g0.w;
                     gr[R][4] = g1.x; gr[R][5] = g1.y; gr[R][6] = g1.z; gr[R][7] = g1.w;
                 } else {
+                    // one load per step through the step strides (consecutive lines are consecutive
+                    // lanes: the columns of dB read 128 contiguous bytes a step)
+                    const int32_t* ip = Il + s0 * sIs;
+                    const float* gp = Gl + s0 * sGs;
 #pragma unroll
                     for (int t = 0; t < RT_STEP; ++t) {
-                        const bool in = valid && c < nch && s0 + t < j.S;
-                        kr[R][t] = in && R_IN(Il + s0 + t, 4, 0) ? __ldg(Il + s0 + t) : -1;
-                        gr[R][t] = in && R_IN(Gl + s0 + t, 4, 1) ? __ldg(Gl + s0 + t) : 0.0f;
+                        const bool in = valid && c < nch && s0 + t < S;
+                        kr[R][t] = in && R_IN(ip, 4, 0) ? __ldg(ip) : -1;
+                        gr[R][t] = in && R_IN(gp, 4, 1) ? __ldg(gp) : 0.0f;
+                        ip += sIs;
+                        gp += sGs;
                     }
                 }
             };
-            // bin of a step relative to the span, -1 when it routes nowhere in this span
+            // bin of a step relative to the span, -1 when it routes nowhere in this span (K < 2^31:
+            // an index below the span, or negative, wraps to a large unsigned value)
+            const unsigned kc32 = (unsigned)kc;
             auto rel = [&](int k) {
-                const int64_t d = (int64_t)k - kc;
-                return (k >= 0 && d >= 0 && d < kn) ? (int)d : -1;
+                const unsigned d = (unsigned)k - kc32;
+                return d < (unsigned)kn ? (int)d : -1;
             };
             auto apply = [&](auto slot) {
                 constexpr int R = decltype(slot)::value;
@@ -336,7 +221,7 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
                 turn(I3{}, c + 3);
             }
             __syncwarp();
-            if (j.sOk == 1) {
+            if (sOk == 1) {
                 // bins contiguous in the gradient: 32 x 32 blocks transposed through a padded
                 // copy so that each store writes 32 consecutive bins of one line; blocks go last
                 // to first, so the copy's extra row lies in a block already written
@@ -356,8 +241,9 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
                     __syncwarp();
                 }
             } else if (valid) {
-                for (int k = 0; k < kn; ++k)
-                    if (R_IN(Ol + (kc + k) * j.sOk, 4, 3)) Ol[(kc + k) * j.sOk] = bins[k * 32 + l];
+                float* op = Ol + kc * sOk;
+                for (int k = 0; k < kn; ++k, op += sOk)
+                    if (R_IN(op, 4, 3)) *op = bins[k * 32 + l];
             }
             __syncwarp();
         }
@@ -592,7 +478,7 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
         count_launches(1);
         return TROP_OK;
     };
-    if (TROP_ROUTE_MATCH && mul) {
+    if (mul) {
         // max-times: each gradient in a launch of the match-rank kernel of its own; the second
         // (dB) starts at once and waits at its end (RouteParams::late_wait), so the two overlap
         if (!dA || p.njobs == 1) return launch_match(p);
@@ -604,32 +490,18 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
         p.late_wait = 1;
         return launch_match(p);
     }
-    // for max-plus and min-plus the rows job (steps contiguous, the common layout of dA) takes
-    // the lane-per-line kernel (measured on the batch-64 256^3 gradient: 42 against 52 us for
-    // both jobs; with max-times' operand gathers it was slower); the other job follows it and
-    // may start at once (see RouteParams::late_wait)
-    if (!mul && dA && lane_ok(p.job[0])) {
-        RouteParams pa = p;
-        pa.njobs = 1;
-        const int64_t groups = (batch * pa.job[0].X + 31) / 32;
-        const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(groups, (int64_t)dev->sm_count * 16));
-        (void)launch_pdl(k_route_lane, dim3(gx), dim3(32), lane_smem(K), s, pa);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_error(e, "k_route_lane");
-        count_launches(1);
-        if (p.njobs == 1) return TROP_OK;
-        p.job[0] = p.job[1];
-        p.njobs = 1;
-        p.late_wait = 1;
+    // max-plus and min-plus: both jobs in one launch of the lane-per-line kernel (measured on the
+    // batch-64 256^3 gradient: 28 us, against 42 us for the rows there and the columns in a
+    // bin-split kernel staging 32 x 32 blocks)
+    int64_t groups = 1;
+    for (int i = 0; i < p.njobs; ++i) {
+        p.job[i].vec = lane_ok(p.job[i]) ? 1 : 0;
+        groups = std::max(groups, (batch * p.job[i].X + 31) / 32);
     }
-    int64_t ctas = 1;
-    for (int q = 0; q < p.njobs; ++q) ctas = std::max(ctas, (batch * p.job[q].X + 31) / 32);
-    const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)dev->sm_count * 16));
-    const dim3 grid(gx, (unsigned)p.njobs);
-    if (mul) (void)launch_pdl(k_winner_route<true>, grid, dim3(BW_THREADS), BW_SMEM, s, p);
-    else (void)launch_pdl(k_winner_route<false>, grid, dim3(BW_THREADS), BW_SMEM, s, p);
+    const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(groups, (int64_t)dev->sm_count * 16));
+    (void)launch_pdl(k_route_lane, dim3(gx, (unsigned)p.njobs), dim3(32), lane_smem(K), s, p);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "k_winner_route");
+    if (e != cudaSuccess) return cuda_error(e, "k_route_lane");
     count_launches(1);
     return TROP_OK;
 }
@@ -640,11 +512,6 @@ int register_backward_kernels()
     for (const void* k : km) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RM_SMEM);
         if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (match route smem)");
-    }
-    const void* ks[] = {(const void*)k_winner_route<true>, (const void*)k_winner_route<false>};
-    for (const void* k : ks) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BW_SMEM);
-        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (winner route smem)");
     }
     cudaError_t e = cudaFuncSetAttribute((const void*)k_route_lane, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)lane_smem(RT_SPAN));
