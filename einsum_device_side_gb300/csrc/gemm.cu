@@ -2020,8 +2020,16 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                              (uint32_t)g.K) &&
                     stream_tickets(s, 2 * half, &p.sched) == TROP_OK) {
                     // two halves of tickets used in turn by the fused GEMMs on a stream; start early
-                    // when the GEMM just before is one of them and wrote nothing this one reads
-                    const LaunchRecord prev = capture_arena() ? LaunchRecord{} : stream_record(s);
+                    // when the GEMM just before is one of them and wrote nothing this one reads.
+                    // Never while the stream is being captured (by this library or by the caller):
+                    // a captured launch replays after arbitrary work.
+                    cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+                    if (cudaStreamIsCapturing(s, &cst) != cudaSuccess) {
+                        cudaGetLastError();
+                        cst = cudaStreamCaptureStatusActive;
+                    }
+                    const bool capturing = capture_arena() || cst != cudaStreamCaptureStatusNone;
+                    const LaunchRecord prev = capturing ? LaunchRecord{} : stream_record(s);
                     const bool follows = prev.valid && prev.seq == launch_seq();
                     const int parity = follows ? prev.parity ^ 1 : 0;
                     p.late = follows && !reads_overlap(g, prev) ? 1 : 0;
@@ -2046,7 +2054,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                     if (rc == TROP_OK) {
                         if (p.late) count_early_start();
                         LaunchRecord cur{};
-                        cur.valid = !capture_arena();
+                        cur.valid = !capturing;
                         cur.seq = launch_seq();
                         cur.parity = parity;
                         output_ranges(g, cur);
