@@ -878,10 +878,13 @@ __device__ __forceinline__ void load_chunk(const float* p, float (&a)[CH])
 
 constexpr int FPW = 32;  // resolve panel columns, one per lane
 #ifndef TROP_FUSED_ROWS
-#define TROP_FUSED_ROWS 128
+#define TROP_FUSED_ROWS 256
 #endif
 constexpr int FRB = TROP_FUSED_ROWS;  // rows of a resolve item
-constexpr int FG = 4;                 // rows of a warp in one load group
+#ifndef TROP_FUSED_FG
+#define TROP_FUSED_FG 4
+#endif
+constexpr int FG = TROP_FUSED_FG;     // rows of a warp in one load group
 constexpr int FWARPS = tile_threads<4>() / 32;
 
 struct __align__(128) FusedResolveSmem {
