@@ -211,7 +211,13 @@ int tropical_permute_pair(const trop_tensor* val_in, const trop_tensor* arg_in, 
  * Element (b,m,k) of A is A[b*sAb + m*sAm + k*sAk]; likewise B and C.
  * argmax (nullable, int32) uses C's strides.  dtype: TROP_F32, TROP_F64,
  * TROP_I32 or TROP_I64, shared by A, B and C (the pointers carry no type: the
- * caller guarantees it).
+ * caller guarantees it).  Integer operands must keep every product inside the
+ * type (a + b, or a * b for max-times); then every result is exact.
+ * Ordering is the stream's: a call's results are complete when the stream
+ * reaches the call's end.  On the GPU an f32 argmax call that directly
+ * follows another on the same stream and reads none of the bytes that one
+ * writes may start loading and computing before it has finished; it stores
+ * nothing before then (trop_stats.gemm_early_starts counts such calls).
  * Errors: INVALID_ARG (negative extent, null pointer with nonzero extent),
  *         DTYPE, OVERFLOW (K > INT32_MAX with argmax), HOST_POINTER,
  *         DEVICE_MISMATCH, CUDA. */
@@ -370,6 +376,9 @@ void tropical_reset_stats(void);
  * the first library call made on the device after that kernel finished (or
  * tropical_sync_pool) returns TROP_ERR_CUDA naming the failure, once.  The
  * values and argmax of the call whose kernel abandoned a tile are undefined.
+ * In the one-launch form (argmax, K <= 256) the resolve work of each batch
+ * also waits, for at most about 1 s, until that batch's tiles are stored; a
+ * wait that gives up there sets the same error word (it is not counted here).
  * Reads a device counter: blocks until the device is idle.  reset != 0 zeroes
  * the counter after reading it.  Returns TROP_OK, or TROP_ERR_INVALID_ARG for a
  * NULL count, or TROP_ERR_CUDA. */

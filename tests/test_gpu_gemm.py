@@ -463,3 +463,18 @@ def test_gemm_after_another_library_kernel_waits(trop):
     rc, ri = oracle.gemm(a, b, 1, nthreads=0)
     assert c.cpu().numpy().tobytes() == rc.tobytes()
     np.testing.assert_array_equal(i.cpu().numpy(), ri)
+
+
+@pytest.mark.parametrize("k", [16, 48, 64, 128, 256])
+@pytest.mark.parametrize("sr", SR)
+def test_one_launch_gemm_ragged_panels_and_short_k(trop, sr, k):
+    """The one-launch GEMM + resolve on ragged shapes: 100 rows (one partial row block), 68
+    columns (16-byte rows of B for TMA; a last panel of 4 columns), K from one 16-wide k-tile
+    up, and enough tiles (80 batches x 4) that no tile is split along k.  Every output against
+    the oracle."""
+    bt, m, n = 80, 100, 68
+    sa, sb = [bt, m, k], [bt, k, n]
+    desc = trop.plan_describe("zmk,zkn->zmn", sa, [m * k, k, 1], sb, [k * n, n, 1])
+    assert "kernel=tma" in desc and "resolve=fused" in desc, desc
+    a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+    _check(trop, a, b, sr)
