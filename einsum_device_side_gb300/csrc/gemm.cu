@@ -1720,9 +1720,14 @@ const char* resolve_kind(const GemmDesc& g, bool vecA)
 #ifndef TROP_TMA_FUSED
 #define TROP_TMA_FUSED 1
 #endif
+// Counters of one launch: the item counter, then a tile count and a resolve count per batch.  A
+// stream's two halves have this fixed size whatever the launch's batch count, so that two
+// launches of different batch counts in turn never share a counter.
+constexpr int64_t FUSED_MAX_BATCH = 4095;
+constexpr size_t FUSED_HALF = 1 + 2 * (size_t)FUSED_MAX_BATCH;
 bool fused_ok(const GemmDesc& g, bool vecA, uint64_t T, int64_t nbatch)
 {
-    if (!TROP_TMA_FUSED || resolve_kind(g, vecA)[0] != 'r') return false;
+    if (!TROP_TMA_FUSED || resolve_kind(g, vecA)[0] != 'r' || nbatch > FUSED_MAX_BATCH) return false;
     const uint64_t items = T + (uint64_t)nbatch * (uint64_t)((g.N + FPW - 1) / FPW) * (uint64_t)((g.M + FRB - 1) / FRB);
     return items < (uint64_t(1) << 31);
 }
@@ -2017,7 +2022,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                 attr[0].val.programmaticStreamSerializationAllowed = 1;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
-                const size_t half = 1 + 2 * (size_t)nbatch;  // tickets of one launch
+                const size_t half = FUSED_HALF;  // tickets of one launch (one half of the stream's two)
                 if (fused_ok(g, p.vecA != 0, T, nbatch) &&
                     make_map(&maps.bp, p.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)nbatch, g.sBk, sBb, FPW,
                              (uint32_t)g.K) &&

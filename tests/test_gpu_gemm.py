@@ -478,3 +478,27 @@ def test_one_launch_gemm_ragged_panels_and_short_k(trop, sr, k):
     assert "kernel=tma" in desc and "resolve=fused" in desc, desc
     a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
     _check(trop, a, b, sr)
+
+
+def test_back_to_back_gemms_of_different_batch_counts(trop):
+    """One-launch GEMMs of different batch counts, alternating on one stream and starting early
+    behind each other: each keeps its own counters (the two halves of the stream's counters
+    have a fixed layout), so every output equals the oracle's and no wait gives up."""
+    shapes = [(0, 24, 256, 256, 256), (2, 80, 100, 68, 64), (1, 40, 192, 128, 128)]
+    work = []
+    for sr, bt, m, n, k in shapes:
+        a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+        rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+        outs = (torch.empty((bt, m, n), device="cuda"), torch.empty((bt, m, n), dtype=torch.int32, device="cuda"))
+        work.append((sr, _dev(a), _dev(b), rc, ri, outs))
+    trop.reset_stats()
+    for rep in range(6):
+        for j in ((0, 1, 2), (2, 0, 1), (1, 2, 0))[rep % 3]:
+            sr, ad, bd, _, _, outs = work[j]
+            trop.gemm(ad, bd, sr, out=outs[0], out_argmax=outs[1])
+    torch.cuda.synchronize()
+    trop.sync_pool()  # raises if a bounded wait gave up
+    assert trop.stats()["gemm_early_starts"] >= 17
+    for sr, ad, bd, rc, ri, outs in work:
+        assert outs[0].cpu().numpy().tobytes() == rc.tobytes()
+        np.testing.assert_array_equal(outs[1].cpu().numpy(), ri)
