@@ -669,7 +669,7 @@ struct __align__(128) TmaTileSmem {
 // Tile t of the TMA-fed argmax GEMM: values and -(chunk + 1) codes through the strides.  With
 // PDL the programmatic-dependent wait (and the signal to the next grid) comes between the
 // barrier set-up and the first copy.  *bat receives the tile's batch.
-template <int SR, bool PDL>
+template <int SR, bool PDL, bool ARG = true>
 __device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams& p, uint32_t t, TmaTileSmem& sm,
                                          uint32_t* bat)
 {
@@ -758,12 +758,17 @@ __device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams&
                         const float2 t0 = O::mul2(make_float2(av[kp], av[kp]), make_float2(bq[kp][jj], bq[kp][jj + 1]));
                         const float2 t1 =
                             O::mul2(make_float2(av[kp + 1], av[kp + 1]), make_float2(bq[kp + 1][jj], bq[kp + 1][jj + 1]));
-                        dst_[i][jj] = O::fold3(ff ? src_[i][jj] : dst_[i][jj], t0.x, t1.x);
-                        dst_[i][jj + 1] = O::fold3(ff ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y, t1.y);
+                        if constexpr (ARG) {
+                            dst_[i][jj] = O::fold3(ff ? src_[i][jj] : dst_[i][jj], t0.x, t1.x);
+                            dst_[i][jj + 1] = O::fold3(ff ? src_[i][jj + 1] : dst_[i][jj + 1], t0.y, t1.y);
+                        } else {  // no argmax: one accumulator set, no chunk marks
+                            best[i][jj] = O::fold3(best[i][jj], t0.x, t1.x);
+                            best[i][jj + 1] = O::fold3(best[i][jj + 1], t0.y, t1.y);
+                        }
                     }
                 }
             }
-            if ((kq + 4) % CH == 0) {
+            if (ARG && (kq + 4) % CH == 0) {
                 // end of a chunk: a strict improvement over the chunk-start value marks it
                 const uint16_t chunk = (uint16_t)((kt * BK + kq + 4) / CH - 1);
 #pragma unroll
@@ -790,15 +795,17 @@ __device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams&
         if (tid == 0)
             for (int k2 = max(0, issued - TMA_STAGES); k2 < issued; ++k2)
                 (void)mbar_wait(&full[k2 % TMA_STAGES], (uint32_t)(k2 / TMA_STAGES) & 1u);
+        if constexpr (ARG) {
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int m = m0 + row_of(tm, i);
-            if (m >= p.M) continue;
-            int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+            for (int i = 0; i < TM; ++i) {
+                const int m = m0 + row_of(tm, i);
+                if (m >= p.M) continue;
+                int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (n0 + tn * 4 + q < p.N && T_IN(irow + (int64_t)(n0 + tn * 4 + q) * p.sIn, 4, 3))
-                    irow[(int64_t)(n0 + tn * 4 + q) * p.sIn] = 0;
+                for (int q = 0; q < 4; ++q)
+                    if (n0 + tn * 4 + q < p.N && T_IN(irow + (int64_t)(n0 + tn * 4 + q) * p.sIn, 4, 3))
+                        irow[(int64_t)(n0 + tn * 4 + q) * p.sIn] = 0;
+            }
         }
         if (tid == 0 && p.err) {
             *(volatile uint32_t*)p.err = 1u;
@@ -813,10 +820,6 @@ __device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams&
         const int m = m0 + row_of(tm, i);
         if (m >= p.M) continue;
         float* crow = p.C + oc + (int64_t)m * p.sCm;
-        int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
-        int32_t code[TN];
-#pragma unroll
-        for (int jj = 0; jj < TN; ++jj) code[jj] = best[i][jj] != zero ? -((int32_t)sid[i * TN + jj][tid] + 1) : 0;
         const int n = n0 + tn * 4;
         if (p.vecC && n + 3 < p.N) {
             if (T_IN(crow + n, 16, 2))
@@ -826,6 +829,11 @@ __device__ __forceinline__ void tma_tile(const TmaMaps& maps, const TiledParams&
             for (int q = 0; q < 4; ++q)
                 if (n + q < p.N && T_IN(crow + (int64_t)(n + q) * p.sCn, 4, 2)) crow[(int64_t)(n + q) * p.sCn] = best[i][q];
         }
+        if constexpr (!ARG) continue;
+        int32_t* irow = p.I + oi + (int64_t)m * p.sIm;
+        int32_t code[TN];
+#pragma unroll
+        for (int jj = 0; jj < TN; ++jj) code[jj] = best[i][jj] != zero ? -((int32_t)sid[i * TN + jj][tid] + 1) : 0;
         if (p.vecI && n + 3 < p.N) {
             if (T_IN(irow + n, 16, 3)) *reinterpret_cast<int4*>(irow + n) = make_int4(code[0], code[1], code[2], code[3]);
         } else {
@@ -843,6 +851,23 @@ __global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_MINB)
     __shared__ TmaTileSmem sm;
     uint32_t b;
     tma_tile<SR, true>(maps, p, blockIdx.x, sm, &b);
+}
+
+// The same TMA-fed tile without argmax (one accumulator set, no chunk marks, C only).  Like the
+// one-launch argmax GEMM below it may start early behind a GEMM that wrote none of its operands
+// (p.late): it then waits for the grid before only ahead of its stores.
+#ifndef TROP_TMA_PLAIN_MINB
+#define TROP_TMA_PLAIN_MINB 4
+#endif
+template <int SR>
+__global__ void __launch_bounds__(tile_threads<4>(), TROP_TMA_PLAIN_MINB)
+    k_gemm_tma_plain(const __grid_constant__ TmaMaps maps, TiledParams p)
+{
+    __shared__ TmaTileSmem sm;
+    if (!p.late) pdl_wait();
+    pdl_signal();
+    uint32_t b;
+    tma_tile<SR, false, false>(maps, p, blockIdx.x, sm, &b);
 }
 
 // ------------------------------------------------------------------ fused GEMM + short-K resolve
@@ -1696,9 +1721,9 @@ int resident_ctas(const void* fn, int threads, size_t smem, std::atomic<int>& ca
 
 // The TMA-fed argmax kernel's layout conditions (the tensor maps may still refuse): one batch
 // axis, whole k-tiles, 16-byte aligned operands with row and batch strides in 16-byte units.
-bool tma_layout_ok(const GemmDesc& g, const Batch& bt, int64_t nbatch)
+bool tma_layout_ok(const GemmDesc& g, const Batch& bt, int64_t nbatch, bool need_argmax = true)
 {
-    if (!g.I || bt.nb > 1 || g.K % BK != 0) return false;
+    if ((need_argmax && !g.I) || bt.nb > 1 || g.K % BK != 0) return false;
     if ((uintptr_t)g.A % 16 || (uintptr_t)g.B % 16 || g.sAm <= 0 || g.sAm % 4 || g.sBk <= 0 || g.sBk % 4) return false;
     if (nbatch > 1 && (bt.sA[0] <= 0 || bt.sA[0] % 4 || bt.sB[0] <= 0 || bt.sB[0] % 4)) return false;
     return true;
@@ -1895,6 +1920,15 @@ bool make_map(CUtensorMap* map, const float* base, uint64_t cols, uint64_t rows,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// the GEMM without argmax by TMA (k_gemm_tma_plain): the TMA layout, and a driver that encodes maps
+#ifndef TROP_TMA_PLAIN
+#define TROP_TMA_PLAIN 1
+#endif
+bool plain_tma_ok(const GemmDesc& g, const Batch& bt, int64_t nbatch)
+{
+    return TROP_TMA_PLAIN && tma_layout_ok(g, bt, nbatch, false) && encode_tiled() != nullptr;
+}
+
 // Stream-K only when the last wave would run at most this full (percent); each stream-K
 // CTA gets at least SK_MIN_UNITS k-tiles (unless a tile has fewer) and a tile is cut into at
 // most SK_MAX_SEGS segments.
@@ -1975,7 +2009,9 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
     uint64_t R = 0, L = 0, n_sk = 0;
     uint64_t G_sk = 0;
     void* ws = nullptr;
-    if (sk_split(T, G, p.nkt, ARG, R, L, n_sk)) {
+    // without argmax, whole tiles by TMA (k_gemm_tma_plain) where the layout allows, no k split
+    const bool plain_tma = !ARG && plain_tma_ok(g, p.bt, nbatch);
+    if (!plain_tma && sk_split(T, G, p.nkt, ARG, R, L, n_sk)) {
         const uint64_t U = R * p.nkt;
         {
             const size_t seg_elems = (size_t)n_sk * 2 * TILE_ELEMS;
@@ -2004,6 +2040,55 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
 
     int rc = TROP_OK;
     bool launched = false, fused = false;
+    // Early start (k_gemm_tma_fused, k_gemm_tma_plain): the last such GEMM on this stream and
+    // whether it is the library's launch just before this one.  Never while the stream is being
+    // captured (by this library or by the caller): a captured launch replays after arbitrary work.
+    bool capturing = capture_arena() != nullptr;
+    if (!capturing) {
+        cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cst) != cudaSuccess) {
+            cudaGetLastError();
+            cst = cudaStreamCaptureStatusActive;
+        }
+        capturing = cst != cudaStreamCaptureStatusNone;
+    }
+    auto record = [&](int parity) {
+        if (p.late) count_early_start();
+        LaunchRecord cur{};
+        cur.valid = !capturing;
+        cur.seq = launch_seq();
+        cur.parity = parity;
+        output_ranges(g, cur);
+        set_stream_record(s, cur);
+    };
+    if constexpr (!ARG) {
+        TmaMaps maps;
+        const int64_t sAb = p.bt.nb ? p.bt.sA[0] : 0, sBb = p.bt.nb ? p.bt.sB[0] : 0;
+        if (plain_tma && make_map(&maps.a, p.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)nbatch, g.sAm, sAb, BK, BM) &&
+            make_map(&maps.b, p.B, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)nbatch, g.sBk, sBb, BN, BK)) {
+            TROP_TRY(device_error_word(&p.err));
+            p.wait_mode = wait_test_mode();
+            const LaunchRecord prev = capturing ? LaunchRecord{} : stream_record(s);
+            const bool follows = prev.valid && prev.seq == launch_seq();
+            p.late = follows && !reads_overlap(g, prev) ? 1 : 0;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)T);
+            cfg.blockDim = dim3(tile_threads<4>());
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tma_plain<SR>, maps, p);
+            rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma_plain") : check_launch("k_gemm_tma_plain");
+            // (no counters of its own: the next one-launch argmax GEMM alternates from the last one's half)
+            if (rc == TROP_OK) record(follows ? prev.parity : 0);
+            launched = true;
+        } else if (plain_tma) {
+            clear_error();  // (no tensor map: the cp.async kernel, whole tiles)
+        }
+    }
     if constexpr (ARG) {
         // whole tiles, one batch axis, whole k-tiles: operands by TMA
         if (!G_sk && tma_layout_ok(g, p.bt, nbatch)) {
@@ -2031,12 +2116,6 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                     // when the GEMM just before is one of them and wrote nothing this one reads.
                     // Never while the stream is being captured (by this library or by the caller):
                     // a captured launch replays after arbitrary work.
-                    cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
-                    if (cudaStreamIsCapturing(s, &cst) != cudaSuccess) {
-                        cudaGetLastError();
-                        cst = cudaStreamCaptureStatusActive;
-                    }
-                    const bool capturing = capture_arena() || cst != cudaStreamCaptureStatusNone;
                     const LaunchRecord prev = capturing ? LaunchRecord{} : stream_record(s);
                     const bool follows = prev.valid && prev.seq == launch_seq();
                     const int parity = follows ? prev.parity ^ 1 : 0;
@@ -2059,15 +2138,7 @@ int run_tiled(const GemmDesc& g, cudaStream_t s, const DeviceInfo* dev)
                                                         : cudaLaunchKernelEx(&cfg, k_gemm_tma_fused<SR, false>, maps, p);
                     rc = e != cudaSuccess ? cuda_error(e, "k_gemm_tma_fused") : check_launch("k_gemm_tma_fused");
                     fused = true;
-                    if (rc == TROP_OK) {
-                        if (p.late) count_early_start();
-                        LaunchRecord cur{};
-                        cur.valid = !capturing;
-                        cur.seq = launch_seq();
-                        cur.parity = parity;
-                        output_ranges(g, cur);
-                        set_stream_record(s, cur);
-                    }
+                    if (rc == TROP_OK) record(parity);
                 } else {
                     clear_error();  // (no tickets: the two-pass form below)
                     const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tma<SR>, maps, p);
@@ -2369,7 +2440,15 @@ void describe_gemm(const GemmDesc& g1, char* buf, size_t n)
         T *= (uint64_t)((g.M + BM - 1) / BM) * (uint64_t)((g.N + BN - 1) / BN);
         const uint64_t nkt = (uint64_t)((g.K + BK - 1) / BK);
         uint64_t R = 0, L = 0, n_sk = 0;
-        const bool split = sk_split(T, (uint64_t)sms * (arg ? TROP_ARG_MINB : TROP_PLAIN_MINB), nkt, arg, R, L, n_sk);
+        bool split = sk_split(T, (uint64_t)sms * (arg ? TROP_ARG_MINB : TROP_PLAIN_MINB), nkt, arg, R, L, n_sk);
+        if (!arg) {
+            // whole tiles by TMA where the layout allows (no k split on that kernel)
+            int64_t nbatch = 1;
+            const Batch bt = make_batch(g, nbatch);
+            const bool tma = TROP_TMA_PLAIN && tma_layout_ok(g, bt, nbatch, false);
+            if (tma) split = false;
+            snprintf(extra, sizeof(extra), " kernel=%s", tma ? "tma" : "tiled");
+        }
         if (arg) {
             // the staged product is contiguous: describe the kernels on that layout
             GemmDesc gs = g;

@@ -140,11 +140,13 @@ def test_full_size_batched_workload(trop, sr):
 # ---------------------------------------------------------------- split tiles (stream-K) and the resolve pass
 
 @pytest.mark.parametrize("sr", SR)
-@pytest.mark.parametrize("batch", [64, 128])
-def test_split_tail_plain_full_size(trop, sr, batch):
-    """Batched 256^3 without argmax: the last partial wave is cut along k and the
-    segments merged by the last CTA to finish; every output vs the oracle."""
-    a, b = synth.gemm_batched_inputs(sr, batch=batch)
+@pytest.mark.parametrize("batch,k,kernel", [(64, 256, "tma"), (128, 256, "tma"), (64, 248, "tiled"),
+                                            (128, 248, "tiled")])
+def test_plain_full_size(trop, sr, batch, k, kernel):
+    """Batched 256 x 256 without argmax, every output vs the oracle.  K = 256: whole tiles by TMA
+    (k_gemm_tma_plain).  K = 248 (not whole 16-wide k-tiles): the cp.async kernel, whose last
+    partial wave is cut along k and the segments merged by the last CTA to finish."""
+    a, b = synth.gemm_batched_inputs(sr, batch=batch, k=k)
     c = trop.gemm(_dev(a), _dev(b), sr, argmax=False)
     torch.cuda.synchronize()
     rc, _ = oracle.gemm(a, b, sr, nthreads=0)
