@@ -121,6 +121,7 @@ def main() -> int:
         case(f"gemm tiled ragged sr{sr}", lambda sr=sr: gemm(sr, (3, 70, 45, 37)))
         case(f"gemm stream-K sr{sr}", lambda sr=sr: gemm(sr, (2, 129, 65, 1030)))
         case(f"gemm no argmax sr{sr}", lambda sr=sr: gemm(sr, (5, 200, 150, 90), argmax=False))
+        case(f"gemm no argmax by TMA sr{sr}", lambda sr=sr: gemm(sr, (8, 128, 136, 64), argmax=False))
         case(f"gemm strided output sr{sr}", lambda sr=sr: gemm(sr, (2, 96, 80, 50), transpose_out=True))
         case(f"gemm thin M sr{sr}", lambda sr=sr: gemm(sr, (40, 3, 512, 64)))
         case(f"gemm f64 sr{sr}", lambda sr=sr: gemm(sr, (2, 70, 45, 37), dtype="f64"))
