@@ -18,6 +18,8 @@
 //                  in shared memory; rows of dA by 16-byte vector loads along
 //                  the line, columns of dB by one load per step (consecutive
 //                  lanes, consecutive columns: 128 contiguous bytes a step).
+//                  Also max-times dB when dA is not wanted, the other
+//                  operand's factors gathered a ring turn ahead.
 //   k_route_match  max-times: a warp per line, the lanes of one bin applied in
 //                  step order, which keeps the gathers of the other operand in
 //                  flight across a whole warp; dA and dB in two launches that
@@ -80,8 +82,9 @@ struct RouteParams {
 // of dB: consecutive lanes are consecutive columns, so a warp reads 128 contiguous bytes a
 // step).  Steps are applied four at a time: the four bins are read together, and a step whose
 // bin an earlier step of the group also hit continues from that step's new value, so every bin
-// still adds its terms in increasing step order.  Max-plus and min-plus only: the term is dC
-// itself.
+// still adds its terms in increasing step order.  The term is dC itself (max-plus, min-plus) or,
+// with MUL (max-times), dC times the other operand's entry at the step's winner, rounded once;
+// those factors are gathered for the next chunk while a chunk is applied.
 constexpr int RT_SPAN = 256;  // bins a lane holds per walk (longer contractions: one walk per span)
 constexpr int RT_STEP = 8;    // steps per chunk
 constexpr int RT_RING = 4;    // chunks in registers: one applied, three in flight
@@ -99,6 +102,7 @@ bool lane_ok(const RouteJob& j)
            ((uintptr_t)j.I % 16) == 0 && ((uintptr_t)j.G % 16) == 0;
 }
 
+template <bool MUL>
 __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
 {
     extern __shared__ __align__(16) float bins[];  // [span][32]: bin k of lane l at k * 32 + l
@@ -115,6 +119,8 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
     const int64_t sIs = jr.sIs, sGs = jr.sGs, sOk = jr.sOk;
     const int32_t* const I0 = jr.I;
     const float* const G0 = jr.G;
+    const float* const P0 = jr.P;
+    const int64_t sPb = jr.sPb, sPk = jr.sPk, sPs = jr.sPs;
     float* const O0 = jr.O;
     const int64_t sIb = jr.sIb, sIx = jr.sIx, sGb = jr.sGb, sGx = jr.sGx, sOb = jr.sOb, sOx = jr.sOx;
 #if TROP_DEBUG_BOUNDS
@@ -128,6 +134,7 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
         const int64_t b = valid ? o / X : 0, x = valid ? o - b * X : 0;
         const int32_t* Il = I0 + b * sIb + x * sIx;
         const float* Gl = G0 + b * sGb + x * sGx;
+        const float* Pl = MUL ? P0 + b * sPb : nullptr;  // the other operand of this line's batch
         float* Ol = O0 + b * sOb + x * sOx;
         for (int64_t kc = 0; kc < K; kc += RT_SPAN) {
             const int kn = (int)min((int64_t)RT_SPAN, K - kc);
@@ -135,6 +142,7 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
             const int64_t nch = (S + RT_STEP - 1) / RT_STEP;
             int kr[RT_RING][RT_STEP];
             float gr[RT_RING][RT_STEP];
+            float pr[2][RT_STEP];  // max-times: the factors of the chunk applied now and of the next
             auto load = [&](auto slot, int64_t c) {
                 constexpr int R = decltype(slot)::value;
                 const int64_t s0 = c * RT_STEP;
@@ -171,8 +179,22 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
                 const unsigned d = (unsigned)k - kc32;
                 return d < (unsigned)kn ? (int)d : -1;
             };
-            auto apply = [&](auto slot) {
-                constexpr int R = decltype(slot)::value;
+            // max-times: the other operand's entry at each step's winner for chunk c (indices in ring
+            // slot KS) into factor slot PS, issued a turn before the chunk is applied; a step that
+            // routes nowhere in this span loads nothing
+            auto gather = [&](auto kslot, auto pslot, int64_t c) {
+                constexpr int KS = decltype(kslot)::value, PS = decltype(pslot)::value;
+                const int64_t s0 = c * RT_STEP;
+#pragma unroll
+                for (int t = 0; t < RT_STEP; ++t) {
+                    const int k = kr[KS][t];
+                    const float* pp = Pl + (int64_t)k * sPk + (s0 + t) * sPs;
+                    pr[PS][t] = rel(k) >= 0 && R_IN(pp, 4, 2) ? __ldg(pp) : 0.0f;
+                }
+            };
+            auto apply = [&](auto slot, auto pslot) {
+                constexpr int R = decltype(slot)::value, PS = decltype(pslot)::value;
+                (void)PS;
 #pragma unroll
                 for (int q = 0; q < RT_STEP; q += 4) {
                     int d[4];
@@ -180,7 +202,8 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         d[t] = rel(kr[R][q + t]);
-                        g[t] = gr[R][q + t];
+                        // max-times: the term is dC times the factor, rounded once before the add
+                        g[t] = MUL ? __fmul_rn(gr[R][q + t], pr[PS][q + t]) : gr[R][q + t];
                     }
                     const float x0 = d[0] >= 0 ? bins[d[0] * 32 + l] : 0.0f;
                     const float x1 = d[1] >= 0 ? bins[d[1] * 32 + l] : 0.0f;
@@ -205,11 +228,14 @@ __global__ void __launch_bounds__(32) k_route_lane(RouteParams p)
             load(I0{}, 0);
             load(I1{}, 1);
             load(I2{}, 2);
-            // one ring turn: chunk c in slot R
+            if constexpr (MUL) gather(I0{}, I0{}, 0);
+            // one ring turn: chunk c in slot R (c = R mod 4, so its factors sit in slot R mod 2)
             auto turn = [&](auto slot, int64_t c) {
                 constexpr int R = decltype(slot)::value;
                 load(std::integral_constant<int, (R + 3) % 4>{}, c + 3);
-                apply(slot);
+                if constexpr (MUL)
+                    gather(std::integral_constant<int, (R + 1) % 4>{}, std::integral_constant<int, (R + 1) % 2>{}, c + 1);
+                apply(slot, std::integral_constant<int, R % 2>{});
             };
             for (int64_t c = 0; c < nch; c += 4) {
                 turn(I0{}, c);
@@ -478,10 +504,27 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
         count_launches(1);
         return TROP_OK;
     };
-    if (mul) {
-        // max-times: each gradient in a launch of the match-rank kernel of its own; the second
-        // (dB) starts at once and waits at its end (RouteParams::late_wait), so the two overlap
-        if (!dA || p.njobs == 1) return launch_match(p);
+    // one launch of the lane-per-line kernel for the jobs of q
+    auto launch_lane = [&](RouteParams& q) -> int {
+        int64_t groups = 1;
+        for (int i = 0; i < q.njobs; ++i) {
+            q.job[i].vec = lane_ok(q.job[i]) ? 1 : 0;
+            groups = std::max(groups, (batch * q.job[i].X + 31) / 32);
+        }
+        const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(groups, (int64_t)dev->sm_count * 16));
+        if (mul) (void)launch_pdl(k_route_lane<true>, dim3(gx, (unsigned)q.njobs), dim3(32), lane_smem(K), s, q);
+        else (void)launch_pdl(k_route_lane<false>, dim3(gx, (unsigned)q.njobs), dim3(32), lane_smem(K), s, q);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_error(e, "k_route_lane");
+        count_launches(1);
+        return TROP_OK;
+    };
+    if (mul && dA) {
+        // max-times with dA: each gradient in a launch of the match-rank kernel of its own, whose
+        // factor gathers (B[b, k, n] across B's rows for dA) are in flight for a whole warp at
+        // once; the second (dB) starts at once and waits at its end (RouteParams::late_wait), so
+        // the two overlap (batch-64 256^3: 64 us; the lane walk for dB beside it, 72 us)
+        if (p.njobs == 1) return launch_match(p);
         RouteParams pa = p;
         pa.njobs = 1;
         TROP_TRY(launch_match(pa));
@@ -492,18 +535,10 @@ int launch_gemm_backward(int semiring, int64_t batch, int64_t M, int64_t N, int6
     }
     // max-plus and min-plus: both jobs in one launch of the lane-per-line kernel (measured on the
     // batch-64 256^3 gradient: 28 us, against 42 us for the rows there and the columns in a
-    // bin-split kernel staging 32 x 32 blocks)
-    int64_t groups = 1;
-    for (int i = 0; i < p.njobs; ++i) {
-        p.job[i].vec = lane_ok(p.job[i]) ? 1 : 0;
-        groups = std::max(groups, (batch * p.job[i].X + 31) / 32);
-    }
-    const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(groups, (int64_t)dev->sm_count * 16));
-    (void)launch_pdl(k_route_lane, dim3(gx, (unsigned)p.njobs), dim3(32), lane_smem(K), s, p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "k_route_lane");
-    count_launches(1);
-    return TROP_OK;
+    // bin-split kernel staging 32 x 32 blocks); max-times dB alone: the lane walk too, its factor
+    // gathers (A[b, m, k], one row of A per step and warp) hidden by its ring (28 us against 35 us
+    // for the match kernel)
+    return launch_lane(p);
 }
 
 int register_backward_kernels()
@@ -513,9 +548,11 @@ int register_backward_kernels()
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RM_SMEM);
         if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (match route smem)");
     }
-    cudaError_t e = cudaFuncSetAttribute((const void*)k_route_lane, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)lane_smem(RT_SPAN));
-    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (lane route smem)");
+    const void* kl[] = {(const void*)k_route_lane<true>, (const void*)k_route_lane<false>};
+    for (const void* k : kl) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lane_smem(RT_SPAN));
+        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute (lane route smem)");
+    }
     return TROP_OK;
 }
 

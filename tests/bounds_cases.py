@@ -162,6 +162,17 @@ def main() -> int:
         same(f"backward sr{sr} {shape} dA", da.cpu().numpy(), ra)
         same(f"backward sr{sr} {shape} dB", db.cpu().numpy(), rb)
 
+    def backward_b_alone(sr, shape, seed):
+        bt, m, n, k = shape
+        a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+        _, i = oracle.gemm(a, b, sr, nthreads=0)
+        dc = synth.uniform_f32(700 + seed, (bt, m, n), -1.0, 1.0)
+        _, db = trop.gemm_backward(d(a), d(b), d(dc), d(i), sr, want_a=False)
+        _, rb = oracle.gemm_backward(a, b, dc, i, sr)
+        same(f"backward dB alone sr{sr} {shape}", db.cpu().numpy(), rb)
+
+    case("backward dB alone sr2", lambda: backward_b_alone(2, (3, 70, 45, 37), 11))
+    case("backward dB alone long K sr2", lambda: backward_b_alone(2, (1, 40, 33, 300), 12))
     for sr in (0, 1, 2):
         case(f"backward sr{sr}", lambda sr=sr: backward(sr, (3, 70, 45, 37), sr))
         case(f"backward long K sr{sr}", lambda sr=sr: backward(sr, (1, 40, 33, 300), 3 + sr))

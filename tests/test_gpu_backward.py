@@ -58,6 +58,11 @@ def test_backward_full_size_batched_workload(trop, sr):
     ra, rb = oracle.gemm_backward(a, b, dc, i.cpu().numpy(), sr)
     assert da.cpu().numpy().tobytes() == ra.tobytes()
     assert db.cpu().numpy().tobytes() == rb.tobytes()
+    # each gradient alone (max-times dB alone takes the lane walk with gathered factors)
+    da1, db1 = trop.gemm_backward(ad, bd, _dev(dc), i, sr, want_b=False)
+    assert db1 is None and da1.cpu().numpy().tobytes() == ra.tobytes()
+    da1, db1 = trop.gemm_backward(ad, bd, _dev(dc), i, sr, want_a=False)
+    assert da1 is None and db1.cpu().numpy().tobytes() == rb.tobytes()
 
 
 def test_backward_strided_operands_and_outputs(trop):
@@ -72,6 +77,35 @@ def test_backward_strided_operands_and_outputs(trop):
     ra, rb = oracle.gemm_backward(a, b, dc, i, 2)
     np.testing.assert_array_equal(da.cpu().numpy(), ra)
     np.testing.assert_array_equal(db.cpu().numpy(), rb)
+
+
+@pytest.mark.parametrize("sr", SR)
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (2, 5, 7, 3), (3, 70, 45, 37), (1, 40, 33, 300), (2, 129, 65, 130)])
+def test_backward_one_gradient_matches_oracle(trop, sr, shape):
+    """dA alone and dB alone, every semiring; K = 300 takes two bin spans."""
+    a, b, dc, i = _case(sr, *shape, seed=9)
+    ra, rb = oracle.gemm_backward(a, b, dc, i, sr)
+    da, db = trop.gemm_backward(_dev(a), _dev(b), _dev(dc), _dev(i), sr, want_b=False)
+    assert db is None and da.cpu().numpy().tobytes() == ra.tobytes()
+    da, db = trop.gemm_backward(_dev(a), _dev(b), _dev(dc), _dev(i), sr, want_a=False)
+    assert da is None and db.cpu().numpy().tobytes() == rb.tobytes()
+
+
+def test_backward_maxtimes_gradient_of_b_alone_strided_with_out_of_range_indices(trop):
+    """max-times dB alone through transposed views of A, dC, the argmax and dB, with indices that
+    route nowhere (-1, K) and K = 300 (two bin spans): the factor gathers follow A's strides."""
+    a, b, dc, i = _case(2, 2, 48, 40, 300, seed=4)
+    i = i.copy()
+    i[0, 3, :5] = -1
+    i[1, 4, 5:9] = 300
+    dct = _dev(np.ascontiguousarray(dc.transpose(0, 2, 1))).transpose(1, 2)
+    it = _dev(np.ascontiguousarray(i.transpose(0, 2, 1))).transpose(1, 2)
+    at = _dev(np.ascontiguousarray(a.transpose(0, 2, 1))).transpose(1, 2)
+    ob = torch.empty((2, 40, 300), device="cuda").transpose(1, 2)
+    da, db = trop.gemm_backward(at, _dev(b), dct, it, 2, want_a=False, out_b=ob)
+    _, rb = oracle.gemm_backward(a, b, dc, i, 2)
+    assert da is None
+    assert db.cpu().numpy().tobytes() == rb.tobytes()
 
 
 def test_backward_one_side_and_out_of_range_indices(trop):
