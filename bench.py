@@ -152,11 +152,12 @@ def barrier_max(value, world):
 
 # ---------------------------------------------------------------------------- CPU oracle
 
-def cpu_sample_rate(target_s=12.0):
-    """Oracle semiring-ops/s on a bounded sample of the headline workload."""
+def cpu_sample_rate(target_s=12.0, threads=None):
+    """Oracle semiring-ops/s on a bounded sample of the headline workload (OpenMP over
+    `threads`, default all cores)."""
     import oracle
     oracle.build()
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     rng = np.random.default_rng(0)
     total_ops, elapsed, outs = 0, 0.0, 0
     n = 4096
@@ -177,7 +178,7 @@ def cpu_sample_rate(target_s=12.0):
         elapsed += t_sr
     return {"value": total_ops / elapsed / 1e9, "unit": "G semiring-ops/s", "cores": cores, "kind": "oracle",
             "sample": f"{outs} sampled outputs (x K=256 terms) of the batch-64 256^3 GEMMs, 3 semirings, "
-                      f"OpenMP over {cores} threads"}
+                      f"OpenMP over {cores} thread{'s' if cores > 1 else ''}"}
 
 
 def run_reference(args, rank, world):
@@ -569,6 +570,8 @@ def run_gpu(args, rank, world, local):
     cpu = None
     if world == 1 and not args.no_cpu:
         cpu = cpu_sample_rate()
+        one = cpu_sample_rate(target_s=3.0, threads=1)
+        cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
     traffic = gemm_traffic()
     achieved = OPS_PER_GEMM / avg_launch / 1e9
     line = {
