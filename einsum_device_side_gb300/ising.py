@@ -8,10 +8,13 @@ sum J s_i s_j, E0 = -W.  In max-plus algebra W is the contraction of one
 Tree (labels: spin (r, c) -> r*C + c):
   * row 0: the first bond is the initial frontier; each further site of the
     row appends its spin:  'X l, l n -> X l n' (no contraction).
-  * each site (r, c), r >= 1: a small diagonal node builds the site tensor
-    Q[l, u, n] = T_left[l, n] + T_up[u, n] ('ln,un->lun', n shared), then
-    the frontier spin u = (r-1, c) is contracted:  'X l u Y, l u n -> X l n Y'
-    (for c = 0 only the up bond: 'u Y, u n -> n Y').
+  * each site (r, c), r >= 1: the frontier spin u = (r-1, c) is contracted
+    with the site tensor Q[l, u, n] = T_left[l, n] + T_up[u, n]:
+    'X l u Y, l u n -> X l n Y' (for c = 0 only the up bond: 'u Y, u n -> n Y').
+    Q depends on two couplings only, so it is formed with the bond tensors
+    when the network is built (2 x 2 x 2, sums of +-1: exact); with
+    site_nodes=True it is a tree node of its own instead ('ln,un->lun', n
+    shared), one small kernel per site.
   * a final trace reduces the whole last row:  'f0 .. f_{C-1} ->' with argmax.
 The frontier always holds one spin per column (2**C entries).  The argmax of
 each contraction node records the winning u; back-tracking from the final
@@ -28,7 +31,12 @@ def bond(j: int) -> np.ndarray:
     return (float(j) * s[:, None] * s[None, :]).astype(np.float32)
 
 
-def build_network(jh: np.ndarray, jv: np.ndarray):
+def site(jl: int, ju: int) -> np.ndarray:
+    """Q[l, u, n] = T_left[l, n] + T_up[u, n] (float32, exact)."""
+    return (bond(jl)[:, None, :] + bond(ju)[None, :, :]).astype(np.float32)
+
+
+def build_network(jh: np.ndarray, jv: np.ndarray, site_nodes: bool = False):
     """Returns (inputs, nodes, n_labels, contraction_nodes).
 
     inputs: list of float32 numpy arrays (bond tensors);
@@ -59,16 +67,20 @@ def build_network(jh: np.ndarray, jv: np.ndarray):
     for r in range(1, R):
         for c in range(C):
             u, n = lab(r - 1, c), lab(r, c)
-            tu = add_input(bond(jv[r - 1, c]))
             out = list(front)
             out[c] = n
             if c == 0:
+                tu = add_input(bond(jv[r - 1, c]))
                 ops.append((state, ("in", tu), list(front), [u, n], out, True))
             else:
                 l = lab(r, c - 1)
-                tl = add_input(bond(jh[r, c - 1]))
-                ops.append((("in", tl), ("in", tu), [l, n], [u, n], [l, u, n], False))
-                q = ("node", len(ops) - 1)
+                if site_nodes:
+                    tu = add_input(bond(jv[r - 1, c]))
+                    tl = add_input(bond(jh[r, c - 1]))
+                    ops.append((("in", tl), ("in", tu), [l, n], [u, n], [l, u, n], False))
+                    q = ("node", len(ops) - 1)
+                else:
+                    q = ("in", add_input(site(jh[r, c - 1], jv[r - 1, c])))
                 ops.append((state, q, list(front), [l, u, n], out, True))
             state = ("node", len(ops) - 1)
             front = out

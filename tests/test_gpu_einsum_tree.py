@@ -226,6 +226,25 @@ def test_ising_workload_24x24_full_size(trop):
     assert oracle.ising_energy(jh, jv, spins) == -w
 
 
+@pytest.mark.parametrize("rows,cols", [(8, 8), (5, 9)])
+def test_ising_site_inputs_and_site_nodes_agree(trop, rows, cols):
+    """The spin glass with its site tensors formed at build time (the default) and with one
+    'ln,un->lun' node per site: the same value and back-tracked spins as the oracle."""
+    from einsum_device_side_gb300 import ising
+    jh, jv = synth.couplings(21, rows, cols)
+    wo, so = oracle.ising_ground(jh, jv, rows, cols, nthreads=0)
+    for site_nodes in (False, True):
+        inputs, nodes, n_labels, need = ising.build_network(jh, jv, site_nodes=site_nodes)
+        dev_in = [_dev(t) for t in inputs]
+        am = [torch.empty([2] * len(nodes[j][4]), dtype=torch.int32, device="cuda") if j in need else None
+              for j in range(len(nodes))]
+        out = torch.empty((), device="cuda")
+        trop.contract_tree(dev_in, nodes, "maxplus", out, am)
+        assign = trop.tree_backtrack(dev_in, nodes, am, n_labels, 0)
+        assert out.item() == wo
+        np.testing.assert_array_equal(ising.spins_from_assignment(assign.cpu().numpy(), rows, cols), so)
+
+
 # ---------------------------------------------------------------- plan cache
 
 def test_plan_cache_lowers_a_repeated_einsum_once(trop):
