@@ -113,15 +113,15 @@ def energy(jh: np.ndarray, jv: np.ndarray, spins: np.ndarray) -> int:
     return int(-(jh * s[:, :-1] * s[:, 1:]).sum() - (jv * s[:-1, :] * s[1:, :]).sum())
 
 
-def ground_state(jh, jv, device="cuda", keep_argmax=True):
+def ground_state(jh, jv, device="cuda", keep_argmax=True, site_nodes=False):
     """Contract the network on the GPU; returns (W, spins, per-node argmax).
 
-    W = max sum J s s (E0 = -W)."""
+    W = max sum J s s (E0 = -W).  site_nodes: as in build_network."""
     import torch
 
     from . import contract_tree, tree_backtrack
 
-    inputs, nodes, n_labels, need = build_network(jh, jv)
+    inputs, nodes, n_labels, need = build_network(jh, jv, site_nodes=site_nodes)
     dev_inputs = [torch.from_numpy(t).to(device) for t in inputs]
     R, C = jh.shape[0], jh.shape[1] + 1
     out = torch.empty((), dtype=torch.float32, device=device)
