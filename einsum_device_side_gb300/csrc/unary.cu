@@ -522,8 +522,8 @@ __global__ void __launch_bounds__(NT) k_reduce_block(const T* __restrict__ in, T
 // 32 consecutive outputs along the fastest output axis (unit stride in the input, so a slice's
 // loads are coalesced) x RS slices of the reduced range per CTA: lane x of slice y takes
 // r = y, y + RS, ...  The slices' partial (value, first index) pairs are merged in shared
-// memory, a better value or an equal one with a smaller index winning: the strict
-// left-to-right result.
+// memory, pairwise in log2(RS) levels, a better value or an equal one with a smaller index
+// winning: the strict left-to-right result.
 template <int SR, typename T, int RS>
 __global__ void __launch_bounds__(32 * RS) k_reduce_tile(const T* __restrict__ in, T* __restrict__ out,
                                                         int32_t* __restrict__ arg, RedParams p)
@@ -557,19 +557,23 @@ __global__ void __launch_bounds__(32 * RS) k_reduce_tile(const T* __restrict__ i
         sv[y][x] = best;
         si[y][x] = idx;
         __syncthreads();
-        if (y == 0 && valid) {
+        // pairwise, in log2(RS) levels: slice y takes slice y + h's pair (the merge is associative
+        // and commutative: the better value, then the smaller index)
 #pragma unroll
-            for (int q = 1; q < RS; ++q) {
-                const T v = sv[q][x];
-                const int64_t i = si[q][x];
+        for (int h = RS / 2; h > 0; h >>= 1) {
+            if (y < h) {
+                const T v = sv[y + h][x];
+                const int64_t i = si[y + h][x];
                 if (S::better(v, best) || (v == best && i < idx)) {
                     best = v;
                     idx = i;
                 }
+                sv[y][x] = best;
+                si[y][x] = idx;
             }
-            red_store(out, oo, best, arg, oa, final_index(idx), p);
+            __syncthreads();
         }
-        __syncthreads();
+        if (y == 0 && valid) red_store(out, oo, best, arg, oa, final_index(idx), p);
     }
 }
 
