@@ -504,3 +504,61 @@ def test_back_to_back_gemms_of_different_batch_counts(trop):
     for sr, ad, bd, rc, ri, outs in work:
         assert outs[0].cpu().numpy().tobytes() == rc.tobytes()
         np.testing.assert_array_equal(outs[1].cpu().numpy(), ri)
+
+
+def test_random_mixed_gemm_sequences_stay_exact(trop):
+    """Seeded random sequences of GEMM calls: mixed shapes and routes (one-launch GEMM at K = 256,
+    64 and 16, the panel resolve at K = 1024, the cp.async tiles on ragged panels), with and
+    without argmax, on two streams, into two output buffers per problem, half of them refilled
+    first.  The last call on each buffer decides its contents, which must equal the oracle's
+    bitwise.  This drives the early start of back-to-back one-launch GEMMs and the alternation
+    of their counter halves through arbitrary interleavings."""
+    import random
+    probs = [(0, 64, 256, 256, 256), (1, 24, 256, 256, 256), (2, 80, 100, 68, 64), (0, 32, 256, 256, 1024),
+             (1, 8, 128, 128, 64), (2, 80, 100, 68, 16), (0, 40, 192, 128, 128), (1, 6, 70, 45, 37)]
+    data = []
+    for sr, bt, m, n, k in probs:
+        a, b = synth.gemm_batched_inputs(sr, batch=bt, m=m, n=n, k=k)
+        rc, ri = oracle.gemm(a, b, sr, nthreads=0)
+        outs = [(torch.empty((bt, m, n), device="cuda"), torch.empty((bt, m, n), dtype=torch.int32, device="cuda"))
+                for _ in range(2)]
+        data.append((sr, _dev(a), _dev(b), _dev(rc), _dev(ri), outs))
+    streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
+    rng = random.Random(5)
+    e0 = trop.stats()["gemm_early_starts"]
+    bad = []
+    for it in range(15):
+        pending = []
+        for _ in range(rng.randint(3, 12)):
+            j = rng.randrange(len(data))
+            sr, ad, bd, rc, ri, outs = data[j]
+            o = rng.randrange(2)
+            st = streams[1] if rng.random() < 0.3 else streams[0]
+            if st is not streams[0]:
+                st.wait_stream(streams[0])
+            with torch.cuda.stream(st):
+                if rng.random() < 0.5:
+                    outs[o][0].fill_(0.0)
+                    outs[o][1].fill_(-9)
+                plain = rng.random() < 0.3
+                if plain:
+                    trop.gemm(ad, bd, sr, argmax=False, out=outs[o][0])
+                else:
+                    trop.gemm(ad, bd, sr, out=outs[o][0], out_argmax=outs[o][1])
+            streams[0].wait_stream(st)
+            pending.append((j, o, plain))
+        torch.cuda.synchronize()
+        seen = set()
+        for j, o, plain in reversed(pending):
+            if (j, o) in seen:
+                continue
+            seen.add((j, o))
+            sr, ad, bd, rc, ri, outs = data[j]
+            ok = torch.equal(outs[o][0].view(torch.int32), rc.view(torch.int32))
+            if not plain:
+                ok = ok and torch.equal(outs[o][1], ri)
+            if not ok:
+                bad.append((it, j, o, plain))
+    trop.sync_pool()  # raises if a bounded wait gave up
+    assert not bad, bad[:10]
+    assert trop.stats()["gemm_early_starts"] > e0
