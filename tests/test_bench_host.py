@@ -35,3 +35,14 @@ def test_traffic_record_parses():
     f = os.path.join(ROOT, "profiles", "k_gemm_tma_fused_traffic.txt")
     kv = dict(line.split(": ", 1) for line in open(f).read().splitlines() if ": " in line)
     assert int(kv["bytes_per_launch"]) > 0 and len(kv["source_code_sha256"]) == 64
+
+
+def test_traffic_record_matches_the_current_gemm_source():
+    """The committed traffic record belongs to gemm.cu as it stands (bench.py then reports it)."""
+    assert bench.gemm_traffic() is not None
+
+
+def test_cpu_baseline_on_one_thread_reports_one_core():
+    r = bench.cpu_sample_rate(target_s=0.3, threads=1)
+    assert r["cores"] == 1 and r["kind"] == "oracle" and r["value"] > 0
+    assert "1 thread" in r["sample"]
